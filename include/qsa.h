@@ -1,0 +1,243 @@
+/*
+ * qsa.h -- C ABI of the GB300 (sm_103a) Qwen Sparse Attention layer-step
+ * library, libqsa.so.
+ *
+ * One QSA layer step over a long KV cache, for decode, verify and prefill:
+ *   1. qsa_pool_index_keys  average every 4 consecutive 128-wide index keys
+ *                           into one pooled block key;
+ *   2. qsa_score_blocks     score every complete block a query row can see as
+ *                           (1/sqrt(128)) * sum over 4 index heads of
+ *                           ReLU(q_h . pooled_block);
+ *   3. qsa_select_topk      keep the 512 best blocks (2,048 tokens), lower id
+ *                           winning ties; the incomplete tail block is always
+ *                           attended and is implied, not listed;
+ *   4. qsa_sparse_attn      exact softmax attention over only the selected
+ *                           rows, 24 query heads over 2 KV heads, each
+ *                           selected K/V row read once per 12-head group,
+ *                           split over the selected rows and over KV segments;
+ *   5. qsa_lse_merge        merge partial results by their log-sum-exp.
+ * Sources: hipfire, "QSA sparse attention and the VMM KV backend", section 02
+ * "How QSA chooses what to read" and section 03 "How hipfire runs it on RDNA"
+ * (steps 1-4); MTPLX pull request #610 (segmented KV cache), "How it works,
+ * in plain terms" and "What changes" (step 5 and KV segments).
+ *
+ * Conventions (all entry points):
+ *  - Every function returns a qsa_status; nothing throws across the ABI.
+ *    On failure, qsa_last_error() gives a one-line reason (per host thread).
+ *  - Tensors are caller-owned DEVICE memory unless marked "host".  The
+ *    library never allocates, frees, copies or resizes caller buffers.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream).  Argument checks run on the host before any
+ *    launch; a launch failure returns QSA_ERR_CUDA.  Errors of kernels that
+ *    already ran surface on the stream as CUDA errors.
+ *  - Descriptor arrays (qsa_seq) are HOST memory and are consumed before the
+ *    call returns; their contents are copied into kernel parameters, so a
+ *    call can be captured into a CUDA graph.
+ *  - Rows: a call covers the query rows of n_seqs sequences, concatenated in
+ *    sequence order (row index r = rows of earlier sequences + j).  Row j of
+ *    a sequence with n_tokens = L and n_rows = M sits at absolute position
+ *    p = L - M + j and sees tokens 0..p (causal).
+ *  - Blocks: block b holds tokens 4b..4b+3.  A row at p sees
+ *    nb(p) = floor((p+1)/4) complete blocks and a tail of (p+1) mod 4 tokens
+ *    4*nb(p)..p.
+ *  - Alignment: every device pointer must be 16-byte aligned and every row
+ *    stride a multiple of 16 bytes (QSA_ERR_MISALIGNED otherwise).
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_VERSION 100            /* 1.0.0 */
+#define QSA_INDEX_DIM 128          /* width of an index key and an index-query head */
+#define QSA_INDEX_HEADS 4          /* index-query heads per query row */
+#define QSA_BLOCK_TOKENS 4         /* tokens pooled into one block key */
+#define QSA_TOP_K 512              /* the method's block budget */
+#define QSA_MAX_TOP_K 1024         /* largest top_k qsa_select_topk accepts */
+#define QSA_MAX_SEGMENTS 12        /* KV segments per sequence */
+#define QSA_MAX_FEW_ROWS 8         /* rows per sequence on the few-row scoring path */
+#define QSA_MAX_BLOCKS (1 << 18)   /* complete blocks per sequence (1,048,576 tokens) */
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
+  QSA_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / head count / size the library does not build */
+  QSA_ERR_MISALIGNED = 3,    /* pointer or stride not 16-byte aligned */
+  QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result */
+  QSA_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
+} qsa_status;
+
+typedef enum qsa_dtype {
+  QSA_F32 = 0,               /* IEEE binary32 */
+  QSA_BF16 = 1               /* bfloat16 */
+} qsa_dtype;
+
+/* One contiguous piece of a sequence's K/V cache (MTPLX pull request #610:
+ * a cache kept as immutable per-turn segments plus a growing tail).
+ * Element (h, t, d) of K -- KV head h, the segment's t-th token, channel d --
+ * is at k[h * head_stride + t * tok_stride + d]; V likewise.  The segment
+ * holds absolute tokens first_token .. first_token + n_tokens - 1.  Segments
+ * of one sequence must not overlap; tokens no segment covers are not
+ * attended. */
+typedef struct qsa_kv_segment {
+  const void* k;             /* device, kv_dtype */
+  const void* v;             /* device, kv_dtype */
+  int64_t first_token;
+  int64_t n_tokens;
+  int64_t head_stride;       /* elements between KV heads */
+  int64_t tok_stride;        /* elements between tokens, >= head_dim */
+} qsa_kv_segment;
+
+/* One sequence of a call (host struct). */
+typedef struct qsa_seq {
+  int64_t n_tokens;          /* L: tokens in the cache, this call's rows included */
+  int32_t n_rows;            /* query rows, 1..L; row j sits at L - n_rows + j */
+  int32_t n_segments;        /* qsa_sparse_attn: KV segments used, 1..QSA_MAX_SEGMENTS */
+  const float* pooled;       /* qsa_score_blocks: device [>= floor(L/4)] x pooled_stride f32 */
+  int64_t pooled_stride;     /* floats between pooled blocks, >= 128 */
+  qsa_kv_segment segments[QSA_MAX_SEGMENTS];
+} qsa_seq;
+
+/* Attention shape and options (host struct). */
+typedef struct qsa_attn_config {
+  int32_t n_q_heads;         /* Hq, e.g. 24 */
+  int32_t n_kv_heads;        /* Hkv, e.g. 2; Hq / Hkv must be <= 16 */
+  int32_t head_dim;          /* 128 or 256 */
+  qsa_dtype q_dtype;         /* dtype of q; must equal kv_dtype */
+  qsa_dtype kv_dtype;        /* dtype of every segment's K and V */
+  qsa_dtype out_dtype;       /* dtype of out */
+  float scale;               /* logit scale; 0 means 1/sqrt(head_dim) */
+  int32_t n_splits;          /* splits of each row's selected rows; 0 = library's choice */
+} qsa_attn_config;
+
+/* Human-readable name of a status code (static storage). */
+const char* qsa_status_string(qsa_status status);
+
+/* Reason for the last failing call on this host thread ("" if none). */
+const char* qsa_last_error(void);
+
+/* QSA_VERSION of the loaded library. */
+int32_t qsa_version(void);
+
+/*
+ * Step 1 -- pooling (hipfire, section 02: every 4 consecutive index keys are
+ * averaged into one pooled block key).
+ *   pooled[b * pooled_stride + d] = ((k[4b][d] + k[4b+1][d]) + k[4b+2][d] + k[4b+3][d]) / 4
+ * in fp32, for b in [first_block, first_block + n_blocks), d < 128, where
+ * k[t][d] = idx_keys[t * tok_stride + d].  Blocks must be complete (the caller
+ * guarantees tokens up to 4*(first_block + n_blocks) - 1 exist).  A decode or
+ * verify step pools only the blocks its new tokens completed.
+ *   idx_keys       device [tokens, tok_stride], idx_dtype
+ *   pooled         device f32, written only at the listed blocks
+ * n_blocks == 0 is a no-op.
+ */
+qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_t tok_stride,
+                               int64_t first_block, int64_t n_blocks, float* pooled,
+                               int64_t pooled_stride, void* stream);
+
+/*
+ * Step 2 -- block scoring (hipfire, section 02: four index-query heads score
+ * every pooled block; section 03: a few-row variant for decode and verify
+ * and a wide variant for prefill).
+ *   scores[r * ld + b] = (1/sqrt(128)) * sum_{h<4} max(0, q_idx[r][h] . pooled_s[b])
+ * for every b < nb(p_r); entries b >= nb(p_r) are left unwritten.
+ *   seqs, n_seqs   host descriptors; uses n_tokens, n_rows, pooled, pooled_stride
+ *   q_idx          device [rows, 4, 128], q_idx_dtype
+ *   scores         device [rows, ld] f32, ld >= max_r nb(p_r)
+ * Arithmetic: fp32-exact products (bf16 index queries against the fp32
+ * pooled key split into three bf16 parts on the tensor pipe; fp32 index
+ * queries on the CUDA cores) with fp32 accumulation.
+ */
+qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
+                            qsa_dtype q_idx_dtype, float* scores, int64_t ld, void* stream);
+
+/*
+ * Scratch bytes qsa_select_topk needs for these sequences (may be 0).
+ */
+size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k);
+
+/*
+ * Step 3 -- top-k block selection (hipfire, section 02: the top-scoring
+ * blocks within a 2,048-token budget, 512 blocks, plus the incomplete block
+ * at the end; section 03: a radix select from the scores).
+ * Per row r: k_r = min(top_k, nb(p_r)) blocks, ordered by score descending,
+ * then block id ascending (ties go to the lower id; -0.0 equals +0.0).
+ *   sel[r * top_k + i], i < cnt[r]   the kept block ids, ascending
+ *   sel[r * top_k + i], i >= cnt[r]  -1
+ *   cnt[r]                           k_r
+ * The tail block (tokens 4*nb(p_r)..p_r) is not listed; qsa_sparse_attn adds
+ * it.  Scores must not be NaN.  top_k in 1..QSA_MAX_TOP_K.
+ *   scores         device [rows, ld] f32 (as written by qsa_score_blocks)
+ *   sel, cnt       device int32 [rows, top_k], [rows]
+ *   workspace      device scratch of >= qsa_select_workspace_size bytes
+ *                  (may be NULL when that size is 0)
+ */
+qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld,
+                           int32_t top_k, int32_t* sel, int32_t* cnt, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
+ * Scratch bytes qsa_sparse_attn needs (split partials and their lse).
+ * sel_ld is the row stride of sel (the top_k used for selection).
+ */
+size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
+                               int32_t sel_ld);
+
+/*
+ * Step 4 -- sparse grouped-query attention over the selected rows (hipfire,
+ * section 02: full attention over only the selected rows, <= 2,048 + 3 per
+ * query; section 03: one workgroup per KV group of 12 query heads, so each
+ * selected row is read once, not once per head), split over each row's
+ * selected rows and over the KV segments and merged by log-sum-exp (MTPLX
+ * pull request #610).
+ * For row r and query head h (KV head g = h / (Hq/Hkv)), the attended rows
+ * are R_r = {4b..4b+3 : b in sel[r][0..cnt[r])} U {4*nb(p_r)..p_r}, kept
+ * where a segment of the row's sequence covers them; with z_t = scale*q.k_t,
+ *   lse[r][h] = log(sum_{t in R_r} exp z_t),
+ *   out[r][h] = sum_{t in R_r} exp(z_t - lse) v_t.
+ * A row with no attended key gets out = 0 and lse = -inf.  fp32 accumulation;
+ * out is rounded once to out_dtype.
+ *   seqs           host; uses n_tokens, n_rows, n_segments, segments
+ *   q              device [rows, Hq, head_dim], cfg->q_dtype
+ *   sel, cnt       device, as written by qsa_select_topk (row stride sel_ld);
+ *                  ids outside 0..nb(p_r)-1 are skipped, never dereferenced
+ *   out            device [rows, Hq, head_dim], cfg->out_dtype
+ *   lse            device [rows, Hq] f32 (natural log); may be NULL
+ *   workspace      device scratch of >= qsa_attn_workspace_size bytes
+ * Supported: head_dim 128 or 256; q and K/V both bf16 or both f32;
+ * Hq / Hkv <= 16.
+ */
+qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
+                           const void* q, const int32_t* sel, const int32_t* cnt, int32_t sel_ld,
+                           void* out, float* lse, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
+ * Step 5 -- log-sum-exp merge of partial attention results (MTPLX pull
+ * request #610: per-segment partials merged by their log-sum-exp equal
+ * single-buffer attention; rows without a visible key merge to zeros, not
+ * NaN; partials stay fp32 and the merge rounds once).
+ * For i < n_rows (a row is one (query row, head) pair):
+ *   m = max_s lse_parts[s][i];  w_s = exp(lse_parts[s][i] - m)
+ *   out[i][:] = sum_s w_s o_parts[s][i][:] / sum_s w_s;  lse_out[i] = m + log(sum_s w_s)
+ * and out = 0, lse_out = -inf when every lse_parts[s][i] is -inf.
+ *   o_parts        device f32 [n_parts, n_rows, head_dim] (normalised partials)
+ *   lse_parts      device f32 [n_parts, n_rows]
+ *   out            device [n_rows, head_dim], out_dtype
+ *   lse_out        device f32 [n_rows]; may be NULL
+ * head_dim must be a multiple of 4; n_parts >= 1.
+ */
+qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts,
+                         int64_t n_rows, int32_t head_dim, void* out, qsa_dtype out_dtype,
+                         float* lse_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,309 @@
+"""Python binding of libqsa.so, the GB300 (sm_103a) QSA layer-step library.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+PyTorch provides device memory and streams.  There is no CPU fallback; if
+the library is missing the calls raise.
+
+The five calls follow one Qwen Sparse Attention layer step (hipfire, "QSA
+sparse attention and the VMM KV backend", sections 02 and 03; MTPLX pull
+request #610 for KV segments and the log-sum-exp merge):
+
+    pool_index_keys -> score_blocks -> select_topk -> sparse_attn (-> lse_merge)
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+from typing import Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqsa.so")
+
+F32, BF16 = 0, 1
+INDEX_DIM = 128
+INDEX_HEADS = 4
+TOP_K = 512
+MAX_TOP_K = 1024
+MAX_SEGMENTS = 12
+
+STATUS = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_MISALIGNED",
+          4: "QSA_ERR_WORKSPACE", 5: "QSA_ERR_CUDA"}
+
+
+class QSAError(RuntimeError):
+    """A library call returned a status other than QSA_OK."""
+
+    def __init__(self, fn: str, status: int, detail: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {detail}")
+        self.status = status
+
+
+class KVSegment(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("first_token", ctypes.c_int64),
+                ("n_tokens", ctypes.c_int64), ("head_stride", ctypes.c_int64), ("tok_stride", ctypes.c_int64)]
+
+
+class SeqDesc(ctypes.Structure):
+    _fields_ = [("n_tokens", ctypes.c_int64), ("n_rows", ctypes.c_int32), ("n_segments", ctypes.c_int32),
+                ("pooled", ctypes.c_void_p), ("pooled_stride", ctypes.c_int64),
+                ("segments", KVSegment * MAX_SEGMENTS)]
+
+
+class AttnConfig(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("n_splits", ctypes.c_int32)]
+
+
+_lib = None
+EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks",
+           "qsa_select_workspace_size", "qsa_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn",
+           "qsa_lse_merge")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqsa.so (built by ``indexed_sparse_attention_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m indexed_sparse_attention_gb300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    seqp = ctypes.POINTER(SeqDesc)
+    L.qsa_status_string.argtypes = [i32]
+    L.qsa_status_string.restype = ctypes.c_char_p
+    L.qsa_last_error.restype = ctypes.c_char_p
+    L.qsa_version.restype = i32
+    L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
+    L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp]
+    L.qsa_select_workspace_size.argtypes = [seqp, i32, i32]
+    L.qsa_select_workspace_size.restype = sz
+    L.qsa_select_topk.argtypes = [seqp, i32, vp, i64, i32, vp, vp, vp, sz, vp]
+    L.qsa_attn_workspace_size.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), i32]
+    L.qsa_attn_workspace_size.restype = sz
+    L.qsa_sparse_attn.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
+    for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_sparse_attn", "qsa_lse_merge"):
+        getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise QSAError(fn, status, lib().qsa_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+@dataclasses.dataclass
+class Segment:
+    """A contiguous run of one sequence's K/V cache: k, v are [Hkv, n, D]
+    views (channel stride 1) holding absolute tokens first_token .. +n-1."""
+    k: torch.Tensor
+    v: torch.Tensor
+    first_token: int = 0
+
+
+@dataclasses.dataclass
+class Seq:
+    """One sequence of a call.  Its n_rows query rows are its last tokens:
+    row j sits at absolute position n_tokens - n_rows + j."""
+    n_tokens: int
+    n_rows: int
+    pooled: torch.Tensor | None = None       # [>= n_tokens // 4, >= 128] f32
+    segments: Sequence[Segment] = ()
+    idx_keys: torch.Tensor | None = None     # [>= n_tokens, 128] index keys (for pooling)
+
+    @property
+    def row_pos(self) -> list[int]:
+        return [self.n_tokens - self.n_rows + j for j in range(self.n_rows)]
+
+
+def make_seq_array(seqs: Sequence[Seq]):
+    """Marshal Seq objects into the C descriptor array (host memory)."""
+    arr = (SeqDesc * len(seqs))()
+    for i, s in enumerate(seqs):
+        d = arr[i]
+        d.n_tokens = int(s.n_tokens)
+        d.n_rows = int(s.n_rows)
+        d.n_segments = len(s.segments)
+        if len(s.segments) > MAX_SEGMENTS:
+            raise ValueError(f"at most {MAX_SEGMENTS} segments per sequence")
+        if s.pooled is not None:
+            if s.pooled.dtype != torch.float32 or s.pooled.stride(-1) != 1:
+                raise TypeError("pooled keys must be f32 with unit channel stride")
+            d.pooled = s.pooled.data_ptr()
+            d.pooled_stride = s.pooled.stride(0)
+        for j, g in enumerate(s.segments):
+            if g.k.stride(-1) != 1 or g.v.stride(-1) != 1 or g.k.stride() != g.v.stride():
+                raise TypeError("segment k/v need unit channel stride and equal strides")
+            sg = d.segments[j]
+            sg.k, sg.v = g.k.data_ptr(), g.v.data_ptr()
+            sg.first_token = int(g.first_token)
+            sg.n_tokens = int(g.k.shape[1])
+            sg.head_stride, sg.tok_stride = int(g.k.stride(0)), int(g.k.stride(1))
+    return arr
+
+
+# ---------------------------------------------------------------------- the five steps
+
+def pool_index_keys(idx_keys: torch.Tensor, pooled: torch.Tensor, first_block: int, n_blocks: int, stream=None):
+    """Step 1: pooled[b] = mean of index keys 4b..4b+3 for the listed blocks."""
+    _check("qsa_pool_index_keys", lib().qsa_pool_index_keys(
+        idx_keys.data_ptr(), _dtype_code(idx_keys), idx_keys.stride(0), int(first_block), int(n_blocks),
+        pooled.data_ptr(), pooled.stride(0), _stream(stream)))
+
+
+def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None):
+    """Step 2: scores[r, b] for every complete block row r sees."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    _check("qsa_score_blocks", lib().qsa_score_blocks(
+        arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0),
+        _stream(stream)))
+
+
+def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, top_k: int = TOP_K,
+                workspace: torch.Tensor | None = None, stream=None, seq_array=None):
+    """Step 3: the top_k best blocks per row, ascending ids, -1 padded."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    need = lib().qsa_select_workspace_size(arr, len(arr), top_k)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
+    _check("qsa_select_topk", lib().qsa_select_topk(
+        arr, len(arr), scores.data_ptr(), scores.stride(0), int(top_k), sel.data_ptr(), cnt.data_ptr(),
+        _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def attn_config(q: torch.Tensor, n_kv_heads: int, out_dtype=None, scale: float = 0.0, n_splits: int = 0):
+    cfg = AttnConfig()
+    cfg.n_q_heads, cfg.head_dim = q.shape[1], q.shape[2]
+    cfg.n_kv_heads = n_kv_heads
+    cfg.q_dtype = cfg.kv_dtype = _dtype_code(q)
+    cfg.out_dtype = _dtype_code(torch.empty(0, dtype=out_dtype)) if out_dtype is not None else F32
+    cfg.scale = float(scale)
+    cfg.n_splits = int(n_splits)
+    return cfg
+
+
+def attn_workspace_size(seqs, cfg: AttnConfig, sel_ld: int, seq_array=None) -> int:
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    return int(lib().qsa_attn_workspace_size(arr, len(arr), ctypes.byref(cfg), int(sel_ld)))
+
+
+def sparse_attn(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out: torch.Tensor,
+                lse: torch.Tensor | None = None, *, n_kv_heads: int = 2, scale: float = 0.0, n_splits: int = 0,
+                workspace: torch.Tensor | None = None, stream=None, seq_array=None, cfg: AttnConfig | None = None):
+    """Step 4 (+ the internal step-5 merge of its splits)."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    if cfg is None:
+        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
+    need = lib().qsa_attn_workspace_size(arr, len(arr), ctypes.byref(cfg), sel.stride(0))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("qsa_sparse_attn", lib().qsa_sparse_attn(
+        arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
+        out.data_ptr(), _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
+
+
+def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,
+              lse_out: torch.Tensor | None = None, stream=None):
+    """Step 5: merge [S, R, D] partials by their log-sum-exp into out [R, D]."""
+    S, R, D = o_parts.shape
+    _check("qsa_lse_merge", lib().qsa_lse_merge(
+        o_parts.data_ptr(), lse_parts.data_ptr(), S, R, D, out.data_ptr(), _dtype_code(out), _ptr(lse_out),
+        _stream(stream)))
+
+
+def n_pooled_slots(n_tokens: int) -> int:
+    """Pooled-key rows a cache of n_tokens needs (one per started block)."""
+    return (int(n_tokens) + 3) // 4
+
+
+def score_scale() -> float:
+    return 1.0 / math.sqrt(INDEX_DIM)
+
+
+class LayerStep:
+    """Preallocated buffers and descriptors for one QSA layer step of a batch
+    of sequences, so the same step can be replayed (or captured in a CUDA
+    graph) without re-marshalling.  Plumbing only: every step is a library
+    call.
+
+    ``run`` pools the blocks that the rows' tokens completed (the blocks
+    ending at positions L - n_rows .. L - 1), scores every visible block,
+    selects the top_k per row and attends over the selection.
+    """
+
+    def __init__(self, seqs: Sequence[Seq], q_idx: torch.Tensor, q: torch.Tensor, *, n_kv_heads: int = 2,
+                 top_k: int = TOP_K, out_dtype=torch.float32, n_splits: int = 0, scale: float = 0.0):
+        self.seqs = list(seqs)
+        self.q_idx, self.q = q_idx, q
+        self.top_k = int(top_k)
+        dev = q.device
+        rows = sum(s.n_rows for s in self.seqs)
+        self.ld = max(1, max(s.n_tokens // 4 for s in self.seqs))
+        self.ld = (self.ld + 3) // 4 * 4
+        self.arr = make_seq_array(self.seqs)
+        self.cfg = attn_config(q, n_kv_heads, out_dtype, scale, n_splits)
+        self.scores = torch.empty((rows, self.ld), dtype=torch.float32, device=dev)
+        self.sel = torch.empty((rows, self.top_k), dtype=torch.int32, device=dev)
+        self.cnt = torch.empty((rows,), dtype=torch.int32, device=dev)
+        self.out = torch.empty((rows, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((rows, q.shape[1]), dtype=torch.float32, device=dev)
+        sel_ws = int(lib().qsa_select_workspace_size(self.arr, len(self.arr), self.top_k))
+        attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
+        self.ws = torch.empty(max(sel_ws, attn_ws, 16), dtype=torch.uint8, device=dev)
+        # Blocks completed by each sequence's new rows: [first, last] of nb(p) over its rows.
+        self.pool_jobs = []
+        for s in self.seqs:
+            if s.idx_keys is None or s.pooled is None:
+                continue
+            b0 = (s.n_tokens - s.n_rows) // 4
+            b1 = s.n_tokens // 4
+            if b1 > b0:
+                self.pool_jobs.append((s.idx_keys, s.pooled, b0, b1 - b0))
+
+    def pool(self, stream=None):
+        for idxk, pooled, b0, n in self.pool_jobs:
+            pool_index_keys(idxk, pooled, b0, n, stream)
+
+    def score(self, stream=None):
+        score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr)
+
+    def select(self, stream=None):
+        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, self.ws, stream, seq_array=self.arr)
+
+    def attend(self, stream=None):
+        sparse_attn(None, self.q, self.sel, self.cnt, self.out, self.lse, workspace=self.ws, stream=stream,
+                    seq_array=self.arr, cfg=self.cfg)
+
+    def run(self, stream=None):
+        self.pool(stream)
+        self.score(stream)
+        self.select(stream)
+        self.attend(stream)
+        return self.out, self.lse

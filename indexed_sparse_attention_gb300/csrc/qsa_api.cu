@@ -1,0 +1,475 @@
+// Host side of the C ABI declared in include/qsa.h: argument checks, the
+// decomposition of a call into launches, and status reporting.  No entry
+// point allocates device memory; scratch comes from the caller's workspace.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "qsa_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qsa_status fail(qsa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+qsa_status ok() {
+  g_last_error.clear();
+  return QSA_OK;
+}
+
+qsa_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(QSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t dtype_size(qsa_dtype d) { return d == QSA_F32 ? 4 : 2; }
+
+bool valid_dtype(int d) { return d == QSA_F32 || d == QSA_BF16; }
+
+// Complete blocks the last (furthest) row of a sequence sees: floor(L / 4).
+int64_t max_visible_blocks(const qsa_seq& s) { return s.n_tokens / 4; }
+
+qsa_status check_rows(const qsa_seq* seqs, int32_t n_seqs, const char* fn, int64_t* total_rows) {
+  if (!seqs || n_seqs < 1) return fail(QSA_ERR_INVALID_ARG, "%s: need at least one sequence", fn);
+  int64_t rows = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const qsa_seq& s = seqs[i];
+    if (s.n_tokens < 1 || s.n_rows < 1 || s.n_rows > s.n_tokens)
+      return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has n_tokens=%lld, n_rows=%d (need 1 <= n_rows <= n_tokens)",
+                  fn, i, (long long)s.n_tokens, s.n_rows);
+    if (max_visible_blocks(s) > QSA_MAX_BLOCKS)
+      return fail(QSA_ERR_UNSUPPORTED, "%s: sequence %d has %lld complete blocks (max %d)", fn, i,
+                  (long long)max_visible_blocks(s), QSA_MAX_BLOCKS);
+    rows += s.n_rows;
+  }
+  if (rows > (int64_t)INT32_MAX / 64) return fail(QSA_ERR_UNSUPPORTED, "%s: too many rows", fn);
+  *total_rows = rows;
+  return QSA_OK;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+std::mutex g_dev_mu;
+int g_sm_count[64];
+
+}  // namespace
+
+namespace qsa {
+cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Entry {
+    int dev;
+    const void* kernel;
+    size_t bytes;
+  };
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  for (const Entry& x : done)
+    if (x.dev == dev && x.kernel == kernel && x.bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.push_back(Entry{dev, kernel, bytes});
+  return e;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+}  // namespace qsa
+
+using namespace qsa;
+
+#define QSA_API extern "C" __attribute__((visibility("default")))
+
+QSA_API const char* qsa_status_string(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "QSA_OK";
+    case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+    case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+    case QSA_ERR_MISALIGNED: return "QSA_ERR_MISALIGNED";
+    case QSA_ERR_WORKSPACE: return "QSA_ERR_WORKSPACE";
+    case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+  }
+  return "QSA_ERR_UNKNOWN";
+}
+
+QSA_API const char* qsa_last_error(void) { return g_last_error.c_str(); }
+
+QSA_API int32_t qsa_version(void) { return QSA_VERSION; }
+
+// ------------------------------------------------------------------ step 1
+QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_t tok_stride, int64_t first_block,
+                               int64_t n_blocks, float* pooled, int64_t pooled_stride, void* stream) {
+  const char* fn = "qsa_pool_index_keys";
+  if (!valid_dtype(idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: idx_dtype %d", fn, (int)idx_dtype);
+  if (first_block < 0 || n_blocks < 0) return fail(QSA_ERR_INVALID_ARG, "%s: negative block range", fn);
+  if (tok_stride < QSA_INDEX_DIM || pooled_stride < QSA_INDEX_DIM)
+    return fail(QSA_ERR_INVALID_ARG, "%s: strides must be >= %d", fn, QSA_INDEX_DIM);
+  if (n_blocks == 0) return ok();
+  if (!idx_keys || !pooled) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(idx_keys) || !aligned16(pooled) || (tok_stride * (int64_t)dtype_size(idx_dtype)) % 16 != 0 ||
+      pooled_stride % 4 != 0)
+    return fail(QSA_ERR_MISALIGNED, "%s: pointers and strides must be 16-byte aligned", fn);
+  cudaError_t e = launch_pool(idx_keys, idx_dtype, tok_stride, first_block, n_blocks, pooled, pooled_stride,
+                              as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
+// ------------------------------------------------------------------ step 2
+template <int NSEQ>
+static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const void* q_idx, qsa_dtype qd,
+                              float* scores, int64_t ld, cudaStream_t st) {
+  ScoreParams<NSEQ> p{};
+  const int tile = score_tile_blocks(qd);
+  int64_t work = 0;
+  int max_rows = 1;
+  for (int i = 0; i < n; ++i) {
+    ScoreSeq& q = p.seq[i];
+    q.pooled = seqs[i].pooled;
+    q.pooled_stride = seqs[i].pooled_stride;
+    q.n_tokens = seqs[i].n_tokens;
+    q.row_begin = row_begin;
+    q.n_rows = seqs[i].n_rows;
+    q.n_tiles = (int32_t)((max_visible_blocks(seqs[i]) + tile - 1) / tile);
+    q.n_groups = (q.n_rows + kRowGroup - 1) / kRowGroup;
+    q.work_begin = work;
+    work += (int64_t)q.n_tiles * q.n_groups;
+    max_rows = std::max(max_rows, std::min(kRowGroup, q.n_rows));
+    row_begin += seqs[i].n_rows;
+  }
+  p.n_seqs = n;
+  p.n_work = work;
+  p.q_idx = q_idx;
+  p.scores = scores;
+  p.ld = ld;
+  cudaError_t e = launch_score<NSEQ>(p, qd, max_rows, st);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_score_blocks");
+  return QSA_OK;
+}
+
+QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
+                            float* scores, int64_t ld, void* stream) {
+  const char* fn = "qsa_score_blocks";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  if (!valid_dtype(q_idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: q_idx_dtype %d", fn, (int)q_idx_dtype);
+  if (!q_idx || !scores) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q_idx) || !aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx/scores not aligned", fn);
+  for (int i = 0; i < n_seqs; ++i) {
+    const qsa_seq& q = seqs[i];
+    if (max_visible_blocks(q) > ld)
+      return fail(QSA_ERR_INVALID_ARG, "%s: ld=%lld < %lld visible blocks of sequence %d", fn, (long long)ld,
+                  (long long)max_visible_blocks(q), i);
+    if (max_visible_blocks(q) > 0) {
+      if (!q.pooled) return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has no pooled keys", fn, i);
+      if (q.pooled_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: pooled_stride < 128", fn);
+      if (!aligned16(q.pooled) || q.pooled_stride % 4 != 0)
+        return fail(QSA_ERR_MISALIGNED, "%s: pooled keys of sequence %d not 16-byte aligned", fn, i);
+    }
+  }
+  cudaStream_t st = as_stream(stream);
+  if (n_seqs == 1) {
+    s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, st);
+  } else {
+    int32_t row_begin = 0;
+    for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
+      const int n = std::min(kLaunchSeqs, n_seqs - c);
+      s = score_chunk<kLaunchSeqs>(seqs + c, n, row_begin, q_idx, q_idx_dtype, scores, ld, st);
+      for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
+    }
+  }
+  return s == QSA_OK ? ok() : s;
+}
+
+// ------------------------------------------------------------------ step 3
+QSA_API size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k) {
+  (void)seqs;
+  (void)n_seqs;
+  (void)top_k;
+  return 0;
+}
+
+template <int NSEQ>
+static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const float* scores, int64_t ld,
+                               int32_t top_k, int32_t* sel, int32_t* cnt, cudaStream_t st) {
+  SelectParams<NSEQ> p{};
+  int rows = 0;
+  int64_t max_nb = 0;
+  p.row_base = row_begin;
+  for (int i = 0; i < n; ++i) {
+    p.seq[i].n_tokens = seqs[i].n_tokens;
+    p.seq[i].row_begin = row_begin + rows;
+    p.seq[i].n_rows = seqs[i].n_rows;
+    rows += seqs[i].n_rows;
+    max_nb = std::max(max_nb, max_visible_blocks(seqs[i]));
+  }
+  p.n_seqs = n;
+  p.scores = scores;
+  p.ld = ld;
+  p.top_k = top_k;
+  p.sel = sel;
+  p.cnt = cnt;
+  cudaError_t e = launch_select<NSEQ>(p, rows, max_nb, st);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_select_topk");
+  return QSA_OK;
+}
+
+QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld, int32_t top_k,
+                           int32_t* sel, int32_t* cnt, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "qsa_select_topk";
+  (void)workspace;
+  (void)workspace_bytes;
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  if (top_k < 1 || top_k > QSA_MAX_TOP_K)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: top_k=%d outside 1..%d", fn, top_k, QSA_MAX_TOP_K);
+  if (!scores || !sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: scores not aligned", fn);
+  for (int i = 0; i < n_seqs; ++i)
+    if (max_visible_blocks(seqs[i]) > ld)
+      return fail(QSA_ERR_INVALID_ARG, "%s: ld smaller than the visible blocks of sequence %d", fn, i);
+  cudaStream_t st = as_stream(stream);
+  if (n_seqs == 1) {
+    s = select_chunk<1>(seqs, 1, 0, scores, ld, top_k, sel, cnt, st);
+  } else {
+    int32_t row_begin = 0;
+    for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
+      const int n = std::min(kLaunchSeqs, n_seqs - c);
+      s = select_chunk<kLaunchSeqs>(seqs + c, n, row_begin, scores, ld, top_k, sel, cnt, st);
+      for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
+    }
+  }
+  return s == QSA_OK ? ok() : s;
+}
+
+// ------------------------------------------------------------------ step 4
+namespace {
+
+struct SplitPlan {
+  int32_t n_splits;
+  int32_t split_tokens;
+};
+
+// Longest selected list any row of the call can have: 4 tokens per listed
+// block (at most min(sel_ld, visible blocks)) plus up to 3 tail tokens.
+int64_t max_list(const qsa_seq* seqs, int32_t n_seqs, int32_t sel_ld) {
+  int64_t m = 0;
+  for (int i = 0; i < n_seqs; ++i) m = std::max(m, 4 * std::min<int64_t>(sel_ld, max_visible_blocks(seqs[i])) + 3);
+  return m;
+}
+
+SplitPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, int32_t sel_ld,
+                      int64_t rows) {
+  const int64_t n_list = max_list(seqs, n_seqs, sel_ld);
+  int64_t n = cfg->n_splits;
+  if (n <= 0) {
+    const int64_t pairs = rows * cfg->n_kv_heads;
+    const int64_t sms = device_sm_count();
+    n = pairs >= sms ? 1 : (sms + pairs - 1) / pairs;
+    n = std::min<int64_t>(n, (n_list + 63) / 64);
+  }
+  n = std::max<int64_t>(1, std::min<int64_t>(n, (n_list + 31) / 32));
+  int64_t per = (n_list + n - 1) / n;
+  per = (per + 31) / 32 * 32;
+  n = (n_list + per - 1) / per;
+  return SplitPlan{(int32_t)n, (int32_t)per};
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t attn_ws_bytes(const SplitPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
+  if (sp.n_splits <= 1) return 0;
+  const size_t parts = (size_t)sp.n_splits * (size_t)rows * (size_t)cfg->n_q_heads;
+  return align256(parts * (size_t)cfg->head_dim * 4) + align256(parts * 4);
+}
+
+qsa_status check_attn_config(const qsa_attn_config* cfg, const char* fn) {
+  if (!cfg) return fail(QSA_ERR_INVALID_ARG, "%s: null config", fn);
+  if (cfg->n_q_heads < 1 || cfg->n_kv_heads < 1 || cfg->n_q_heads % cfg->n_kv_heads != 0)
+    return fail(QSA_ERR_INVALID_ARG, "%s: n_q_heads=%d must be a positive multiple of n_kv_heads=%d", fn,
+                cfg->n_q_heads, cfg->n_kv_heads);
+  if (cfg->n_q_heads / cfg->n_kv_heads > 16)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: more than 16 query heads per KV head", fn);
+  if (cfg->head_dim != 128 && cfg->head_dim != 256)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: head_dim=%d (supported: 128, 256)", fn, cfg->head_dim);
+  if (!valid_dtype(cfg->q_dtype) || !valid_dtype(cfg->kv_dtype) || !valid_dtype(cfg->out_dtype))
+    return fail(QSA_ERR_UNSUPPORTED, "%s: unknown dtype", fn);
+  if (cfg->q_dtype != cfg->kv_dtype) return fail(QSA_ERR_UNSUPPORTED, "%s: q_dtype must equal kv_dtype", fn);
+  if (!(cfg->scale >= 0.f) || isinf(cfg->scale)) return fail(QSA_ERR_INVALID_ARG, "%s: bad scale", fn);
+  return QSA_OK;
+}
+
+qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, const char* fn) {
+  const int64_t es = (int64_t)dtype_size(cfg->kv_dtype);
+  for (int i = 0; i < n_seqs; ++i) {
+    const qsa_seq& s = seqs[i];
+    if (s.n_segments < 1 || s.n_segments > QSA_MAX_SEGMENTS)
+      return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has %d segments (1..%d)", fn, i, s.n_segments,
+                  QSA_MAX_SEGMENTS);
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    for (int j = 0; j < s.n_segments; ++j) {
+      const qsa_kv_segment& g = s.segments[j];
+      if (!g.k || !g.v) return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has a null K/V", fn, i, j);
+      if (g.first_token < 0 || g.n_tokens < 0)
+        return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has a negative range", fn, i, j);
+      if (g.tok_stride < cfg->head_dim || g.head_stride < 0)
+        return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has bad strides", fn, i, j);
+      if (!aligned16(g.k) || !aligned16(g.v) || (g.tok_stride * es) % 16 != 0 || (g.head_stride * es) % 16 != 0)
+        return fail(QSA_ERR_MISALIGNED, "%s: sequence %d segment %d K/V not 16-byte aligned", fn, i, j);
+      ranges.emplace_back(g.first_token, g.first_token + g.n_tokens);
+    }
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t j = 1; j < ranges.size(); ++j)
+      if (ranges[j].first < ranges[j - 1].second)
+        return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has overlapping segments", fn, i);
+  }
+  return QSA_OK;
+}
+
+template <int NSEQ>
+qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_attn_config* cfg, const void* q,
+                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const SplitPlan& sp, int64_t total_rows,
+                      void* out, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
+  AttnParams<NSEQ> p{};
+  int rows = 0, nseg = 0;
+  p.row_base = row_begin;
+  for (int i = 0; i < n; ++i) {
+    AttnSeq& a = p.seq[i];
+    a.n_tokens = seqs[i].n_tokens;
+    a.row_begin = row_begin + rows;
+    a.n_rows = seqs[i].n_rows;
+    a.seg_begin = nseg;
+    a.n_segs = seqs[i].n_segments;
+    for (int j = 0; j < seqs[i].n_segments; ++j) {
+      const qsa_kv_segment& g = seqs[i].segments[j];
+      Segment& d = p.seg[nseg++];
+      d.k = g.k;
+      d.v = g.v;
+      d.first = g.first_token;
+      d.n = g.n_tokens;
+      d.head_stride = g.head_stride;
+      d.tok_stride = g.tok_stride;
+    }
+    rows += seqs[i].n_rows;
+  }
+  p.n_seqs = n;
+  p.q = q;
+  p.sel = sel;
+  p.cnt = cnt;
+  p.sel_ld = sel_ld;
+  p.n_q_heads = cfg->n_q_heads;
+  p.group = cfg->n_q_heads / cfg->n_kv_heads;
+  p.head_dim = cfg->head_dim;
+  p.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
+  p.n_splits = sp.n_splits;
+  p.split_tokens = sp.split_tokens;
+  p.total_rows = (int32_t)total_rows;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.out = out;
+  p.lse = lse;
+  p.out_dtype = cfg->out_dtype;
+  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, st);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn");
+  return QSA_OK;
+}
+
+}  // namespace
+
+QSA_API size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, int32_t sel_ld) {
+  int64_t rows = 0;
+  if (check_rows(seqs, n_seqs, "qsa_attn_workspace_size", &rows) != QSA_OK) return 0;
+  if (check_attn_config(cfg, "qsa_attn_workspace_size") != QSA_OK || sel_ld < 1) return 0;
+  return attn_ws_bytes(plan_splits(seqs, n_seqs, cfg, sel_ld, rows), rows, cfg);
+}
+
+QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, const void* q,
+                           const int32_t* sel, const int32_t* cnt, int32_t sel_ld, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "qsa_sparse_attn";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  if ((s = check_attn_config(cfg, fn)) != QSA_OK) return s;
+  if (sel_ld < 1) return fail(QSA_ERR_INVALID_ARG, "%s: sel_ld < 1", fn);
+  if (!q || !sel || !cnt || !out) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q) || !aligned16(out)) return fail(QSA_ERR_MISALIGNED, "%s: q/out not 16-byte aligned", fn);
+  if ((s = check_segments(seqs, n_seqs, cfg, fn)) != QSA_OK) return s;
+  const SplitPlan sp = plan_splits(seqs, n_seqs, cfg, sel_ld, rows);
+  const size_t need = attn_ws_bytes(sp, rows, cfg);
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (need > 0 && !aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  if (sp.n_splits > 1) {
+    const size_t parts = (size_t)sp.n_splits * (size_t)rows * (size_t)cfg->n_q_heads;
+    part_o = static_cast<float*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(parts * (size_t)cfg->head_dim * 4));
+  }
+  cudaStream_t st = as_stream(stream);
+  if (n_seqs == 1) {
+    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o, part_lse, st);
+  } else {
+    int32_t row_begin = 0;
+    for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
+      const int n = std::min(kLaunchSeqs, n_seqs - c);
+      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o,
+                                  part_lse, st);
+      for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
+    }
+  }
+  if (s != QSA_OK) return s;
+  if (sp.n_splits > 1) {
+    cudaError_t e = launch_merge(part_o, part_lse, sp.n_splits, rows * cfg->n_q_heads, cfg->head_dim, out,
+                                 cfg->out_dtype, lse, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+  }
+  return ok();
+}
+
+// ------------------------------------------------------------------ step 5
+QSA_API qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t n_rows,
+                         int32_t head_dim, void* out, qsa_dtype out_dtype, float* lse_out, void* stream) {
+  const char* fn = "qsa_lse_merge";
+  if (n_parts < 1 || n_rows < 0) return fail(QSA_ERR_INVALID_ARG, "%s: n_parts >= 1 and n_rows >= 0 required", fn);
+  if (head_dim < 4 || head_dim % 4 != 0) return fail(QSA_ERR_UNSUPPORTED, "%s: head_dim must be a multiple of 4", fn);
+  if (!valid_dtype(out_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: out_dtype %d", fn, (int)out_dtype);
+  if (n_rows == 0) return ok();
+  if (!o_parts || !lse_parts || !out) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(o_parts) || !aligned16(out)) return fail(QSA_ERR_MISALIGNED, "%s: o_parts/out not aligned", fn);
+  cudaError_t e = launch_merge(o_parts, lse_parts, n_parts, n_rows, head_dim, out, out_dtype, lse_out,
+                               as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+

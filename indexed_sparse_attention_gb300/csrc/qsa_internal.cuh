@@ -1,0 +1,142 @@
+// Internal declarations shared by the CUDA translation units of libqsa.so.
+// Kernel parameters are passed by value (so a call can be captured in a CUDA
+// graph); sequence and segment tables are copied into them on the host.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qsa.h"
+
+namespace qsa {
+
+// Sequences one launch carries; larger calls are issued in chunks.
+constexpr int kLaunchSeqs = 8;
+// Query rows of one scoring row-group (4 index heads each: 32 MMA columns).
+constexpr int kRowGroup = 8;
+// Blocks per scoring tile (the MMA M dimension).
+constexpr int kScoreTile = 16;
+
+// ---------------------------------------------------------------- scoring
+struct ScoreSeq {
+  const float* pooled;
+  int64_t pooled_stride;
+  int64_t n_tokens;
+  int64_t work_begin;    // first flattened (tile, row-group) item of this sequence
+  int32_t row_begin;     // global index of the sequence's first row
+  int32_t n_rows;
+  int32_t n_tiles;       // ceil(floor(L/4) / kScoreTile)
+  int32_t n_groups;      // ceil(n_rows / kRowGroup)
+};
+
+template <int NSEQ>
+struct ScoreParams {
+  ScoreSeq seq[NSEQ];
+  int32_t n_seqs;
+  int64_t n_work;        // total (tile, row-group) items
+  const void* q_idx;     // [rows, 4, 128]
+  float* scores;
+  int64_t ld;
+};
+
+// ---------------------------------------------------------------- selection
+struct RowSeq {
+  int64_t n_tokens;
+  int32_t row_begin;
+  int32_t n_rows;
+};
+
+template <int NSEQ>
+struct SelectParams {
+  RowSeq seq[NSEQ];
+  int32_t n_seqs;
+  int32_t row_base;      // global index of this launch's first row
+  const float* scores;
+  int64_t ld;
+  int32_t top_k;
+  int32_t* sel;
+  int32_t* cnt;
+};
+
+// ---------------------------------------------------------------- attention
+struct Segment {
+  const void* k;
+  const void* v;
+  int64_t first;
+  int64_t n;
+  int64_t head_stride;
+  int64_t tok_stride;
+};
+
+struct AttnSeq {
+  int64_t n_tokens;
+  int32_t row_begin;
+  int32_t n_rows;
+  int32_t seg_begin;
+  int32_t n_segs;
+};
+
+template <int NSEQ>
+struct AttnParams {
+  AttnSeq seq[NSEQ];
+  Segment seg[NSEQ * QSA_MAX_SEGMENTS];
+  int32_t n_seqs;
+  int32_t row_base;        // global index of this launch's first row
+  const void* q;           // [rows, Hq, D]
+  const int32_t* sel;
+  const int32_t* cnt;
+  int32_t sel_ld;
+  int32_t n_q_heads;
+  int32_t group;           // query heads per KV head
+  int32_t head_dim;
+  float scale;             // logit scale
+  int32_t n_splits;
+  int32_t split_tokens;    // selected-list entries per split
+  int32_t total_rows;      // rows of the whole call (partial buffer stride)
+  float* part_o;           // [n_splits, total_rows, Hq, D] when n_splits > 1
+  float* part_lse;         // [n_splits, total_rows, Hq]
+  void* out;               // [total_rows, Hq, D] when n_splits == 1
+  float* lse;              // [total_rows, Hq] or null
+  int32_t out_dtype;
+};
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64_t first_block,
+                        int64_t n_blocks, float* pooled, int64_t pstride, cudaStream_t st);
+
+template <int NSEQ>
+cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group,
+                         cudaStream_t st);
+
+template <int NSEQ>
+cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
+
+template <int NSEQ>
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st);
+
+cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows,
+                         int head_dim, void* out, int out_dtype, float* lse_out, cudaStream_t st);
+
+// Shared-memory bytes the selection kernel needs for rows of up to max_nb blocks.
+size_t select_smem_bytes(int64_t max_nb);
+
+int device_sm_count();
+
+// Raise a kernel's dynamic shared-memory limit (once per device and size).
+cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes);
+
+// Blocks per scoring work item for the kernel that serves q_dtype.
+int score_tile_blocks(qsa_dtype q_dtype);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Row r of a sequence at n_tokens L with n_rows M sits at L - M + j.
+__device__ __forceinline__ int64_t row_position(int64_t L, int32_t n_rows, int32_t j) {
+  return L - n_rows + j;
+}
+__device__ __forceinline__ int64_t visible_blocks(int64_t p) { return (p + 1) >> 2; }
+
+}  // namespace qsa

@@ -1,0 +1,276 @@
+// Steps 1 and 2 of the QSA layer step: pooling index keys into block keys and
+// scoring the pooled blocks (hipfire, "QSA sparse attention and the VMM KV
+// backend", section 02 "How QSA chooses what to read"; section 03 names a
+// few-row scoring variant for decode/verify and a wide one for prefill).
+//
+// Scoring is a streaming pass over the pooled keys: every 512-byte pooled
+// block is read once per row-group of <= 8 query rows.  For bf16 index
+// queries the dot products run on the tensor pipe (mma.sync m16n8k16): the
+// fp32 pooled key is split into three bf16 parts hi + mid + lo that sum to it
+// exactly, and bf16 x bf16 products are exact in fp32, so the result carries
+// fp32-accumulation error only.  fp32 index queries take a CUDA-core kernel.
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+namespace {
+
+constexpr float kScoreScale = 0.08838834764831845f;  // 1/sqrt(128)
+
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+  float4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// bf16x2 of (lo_elem, hi_elem), round to nearest even; lo_elem in bits 0..15.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
+  return r;
+}
+
+// Split the fp32 pair (x, y) into three bf16x2 words with x = hx + mx + lx
+// exactly (each residual is the exact rounding error of the previous step).
+__device__ __forceinline__ void split3(float x, float y, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  hi = pack_bf16x2(x, y);
+  const float rx = x - bf16_lo(hi), ry = y - bf16_hi(hi);
+  mid = pack_bf16x2(rx, ry);
+  const float sx = rx - bf16_lo(mid), sy = ry - bf16_hi(mid);
+  lo = pack_bf16x2(sx, sy);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ pooling
+__global__ void pool_kernel(const void* __restrict__ idx, int dtype, int64_t tok_stride, int64_t first_block,
+                            int64_t n_blocks, float* __restrict__ pooled, int64_t pstride) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (block, 4-channel group)
+  if (i >= n_blocks * (QSA_INDEX_DIM / 4)) return;
+  const int64_t b = first_block + i / (QSA_INDEX_DIM / 4);
+  const int d = (int)(i % (QSA_INDEX_DIM / 4)) * 4;
+  float4 k[4];
+  if (dtype == QSA_F32) {
+    const float* src = static_cast<const float*>(idx) + 4 * b * tok_stride + d;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k[j] = *reinterpret_cast<const float4*>(src + j * tok_stride);
+  } else {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(idx) + 4 * b * tok_stride + d;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src + j * tok_stride);
+      k[j] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+  }
+  float4 m;
+  m.x = (((k[0].x + k[1].x) + k[2].x) + k[3].x) * 0.25f;
+  m.y = (((k[0].y + k[1].y) + k[2].y) + k[3].y) * 0.25f;
+  m.z = (((k[0].z + k[1].z) + k[2].z) + k[3].z) * 0.25f;
+  m.w = (((k[0].w + k[1].w) + k[2].w) + k[3].w) * 0.25f;
+  *reinterpret_cast<float4*>(pooled + b * pstride + d) = m;
+}
+
+template <int NSEQ>
+__device__ __forceinline__ int find_seq_by_work(const ScoreParams<NSEQ>& p, int64_t item) {
+  int s = 0;
+#pragma unroll
+  for (int i = 1; i < NSEQ; ++i)
+    if (i < p.n_seqs && item >= p.seq[i].work_begin) s = i;
+  return s;
+}
+
+// ------------------------------------------------------------------ scoring, tensor pipe
+// One warp per (16-block tile, group of <= 8 rows).  MMA columns are
+// (row, head) pairs n = 4*row + head; NT n-tiles of 8 columns cover 2*NT rows.
+// The 128 channels are visited in 8 k-steps of 16; inside a k-step, thread
+// quad t holds physical channels 4t..4t+3, i.e. logical fragment columns
+// (2t, 2t+1) <- channels (4t, 4t+1) and (2t+8, 2t+9) <- channels (4t+2, 4t+3).
+// A and B use the same channel permutation, so the dot products are unchanged
+// and each thread reads one float4 per row per k-step (fully used sectors).
+template <int NT, int NSEQ>
+__global__ void __launch_bounds__(256) score_mma_kernel(const ScoreParams<NSEQ> p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t item = (int64_t)blockIdx.x * 8 + warp;
+  if (item >= p.n_work) return;
+  const int si = find_seq_by_work(p, item);
+  const ScoreSeq& sq = p.seq[si];
+  const int64_t w = item - sq.work_begin;
+  const int64_t tile = w / sq.n_groups;
+  const int grp = (int)(w - tile * sq.n_groups);
+  const int row0 = grp * kRowGroup;                 // first row of the group within the sequence
+  const int rows = min(kRowGroup, sq.n_rows - row0);
+  const int64_t b0 = tile * kScoreTile;
+  // Complete blocks the group's last row sees bound every row of the group.
+  const int64_t nb_last = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + rows - 1));
+  if (b0 >= nb_last) return;
+
+  const int g = lane >> 2, t = lane & 3;
+
+  // A operand: rows b0+g and b0+g+8 of the pooled tile, one float4 per k-step.
+  float4 ra[8], rb[8];
+  {
+    const int64_t ba = b0 + g, bb = b0 + g + 8;
+    const float* pa = sq.pooled + ba * sq.pooled_stride + 4 * t;
+    const float* pb = sq.pooled + bb * sq.pooled_stride + 4 * t;
+    const bool va = ba < nb_last, vb = bb < nb_last;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      ra[s] = va ? ld_stream4(pa + 16 * s) : make_float4(0.f, 0.f, 0.f, 0.f);
+      rb[s] = vb ? ld_stream4(pb + 16 * s) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  // B operand: the index queries, bf16 [rows, 4, 128].
+  uint32_t bq[NT][8][2];
+  {
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int n = 8 * j + g, r = n >> 2, h = n & 3;
+      if (r < rows) {
+        const __nv_bfloat16* src =
+            qb + ((int64_t)(sq.row_begin + row0 + r) * QSA_INDEX_HEADS + h) * QSA_INDEX_DIM + 4 * t;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint2 v = *reinterpret_cast<const uint2*>(src + 16 * s);
+          bq[j][s][0] = v.x;
+          bq[j][s][1] = v.y;
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < 8; ++s) bq[j][s][0] = bq[j][s][1] = 0u;
+      }
+    }
+  }
+  float acc[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
+    split3(ra[s].x, ra[s].y, h0, m0, l0);  // row g,   columns 2t, 2t+1
+    split3(rb[s].x, rb[s].y, h1, m1, l1);  // row g+8, columns 2t, 2t+1
+    split3(ra[s].z, ra[s].w, h2, m2, l2);  // row g,   columns 2t+8, 2t+9
+    split3(rb[s].z, rb[s].w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      mma_bf16(acc[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
+      mma_bf16(acc[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
+      mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
+    }
+  }
+  // Epilogue: thread (g, t) holds columns 8j+2t, 8j+2t+1 = heads 2(t&1), 2(t&1)+1
+  // of row 2j + (t>>1); its neighbour t^1 holds the other two heads.
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    float v0 = fmaxf(acc[j][0], 0.f) + fmaxf(acc[j][1], 0.f);
+    float v1 = fmaxf(acc[j][2], 0.f) + fmaxf(acc[j][3], 0.f);
+    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+    const int r = 2 * j + (t >> 1);
+    if ((t & 1) == 0 && r < rows) {
+      const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + r));
+      float* dst = p.scores + (int64_t)(sq.row_begin + row0 + r) * p.ld;
+      if (b0 + g < nb) dst[b0 + g] = v0 * kScoreScale;
+      if (b0 + g + 8 < nb) dst[b0 + g + 8] = v1 * kScoreScale;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
+// One CTA per (32-block tile, group of <= 8 rows); lane = (row, head) pair,
+// warp w = blocks 4w..4w+3 of the tile.
+constexpr int kSimtTile = 32;
+
+template <int NSEQ>
+__global__ void __launch_bounds__(256) score_simt_kernel(const ScoreParams<NSEQ> p) {
+  __shared__ float q_s[32][QSA_INDEX_DIM + 1];
+  __shared__ float k_s[kSimtTile][QSA_INDEX_DIM + 1];
+  const int64_t item = blockIdx.x;
+  if (item >= p.n_work) return;
+  const int si = find_seq_by_work(p, item);
+  const ScoreSeq& sq = p.seq[si];
+  const int64_t w = item - sq.work_begin;
+  const int64_t tile = w / sq.n_groups;
+  const int grp = (int)(w - tile * sq.n_groups);
+  const int row0 = grp * kRowGroup;
+  const int rows = min(kRowGroup, sq.n_rows - row0);
+  const int64_t b0 = tile * kSimtTile;
+  const int64_t nb_last = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + rows - 1));
+  if (b0 >= nb_last) return;
+
+  const float* qf = static_cast<const float*>(p.q_idx);
+  for (int i = threadIdx.x; i < 32 * QSA_INDEX_DIM; i += blockDim.x) {
+    const int pair = i / QSA_INDEX_DIM, d = i % QSA_INDEX_DIM, r = pair >> 2, h = pair & 3;
+    q_s[pair][d] = r < rows
+                       ? qf[((int64_t)(sq.row_begin + row0 + r) * QSA_INDEX_HEADS + h) * QSA_INDEX_DIM + d]
+                       : 0.f;
+    const int64_t b = b0 + pair;
+    k_s[pair][d] = b < nb_last ? sq.pooled[b * sq.pooled_stride + d] : 0.f;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int d = 0; d < QSA_INDEX_DIM; ++d) {
+    const float qv = q_s[lane][d];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = fmaf(qv, k_s[4 * warp + j][d], acc[j]);
+  }
+  const int r = lane >> 2;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float v = fmaxf(acc[j], 0.f);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    const int64_t b = b0 + 4 * warp + j;
+    if ((lane & 3) == 0 && r < rows) {
+      const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + r));
+      if (b < nb) p.scores[(int64_t)(sq.row_begin + row0 + r) * p.ld + b] = v * kScoreScale;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64_t first_block, int64_t n_blocks,
+                        float* pooled, int64_t pstride, cudaStream_t st) {
+  const int64_t threads = n_blocks * (QSA_INDEX_DIM / 4);
+  const int bs = 256;
+  const int64_t grid = (threads + bs - 1) / bs;
+  pool_kernel<<<(unsigned)grid, bs, 0, st>>>(idx, (int)dt, tok_stride, first_block, n_blocks, pooled, pstride);
+  return cudaGetLastError();
+}
+
+// The work decomposition (tile size) differs between the two kernels; the host
+// fills n_tiles / work_begin for kScoreTile (bf16) or kSimtTile (fp32).
+int score_tile_blocks(qsa_dtype q_dtype) { return q_dtype == QSA_BF16 ? kScoreTile : kSimtTile; }
+
+template <int NSEQ>
+cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
+  if (p.n_work == 0) return cudaSuccess;
+  if (q_dtype == QSA_F32) {
+    score_simt_kernel<NSEQ><<<(unsigned)p.n_work, 256, 0, st>>>(p);
+  } else {
+    const unsigned grid = (unsigned)((p.n_work + 7) / 8);
+    if (max_rows_per_group <= 2)
+      score_mma_kernel<1, NSEQ><<<grid, 256, 0, st>>>(p);
+    else if (max_rows_per_group <= 4)
+      score_mma_kernel<2, NSEQ><<<grid, 256, 0, st>>>(p);
+    else
+      score_mma_kernel<4, NSEQ><<<grid, 256, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);
+template cudaError_t launch_score<kLaunchSeqs>(const ScoreParams<kLaunchSeqs>&, qsa_dtype, int, cudaStream_t);
+
+}  // namespace qsa

@@ -1,0 +1,146 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before any launch.
+
+Device pointers below are fake aligned addresses: host-side checks never
+dereference them, and every call here fails validation before it would
+reach CUDA (or is a documented no-op).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import indexed_sparse_attention_gb300 as qsa
+from indexed_sparse_attention_gb300 import build as qsa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+FAKE = 0x10000        # aligned, never dereferenced on the host
+FAKE_MIS = 0x10004    # 4-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def L():
+    qsa_build.build()
+    return qsa.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?(qsa_[a-z_]+)\(", text, re.M)))
+
+
+def test_header_declares_the_five_steps():
+    names = _declared()
+    for n in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_sparse_attn", "qsa_lse_merge"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert set(qsa.EXPORTS) <= set(_declared())
+
+
+def test_status_strings_and_version(L):
+    assert L.qsa_version() == 100
+    for code, name in qsa.STATUS.items():
+        assert L.qsa_status_string(code).decode() == name
+    assert L.qsa_status_string(99).decode() == "QSA_ERR_UNKNOWN"
+
+
+def _seq(n_tokens=4099, n_rows=4, pooled=FAKE, n_segments=1, segs=None):
+    arr = (qsa.SeqDesc * 1)()
+    d = arr[0]
+    d.n_tokens, d.n_rows, d.n_segments = n_tokens, n_rows, n_segments
+    d.pooled, d.pooled_stride = pooled, 128
+    for j, (first, n) in enumerate(segs or [(0, n_tokens)]):
+        s = d.segments[j]
+        s.k, s.v, s.first_token, s.n_tokens = FAKE, FAKE, first, n
+        s.head_stride, s.tok_stride = n * 256, 256
+    return arr
+
+
+def _cfg(**kw):
+    c = qsa.AttnConfig()
+    c.n_q_heads, c.n_kv_heads, c.head_dim = 24, 2, 256
+    c.q_dtype = c.kv_dtype = qsa.BF16
+    c.out_dtype = qsa.F32
+    c.scale, c.n_splits = 0.0, 0
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_pool_validation(L):
+    assert L.qsa_pool_index_keys(FAKE, 7, 128, 0, 4, FAKE, 128, None) == 2
+    assert L.qsa_pool_index_keys(FAKE, qsa.F32, 128, -1, 4, FAKE, 128, None) == 1
+    assert L.qsa_pool_index_keys(FAKE, qsa.F32, 64, 0, 4, FAKE, 128, None) == 1
+    assert L.qsa_pool_index_keys(FAKE_MIS, qsa.F32, 128, 0, 4, FAKE, 128, None) == 3
+    assert L.qsa_pool_index_keys(FAKE, qsa.BF16, 132, 0, 4, FAKE, 128, None) == 3   # 264-byte rows
+    assert L.qsa_pool_index_keys(None, qsa.F32, 128, 0, 4, FAKE, 128, None) == 1
+    assert "null" in L.qsa_last_error().decode()
+    assert L.qsa_pool_index_keys(None, qsa.F32, 128, 0, 0, None, 128, None) == 0     # empty range: no-op
+    assert L.qsa_last_error().decode() == ""
+
+
+def test_score_validation(L):
+    seq = _seq()
+    assert L.qsa_score_blocks(seq, 0, FAKE, qsa.BF16, FAKE, 1024, None) == 1
+    assert L.qsa_score_blocks(seq, 1, FAKE, 9, FAKE, 1024, None) == 2
+    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1023, None) == 1       # ld < 1,024 blocks
+    assert L.qsa_score_blocks(seq, 1, FAKE_MIS, qsa.BF16, FAKE, 1024, None) == 3
+    assert L.qsa_score_blocks(_seq(pooled=None), 1, FAKE, qsa.BF16, FAKE, 1024, None) == 1
+    assert L.qsa_score_blocks(_seq(n_rows=5000), 1, FAKE, qsa.BF16, FAKE, 1024, None) == 1
+    assert L.qsa_score_blocks(_seq(n_tokens=4 * (1 << 18) + 4), 1, FAKE, qsa.BF16, FAKE, 1 << 20, None) == 2
+
+
+def test_select_validation(L):
+    seq = _seq()
+    assert L.qsa_select_workspace_size(seq, 1, 512) == 0
+    assert L.qsa_select_topk(seq, 1, FAKE, 1024, 0, FAKE, FAKE, None, 0, None) == 2
+    assert L.qsa_select_topk(seq, 1, FAKE, 1024, 2048, FAKE, FAKE, None, 0, None) == 2
+    assert L.qsa_select_topk(seq, 1, FAKE, 1000, 512, FAKE, FAKE, None, 0, None) == 1
+    assert L.qsa_select_topk(seq, 1, FAKE, 1024, 512, None, FAKE, None, 0, None) == 1
+
+
+def test_attn_validation(L):
+    seq = _seq()
+    c = _cfg()
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(_cfg(head_dim=64)), FAKE, FAKE, FAKE, 512, FAKE, None, None, 0,
+                             None) == 2
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(_cfg(n_q_heads=25)), FAKE, FAKE, FAKE, 512, FAKE, None, None,
+                             0, None) == 1
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(_cfg(n_q_heads=34, n_kv_heads=2)), FAKE, FAKE, FAKE, 512, FAKE,
+                             None, None, 0, None) == 2                                # 17 heads per KV head
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(_cfg(q_dtype=qsa.F32)), FAKE, FAKE, FAKE, 512, FAKE, None,
+                             None, 0, None) == 2
+    assert L.qsa_sparse_attn(_seq(n_segments=0), 1, ctypes.byref(c), FAKE, FAKE, FAKE, 512, FAKE, None, None, 0,
+                             None) == 1
+    assert L.qsa_sparse_attn(_seq(n_segments=2, segs=[(0, 3000), (2999, 1100)]), 1, ctypes.byref(c), FAKE, FAKE,
+                             FAKE, 512, FAKE, None, None, 0, None) == 1             # overlapping segments
+    assert "overlapping" in L.qsa_last_error().decode()
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c), FAKE_MIS, FAKE, FAKE, 512, FAKE, None, None, 0, None) == 3
+    need = L.qsa_attn_workspace_size(seq, 1, ctypes.byref(c), 512)
+    assert need > 0   # 4 rows x 2 KV heads leave most SMs idle: the call splits
+    assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c), FAKE, FAKE, FAKE, 512, FAKE, None, FAKE, need - 1,
+                             None) == 4
+    # A fixed single split needs no workspace.
+    assert L.qsa_attn_workspace_size(seq, 1, ctypes.byref(_cfg(n_splits=1)), 512) == 0
+
+
+def test_merge_validation(L):
+    assert L.qsa_lse_merge(FAKE, FAKE, 0, 10, 256, FAKE, qsa.F32, None, None) == 1
+    assert L.qsa_lse_merge(FAKE, FAKE, 2, 10, 6, FAKE, qsa.F32, None, None) == 2
+    assert L.qsa_lse_merge(FAKE, FAKE, 2, 10, 256, FAKE, 5, None, None) == 2
+    assert L.qsa_lse_merge(FAKE_MIS, FAKE, 2, 10, 256, FAKE, qsa.F32, None, None) == 3
+    assert L.qsa_lse_merge(None, None, 2, 0, 256, None, qsa.F32, None, None) == 0   # no rows: no-op
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(qsa, "_lib", None)
+    monkeypatch.setattr(qsa, "LIB_PATH", str(tmp_path / "libqsa.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        qsa.lib()

@@ -1,0 +1,338 @@
+"""GPU parity: every step of the CUDA library against the fp64 oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that still span
+several tiles and a ragged tail.  Tolerances are stated in qsa_cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import indexed_sparse_attention_gb300 as qsa
+import oracle
+from qsa_cases import (assert_attn_close, assert_scores_close, assert_selection_close, dev, oracle_layer,
+                       pool_all, pooled_buffer, score_bound, to_np, DeviceLayer)
+from workloads import make_layer, segment_cuts
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from indexed_sparse_attention_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+
+
+# ------------------------------------------------------------------ step 1
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_pool_matches_oracle(dtype):
+    x = make_layer(L=4099, M=4, dtype=dtype, seed=0)
+    idxk = x.idxk.to(dev())
+    pooled = pooled_buffer(x.L, dev())
+    pool_all(idxk, pooled, x.L)
+    got = to_np(pooled)[:1024].astype(np.float64)
+    want = oracle.pool(x.idxk)
+    np.testing.assert_allclose(got, want, rtol=2.5e-7, atol=1e-30)
+    assert np.isnan(to_np(pooled)[1024]).all()              # the incomplete block is not pooled
+    # A sub-range writes only its blocks.
+    part = pooled_buffer(x.L, dev())
+    qsa.pool_index_keys(idxk, part, 10, 7)
+    p = to_np(part)
+    np.testing.assert_allclose(p[10:17], want[10:17], rtol=2.5e-7)
+    assert np.isnan(p[:10]).all() and np.isnan(p[17:]).all()
+
+
+# ------------------------------------------------------------------ step 2
+@pytest.mark.parametrize("dtype,L,M", [(torch.float32, 4099, 4), (torch.bfloat16, 4099, 4),
+                                       (torch.bfloat16, 5003, 8), (torch.bfloat16, 777, 1),
+                                       (torch.float32, 3001, 3), (torch.bfloat16, 2100, 37)])
+def test_scores_match_oracle(dtype, L, M):
+    x = make_layer(L=L, M=M, dtype=dtype, seed=1)
+    pooled_ref = oracle.pool(x.idxk)
+    # The GPU scores the oracle's pooled keys rounded to fp32 ...
+    pooled = torch.from_numpy(pooled_ref.astype(np.float32)).to(dev())
+    q_idx = x.q_idx.to(dev())
+    ld = (L // 4 + 7) // 8 * 8
+    scores = torch.full((M, ld), float("nan"), device=dev())
+    seq = qsa.Seq(L, M, pooled)
+    qsa.score_blocks([seq], q_idx, scores)
+    ref = oracle.score(x.q_idx, pooled_ref.astype(np.float32).astype(np.float64), x.row_pos, ld=ld)
+    bound = score_bound(x.q_idx, pooled_ref, x.row_pos)
+    got = to_np(scores)
+    assert_scores_close(got, ref, bound, x.row_pos)
+    for r, p in enumerate(x.row_pos):                       # blocks a row cannot see stay unwritten
+        assert np.isnan(got[r, oracle.visible_blocks(p):]).all()
+    # ... and the chained GPU pool gives scores within the same bound.
+    gp = pooled_buffer(L, dev())
+    pool_all(x.idxk.to(dev()), gp, L)
+    qsa.score_blocks([qsa.Seq(L, M, gp)], q_idx, scores)
+    ref2 = oracle.score(x.q_idx, pooled_ref, x.row_pos, ld=ld)
+    assert_scores_close(to_np(scores), ref2, 2 * bound, x.row_pos)
+
+
+def test_scores_zero_query_and_nonnegative():
+    x = make_layer(L=1600, M=2, dtype=torch.bfloat16, seed=2)
+    pooled = pooled_buffer(x.L, dev())
+    pool_all(x.idxk.to(dev()), pooled, x.L)
+    scores = torch.empty((2, 400), device=dev())
+    qsa.score_blocks([qsa.Seq(x.L, 2, pooled)], torch.zeros_like(x.q_idx).to(dev()), scores)
+    assert (to_np(scores) == 0).all()
+    qsa.score_blocks([qsa.Seq(x.L, 2, pooled)], x.q_idx.to(dev()), scores)
+    assert (to_np(scores) >= 0).all()
+
+
+# ------------------------------------------------------------------ step 3
+def _select_gpu(scores_f32: np.ndarray, row_pos, L, top_k=512):
+    M, ld = scores_f32.shape
+    n_rows = len(row_pos)
+    s = torch.from_numpy(np.ascontiguousarray(scores_f32)).to(dev())
+    sel = torch.full((M, top_k), -7, dtype=torch.int32, device=dev())
+    cnt = torch.full((M,), -7, dtype=torch.int32, device=dev())
+    qsa.select_topk([qsa.Seq(L, n_rows)], s, sel, cnt, top_k)
+    return to_np(sel), to_np(cnt)
+
+
+def _select_case(scores_f32, L, M, top_k=512):
+    row_pos = [L - M + j for j in range(M)]
+    sel, cnt = _select_gpu(scores_f32, row_pos, L, top_k)
+    rs, rc, _ = oracle.select(scores_f32.astype(np.float64), row_pos, top_k)
+    np.testing.assert_array_equal(cnt, rc)
+    np.testing.assert_array_equal(sel, rs)
+
+
+@pytest.mark.parametrize("L,M,kind", [(4099, 4, "normal"), (261_120, 4, "normal"), (65_536, 1, "normal"),
+                                      (9001, 3, "coarse"), (9001, 3, "zeros"), (9001, 2, "signed_zeros"),
+                                      (9001, 2, "increasing"), (2051, 4, "normal"), (2052, 1, "normal"),
+                                      (2049, 2, "normal"), (13, 4, "normal"), (1 << 20, 1, "coarse")])
+def test_select_bit_exact_on_fp32_scores(L, M, kind):
+    rng = np.random.default_rng(L + M)
+    nb = L // 4
+    ld = (nb + 3) // 4 * 4
+    s = np.zeros((M, ld), dtype=np.float32)
+    if kind == "normal":
+        s[:, :nb] = np.abs(rng.standard_normal((M, nb))).astype(np.float32) * 3
+    elif kind == "coarse":
+        s[:, :nb] = rng.integers(0, 40, size=(M, nb)).astype(np.float32) * 0.125
+    elif kind == "signed_zeros":
+        s[:, :nb] = np.where(rng.random((M, nb)) < 0.5, np.float32(-0.0), np.float32(0.0))
+        s[:, 7::97] = 1.5
+    elif kind == "increasing":
+        s[:, :nb] = np.arange(nb, dtype=np.float32)[None]
+    _select_case(s, L, M)
+
+
+@pytest.mark.parametrize("top_k", [1, 7, 64, 512, 1000, 1024])
+def test_select_other_budgets(top_k):
+    rng = np.random.default_rng(top_k)
+    L, M = 20_011, 2
+    s = (rng.integers(0, 300, size=(M, L // 4)) * 0.5).astype(np.float32)
+    _select_case(s, L, M, top_k)
+
+
+def test_select_ragged_sequences():
+    rng = np.random.default_rng(5)
+    Ls, Ms = [4099, 700, 30_000, 9, 2052, 65_540, 5000, 8001, 12_345], [4, 1, 2, 3, 1, 4, 8, 1, 2]
+    ld = max(L // 4 for L in Ls)
+    rows = sum(Ms)
+    s = np.abs(rng.standard_normal((rows, ld))).astype(np.float32)
+    s[3] = np.round(s[3] * 4) / 4   # ties
+    seqs = [qsa.Seq(L, M) for L, M in zip(Ls, Ms)]
+    sd = torch.from_numpy(s).to(dev())
+    sel = torch.empty((rows, 512), dtype=torch.int32, device=dev())
+    cnt = torch.empty((rows,), dtype=torch.int32, device=dev())
+    qsa.select_topk(seqs, sd, sel, cnt)
+    pos = [p for sq in seqs for p in sq.row_pos]
+    rs, rc, _ = oracle.select(s.astype(np.float64), pos)
+    np.testing.assert_array_equal(to_np(cnt), rc)
+    np.testing.assert_array_equal(to_np(sel), rs)
+
+
+# ------------------------------------------------------------------ step 4 (given the oracle's selection)
+def _oracle_selection(x):
+    pooled = oracle.pool(x.idxk)
+    s = oracle.score(x.q_idx, pooled, x.row_pos)
+    return oracle.select(s, x.row_pos)
+
+
+def _attn_gpu(x, sel, cnt, *, segments=None, out_dtype=torch.float32, n_splits=0, device=None):
+    device = device or dev()
+    q = x.q.to(device)
+    k, v = x.k.to(device), x.v.to(device)
+    segs = segments(k, v) if segments else [qsa.Segment(k, v, 0)]
+    out = torch.full((x.M, x.q.shape[1], x.q.shape[2]), float("nan"), dtype=out_dtype, device=device)
+    lse = torch.full((x.M, x.q.shape[1]), float("nan"), device=device)
+    seld = torch.from_numpy(np.ascontiguousarray(sel)).to(device)
+    cntd = torch.from_numpy(np.ascontiguousarray(cnt)).to(device)
+    qsa.sparse_attn([qsa.Seq(x.L, x.M, segments=segs)], q, seld, cntd, out, lse, n_splits=n_splits)
+    torch.cuda.synchronize()
+    return to_np(out.float()), to_np(lse)
+
+
+@pytest.mark.parametrize("dtype,D", [(torch.float32, 256), (torch.bfloat16, 256), (torch.float32, 128),
+                                     (torch.bfloat16, 128)])
+@pytest.mark.parametrize("n_splits", [0, 1, 3])
+def test_attention_matches_oracle(dtype, D, n_splits):
+    x = make_layer(L=4099, M=4, dtype=dtype, seed=3, head_dim=D)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt, n_splits=n_splits)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, dtype == torch.bfloat16)
+
+
+def test_attention_bf16_output():
+    x = make_layer(L=6007, M=2, dtype=torch.bfloat16, seed=4)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt, out_dtype=torch.bfloat16)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+@pytest.mark.parametrize("L,M", [(1, 1), (2, 2), (3, 1), (4, 4), (5, 3), (7, 1), (9, 4), (2051, 4), (2052, 1),
+                                 (2055, 4), (4096, 1), (333, 8)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_attention_degenerate_sizes(L, M, dtype):
+    x = make_layer(L=L, M=M, dtype=dtype, seed=L, head_dim=128)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, dtype == torch.bfloat16)
+
+
+def test_attention_skips_invalid_ids():
+    # Out-of-range ids in the selection are skipped (never dereferenced);
+    # the result equals attention without them.
+    x = make_layer(L=3001, M=2, dtype=torch.bfloat16, seed=6)
+    sel, cnt, _ = _oracle_selection(x)
+    bad = sel.copy()
+    bad[0, 3] = 10_000_000
+    bad[1, 5] = -5
+    out, lse = _attn_gpu(x, bad, cnt)
+    keep0 = np.delete(sel[0, :cnt[0]], 3)
+    keep1 = np.delete(sel[1, :cnt[1]], 5)
+    ref_sel = np.full_like(sel, -1)
+    ref_sel[0, :len(keep0)] = keep0
+    ref_sel[1, :len(keep1)] = keep1
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, ref_sel, [len(keep0), len(keep1)])
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+# ------------------------------------------------------------------ segments and step 5
+def _segment_views(cuts):
+    def make(k, v):
+        # Each segment is a separate allocation holding its tokens.
+        return [qsa.Segment(k[:, f:f + n].clone(), v[:, f:f + n].clone(), f) for f, n in cuts]
+    return make
+
+
+@pytest.mark.parametrize("D", [256, 128])
+def test_segmented_equals_single_buffer_and_oracle(D):
+    x = make_layer(L=9001, M=4, dtype=torch.bfloat16, seed=7, head_dim=D)
+    sel, cnt, _ = _oracle_selection(x)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    cuts = segment_cuts(x.L, 12, seed=1)
+    single, single_lse = _attn_gpu(x, sel, cnt)
+    seg, seg_lse = _attn_gpu(x, sel, cnt, segments=_segment_views(cuts))
+    assert_attn_close(seg, seg_lse, ref_out, ref_lse, True)
+    np.testing.assert_allclose(seg, single, atol=2e-3)
+    # Per-segment calls merged by the step-5 entry point.
+    parts_o, parts_l = [], []
+    for f, n in cuts:
+        o, l = _attn_gpu(x, sel, cnt, segments=_segment_views([(f, n)]))
+        parts_o.append(o.reshape(-1, D))
+        parts_l.append(l.reshape(-1))
+    po = torch.from_numpy(np.stack(parts_o)).to(dev())
+    pl = torch.from_numpy(np.stack(parts_l)).to(dev())
+    merged = torch.empty((po.shape[1], D), device=dev())
+    mlse = torch.empty((po.shape[1],), device=dev())
+    qsa.lse_merge(po, pl, merged, mlse)
+    assert_attn_close(to_np(merged).reshape(ref_out.shape), to_np(mlse).reshape(ref_lse.shape), ref_out, ref_lse,
+                      True)
+
+
+def test_segment_hole_matches_visibility_mask():
+    x = make_layer(L=7000, M=3, dtype=torch.bfloat16, seed=8)
+    sel, cnt, _ = _oracle_selection(x)
+    cuts = segment_cuts(x.L, 5, seed=2)
+    kept = cuts[:2] + cuts[3:]
+    vis = np.zeros(x.L, dtype=bool)
+    for f, n in kept:
+        vis[f:f + n] = True
+    out, lse = _attn_gpu(x, sel, cnt, segments=_segment_views(kept))
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt, visible=vis)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+    # Only a segment far from every selected row: no visible key -> zeros, -inf.
+    far = lambda k, v: [qsa.Segment(k[:, 0:4].clone(), v[:, 0:4].clone(), 10 ** 9)]
+    out0, lse0 = _attn_gpu(x, sel, cnt, segments=far)
+    assert (out0 == 0).all() and np.isneginf(lse0).all()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_lse_merge_matches_oracle(out_dtype):
+    rng = np.random.default_rng(9)
+    S, R, D = 5, 300, 256
+    o = rng.standard_normal((S, R, D)).astype(np.float32)
+    l = (rng.standard_normal((S, R)) * 4).astype(np.float32)
+    l[:, 7] = -np.inf                    # a row no part saw a key for
+    l[2, 11:40] = -np.inf                # parts without keys for some rows
+    out = torch.empty((R, D), dtype=out_dtype, device=dev())
+    lse = torch.empty((R,), device=dev())
+    qsa.lse_merge(torch.from_numpy(o).to(dev()), torch.from_numpy(l).to(dev()), out, lse)
+    ref_o, ref_l = oracle.lse_merge(o.astype(np.float64), l.astype(np.float64))
+    got = to_np(out.float())
+    assert not np.isnan(got).any()
+    tol = 1e-5 if out_dtype == torch.float32 else 1e-2
+    np.testing.assert_allclose(got, ref_o, atol=tol, rtol=tol)
+    fin = np.isfinite(ref_l)
+    np.testing.assert_allclose(to_np(lse)[fin], ref_l[fin], atol=1e-5)
+    assert np.isneginf(to_np(lse)[~fin]).all() and (got[7] == 0).all()
+
+
+# ------------------------------------------------------------------ whole layer step
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_layer_step_tiny_verify(dtype):
+    # 4,099 tokens, four verify rows at 4,095..4,098, 64 planted blocks.
+    x = make_layer(L=4099, M=4, dtype=dtype, seed=0, n_planted=64)
+    g = DeviceLayer(x).run()
+    ref = oracle_layer(x)
+    pooled_ref = oracle.pool(x.idxk)
+    bound = score_bound(x.q_idx, pooled_ref, x.row_pos)
+    nb = ref["scores"].shape[1]
+    assert_scores_close(to_np(g.scores)[:, :nb], ref["scores"], 2 * bound, x.row_pos)
+    sel, cnt = to_np(g.sel), to_np(g.cnt)
+    assert_selection_close(sel, cnt, ref["sel"], ref["cnt"], ref["tau"], ref["scores"], x.row_pos)
+    # Attention over the GPU's own selection against the oracle on that selection.
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(to_np(g.out), to_np(g.lse), ref_out, ref_lse, dtype == torch.bfloat16)
+    # The tail is attended: the row at 4,098 has 2,048 + 3 rows (lse vs q=0 is checked by the oracle pins).
+    assert list(cnt) == [512] * 4
+
+
+def test_layer_step_ragged_batch_small():
+    # Several sequences in one call (decode and verify rows), bf16, segmented K/V.
+    Ls, Ms, nsegs = [4099, 9001, 2051, 17_000], [1, 4, 2, 4], [3, 12, 1, 5]
+    xs = [make_layer(L=L, M=M, dtype=torch.bfloat16, seed=20 + i, head_dim=128) for i, (L, M) in
+          enumerate(zip(Ls, Ms))]
+    seqs, keep = [], []
+    for i, x in enumerate(xs):
+        k, v = x.k.to(dev()), x.v.to(dev())
+        idxk = x.idxk.to(dev())
+        pooled = pooled_buffer(x.L, dev())
+        pool_all(idxk, pooled, x.L)
+        segs = _segment_views(segment_cuts(x.L, nsegs[i], seed=i))(k, v)
+        seqs.append(qsa.Seq(x.L, x.M, pooled, segs, idx_keys=idxk))
+        keep += [k, v, idxk, pooled]
+    q_idx = torch.cat([x.q_idx for x in xs]).to(dev())
+    q = torch.cat([x.q for x in xs]).to(dev())
+    step = qsa.LayerStep(seqs, q_idx, q)
+    step.run()
+    torch.cuda.synchronize()
+    row = 0
+    for x in xs:
+        ref = oracle_layer(x)
+        rows = slice(row, row + x.M)
+        sel, cnt = to_np(step.sel)[rows], to_np(step.cnt)[rows]
+        assert_selection_close(sel, cnt, ref["sel"], ref["cnt"], ref["tau"], ref["scores"], x.row_pos)
+        ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+        assert_attn_close(to_np(step.out)[rows], to_np(step.lse)[rows], ref_out, ref_lse, True)
+        row += x.M
