@@ -33,13 +33,17 @@ def test_pool_matches_oracle(dtype):
     pool_all(idxk, pooled, x.L)
     got = to_np(pooled)[:1024].astype(np.float64)
     want = oracle.pool(x.idxk)
-    np.testing.assert_allclose(got, want, rtol=2.5e-7, atol=1e-30)
+    # Three fp32 additions and an exact scaling: |err| <= 3 u * mean_j |k_j| + u |mean|.
+    u = 2.0 ** -24
+    mag = np.abs(x.idxk.double().numpy()[:4096]).reshape(1024, 4, 128).mean(axis=1)
+    bound = 3 * u * mag + u * np.abs(want)
+    assert (np.abs(got - want) <= bound).all()
     assert np.isnan(to_np(pooled)[1024]).all()              # the incomplete block is not pooled
     # A sub-range writes only its blocks.
     part = pooled_buffer(x.L, dev())
     qsa.pool_index_keys(idxk, part, 10, 7)
     p = to_np(part)
-    np.testing.assert_allclose(p[10:17], want[10:17], rtol=2.5e-7)
+    assert (np.abs(p[10:17] - want[10:17]) <= bound[10:17]).all()
     assert np.isnan(p[:10]).all() and np.isnan(p[17:]).all()
 
 
@@ -77,9 +81,11 @@ def test_scores_zero_query_and_nonnegative():
     pool_all(x.idxk.to(dev()), pooled, x.L)
     scores = torch.empty((2, 400), device=dev())
     qsa.score_blocks([qsa.Seq(x.L, 2, pooled)], torch.zeros_like(x.q_idx).to(dev()), scores)
-    assert (to_np(scores) == 0).all()
+    got = to_np(scores)
+    assert (got[0, :399] == 0).all() and (got[1] == 0).all()      # rows at 1,598 and 1,599
     qsa.score_blocks([qsa.Seq(x.L, 2, pooled)], x.q_idx.to(dev()), scores)
-    assert (to_np(scores) >= 0).all()
+    got = to_np(scores)
+    assert (got[0, :399] >= 0).all() and (got[1] >= 0).all()
 
 
 # ------------------------------------------------------------------ step 3
