@@ -1,0 +1,449 @@
+"""Benchmark of the QSA layer step on GB300.
+
+Default workload: the fixed four-row verify at a 261,120-token context,
+bf16 K/V and index keys (pooled keys fp32), 24 query heads over 2 KV heads,
+head_dim 256, 12 independent QSA layers, top 512 blocks plus the tail.
+One bench "step" is one pass of the whole hot path -- pool the block the new
+rows completed, score every visible block, select the top 512, sparse
+attention with its split merge -- over all 12 layers, layer after layer on
+one stream, captured once in a CUDA graph.  The metric is QSA layer-steps/s.
+
+Prints ONE JSON line (rank 0).  See the design doc for the accounting.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--layers N] [--impl ours|reference] [--no-cpu-baseline]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_layer  # noqa: E402
+
+METRIC = "QSA layer-steps/s at 261,120-ctx verify M=4; HBM GB/s as % of GB300 roofline"
+UNIT = "layer-steps/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ---------------------------------------------------------------------- workload setup
+
+class Layer:
+    """Device-resident state of one QSA layer for one sequence."""
+
+    def __init__(self, L, M, dtype, seed, layer, n_planted, head_dim, device):
+        import indexed_sparse_attention_gb300 as qsa
+        x = make_layer(L=L, M=M, dtype=dtype, seed=seed, layer=layer, n_planted=n_planted, head_dim=head_dim,
+                       device=device)
+        self.x = x
+        self.pooled = torch.empty((qsa.n_pooled_slots(L), 128), dtype=torch.float32, device=device)
+        first_new = (L - M) // 4
+        if first_new:
+            qsa.pool_index_keys(x.idxk, self.pooled, 0, first_new)    # state from earlier steps (untimed)
+        self.seq = qsa.Seq(L, M, self.pooled, [qsa.Segment(x.k, x.v, 0)], idx_keys=x.idxk)
+        self.step = qsa.LayerStep([self.seq], x.q_idx, x.q, out_dtype=torch.float32)
+
+
+def build_layers(spec, n_layers, device, seed=0):
+    return [Layer(spec["L"], spec["M"], spec["dtype"], seed, l, spec["n_planted"], spec["head_dim"], device)
+            for l in range(n_layers)]
+
+
+def launches_per_layer(layer) -> int:
+    st = layer.step
+    n = len(st.pool_jobs) + 1 + 1 + 1            # pool, score, select, attention
+    ws_needed = st.ws.numel() > 16
+    return n + (1 if ws_needed else 0)           # + split merge
+
+
+def algorithmic_bytes(layer) -> dict:
+    """Bytes one layer-step must move (measurement)."""
+    x = layer.x
+    L, M = x.L, x.M
+    kv_es = x.k.element_size()
+    D, Hq, Hkv = x.q.shape[2], x.q.shape[1], x.k.shape[0]
+    idx_es = x.idxk.element_size()
+    nb_max = L // 4
+    new_blocks = sum(n for *_, n in layer.step.pool_jobs)
+    pool_b = new_blocks * (4 * 128 * idx_es + 128 * 4)
+    score_b = nb_max * 128 * 4 + x.q_idx.numel() * x.q_idx.element_size() + sum(
+        ((p + 1) // 4) * 4 for p in x.row_pos)
+    rows = []
+    for p in x.row_pos:
+        nb = (p + 1) // 4
+        rows.append(4 * min(512, nb) + (p + 1) % 4)
+    attn_b = sum(rows) * Hkv * D * 2 * kv_es + x.q.numel() * x.q.element_size() + M * Hq * (D * 4 + 4)
+    return {"pool": pool_b, "score": score_b, "attn": attn_b, "total": pool_b + score_b + attn_b,
+            "score_pooled_only": nb_max * 128 * 4}
+
+
+# ---------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [p.strip() for p in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- distributed plumbing
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------- the CPU oracle leg
+
+def oracle_layer_steps(layers_host, n_threads, budget_s):
+    """Time the oracle on host copies: per layer-step, pool the new block(s),
+    score all visible blocks, select, attend.  Returns (layer-steps, seconds)."""
+    import oracle
+    oracle.set_threads(n_threads)
+    done, elapsed = 0, 0.0
+    for h in layers_host:
+        t0 = time.perf_counter()
+        new = oracle.pool(h["idxk"], h["b0"], h["nb"] - h["b0"]) if h["nb"] > h["b0"] else None
+        pooled = h["pooled_old"] if new is None else __import__("numpy").concatenate([h["pooled_old"], new])
+        s = oracle.score(h["q_idx"], pooled, h["row_pos"])
+        sel, cnt, _ = oracle.select(s, h["row_pos"])
+        oracle.attn(h["q"], h["k"], h["v"], h["row_pos"], sel, cnt)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        if elapsed >= budget_s:
+            break
+    return done, elapsed
+
+
+def host_layer(layer):
+    """Host copies of one layer's inputs for the oracle; pooled keys of the
+    blocks before this step are state (pooled here, untimed)."""
+    import oracle
+    x = layer.x
+    idxk = x.idxk.cpu()
+    b0 = (x.L - x.M) // 4
+    return {"idxk": idxk, "q_idx": x.q_idx.cpu(), "q": x.q.cpu(), "k": x.k.cpu(), "v": x.v.cpu(),
+            "row_pos": x.row_pos, "b0": b0, "nb": x.L // 4, "pooled_old": oracle.pool(idxk, 0, b0)}
+
+
+def cpu_baseline(layers, budget_s=20.0, max_layers=3):
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    hosts = [host_layer(l) for l in layers[:max_layers]]
+    n, secs = oracle_layer_steps(hosts, cores, budget_s)
+    return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the workload's layer-steps (pool new block, score all blocks, select, "
+                      f"attention over all rows and heads) in fp64 C with OpenMP, {secs:.2f} s"}
+
+
+# ---------------------------------------------------------------------- main
+
+def run_reference(args, spec, world, rank):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    n_layers = min(args.layers or spec["layers"], 2)
+    layers = build_layers(spec, n_layers, dev)
+    hosts = [host_layer(l) for l in layers]
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    for i in range(args.warmup):
+        oracle_layer_steps([hosts[i % len(hosts)]], cores, 1e9)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_layer_steps([hosts[i % len(hosts)]], cores, 1e9)
+    secs = time.perf_counter() - t0
+    value = args.steps / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, "layer_steps_per_step": 1,
+                                            "context": spec["L"], "rows": spec["M"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one layer-step of the workload per step, fp64 C oracle with OpenMP"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="verify_m4_261k_bf16",
+                    choices=["verify_m4_261k_bf16", "decode_m1_65k_bf16"])
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's 12)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-reps", type=int, default=200)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    spec = WORKLOADS[args.workload]
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, spec, world, rank)
+        barrier(world)
+        return
+
+    import indexed_sparse_attention_gb300 as qsa
+    from indexed_sparse_attention_gb300 import build as qsa_build
+    if rank == 0:
+        qsa_build.build()
+    barrier(world)
+    qsa.lib()
+    dev = torch.device("cuda", local)
+    n_layers = args.layers or spec["layers"]
+    layers = build_layers(spec, n_layers, dev, seed=rank)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+
+    def step_all():
+        for l in layers:
+            l.step.run()
+
+    # Eager warm-up (sets kernel attributes outside capture), then capture.
+    with torch.cuda.stream(stream):
+        step_all()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step_all()
+    torch.cuda.synchronize()
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t_end.record(stream)
+    t_end.synchronize()
+    torch.cuda.synchronize()
+    ms = t_start.elapsed_time(t_end)
+    # Keep the clocks sampler fed for >= 1 s of load when the timed region was short.
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - wall0 < 1.2:
+            for _ in range(50):
+                graph.replay()
+            torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    layer_steps = n_layers * args.steps * world
+    value = layer_steps / (ms / 1e3)
+
+    # Dominant kernel (block scoring): 12 back-to-back launches in a graph, timed live.
+    kgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kgraph, stream=stream):
+        for l in layers:
+            l.step.score()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            kgraph.replay()
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(args.kernel_reps):
+            kgraph.replay()
+        k1.record(stream)
+    k1.synchronize()
+    score_us = 1e3 * k0.elapsed_time(k1) / (args.kernel_reps * n_layers)
+
+    # End to end through the public API with host buffers: per step, the new
+    # rows' q, index queries, K/V and index keys of every layer go host ->
+    # device into the caches, the layer chain runs, outputs come back.
+    M = spec["M"]
+    L = spec["L"]
+    h2d_items, d2h_items = [], []
+    for l in layers:
+        x = l.x
+        for t in (x.q, x.q_idx, x.k[:, L - M:], x.v[:, L - M:], x.idxk[L - M:]):
+            h2d_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
+        for t in (l.step.out, l.step.lse):
+            d2h_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
+    for d, h in h2d_items:
+        h.copy_(d.cpu())
+    h2d = sum(h.numel() * h.element_size() for _, h in h2d_items)
+    d2h = sum(h.numel() * h.element_size() for _, h in d2h_items)
+
+    def e2e_step():
+        for d, h in h2d_items:
+            d.copy_(h, non_blocking=True)
+        for l in layers:
+            l.step.run()
+        for d, h in d2h_items:
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(10, min(args.steps, 200))
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = n_layers * e2e_steps * world / (e2e_ms / 1e3)
+
+    ab = algorithmic_bytes(layers[0])
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak_gbs, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        peak_gbs, peak_src = 6800.0, "fallback"
+    score_gbs = ab["score"] / (score_us * 1e-6) / 1e9
+    step_gbs = ab["total"] * n_layers / (ms_per_step * 1e-3) / 1e9
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    if os.path.exists(tf):
+        try:
+            t = json.load(open(tf))
+            if t.get("workload") == args.workload and t.get("kernel_rev") == SCORE_KERNEL_REV:
+                traffic = t["dram_bytes_per_launch"]
+        except (OSError, ValueError, KeyError):
+            traffic = None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers)
+
+    launches = sum(launches_per_layer(l) for l in layers) * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "context": L, "rows": M, "layers_per_step": n_layers,
+                   "q_heads": 24, "kv_heads": 2, "head_dim": spec["head_dim"], "top_k_blocks": 512,
+                   "index_heads": 4, "index_dim": 128, "graph": "one CUDA graph per step (all layers)",
+                   "l2": f"inputs larger than L2: {n_layers} distinct layers, "
+                         f"{ab['total'] * n_layers / 2**20:.0f} MiB algorithmic bytes per step",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_layer_step": 1e3 * ms_per_step / n_layers,
+        "algorithmic_bytes_per_layer_step": ab["total"],
+        "step_hbm_gbs": step_gbs,
+        "step_frac_of_peak": step_gbs / peak_gbs,
+        "roofline": {"kernel": "score_blocks", "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
+                     "unit": "GB/s", "frac": score_gbs / peak_gbs, "traffic": traffic,
+                     "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
+                     "algorithmic_bytes_per_launch": ab["score"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier(world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# Revision tag of the scoring kernel whose DRAM counters profiles/ holds.
+SCORE_KERNEL_REV = "score_mma_v1"
+
+if __name__ == "__main__":
+    main()

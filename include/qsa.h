@@ -68,7 +68,8 @@ typedef enum qsa_status {
   QSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
   QSA_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / head count / size the library does not build */
   QSA_ERR_MISALIGNED = 3,    /* pointer or stride not 16-byte aligned */
-  QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result */
+  QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result
+                                (no current kernel needs scratch; kept for the ABI) */
   QSA_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
 } qsa_status;
 
@@ -112,7 +113,7 @@ typedef struct qsa_attn_config {
   qsa_dtype kv_dtype;        /* dtype of every segment's K and V */
   qsa_dtype out_dtype;       /* dtype of out */
   float scale;               /* logit scale; 0 means 1/sqrt(head_dim) */
-  int32_t n_splits;          /* splits of each row's selected rows; 0 = library's choice */
+  int32_t n_splits;          /* splits of each row's selected rows, <= 16; 0 = library's choice */
 } qsa_attn_config;
 
 /* Human-readable name of a status code (static storage). */
@@ -157,7 +158,9 @@ qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_i
                             qsa_dtype q_idx_dtype, float* scores, int64_t ld, void* stream);
 
 /*
- * Scratch bytes qsa_select_topk needs for these sequences (may be 0).
+ * Scratch bytes qsa_select_topk needs for these sequences.  The current
+ * kernels keep all selection state in shared memory and return 0; the
+ * workspace arguments are kept so that variants needing scratch keep the ABI.
  */
 size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k);
 
@@ -176,14 +179,18 @@ size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t to
  *   sel, cnt       device int32 [rows, top_k], [rows]
  *   workspace      device scratch of >= qsa_select_workspace_size bytes
  *                  (may be NULL when that size is 0)
+ * One thread-block cluster of up to 16 CTAs handles a row: per-CTA histograms
+ * of the top 12 key bits are summed through distributed shared memory.
  */
 qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld,
                            int32_t top_k, int32_t* sel, int32_t* cnt, void* workspace,
                            size_t workspace_bytes, void* stream);
 
 /*
- * Scratch bytes qsa_sparse_attn needs (split partials and their lse).
- * sel_ld is the row stride of sel (the top_k used for selection).
+ * Scratch bytes qsa_sparse_attn needs.  The splits of one (row, KV group) run
+ * as one thread-block cluster and merge their partials through distributed
+ * shared memory, so the current kernels return 0.  sel_ld is the row stride
+ * of sel (the top_k used for selection).
  */
 size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
                                int32_t sel_ld);
@@ -208,7 +215,11 @@ size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_at
  *                  ids outside 0..nb(p_r)-1 are skipped, never dereferenced
  *   out            device [rows, Hq, head_dim], cfg->out_dtype
  *   lse            device [rows, Hq] f32 (natural log); may be NULL
- *   workspace      device scratch of >= qsa_attn_workspace_size bytes
+ *   workspace      device scratch of >= qsa_attn_workspace_size bytes (may be
+ *                  NULL when that size is 0)
+ * Each row's selected list is cut into cfg->n_splits splits (at most 16; 0 =
+ * library's choice); the splits of one (row, KV group) form one cluster and
+ * are merged there by the log-sum-exp rule of qsa_lse_merge.
  * Supported: head_dim 128 or 256; q and K/V both bf16 or both f32;
  * Hq / Hkv <= 16.
  */

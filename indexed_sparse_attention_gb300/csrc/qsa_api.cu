@@ -89,6 +89,41 @@ cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes) {
   return e;
 }
 
+cudaError_t allow_cluster16(const void* kernel, int threads, size_t smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  struct Entry {
+    int dev;
+    const void* kernel;
+    size_t smem;
+    cudaError_t result;
+  };
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  for (const Entry& x : done)
+    if (x.dev == dev && x.kernel == kernel && x.smem == smem) return x.result;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+    if (e == cudaSuccess && n < 1) e = cudaErrorNotSupported;
+  }
+  done.push_back(Entry{dev, kernel, smem, e});
+  return e;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
@@ -276,6 +311,7 @@ namespace {
 struct SplitPlan {
   int32_t n_splits;
   int32_t split_tokens;
+  int32_t stages;
 };
 
 // Longest selected list any row of the call can have: 4 tokens per listed
@@ -286,29 +322,30 @@ int64_t max_list(const qsa_seq* seqs, int32_t n_seqs, int32_t sel_ld) {
   return m;
 }
 
+// Splits per (row, KV group) -- one thread-block cluster -- aiming at about
+// two CTAs per SM, each split at least 32 selected rows long.
 SplitPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, int32_t sel_ld,
                       int64_t rows) {
   const int64_t n_list = max_list(seqs, n_seqs, sel_ld);
+  const int64_t pairs = rows * cfg->n_kv_heads;
+  const int64_t sms = device_sm_count();
   int64_t n = cfg->n_splits;
-  if (n <= 0) {
-    const int64_t pairs = rows * cfg->n_kv_heads;
-    const int64_t sms = device_sm_count();
-    n = pairs >= sms ? 1 : (sms + pairs - 1) / pairs;
-    n = std::min<int64_t>(n, (n_list + 63) / 64);
-  }
+  if (n <= 0) n = (2 * sms + pairs - 1) / pairs;
   n = std::max<int64_t>(1, std::min<int64_t>(n, (n_list + 31) / 32));
-  int64_t per = (n_list + n - 1) / n;
-  per = (per + 31) / 32 * 32;
+  int stages = attn_stages(pairs * std::min<int64_t>(n, 16));
+  const int max_splits = attn_max_splits(cfg->kv_dtype, cfg->head_dim, stages);
+  n = std::min<int64_t>(n, max_splits);
+  stages = attn_stages(pairs * n);
+  const int64_t per = (n_list + n - 1) / n;
   n = (n_list + per - 1) / per;
-  return SplitPlan{(int32_t)n, (int32_t)per};
+  return SplitPlan{(int32_t)n, (int32_t)per, (int32_t)stages};
 }
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
 size_t attn_ws_bytes(const SplitPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
-  if (sp.n_splits <= 1) return 0;
-  const size_t parts = (size_t)sp.n_splits * (size_t)rows * (size_t)cfg->n_q_heads;
-  return align256(parts * (size_t)cfg->head_dim * 4) + align256(parts * 4);
+  (void)sp;
+  (void)rows;
+  (void)cfg;
+  return 0;  // splits merge inside their cluster: no scratch
 }
 
 qsa_status check_attn_config(const qsa_attn_config* cfg, const char* fn) {
@@ -356,8 +393,8 @@ qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_co
 
 template <int NSEQ>
 qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_attn_config* cfg, const void* q,
-                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const SplitPlan& sp, int64_t total_rows,
-                      void* out, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
+                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const SplitPlan& sp, void* out,
+                      float* lse, cudaStream_t st) {
   AttnParams<NSEQ> p{};
   int rows = 0, nseg = 0;
   p.row_base = row_begin;
@@ -391,13 +428,10 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
   p.n_splits = sp.n_splits;
   p.split_tokens = sp.split_tokens;
-  p.total_rows = (int32_t)total_rows;
-  p.part_o = part_o;
-  p.part_lse = part_lse;
   p.out = out;
   p.lse = lse;
   p.out_dtype = cfg->out_dtype;
-  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, st);
+  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, sp.stages, st);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn");
   return QSA_OK;
 }
@@ -429,31 +463,18 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
     return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? workspace_bytes : (size_t)0);
   if (need > 0 && !aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
-  float* part_o = nullptr;
-  float* part_lse = nullptr;
-  if (sp.n_splits > 1) {
-    const size_t parts = (size_t)sp.n_splits * (size_t)rows * (size_t)cfg->n_q_heads;
-    part_o = static_cast<float*>(workspace);
-    part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(parts * (size_t)cfg->head_dim * 4));
-  }
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o, part_lse, st);
+    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, out, lse, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o,
-                                  part_lse, st);
+      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, out, lse, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
   if (s != QSA_OK) return s;
-  if (sp.n_splits > 1) {
-    cudaError_t e = launch_merge(part_o, part_lse, sp.n_splits, rows * cfg->n_q_heads, cfg->head_dim, out,
-                                 cfg->out_dtype, lse, st);
-    if (e != cudaSuccess) return cuda_fail(e, fn);
-  }
   return ok();
 }
 

@@ -17,9 +17,12 @@
 // against 32 gathered tokens), with an fp32 online softmax; fp32 K/V take a
 // CUDA-core kernel.  Partials (normalised output, lse) of several splits are
 // merged by the step-5 kernel.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "qsa_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace qsa {
 
@@ -27,6 +30,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxSplits = 16;   // splits of one (row, KV group) = CTAs of one cluster
 
 // Per-row context: position, visible blocks, selected list length.
 struct RowCtx {
@@ -104,7 +108,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
                "r"(valid ? 16 : 0));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, const void* p) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -125,48 +132,110 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Write one (row, head) result: to the final output when there is a single
-// split, else to the split's partial slot.
+// ------------------------------------------------------------------ split merge (step 5, in-cluster)
+// Each CTA of a cluster holds the partial of one split of the same (row, KV
+// group): unnormalised output o_s[16][D] (fp32), running max m_s[16] of the
+// base-2 logits and running sum l_s[16].  After a cluster barrier, CTA c
+// merges the 4-channel groups c, c+S, ... of every head across the cluster
+// through
+// distributed shared memory:
+//   M = max_q m_q,  w_q = 2^(m_q - M),  out = sum_q w_q o_q / sum_q w_q l_q,
+//   lse = (M + log2 sum_q w_q l_q) * ln 2,
+// and a head whose splits saw no key gets out = 0 and lse = -inf.
+struct MergeSmem {
+  float w[16][kMaxSplits];
+  float inv[16];
+  float lse[16];
+};
+
 template <int NSEQ>
-__device__ __forceinline__ float* partial_row(const AttnParams<NSEQ>& p, int split, int r, int head) {
-  return p.part_o + (((int64_t)split * p.total_rows + r) * p.n_q_heads + head) * p.head_dim;
+__device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, int D, float* o_s, float* m_s,
+                            float* l_s, MergeSmem* ms) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int c = (int)cluster.block_rank();
+  const int tid = threadIdx.x, nt = blockDim.x;
+  cluster.sync();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int q = 0; q < S; ++q) M = fmaxf(M, *cluster.map_shared_rank(m_s + tid, q));
+    float Lsum = 0.f;
+    for (int q = 0; q < S; ++q) {
+      const float mq = *cluster.map_shared_rank(m_s + tid, q);
+      const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
+      ms->w[tid][q] = w;
+      Lsum += w * *cluster.map_shared_rank(l_s + tid, q);
+    }
+    ms->inv[tid] = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    ms->lse[tid] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();
+  // 4-channel groups c, c + S, c + 2S, ... of every head belong to this CTA
+  // (any S <= 16; D / 4 >= 32 groups, so every CTA has at least one).
+  const int nq = (D / 4 - c + S - 1) / S;
+  for (int idx = tid; idx < G * nq; idx += nt) {
+    const int h = idx / nq;
+    const int d = 4 * (c + (idx % nq) * S);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < S; ++q) {
+      const float w = ms->w[h][q];
+      const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s + h * D + d, q));
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    const float inv = ms->inv[h];
+    const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
+    if (p.out_dtype == QSA_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
+      o2[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      o2[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+  }
+  if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->lse[tid];
+  cluster.sync();  // keep this CTA's partial alive until every peer has read it
 }
 
 // ------------------------------------------------------------------ tensor-pipe kernel (bf16 K/V)
 constexpr int kTT = 32;        // tokens per tile
 constexpr int kPStride = 40;   // bf16 per P row: 80-byte rows keep ldmatrix conflict-free
 
-template <int D>
+template <int D, int STAGES>
 struct MmaSmem {
   static constexpr int CH = D / 8;  // 16-byte chunks per K/V/Q row
   static constexpr size_t q = 16 * D * 2;
-  static constexpr size_t kv_stage = kTT * D * 2;
+  static constexpr size_t kv_tile = kTT * D * 2;            // one K or V tile
   static constexpr size_t s = 16 * (kTT + 4) * 4;
   static constexpr size_t pm = 16 * kPStride * 2;
-  static constexpr size_t off_k = q;
-  static constexpr size_t off_v = off_k + 2 * kv_stage;
-  static constexpr size_t off_s = off_v + 2 * kv_stage;
+  static constexpr size_t off_kv = q;                        // [STAGES][K tile, V tile]
+  static constexpr size_t off_s = off_kv + STAGES * 2 * kv_tile;
   static constexpr size_t off_p = off_s + s;
-  static constexpr size_t off_m = off_p + pm;           // m, l, alpha: 3 x 16 floats
+  static constexpr size_t off_m = off_p + pm;                // m, l, alpha: 3 x 16 floats
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
-  static constexpr size_t bytes = off_valid + 2 * kTT * 4;
+  static constexpr size_t off_merge = off_valid + STAGES * kTT * 4;
+  static constexpr size_t bytes = off_merge + sizeof(MergeSmem);
+  static_assert(16 * D * 4 <= STAGES * 2 * kv_tile, "merge partial must fit the K/V stages");
 };
 
-template <int D, int NSEQ>
+template <int D, int STAGES, int NSEQ>
 __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p) {
-  using L = MmaSmem<D>;
+  using L = MmaSmem<D, STAGES>;
   constexpr int CH = L::CH;
   constexpr int NTD = D / 32;  // 8-channel n-tiles per warp in P.V (D/4 channels per warp)
   extern __shared__ __align__(128) uint8_t smem[];
   __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem);
-  __nv_bfloat16* k_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_k);
-  __nv_bfloat16* v_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_v);
+  __nv_bfloat16* kv_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_kv);
   float* s_s = reinterpret_cast<float*>(smem + L::off_s);
   __nv_bfloat16* p_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_p);
   float* m_s = reinterpret_cast<float*>(smem + L::off_m);
   float* l_s = m_s + 16;
   float* a_s = m_s + 32;
   int* valid_s = reinterpret_cast<int*>(smem + L::off_valid);
+  MergeSmem* msm = reinterpret_cast<MergeSmem*>(smem + L::off_merge);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
@@ -175,9 +244,38 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   const int64_t i0 = (int64_t)split * p.split_tokens;
   const int64_t i1 = min(c.n_list, i0 + p.split_tokens);
   const int n_tiles = i1 > i0 ? (int)((i1 - i0 + kTT - 1) / kTT) : 0;
-
-  // Q of the group's heads (rows >= G zero), swizzled: chunk c of row h at c ^ (h & 7).
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
+
+  // Gather of one tile into a stage: thread -> token slot tid/4, chunks (tid&3) + 4j,
+  // swizzled: chunk c of token row t lands at c ^ (t & 7).
+  auto load_tile = [&](int it, int stage) {
+    const int tk = tid >> 2, q4 = tid & 3;
+    const int64_t i = i0 + (int64_t)it * kTT + tk;
+    int seg = 0;
+    int64_t off = 0;
+    const bool ok = i < i1 && locate(p, c, i, g, seg, off);
+    const __nv_bfloat16* ks = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].k) + off : qg;
+    const __nv_bfloat16* vs = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].v) + off : qg;
+    __nv_bfloat16* kd = kv_s + (size_t)stage * 2 * kTT * D + tk * D;
+    __nv_bfloat16* vd = kd + kTT * D;
+#pragma unroll
+    for (int j = 0; j < CH / 4; ++j) {
+      const int ch = q4 + 4 * j;
+      const int pc = ch ^ (tk & 7);
+      cp_async16(kd + pc * 8, ks + (ok ? ch * 8 : 0), ok);
+      cp_async16(vd + pc * 8, vs + (ok ? ch * 8 : 0), ok);
+    }
+    if (q4 == 0) valid_s[stage * kTT + tk] = ok ? 1 : 0;
+  };
+
+  // Put every stage's gather in flight first (one commit group per stage).
+#pragma unroll
+  for (int st = 0; st < STAGES; ++st) {
+    if (st < n_tiles) load_tile(st, st);
+    cp_async_commit();
+  }
+
+  // Q of the group's heads (rows >= G zero), swizzled like the K/V tiles.
   for (int idx = tid; idx < 16 * CH; idx += 128) {
     const int row = idx / CH, ch = idx % CH;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -190,32 +288,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
     l_s[tid] = 0.f;
     a_s[tid] = 1.f;
   }
-
-  // Gather of one tile: thread -> token slot tid/4, chunks (tid&3) + 4j.
-  auto load_tile = [&](int it, int stage) {
-    const int tk = tid >> 2, q4 = tid & 3;
-    const int64_t i = i0 + (int64_t)it * kTT + tk;
-    int seg = 0;
-    int64_t off = 0;
-    const bool ok = i < i1 && locate(p, c, i, g, seg, off);
-    const __nv_bfloat16* ks = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].k) + off : qg;
-    const __nv_bfloat16* vs = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].v) + off : qg;
-    __nv_bfloat16* kd = k_s + (size_t)stage * kTT * D + tk * D;
-    __nv_bfloat16* vd = v_s + (size_t)stage * kTT * D + tk * D;
-#pragma unroll
-    for (int j = 0; j < CH / 4; ++j) {
-      const int ch = q4 + 4 * j;
-      const int pc = ch ^ (tk & 7);
-      cp_async16(kd + pc * 8, ks + (ok ? ch * 8 : 0), ok);
-      cp_async16(vd + pc * 8, vs + (ok ? ch * 8 : 0), ok);
-    }
-    if (q4 == 0) valid_s[stage * kTT + tk] = ok ? 1 : 0;
-  };
-
-  if (n_tiles > 0) load_tile(0, 0);
-  cp_async_commit();
   __syncthreads();
-
   uint32_t qf[D / 16][4];
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
@@ -231,13 +304,11 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   const int gq = lane >> 2, t4 = lane & 3;
 
   for (int it = 0; it < n_tiles; ++it) {
-    const int stage = it & 1;
-    if (it + 1 < n_tiles) load_tile(it + 1, stage ^ 1);
-    cp_async_commit();
-    cp_async_wait1();
+    const int stage = it % STAGES;
+    cp_async_wait<STAGES - 1>();
     __syncthreads();
-    const __nv_bfloat16* kt = k_s + (size_t)stage * kTT * D;
-    const __nv_bfloat16* vt = v_s + (size_t)stage * kTT * D;
+    const __nv_bfloat16* kt = kv_s + (size_t)stage * 2 * kTT * D;
+    const __nv_bfloat16* vt = kt + kTT * D;
     // S = Q K^T for tokens 8w..8w+7 of the tile.
     {
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -304,62 +375,56 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
       }
     }
     __syncthreads();
+    if (it + STAGES < n_tiles) load_tile(it + STAGES, stage);
+    cp_async_commit();
   }
+  cp_async_wait<0>();
+  __syncthreads();
 
-  // Finalise: normalised output and lse (natural log) for heads gq, gq+8.
+  // Unnormalised partial into shared memory (over the K/V stages), then merge.
+  float* o_s = reinterpret_cast<float*>(kv_s);
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int row = gq + 8 * half;
-    if (row >= G) continue;
-    const float l = n_tiles > 0 ? l_s[row] : 0.f;
-    const float m = n_tiles > 0 ? m_s[row] : -INFINITY;
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-    const int head = head0 + row;
-    if (p.n_splits == 1) {
-      const int64_t base = ((int64_t)r * p.n_q_heads + head) * D;
 #pragma unroll
-      for (int j = 0; j < NTD; ++j) {
-        const int d = warp * (D / 4) + j * 8 + 2 * t4;
-        const float x0 = o[j][2 * half] * inv, x1 = o[j][2 * half + 1] * inv;
-        if (p.out_dtype == QSA_F32) {
-          *reinterpret_cast<float2*>(static_cast<float*>(p.out) + base + d) = make_float2(x0, x1);
-        } else {
-          *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + base + d) =
-              __floats2bfloat162_rn(x0, x1);
-        }
-      }
-      if (warp == 0 && t4 == 0 && p.lse) p.lse[(int64_t)r * p.n_q_heads + head] = lse;
-    } else {
-      float* dst = partial_row(p, split, r, head);
-#pragma unroll
-      for (int j = 0; j < NTD; ++j) {
-        const int d = warp * (D / 4) + j * 8 + 2 * t4;
-        *reinterpret_cast<float2*>(dst + d) = make_float2(o[j][2 * half] * inv, o[j][2 * half + 1] * inv);
-      }
-      if (warp == 0 && t4 == 0)
-        p.part_lse[((int64_t)split * p.total_rows + r) * p.n_q_heads + head] = lse;
+    for (int j = 0; j < NTD; ++j) {
+      const int d = warp * (D / 4) + j * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(o_s + row * D + d) = make_float2(o[j][2 * half], o[j][2 * half + 1]);
     }
   }
+  merge_store(p, r, head0, G, D, o_s, m_s, l_s, msm);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel (fp32 K/V)
 // Thread -> channel d = tid % D and heads hs, hs + HS, ... (HS = 256 / D).
 constexpr int kSimtTT = 32;
 
+template <int D>
+struct SimtSmem {
+  static constexpr size_t q = 16 * D;                 // floats
+  static constexpr size_t k = kSimtTT * (D + 1);
+  static constexpr size_t v = kSimtTT * D;
+  static constexpr size_t z = 16 * 33;
+  static constexpr size_t floats = q + k + v + z + 3 * 16;
+  static constexpr size_t bytes = floats * 4 + kSimtTT * 4 + sizeof(MergeSmem);
+  static_assert(16 * D <= k + v, "merge partial must fit the K/V tiles");
+};
+
 template <int D, int NSEQ>
 __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p) {
+  using L = SimtSmem<D>;
   constexpr int HS = 256 / D;
   constexpr int MAXH = 16 / HS;
   extern __shared__ __align__(16) float fsm[];
   float* q_s = fsm;                          // [16][D]
-  float* k_s = q_s + 16 * D;                 // [32][D+1]
-  float* v_s = k_s + kSimtTT * (D + 1);      // [32][D]
-  float* z_s = v_s + kSimtTT * D;            // [16][33]
-  float* m_s = z_s + 16 * 33;
+  float* k_s = q_s + L::q;                   // [32][D+1]
+  float* v_s = k_s + L::k;                   // [32][D]
+  float* z_s = v_s + L::v;                   // [16][33]
+  float* m_s = z_s + L::z;
   float* l_s = m_s + 16;
   float* a_s = l_s + 16;
   int* ok_s = reinterpret_cast<int*>(a_s + 16);
+  MergeSmem* msm = reinterpret_cast<MergeSmem*>(ok_s + kSimtTT);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
@@ -367,6 +432,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
   const RowCtx c = make_row_ctx(p, r);
   const int64_t i0 = (int64_t)split * p.split_tokens;
   const int64_t i1 = min(c.n_list, i0 + p.split_tokens);
+  const float zscale = p.scale * kLog2e;
 
   const float* qg = static_cast<const float*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
   for (int idx = tid; idx < G * D; idx += 256) q_s[idx] = qg[idx];
@@ -399,18 +465,18 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
       const int hh = pr / kSimtTT, tk = pr % kSimtTT;
       float dot = 0.f;
       for (int dd = 0; dd < D; ++dd) dot = fmaf(q_s[hh * D + dd], k_s[tk * (D + 1) + dd], dot);
-      z_s[hh * 33 + tk] = ok_s[tk] ? dot * p.scale : -INFINITY;
+      z_s[hh * 33 + tk] = ok_s[tk] ? dot * zscale : -INFINITY;
     }
     __syncthreads();
     for (int hh = warp; hh < G; hh += 8) {
       const float z = z_s[hh * 33 + lane];
       const float mo = m_s[hh];
       const float mn = fmaxf(mo, warp_max(z));
-      const float pz = mn == -INFINITY ? 0.f : expf(z - mn);
+      const float pz = mn == -INFINITY ? 0.f : exp2f(z - mn);
       const float sum = warp_sum(pz);
       z_s[hh * 33 + lane] = pz;
       if (lane == 0) {
-        const float alpha = mo == -INFINITY ? 0.f : expf(mo - mn);
+        const float alpha = mo == -INFINITY ? 0.f : exp2f(mo - mn);
         a_s[hh] = alpha;
         m_s[hh] = mn;
         l_s[hh] = l_s[hh] * alpha + sum;
@@ -428,35 +494,19 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
     }
     __syncthreads();
   }
-  const bool any = i1 > i0;
+  float* o_s = k_s;  // [16][D] over the K/V tiles
 #pragma unroll
   for (int j = 0; j < MAXH; ++j) {
     const int hh = hs + j * HS;
-    if (hh >= G) continue;
-    const float l = any ? l_s[hh] : 0.f;
-    const float m = any ? m_s[hh] : -INFINITY;
-    const float x = l > 0.f ? acc[j] / l : 0.f;
-    const float lse = l > 0.f ? m + logf(l) : -INFINITY;
-    const int head = head0 + hh;
-    if (p.n_splits == 1) {
-      const int64_t o = ((int64_t)r * p.n_q_heads + head) * D + d;
-      if (p.out_dtype == QSA_F32) static_cast<float*>(p.out)[o] = x;
-      else static_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16(x);
-      if (d == 0 && p.lse) p.lse[(int64_t)r * p.n_q_heads + head] = lse;
-    } else {
-      partial_row(p, split, r, head)[d] = x;
-      if (d == 0) p.part_lse[((int64_t)split * p.total_rows + r) * p.n_q_heads + head] = lse;
-    }
+    if (hh < 16) o_s[hh * D + d] = hh < G ? acc[j] : 0.f;
   }
+  merge_store(p, r, head0, G, D, o_s, m_s, l_s, msm);
 }
 
-template <int D>
-constexpr size_t simt_smem_bytes() {
-  return sizeof(float) * (16 * D + kSimtTT * (D + 1) + kSimtTT * D + 16 * 33 + 3 * 16) + sizeof(int) * kSimtTT;
-}
 
-// ------------------------------------------------------------------ step 5: log-sum-exp merge
-// Thread -> (row, 4 channels).
+// ------------------------------------------------------------------ step 5 entry point: merge of given partials
+// Thread -> (row, 4 channels).  The partials' lse values are read first in
+// batches, so each thread's loads are independent of one another.
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_parts,
                                                      const float* __restrict__ lse_parts, int n_parts,
                                                      int64_t n_rows, int head_dim, void* __restrict__ out,
@@ -467,67 +517,125 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   const int64_t row = idx / q;
   const int d = (int)(idx % q) * 4;
   float m = -INFINITY;
-  for (int s = 0; s < n_parts; ++s) m = fmaxf(m, lse_parts[(int64_t)s * n_rows + row]);
+  for (int s0 = 0; s0 < n_parts; s0 += 8) {
+    float l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) l[j] = s0 + j < n_parts ? __ldg(lse_parts + (int64_t)(s0 + j) * n_rows + row) : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, l[j]);
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (m != -INFINITY) {
-    for (int s = 0; s < n_parts; ++s) {
-      const float ls = lse_parts[(int64_t)s * n_rows + row];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - m);
-      const float4 v = *reinterpret_cast<const float4*>(o_parts + ((int64_t)s * n_rows + row) * head_dim + d);
-      wsum += w;
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+    for (int s0 = 0; s0 < n_parts; s0 += 4) {
+      float w[4];
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool in = s0 + j < n_parts;
+        const float ls = in ? __ldg(lse_parts + (int64_t)(s0 + j) * n_rows + row) : -INFINITY;
+        w[j] = ls == -INFINITY ? 0.f : expf(ls - m);
+        v[j] = in && ls != -INFINITY
+                   ? __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)(s0 + j) * n_rows + row) * head_dim + d))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wsum += w[j];
+        acc.x = fmaf(w[j], v[j].x, acc.x);
+        acc.y = fmaf(w[j], v[j].y, acc.y);
+        acc.z = fmaf(w[j], v[j].z, acc.z);
+        acc.w = fmaf(w[j], v[j].w, acc.w);
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  const float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   if (out_dtype == QSA_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(out) + row * head_dim + d) = r;
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + row * head_dim + d) = res;
   } else {
     __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(out) + row * head_dim + d);
-    o2[0] = __floats2bfloat162_rn(r.x, r.y);
-    o2[1] = __floats2bfloat162_rn(r.z, r.w);
+    o2[0] = __floats2bfloat162_rn(res.x, res.y);
+    o2[1] = __floats2bfloat162_rn(res.z, res.w);
   }
   if (d == 0 && lse_out) lse_out[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
-}  // namespace
-
-template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st) {
-  if (n_rows == 0) return cudaSuccess;
-  const dim3 grid((unsigned)p.n_splits, (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows);
-  cudaError_t e;
-  if (kv_dtype == QSA_BF16) {
-    if (p.head_dim == 256) {
-      const size_t sm = MmaSmem<256>::bytes;
-      if ((e = allow_dynamic_smem((const void*)attn_mma_kernel<256, NSEQ>, sm)) != cudaSuccess) return e;
-      attn_mma_kernel<256, NSEQ><<<grid, 128, sm, st>>>(p);
-    } else {
-      const size_t sm = MmaSmem<128>::bytes;
-      if ((e = allow_dynamic_smem((const void*)attn_mma_kernel<128, NSEQ>, sm)) != cudaSuccess) return e;
-      attn_mma_kernel<128, NSEQ><<<grid, 128, sm, st>>>(p);
-    }
-  } else {
-    if (p.head_dim == 256) {
-      const size_t sm = simt_smem_bytes<256>();
-      if ((e = allow_dynamic_smem((const void*)attn_simt_kernel<256, NSEQ>, sm)) != cudaSuccess) return e;
-      attn_simt_kernel<256, NSEQ><<<grid, 256, sm, st>>>(p);
-    } else {
-      const size_t sm = simt_smem_bytes<128>();
-      if ((e = allow_dynamic_smem((const void*)attn_simt_kernel<128, NSEQ>, sm)) != cudaSuccess) return e;
-      attn_simt_kernel<128, NSEQ><<<grid, 256, sm, st>>>(p);
-    }
+template <int NSEQ, typename Kern>
+cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_rows, int threads, size_t smem,
+                               cudaStream_t st) {
+  cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);
+  if (e != cudaSuccess) return e;
+  const int S = p.n_splits;
+  if (S > 8) {
+    e = allow_cluster16((const void*)kernel, threads, smem);
+    if (e != cudaSuccess) return e;
   }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)S, (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, cudaStream_t);
-template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, cudaStream_t);
+}  // namespace
+
+// Deep prefetch (4 tiles in flight, one CTA per SM at head_dim 256) when the
+// launch has no more CTAs than SMs; otherwise 2 tiles and more CTAs per SM.
+int attn_stages(int64_t ctas) { return ctas <= device_sm_count() ? 4 : 2; }
+
+int attn_max_splits(qsa_dtype kv_dtype, int head_dim, int stages) {
+  const void* k;
+  size_t smem;
+  int threads;
+  if (kv_dtype == QSA_BF16) {
+    threads = 128;
+    if (head_dim == 256) {
+      k = stages == 4 ? (const void*)attn_mma_kernel<256, 4, 1> : (const void*)attn_mma_kernel<256, 2, 1>;
+      smem = stages == 4 ? MmaSmem<256, 4>::bytes : MmaSmem<256, 2>::bytes;
+    } else {
+      k = stages == 4 ? (const void*)attn_mma_kernel<128, 4, 1> : (const void*)attn_mma_kernel<128, 2, 1>;
+      smem = stages == 4 ? MmaSmem<128, 4>::bytes : MmaSmem<128, 2>::bytes;
+    }
+  } else {
+    threads = 256;
+    k = head_dim == 256 ? (const void*)attn_simt_kernel<256, 1> : (const void*)attn_simt_kernel<128, 1>;
+    smem = head_dim == 256 ? SimtSmem<256>::bytes : SimtSmem<128>::bytes;
+  }
+  if (allow_dynamic_smem(k, smem) != cudaSuccess) return 8;
+  return allow_cluster16(k, threads, smem) == cudaSuccess ? kMaxSplits : 8;
+}
+
+template <int NSEQ>
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  if (kv_dtype == QSA_BF16) {
+    if (p.head_dim == 256) {
+      if (stages == 4)
+        return launch_attn_kernel(attn_mma_kernel<256, 4, NSEQ>, p, n_rows, 128, MmaSmem<256, 4>::bytes, st);
+      return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ>, p, n_rows, 128, MmaSmem<256, 2>::bytes, st);
+    }
+    if (stages == 4)
+      return launch_attn_kernel(attn_mma_kernel<128, 4, NSEQ>, p, n_rows, 128, MmaSmem<128, 4>::bytes, st);
+    return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ>, p, n_rows, 128, MmaSmem<128, 2>::bytes, st);
+  }
+  if (p.head_dim == 256)
+    return launch_attn_kernel(attn_simt_kernel<256, NSEQ>, p, n_rows, 256, SimtSmem<256>::bytes, st);
+  return launch_attn_kernel(attn_simt_kernel<128, NSEQ>, p, n_rows, 256, SimtSmem<128>::bytes, st);
+}
+
+template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, int, cudaStream_t);
+template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, int, cudaStream_t);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows, int head_dim,
                          void* out, int out_dtype, float* lse_out, cudaStream_t st) {

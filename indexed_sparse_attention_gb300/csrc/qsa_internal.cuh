@@ -91,13 +91,10 @@ struct AttnParams {
   int32_t group;           // query heads per KV head
   int32_t head_dim;
   float scale;             // logit scale
-  int32_t n_splits;
+  int32_t n_splits;        // CTAs (one cluster) per (row, KV group), <= 16
   int32_t split_tokens;    // selected-list entries per split
-  int32_t total_rows;      // rows of the whole call (partial buffer stride)
-  float* part_o;           // [n_splits, total_rows, Hq, D] when n_splits > 1
-  float* part_lse;         // [n_splits, total_rows, Hq]
-  void* out;               // [total_rows, Hq, D] when n_splits == 1
-  float* lse;              // [total_rows, Hq] or null
+  void* out;               // [rows, Hq, D]
+  float* lse;              // [rows, Hq] or null
   int32_t out_dtype;
 };
 
@@ -113,18 +110,25 @@ template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 
 template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st);
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st);
+
+// Tiles in flight per attention CTA for a launch of `ctas` CTAs (2 or 4).
+int attn_stages(int64_t ctas);
+
+// Largest split count (cluster size) the attention kernel can launch with.
+int attn_max_splits(qsa_dtype kv_dtype, int head_dim, int stages);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows,
                          int head_dim, void* out, int out_dtype, float* lse_out, cudaStream_t st);
-
-// Shared-memory bytes the selection kernel needs for rows of up to max_nb blocks.
-size_t select_smem_bytes(int64_t max_nb);
 
 int device_sm_count();
 
 // Raise a kernel's dynamic shared-memory limit (once per device and size).
 cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes);
+
+// Allow 16-CTA clusters for a kernel (once per device); cudaErrorNotSupported
+// when no 16-CTA cluster of that shape can be resident.
+cudaError_t allow_cluster16(const void* kernel, int threads, size_t smem);
 
 // Blocks per scoring work item for the kernel that serves q_dtype.
 int score_tile_blocks(qsa_dtype q_dtype);
