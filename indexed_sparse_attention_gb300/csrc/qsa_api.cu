@@ -311,7 +311,6 @@ namespace {
 struct SplitPlan {
   int32_t n_splits;
   int32_t split_tokens;
-  int32_t stages;
 };
 
 // Longest selected list any row of the call can have: 4 tokens per listed
@@ -332,13 +331,10 @@ SplitPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config
   int64_t n = cfg->n_splits;
   if (n <= 0) n = (2 * sms + pairs - 1) / pairs;
   n = std::max<int64_t>(1, std::min<int64_t>(n, (n_list + 31) / 32));
-  int stages = attn_stages(pairs * std::min<int64_t>(n, 16));
-  const int max_splits = attn_max_splits(cfg->kv_dtype, cfg->head_dim, stages);
-  n = std::min<int64_t>(n, max_splits);
-  stages = attn_stages(pairs * n);
+  n = std::min<int64_t>(n, attn_max_splits(cfg->kv_dtype, cfg->head_dim));
   const int64_t per = (n_list + n - 1) / n;
   n = (n_list + per - 1) / per;
-  return SplitPlan{(int32_t)n, (int32_t)per, (int32_t)stages};
+  return SplitPlan{(int32_t)n, (int32_t)per};
 }
 
 size_t attn_ws_bytes(const SplitPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
@@ -431,7 +427,7 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.out = out;
   p.lse = lse;
   p.out_dtype = cfg->out_dtype;
-  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, sp.stages, st);
+  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, st);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn");
   return QSA_OK;
 }

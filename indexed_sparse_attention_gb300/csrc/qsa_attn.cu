@@ -143,6 +143,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 //   lse = (M + log2 sum_q w_q l_q) * ln 2,
 // and a head whose splits saw no key gets out = 0 and lse = -inf.
 struct MergeSmem {
+  float mq[16][kMaxSplits];
+  float lq[16][kMaxSplits];
   float w[16][kMaxSplits];
   float inv[16];
   float lse[16];
@@ -156,15 +158,22 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
   const int c = (int)cluster.block_rank();
   const int tid = threadIdx.x, nt = blockDim.x;
   cluster.sync();
+  // Every split's running max and sum, one (head, split) pair per thread.
+  for (int t = tid; t < G * S; t += nt) {
+    const int h = t / S, q = t % S;
+    ms->mq[h][q] = *cluster.map_shared_rank(m_s + h, q);
+    ms->lq[h][q] = *cluster.map_shared_rank(l_s + h, q);
+  }
+  __syncthreads();
   if (tid < G) {
     float M = -INFINITY;
-    for (int q = 0; q < S; ++q) M = fmaxf(M, *cluster.map_shared_rank(m_s + tid, q));
+    for (int q = 0; q < S; ++q) M = fmaxf(M, ms->mq[tid][q]);
     float Lsum = 0.f;
     for (int q = 0; q < S; ++q) {
-      const float mq = *cluster.map_shared_rank(m_s + tid, q);
+      const float mq = ms->mq[tid][q];
       const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
       ms->w[tid][q] = w;
-      Lsum += w * *cluster.map_shared_rank(l_s + tid, q);
+      Lsum += w * ms->lq[tid][q];
     }
     ms->inv[tid] = Lsum > 0.f ? 1.f / Lsum : 0.f;
     ms->lse[tid] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
@@ -176,14 +185,20 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
   for (int idx = tid; idx < G * nq; idx += nt) {
     const int h = idx / nq;
     const int d = 4 * (c + (idx % nq) * S);
+    float4 v[kMaxSplits];
+#pragma unroll
+    for (int q = 0; q < kMaxSplits; ++q)
+      if (q < S) v[q] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s + h * D + d, q));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < S; ++q) {
-      const float w = ms->w[h][q];
-      const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s + h * D + d, q));
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
+#pragma unroll
+    for (int q = 0; q < kMaxSplits; ++q) {
+      if (q < S) {
+        const float w = ms->w[h][q];
+        acc.x = fmaf(w, v[q].x, acc.x);
+        acc.y = fmaf(w, v[q].y, acc.y);
+        acc.z = fmaf(w, v[q].z, acc.z);
+        acc.w = fmaf(w, v[q].w, acc.w);
+      }
     }
     const float inv = ms->inv[h];
     const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
@@ -201,31 +216,40 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
 }
 
 // ------------------------------------------------------------------ tensor-pipe kernel (bf16 K/V)
+// 8 warps.  Per 32-token tile: warp w computes the logits of tokens
+// 8(w%4)..8(w%4)+7 over half w/4 of the channels (the two halves are added
+// in shared memory), then softmax rows w and w+8, then P.V for channels
+// [w*D/8, (w+1)*D/8).
 constexpr int kTT = 32;        // tokens per tile
 constexpr int kPStride = 40;   // bf16 per P row: 80-byte rows keep ldmatrix conflict-free
+constexpr int kSStride = kTT + 4;
+constexpr int kAttnThreads = 256;
 
-template <int D, int STAGES>
+template <int D>
 struct MmaSmem {
-  static constexpr int CH = D / 8;  // 16-byte chunks per K/V/Q row
+  static constexpr int STAGES = D == 256 ? 2 : 4;     // two CTAs per SM either way
+  static constexpr int CH = D / 8;                     // 16-byte chunks per K/V/Q row
   static constexpr size_t q = 16 * D * 2;
-  static constexpr size_t kv_tile = kTT * D * 2;            // one K or V tile
-  static constexpr size_t s = 16 * (kTT + 4) * 4;
+  static constexpr size_t kv_tile = kTT * D * 2;       // one K or V tile
+  static constexpr size_t s = 2 * 16 * kSStride * 4;   // logits, one plane per channel half
   static constexpr size_t pm = 16 * kPStride * 2;
-  static constexpr size_t off_kv = q;                        // [STAGES][K tile, V tile]
+  static constexpr size_t off_kv = q;                  // [STAGES][K tile, V tile]
   static constexpr size_t off_s = off_kv + STAGES * 2 * kv_tile;
   static constexpr size_t off_p = off_s + s;
-  static constexpr size_t off_m = off_p + pm;                // m, l, alpha: 3 x 16 floats
+  static constexpr size_t off_m = off_p + pm;          // m, l, alpha: 3 x 16 floats
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
   static constexpr size_t off_merge = off_valid + STAGES * kTT * 4;
   static constexpr size_t bytes = off_merge + sizeof(MergeSmem);
   static_assert(16 * D * 4 <= STAGES * 2 * kv_tile, "merge partial must fit the K/V stages");
 };
 
-template <int D, int STAGES, int NSEQ>
-__global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p) {
-  using L = MmaSmem<D, STAGES>;
+template <int D, int NSEQ>
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnParams<NSEQ> p) {
+  using L = MmaSmem<D>;
+  constexpr int STAGES = L::STAGES;
   constexpr int CH = L::CH;
-  constexpr int NTD = D / 32;  // 8-channel n-tiles per warp in P.V (D/4 channels per warp)
+  constexpr int KH = D / 32;   // k-steps (16 channels each) per channel half
+  constexpr int NTD = D / 64;  // 8-channel n-tiles per warp in P.V
   extern __shared__ __align__(128) uint8_t smem[];
   __nv_bfloat16* q_s = reinterpret_cast<__nv_bfloat16*>(smem);
   __nv_bfloat16* kv_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_kv);
@@ -238,6 +262,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   MergeSmem* msm = reinterpret_cast<MergeSmem*>(smem + L::off_merge);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quarter = warp & 3, half = warp >> 2;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
   const int G = p.group, head0 = g * G;
   const RowCtx c = make_row_ctx(p, r);
@@ -246,10 +271,10 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   const int n_tiles = i1 > i0 ? (int)((i1 - i0 + kTT - 1) / kTT) : 0;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
 
-  // Gather of one tile into a stage: thread -> token slot tid/4, chunks (tid&3) + 4j,
+  // Gather of one tile into a stage: thread -> token slot tid/8, chunks (tid&7) + 8j,
   // swizzled: chunk c of token row t lands at c ^ (t & 7).
   auto load_tile = [&](int it, int stage) {
-    const int tk = tid >> 2, q4 = tid & 3;
+    const int tk = tid >> 3, q8 = tid & 7;
     const int64_t i = i0 + (int64_t)it * kTT + tk;
     int seg = 0;
     int64_t off = 0;
@@ -259,13 +284,13 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
     __nv_bfloat16* kd = kv_s + (size_t)stage * 2 * kTT * D + tk * D;
     __nv_bfloat16* vd = kd + kTT * D;
 #pragma unroll
-    for (int j = 0; j < CH / 4; ++j) {
-      const int ch = q4 + 4 * j;
+    for (int j = 0; j < CH / 8; ++j) {
+      const int ch = q8 + 8 * j;
       const int pc = ch ^ (tk & 7);
       cp_async16(kd + pc * 8, ks + (ok ? ch * 8 : 0), ok);
       cp_async16(vd + pc * 8, vs + (ok ? ch * 8 : 0), ok);
     }
-    if (q4 == 0) valid_s[stage * kTT + tk] = ok ? 1 : 0;
+    if (q8 == 0) valid_s[stage * kTT + tk] = ok ? 1 : 0;
   };
 
   // Put every stage's gather in flight first (one commit group per stage).
@@ -276,25 +301,25 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   }
 
   // Q of the group's heads (rows >= G zero), swizzled like the K/V tiles.
-  for (int idx = tid; idx < 16 * CH; idx += 128) {
+  for (int idx = tid; idx < 16 * CH; idx += kAttnThreads) {
     const int row = idx / CH, ch = idx % CH;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (row < G) v = *reinterpret_cast<const uint4*>(qg + (int64_t)row * D + ch * 8);
     *reinterpret_cast<uint4*>(q_s + (row * CH + (ch ^ (row & 7))) * 8) = v;
   }
-  for (int idx = tid; idx < 16 * kPStride; idx += 128) p_s[idx] = __float2bfloat16(0.f);
+  for (int idx = tid; idx < 16 * kPStride; idx += kAttnThreads) p_s[idx] = __float2bfloat16(0.f);
   if (tid < 16) {
     m_s[tid] = -INFINITY;
     l_s[tid] = 0.f;
     a_s[tid] = 1.f;
   }
   __syncthreads();
-  uint32_t qf[D / 16][4];
+  uint32_t qf[KH][4];
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
+  for (int i = 0; i < KH; ++i) {
     const int row = (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int ch = 2 * ks + (lane >> 4);
-    ldsm_x4(qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], q_s + (row * CH + (ch ^ (row & 7))) * 8);
+    const int ch = 2 * (half * KH + i) + (lane >> 4);
+    ldsm_x4(qf[i][0], qf[i][1], qf[i][2], qf[i][3], q_s + (row * CH + (ch ^ (row & 7))) * 8);
   }
 
   float o[NTD][4];
@@ -309,43 +334,74 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
     __syncthreads();
     const __nv_bfloat16* kt = kv_s + (size_t)stage * 2 * kTT * D;
     const __nv_bfloat16* vt = kt + kTT * D;
-    // S = Q K^T for tokens 8w..8w+7 of the tile.
+    // Partial logits of tokens 8*quarter.. over this warp's channel half, two chains.
     {
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int tk = 8 * warp + (lane & 7);
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tk = 8 * quarter + (lane & 7);
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ks += 2) {
+      for (int i = 0; i < KH; i += 2) {
         uint32_t b0, b1, b2, b3;
-        const int ch = 2 * ks + (lane >> 3);
+        const int ch = 2 * (half * KH + i) + (lane >> 3);
         ldsm_x4(b0, b1, b2, b3, kt + (tk * CH + (ch ^ (tk & 7))) * 8);
-        mma_bf16(sacc, qf[ks], b0, b1);
-        mma_bf16(sacc, qf[ks + 1], b2, b3);
+        mma_bf16(sa, qf[i], b0, b1);
+        mma_bf16(sb, qf[i + 1], b2, b3);
       }
-      const int col = 8 * warp + 2 * t4;
-      const bool v0 = valid_s[stage * kTT + col] != 0, v1 = valid_s[stage * kTT + col + 1] != 0;
-      s_s[gq * (kTT + 4) + col] = v0 ? sacc[0] * zscale : -INFINITY;
-      s_s[gq * (kTT + 4) + col + 1] = v1 ? sacc[1] * zscale : -INFINITY;
-      s_s[(gq + 8) * (kTT + 4) + col] = v0 ? sacc[2] * zscale : -INFINITY;
-      s_s[(gq + 8) * (kTT + 4) + col + 1] = v1 ? sacc[3] * zscale : -INFINITY;
+      float* sp = s_s + half * 16 * kSStride;
+      const int col = 8 * quarter + 2 * t4;
+      *reinterpret_cast<float2*>(sp + gq * kSStride + col) = make_float2(sa[0] + sb[0], sa[1] + sb[1]);
+      *reinterpret_cast<float2*>(sp + (gq + 8) * kSStride + col) = make_float2(sa[2] + sb[2], sa[3] + sb[3]);
     }
     __syncthreads();
-    // Online softmax, one warp per head row, one lane per token (base-2 logits).
-    for (int rr = warp; rr < G; rr += 4) {
-      const float z = s_s[rr * (kTT + 4) + lane];
-      const float mo = m_s[rr];
-      const float mn = fmaxf(mo, warp_max(z));
-      const float pz = mn == -INFINITY ? 0.f : exp2f(z - mn);
-      const float sum = warp_sum(pz);
-      p_s[rr * kPStride + lane] = __float2bfloat16(pz);
-      if (lane == 0) {
-        const float alpha = mo == -INFINITY ? 0.f : exp2f(mo - mn);
-        a_s[rr] = alpha;
-        m_s[rr] = mn;
-        l_s[rr] = l_s[rr] * alpha + sum;
+    // Online softmax of rows warp and warp+8 (base-2 logits), one lane per token.
+    {
+      const bool valid = valid_s[stage * kTT + lane] != 0;
+      float z[2], mo[2], mx[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int rr = warp + 8 * j;
+        z[j] = -INFINITY;
+        mo[j] = -INFINITY;
+        if (rr < G) {
+          const float s0 = s_s[rr * kSStride + lane] + s_s[16 * kSStride + rr * kSStride + lane];
+          z[j] = valid ? s0 * zscale : -INFINITY;
+          mo[j] = m_s[rr];
+        }
+        mx[j] = z[j];
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+      }
+      float pz[2], sm[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float mn = fmaxf(mo[j], mx[j]);
+        pz[j] = mn == -INFINITY ? 0.f : exp2f(z[j] - mn);
+        sm[j] = pz[j];
+        mx[j] = mn;
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) {
+        sm[0] += __shfl_xor_sync(0xffffffffu, sm[0], off);
+        sm[1] += __shfl_xor_sync(0xffffffffu, sm[1], off);
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int rr = warp + 8 * j;
+        if (rr < G) {
+          p_s[rr * kPStride + lane] = __float2bfloat16(pz[j]);
+          if (lane == 0) {
+            const float alpha = mo[j] == -INFINITY ? 0.f : exp2f(mo[j] - mx[j]);
+            a_s[rr] = alpha;
+            m_s[rr] = mx[j];
+            l_s[rr] = l_s[rr] * alpha + sm[j];
+          }
+        }
       }
     }
     __syncthreads();
-    // O += P V over channels [warp*D/4, (warp+1)*D/4).
+    // O += P V over channels [warp*D/8, (warp+1)*D/8).
     {
       const float al0 = gq < G ? a_s[gq] : 1.f, al1 = gq + 8 < G ? a_s[gq + 8] : 1.f;
 #pragma unroll
@@ -366,7 +422,7 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
         const int tk = kk * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
 #pragma unroll
         for (int j = 0; j < NTD; j += 2) {
-          const int ch = warp * (D / 32) + j + (lane >> 4);
+          const int ch = warp * NTD + j + (lane >> 4);
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(b0, b1, b2, b3, vt + (tk * CH + (ch ^ (tk & 7))) * 8);
           mma_bf16(o[j], pa, b0, b1);
@@ -384,12 +440,12 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnParams<NSEQ> p)
   // Unnormalised partial into shared memory (over the K/V stages), then merge.
   float* o_s = reinterpret_cast<float*>(kv_s);
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int row = gq + 8 * half;
+  for (int hf = 0; hf < 2; ++hf) {
+    const int row = gq + 8 * hf;
 #pragma unroll
     for (int j = 0; j < NTD; ++j) {
-      const int d = warp * (D / 4) + j * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(o_s + row * D + d) = make_float2(o[j][2 * half], o[j][2 * half + 1]);
+      const int d = warp * (D / 8) + j * 8 + 2 * t4;
+      *reinterpret_cast<float2*>(o_s + row * D + d) = make_float2(o[j][2 * hf], o[j][2 * hf + 1]);
     }
   }
   merge_store(p, r, head0, G, D, o_s, m_s, l_s, msm);
@@ -590,23 +646,14 @@ cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_row
 
 }  // namespace
 
-// Deep prefetch (4 tiles in flight, one CTA per SM at head_dim 256) when the
-// launch has no more CTAs than SMs; otherwise 2 tiles and more CTAs per SM.
-int attn_stages(int64_t ctas) { return ctas <= device_sm_count() ? 4 : 2; }
-
-int attn_max_splits(qsa_dtype kv_dtype, int head_dim, int stages) {
+int attn_max_splits(qsa_dtype kv_dtype, int head_dim) {
   const void* k;
   size_t smem;
   int threads;
   if (kv_dtype == QSA_BF16) {
-    threads = 128;
-    if (head_dim == 256) {
-      k = stages == 4 ? (const void*)attn_mma_kernel<256, 4, 1> : (const void*)attn_mma_kernel<256, 2, 1>;
-      smem = stages == 4 ? MmaSmem<256, 4>::bytes : MmaSmem<256, 2>::bytes;
-    } else {
-      k = stages == 4 ? (const void*)attn_mma_kernel<128, 4, 1> : (const void*)attn_mma_kernel<128, 2, 1>;
-      smem = stages == 4 ? MmaSmem<128, 4>::bytes : MmaSmem<128, 2>::bytes;
-    }
+    threads = kAttnThreads;
+    k = head_dim == 256 ? (const void*)attn_mma_kernel<256, 1> : (const void*)attn_mma_kernel<128, 1>;
+    smem = head_dim == 256 ? MmaSmem<256>::bytes : MmaSmem<128>::bytes;
   } else {
     threads = 256;
     k = head_dim == 256 ? (const void*)attn_simt_kernel<256, 1> : (const void*)attn_simt_kernel<128, 1>;
@@ -617,25 +664,20 @@ int attn_max_splits(qsa_dtype kv_dtype, int head_dim, int stages) {
 }
 
 template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
   if (kv_dtype == QSA_BF16) {
-    if (p.head_dim == 256) {
-      if (stages == 4)
-        return launch_attn_kernel(attn_mma_kernel<256, 4, NSEQ>, p, n_rows, 128, MmaSmem<256, 4>::bytes, st);
-      return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ>, p, n_rows, 128, MmaSmem<256, 2>::bytes, st);
-    }
-    if (stages == 4)
-      return launch_attn_kernel(attn_mma_kernel<128, 4, NSEQ>, p, n_rows, 128, MmaSmem<128, 4>::bytes, st);
-    return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ>, p, n_rows, 128, MmaSmem<128, 2>::bytes, st);
+    if (p.head_dim == 256)
+      return launch_attn_kernel(attn_mma_kernel<256, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256>::bytes, st);
+    return launch_attn_kernel(attn_mma_kernel<128, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128>::bytes, st);
   }
   if (p.head_dim == 256)
     return launch_attn_kernel(attn_simt_kernel<256, NSEQ>, p, n_rows, 256, SimtSmem<256>::bytes, st);
   return launch_attn_kernel(attn_simt_kernel<128, NSEQ>, p, n_rows, 256, SimtSmem<128>::bytes, st);
 }
 
-template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, int, cudaStream_t);
-template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, int, cudaStream_t);
+template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, cudaStream_t);
+template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, cudaStream_t);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows, int head_dim,
                          void* out, int out_dtype, float* lse_out, cudaStream_t st) {

@@ -110,13 +110,10 @@ template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 
 template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st);
-
-// Tiles in flight per attention CTA for a launch of `ctas` CTAs (2 or 4).
-int attn_stages(int64_t ctas);
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st);
 
 // Largest split count (cluster size) the attention kernel can launch with.
-int attn_max_splits(qsa_dtype kv_dtype, int head_dim, int stages);
+int attn_max_splits(qsa_dtype kv_dtype, int head_dim);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows,
                          int head_dim, void* out, int out_dtype, float* lse_out, cudaStream_t st);

@@ -17,14 +17,6 @@ namespace {
 
 constexpr float kScoreScale = 0.08838834764831845f;  // 1/sqrt(128)
 
-__device__ __forceinline__ float4 ld_stream4(const float* p) {
-  float4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "l"(p));
-  return v;
-}
-
 // bf16x2 of (lo_elem, hi_elem), round to nearest even; lo_elem in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo_elem, float hi_elem) {
   uint32_t r;
@@ -89,100 +81,169 @@ __device__ __forceinline__ int find_seq_by_work(const ScoreParams<NSEQ>& p, int6
 }
 
 // ------------------------------------------------------------------ scoring, tensor pipe
-// One warp per (16-block tile, group of <= 8 rows).  MMA columns are
-// (row, head) pairs n = 4*row + head; NT n-tiles of 8 columns cover 2*NT rows.
-// The 128 channels are visited in 8 k-steps of 16; inside a k-step, thread
-// quad t holds physical channels 4t..4t+3, i.e. logical fragment columns
-// (2t, 2t+1) <- channels (4t, 4t+1) and (2t+8, 2t+9) <- channels (4t+2, 4t+3).
-// A and B use the same channel permutation, so the dot products are unchanged
-// and each thread reads one float4 per row per k-step (fully used sectors).
-template <int NT, int NSEQ>
-__global__ void __launch_bounds__(256) score_mma_kernel(const ScoreParams<NSEQ> p) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t item = (int64_t)blockIdx.x * 8 + warp;
-  if (item >= p.n_work) return;
-  const int si = find_seq_by_work(p, item);
-  const ScoreSeq& sq = p.seq[si];
+// Persistent warps: warp w of the grid takes work items w, w + W, w + 2W, ...
+// (W = warps in the grid); an item is one (16-block tile, group of <= 8
+// rows).  Each warp streams its tiles' pooled keys into shared memory with
+// cp.async, two tiles in flight, and runs the MMAs on the tile that landed.
+// MMA columns are (row, head) pairs n = 4*row + head; NT n-tiles of 8
+// columns cover 2*NT rows.  The 128 channels are visited in 8 k-steps of 16;
+// inside a k-step, thread quad t holds physical channels 4t..4t+3, i.e.
+// logical fragment columns (2t, 2t+1) <- channels (4t, 4t+1) and
+// (2t+8, 2t+9) <- channels (4t+2, 4t+3).  A and B use the same channel
+// permutation, so the dot products are unchanged and each thread reads one
+// float4 per row per k-step.
+constexpr int kScoreWarps = 8;
+constexpr int kScoreStages = 2;
+constexpr int kRowPitch = 144;   // floats per staged row: 576 bytes keep the float4 reads conflict-free
+constexpr int kStageFloats = kScoreTile * kRowPitch;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src), "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+struct ScoreItem {
+  int64_t b0;        // first block of the tile
+  int64_t nb_last;   // complete blocks the group's last row sees
+  int si;            // sequence
+  int row0, rows;    // rows of the group within the sequence
+  bool valid;        // item exists
+  bool active;       // item has visible blocks
+};
+
+template <int NSEQ>
+__device__ __forceinline__ ScoreItem score_item(const ScoreParams<NSEQ>& p, int64_t item) {
+  ScoreItem x;
+  x.valid = item < p.n_work;
+  x.active = false;
+  x.si = 0;
+  x.b0 = 0;
+  x.nb_last = 0;
+  x.row0 = 0;
+  x.rows = 0;
+  if (!x.valid) return x;
+  x.si = find_seq_by_work(p, item);
+  const ScoreSeq& sq = p.seq[x.si];
   const int64_t w = item - sq.work_begin;
   const int64_t tile = w / sq.n_groups;
   const int grp = (int)(w - tile * sq.n_groups);
-  const int row0 = grp * kRowGroup;                 // first row of the group within the sequence
-  const int rows = min(kRowGroup, sq.n_rows - row0);
-  const int64_t b0 = tile * kScoreTile;
-  // Complete blocks the group's last row sees bound every row of the group.
-  const int64_t nb_last = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + rows - 1));
-  if (b0 >= nb_last) return;
+  x.row0 = grp * kRowGroup;
+  x.rows = min(kRowGroup, sq.n_rows - x.row0);
+  x.b0 = tile * kScoreTile;
+  x.nb_last = visible_blocks(row_position(sq.n_tokens, sq.n_rows, x.row0 + x.rows - 1));
+  x.active = x.b0 < x.nb_last;
+  return x;
+}
 
+template <int NT, int NSEQ>
+__global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const ScoreParams<NSEQ> p) {
+  extern __shared__ float4 score_smem4[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
+  float* my = reinterpret_cast<float*>(score_smem4) + warp * kScoreStages * kStageFloats;
+  const int64_t W = (int64_t)gridDim.x * kScoreWarps;
+  int64_t item = (int64_t)blockIdx.x * kScoreWarps + warp;
 
-  // A operand: rows b0+g and b0+g+8 of the pooled tile, one float4 per k-step.
-  float4 ra[8], rb[8];
-  {
-    const int64_t ba = b0 + g, bb = b0 + g + 8;
-    const float* pa = sq.pooled + ba * sq.pooled_stride + 4 * t;
-    const float* pb = sq.pooled + bb * sq.pooled_stride + 4 * t;
-    const bool va = ba < nb_last, vb = bb < nb_last;
+  // 16 rows x 32 chunks of 16 bytes; lane takes chunks lane, lane + 32, ...
+  auto issue = [&](const ScoreItem& x, int stage) {
+    if (!x.active) return;
+    const ScoreSeq& sq = p.seq[x.si];
+    float* dst = my + stage * kStageFloats;
+    const float* src = sq.pooled + x.b0 * sq.pooled_stride;
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      ra[s] = va ? ld_stream4(pa + 16 * s) : make_float4(0.f, 0.f, 0.f, 0.f);
-      rb[s] = vb ? ld_stream4(pb + 16 * s) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < 16; ++j) {
+      const int c = lane + 32 * j, row = c >> 5, col = c & 31;
+      const bool ok = x.b0 + row < x.nb_last;
+      cp_async16(dst + row * kRowPitch + col * 4, ok ? src + row * sq.pooled_stride + col * 4 : src, ok);
     }
-  }
-  // B operand: the index queries, bf16 [rows, 4, 128].
+  };
+
+  ScoreItem cur = score_item(p, item);
+  ScoreItem nxt = score_item(p, item + W);
+  issue(cur, 0);
+  cp_async_commit();
+  issue(nxt, 1);
+  cp_async_commit();
+
   uint32_t bq[NT][8][2];
-  {
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
+  int bq_si = -1, bq_row0 = -1;
+  int stage = 0;
+  while (cur.valid) {
+    cp_async_wait<1>();
+    __syncwarp();
+    if (cur.active) {
+      const ScoreSeq& sq = p.seq[cur.si];
+      if (cur.si != bq_si || cur.row0 != bq_row0) {
+        // B operand: the group's index queries, bf16 [rows, 4, 128].
+        const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int n = 8 * j + g, r = n >> 2, h = n & 3;
-      if (r < rows) {
-        const __nv_bfloat16* src =
-            qb + ((int64_t)(sq.row_begin + row0 + r) * QSA_INDEX_HEADS + h) * QSA_INDEX_DIM + 4 * t;
+        for (int j = 0; j < NT; ++j) {
+          const int n = 8 * j + g, r = n >> 2, h = n & 3;
+          const __nv_bfloat16* src =
+              qb + ((int64_t)(sq.row_begin + cur.row0 + r) * QSA_INDEX_HEADS + h) * QSA_INDEX_DIM + 4 * t;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src + 16 * s);
-          bq[j][s][0] = v.x;
-          bq[j][s][1] = v.y;
+          for (int s = 0; s < 8; ++s) {
+            uint2 v = make_uint2(0u, 0u);
+            if (r < cur.rows) v = *reinterpret_cast<const uint2*>(src + 16 * s);
+            bq[j][s][0] = v.x;
+            bq[j][s][1] = v.y;
+          }
         }
-      } else {
+        bq_si = cur.si;
+        bq_row0 = cur.row0;
+      }
+      const float* a = my + stage * kStageFloats;
+      float acc[NT][4];
 #pragma unroll
-        for (int s = 0; s < 8; ++s) bq[j][s][0] = bq[j][s][1] = 0u;
+      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float4 ra = *reinterpret_cast<const float4*>(a + g * kRowPitch + 16 * s + 4 * t);
+        const float4 rb = *reinterpret_cast<const float4*>(a + (g + 8) * kRowPitch + 16 * s + 4 * t);
+        uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
+        split3(ra.x, ra.y, h0, m0, l0);  // row g,   columns 2t, 2t+1
+        split3(rb.x, rb.y, h1, m1, l1);  // row g+8, columns 2t, 2t+1
+        split3(ra.z, ra.w, h2, m2, l2);  // row g,   columns 2t+8, 2t+9
+        split3(rb.z, rb.w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          mma_bf16(acc[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
+          mma_bf16(acc[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
+          mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
+        }
+      }
+      // Epilogue: thread (g, t) holds columns 8j+2t, 8j+2t+1 = heads 2(t&1),
+      // 2(t&1)+1 of row 2j + (t>>1); its neighbour t^1 holds the other two.
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float v0 = fmaxf(acc[j][0], 0.f) + fmaxf(acc[j][1], 0.f);
+        float v1 = fmaxf(acc[j][2], 0.f) + fmaxf(acc[j][3], 0.f);
+        v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+        v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        const int r = 2 * j + (t >> 1);
+        if ((t & 1) == 0 && r < cur.rows) {
+          const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, cur.row0 + r));
+          float* dst = p.scores + (int64_t)(sq.row_begin + cur.row0 + r) * p.ld;
+          if (cur.b0 + g < nb) dst[cur.b0 + g] = v0 * kScoreScale;
+          if (cur.b0 + g + 8 < nb) dst[cur.b0 + g + 8] = v1 * kScoreScale;
+        }
       }
     }
+    __syncwarp();
+    const ScoreItem n2 = score_item(p, item + 2 * W);
+    issue(n2, stage);
+    cp_async_commit();
+    cur = nxt;
+    nxt = n2;
+    item += W;
+    stage ^= 1;
   }
-  float acc[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
-    split3(ra[s].x, ra[s].y, h0, m0, l0);  // row g,   columns 2t, 2t+1
-    split3(rb[s].x, rb[s].y, h1, m1, l1);  // row g+8, columns 2t, 2t+1
-    split3(ra[s].z, ra[s].w, h2, m2, l2);  // row g,   columns 2t+8, 2t+9
-    split3(rb[s].z, rb[s].w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      mma_bf16(acc[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
-      mma_bf16(acc[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
-      mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
-    }
-  }
-  // Epilogue: thread (g, t) holds columns 8j+2t, 8j+2t+1 = heads 2(t&1), 2(t&1)+1
-  // of row 2j + (t>>1); its neighbour t^1 holds the other two heads.
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    float v0 = fmaxf(acc[j][0], 0.f) + fmaxf(acc[j][1], 0.f);
-    float v1 = fmaxf(acc[j][2], 0.f) + fmaxf(acc[j][3], 0.f);
-    v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
-    v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
-    const int r = 2 * j + (t >> 1);
-    if ((t & 1) == 0 && r < rows) {
-      const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + r));
-      float* dst = p.scores + (int64_t)(sq.row_begin + row0 + r) * p.ld;
-      if (b0 + g < nb) dst[b0 + g] = v0 * kScoreScale;
-      if (b0 + g + 8 < nb) dst[b0 + g + 8] = v1 * kScoreScale;
-    }
-  }
+  cp_async_wait<0>();
 }
 
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
@@ -258,15 +319,22 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
   if (p.n_work == 0) return cudaSuccess;
   if (q_dtype == QSA_F32) {
     score_simt_kernel<NSEQ><<<(unsigned)p.n_work, 256, 0, st>>>(p);
-  } else {
-    const unsigned grid = (unsigned)((p.n_work + 7) / 8);
-    if (max_rows_per_group <= 2)
-      score_mma_kernel<1, NSEQ><<<grid, 256, 0, st>>>(p);
-    else if (max_rows_per_group <= 4)
-      score_mma_kernel<2, NSEQ><<<grid, 256, 0, st>>>(p);
-    else
-      score_mma_kernel<4, NSEQ><<<grid, 256, 0, st>>>(p);
+    return cudaGetLastError();
   }
+  const size_t smem = sizeof(float) * kScoreWarps * kScoreStages * kStageFloats;
+  const int64_t need = (p.n_work + kScoreWarps - 1) / kScoreWarps;
+  const unsigned grid = (unsigned)(need < device_sm_count() ? need : device_sm_count());
+  const void* k = max_rows_per_group <= 2   ? (const void*)score_mma_kernel<1, NSEQ>
+                  : max_rows_per_group <= 4 ? (const void*)score_mma_kernel<2, NSEQ>
+                                            : (const void*)score_mma_kernel<4, NSEQ>;
+  cudaError_t e = allow_dynamic_smem(k, smem);
+  if (e != cudaSuccess) return e;
+  if (max_rows_per_group <= 2)
+    score_mma_kernel<1, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
+  else if (max_rows_per_group <= 4)
+    score_mma_kernel<2, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
+  else
+    score_mma_kernel<4, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
   return cudaGetLastError();
 }
 
