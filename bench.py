@@ -330,21 +330,28 @@ def main():
     layer_steps = n_layers * args.steps * world
     value = layer_steps / (ms / 1e3)
 
-    # Dominant kernel (block scoring): 12 back-to-back launches in a graph, timed live.
-    kgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(kgraph, stream=stream):
-        for l in layers:
-            l.step.score()
-    with torch.cuda.stream(stream):
-        for _ in range(5):
-            kgraph.replay()
-        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        k0.record(stream)
-        for _ in range(args.kernel_reps):
-            kgraph.replay()
-        k1.record(stream)
-    k1.synchronize()
-    score_us = 1e3 * k0.elapsed_time(k1) / (args.kernel_reps * n_layers)
+    # Each step kind on its own: a graph of its 12 back-to-back launches (one
+    # per layer), timed live.  Scoring is the dominant kernel (the roofline
+    # line); the others show where the rest of the step goes.
+    def time_kind(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for l in layers:
+                fn(l.step)
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.kernel_reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / (args.kernel_reps * n_layers)
+
+    kernel_us = {"pool": time_kind(lambda st: st.pool()), "score": time_kind(lambda st: st.score()),
+                 "select": time_kind(lambda st: st.select()), "attend": time_kind(lambda st: st.attend())}
+    score_us = kernel_us["score"]
 
     # End to end through the public API with host buffers: per step, the new
     # rows' q, index queries, K/V and index keys of every layer go host ->
@@ -432,6 +439,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
+        "us_per_launch_by_step": kernel_us,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
     }
     if rank == 0:

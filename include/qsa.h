@@ -68,8 +68,7 @@ typedef enum qsa_status {
   QSA_ERR_INVALID_ARG = 1,   /* null pointer, negative size, inconsistent shapes */
   QSA_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / head count / size the library does not build */
   QSA_ERR_MISALIGNED = 3,    /* pointer or stride not 16-byte aligned */
-  QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result
-                                (no current kernel needs scratch; kept for the ABI) */
+  QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result */
   QSA_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
 } qsa_status;
 
@@ -113,7 +112,7 @@ typedef struct qsa_attn_config {
   qsa_dtype kv_dtype;        /* dtype of every segment's K and V */
   qsa_dtype out_dtype;       /* dtype of out */
   float scale;               /* logit scale; 0 means 1/sqrt(head_dim) */
-  int32_t n_splits;          /* splits of each row's selected rows, <= 16; 0 = library's choice */
+  int32_t n_splits;          /* splits of each row's selected rows, <= 256; 0 = library's choice */
 } qsa_attn_config;
 
 /* Human-readable name of a status code (static storage). */
@@ -187,10 +186,13 @@ qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* sco
                            size_t workspace_bytes, void* stream);
 
 /*
- * Scratch bytes qsa_sparse_attn needs.  The splits of one (row, KV group) run
- * as one thread-block cluster and merge their partials through distributed
- * shared memory, so the current kernels return 0.  sel_ld is the row stride
- * of sel (the top_k used for selection).
+ * Scratch bytes qsa_sparse_attn needs for this call.  The splits of one
+ * (row, KV group) run as thread-block clusters of up to 8 (16 when forced)
+ * CTAs and merge inside a cluster through distributed shared memory; when a
+ * (row, KV group) spans several clusters, each cluster leaves a merged
+ * partial in the workspace and the last one to finish merges them.  Returns 0
+ * when one cluster per (row, KV group) suffices.  sel_ld is the row stride of
+ * sel (the top_k used for selection).
  */
 size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
                                int32_t sel_ld);
@@ -216,10 +218,12 @@ size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_at
  *   out            device [rows, Hq, head_dim], cfg->out_dtype
  *   lse            device [rows, Hq] f32 (natural log); may be NULL
  *   workspace      device scratch of >= qsa_attn_workspace_size bytes (may be
- *                  NULL when that size is 0)
- * Each row's selected list is cut into cfg->n_splits splits (at most 16; 0 =
- * library's choice); the splits of one (row, KV group) form one cluster and
- * are merged there by the log-sum-exp rule of qsa_lse_merge.
+ *                  NULL when that size is 0).  It must be zero-filled before
+ *                  its first use; every call leaves it zero-filled again.  Two
+ *                  calls that share a workspace must not run concurrently.
+ * Each row's selected list is cut into splits (cfg->n_splits, at most 256;
+ * 0 = library's choice); splits merge by the log-sum-exp rule of
+ * qsa_lse_merge, inside their cluster and then across clusters.
  * Supported: head_dim 128 or 256; q and K/V both bf16 or both f32;
  * Hq / Hkv <= 16.
  */

@@ -222,7 +222,7 @@ def sparse_attn(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out
         cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
     need = lib().qsa_attn_workspace_size(arr, len(arr), ctypes.byref(cfg), sel.stride(0))
     if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)   # zero-filled before first use
     _check("qsa_sparse_attn", lib().qsa_sparse_attn(
         arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
         out.data_ptr(), _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -276,7 +276,9 @@ class LayerStep:
         self.lse = torch.empty((rows, q.shape[1]), dtype=torch.float32, device=dev)
         sel_ws = int(lib().qsa_select_workspace_size(self.arr, len(self.arr), self.top_k))
         attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
-        self.ws = torch.empty(max(sel_ws, attn_ws, 16), dtype=torch.uint8, device=dev)
+        # Workspaces start zero-filled; the library returns them zero-filled.
+        self.sel_ws = torch.zeros(max(sel_ws, 16), dtype=torch.uint8, device=dev)
+        self.ws = torch.zeros(max(attn_ws, 16), dtype=torch.uint8, device=dev)
         # Blocks completed by each sequence's new rows: [first, last] of nb(p) over its rows.
         self.pool_jobs = []
         for s in self.seqs:
@@ -295,7 +297,7 @@ class LayerStep:
         score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr)
 
     def select(self, stream=None):
-        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, self.ws, stream, seq_array=self.arr)
+        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, self.sel_ws, stream, seq_array=self.arr)
 
     def attend(self, stream=None):
         sparse_attn(None, self.q, self.sel, self.cnt, self.out, self.lse, workspace=self.ws, stream=stream,

@@ -308,11 +308,6 @@ QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const fl
 // ------------------------------------------------------------------ step 4
 namespace {
 
-struct SplitPlan {
-  int32_t n_splits;
-  int32_t split_tokens;
-};
-
 // Longest selected list any row of the call can have: 4 tokens per listed
 // block (at most min(sel_ld, visible blocks)) plus up to 3 tail tokens.
 int64_t max_list(const qsa_seq* seqs, int32_t n_seqs, int32_t sel_ld) {
@@ -321,27 +316,13 @@ int64_t max_list(const qsa_seq* seqs, int32_t n_seqs, int32_t sel_ld) {
   return m;
 }
 
-// Splits per (row, KV group) -- one thread-block cluster -- aiming at about
-// two CTAs per SM, each split at least 32 selected rows long.
-SplitPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, int32_t sel_ld,
-                      int64_t rows) {
-  const int64_t n_list = max_list(seqs, n_seqs, sel_ld);
-  const int64_t pairs = rows * cfg->n_kv_heads;
-  const int64_t sms = device_sm_count();
-  int64_t n = cfg->n_splits;
-  if (n <= 0) n = (2 * sms + pairs - 1) / pairs;
-  n = std::max<int64_t>(1, std::min<int64_t>(n, (n_list + 31) / 32));
-  n = std::min<int64_t>(n, attn_max_splits(cfg->kv_dtype, cfg->head_dim));
-  const int64_t per = (n_list + n - 1) / n;
-  n = (n_list + per - 1) / per;
-  return SplitPlan{(int32_t)n, (int32_t)per};
+AttnPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, int32_t sel_ld, int64_t rows) {
+  return attn_plan(cfg->kv_dtype, cfg->head_dim, rows * cfg->n_kv_heads, max_list(seqs, n_seqs, sel_ld),
+                   cfg->n_splits);
 }
 
-size_t attn_ws_bytes(const SplitPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
-  (void)sp;
-  (void)rows;
-  (void)cfg;
-  return 0;  // splits merge inside their cluster: no scratch
+size_t attn_ws_bytes(const AttnPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
+  return attn_workspace_bytes(sp, rows * cfg->n_kv_heads, cfg->n_q_heads / cfg->n_kv_heads, cfg->head_dim);
 }
 
 qsa_status check_attn_config(const qsa_attn_config* cfg, const char* fn) {
@@ -389,8 +370,8 @@ qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_co
 
 template <int NSEQ>
 qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_attn_config* cfg, const void* q,
-                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const SplitPlan& sp, void* out,
-                      float* lse, cudaStream_t st) {
+                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const AttnPlan& sp, void* out,
+                      float* lse, uint32_t* counters, float* part_lse, float* part_o, cudaStream_t st) {
   AttnParams<NSEQ> p{};
   int rows = 0, nseg = 0;
   p.row_base = row_begin;
@@ -422,12 +403,16 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.group = cfg->n_q_heads / cfg->n_kv_heads;
   p.head_dim = cfg->head_dim;
   p.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
-  p.n_splits = sp.n_splits;
+  p.cluster_size = sp.cluster_size;
+  p.n_clusters = sp.n_clusters;
   p.split_tokens = sp.split_tokens;
+  p.counters = counters;
+  p.part_lse = part_lse;
+  p.part_o = part_o;
   p.out = out;
   p.lse = lse;
   p.out_dtype = cfg->out_dtype;
-  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, st);
+  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, sp.stages, st);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn");
   return QSA_OK;
 }
@@ -453,20 +438,27 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
   if (!q || !sel || !cnt || !out) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (!aligned16(q) || !aligned16(out)) return fail(QSA_ERR_MISALIGNED, "%s: q/out not 16-byte aligned", fn);
   if ((s = check_segments(seqs, n_seqs, cfg, fn)) != QSA_OK) return s;
-  const SplitPlan sp = plan_splits(seqs, n_seqs, cfg, sel_ld, rows);
+  const AttnPlan sp = plan_splits(seqs, n_seqs, cfg, sel_ld, rows);
   const size_t need = attn_ws_bytes(sp, rows, cfg);
   if (need > 0 && (!workspace || workspace_bytes < need))
     return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? workspace_bytes : (size_t)0);
   if (need > 0 && !aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
+  uint32_t* counters = nullptr;
+  float* part_lse = nullptr;
+  float* part_o = nullptr;
+  if (need > 0)
+    attn_workspace_layout(sp, rows * cfg->n_kv_heads, cfg->n_q_heads / cfg->n_kv_heads, workspace, &counters,
+                          &part_lse, &part_o);
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, out, lse, st);
+    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, out, lse, counters, part_lse, part_o, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, out, lse, st);
+      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, out, lse, counters,
+                                  part_lse, part_o, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }

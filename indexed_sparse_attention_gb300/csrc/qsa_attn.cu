@@ -20,6 +20,10 @@
 #include <cooperative_groups.h>
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
 #include "qsa_internal.cuh"
 
 namespace cg = cooperative_groups;
@@ -63,15 +67,26 @@ __device__ __forceinline__ RowCtx make_row_ctx(const AttnParams<NSEQ>& p, int r)
   return c;
 }
 
+// The block ids a split needs, staged in shared memory once: entries
+// [blk0, blk0 + n) of the row's selection (n <= kIdCache).
+constexpr int kIdCache = 512;
+
+struct IdCache {
+  const int32_t* ids;   // shared memory
+  int64_t blk0;
+  int n;
+};
+
 // Entry i of the row's selected list -> element offset of (KV head g, token)
 // in its segment, and the segment.  False when the entry names an invalid
 // block id or a token no segment covers.
 template <int NSEQ>
-__device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& c, int64_t i, int g,
-                                       int& seg, int64_t& off) {
+__device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& c, const IdCache& ic, int64_t i,
+                                       int g, int& seg, int64_t& off) {
   int64_t t;
   if (i < 4 * (int64_t)c.cnt) {
-    const int32_t b = __ldg(c.sel_row + (i >> 2));
+    const int64_t k = (i >> 2) - ic.blk0;
+    const int32_t b = (k >= 0 && k < ic.n) ? ic.ids[k] : __ldg(c.sel_row + (i >> 2));
     if (b < 0 || (int64_t)b >= c.nb) return false;
     t = 4 * (int64_t)b + (i & 3);
   } else {
@@ -86,6 +101,19 @@ __device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& 
     }
   }
   return false;
+}
+
+// Stage the ids of list entries [i0, i1) into ids_s (all threads call).
+__device__ __forceinline__ IdCache stage_ids(const RowCtx& c, int64_t i0, int64_t i1, int32_t* ids_s) {
+  IdCache ic;
+  ic.ids = ids_s;
+  ic.blk0 = i0 >> 2;
+  const int64_t last = min(i1, 4 * (int64_t)c.cnt);   // entries past 4*cnt are tail tokens
+  int64_t n = last > i0 ? ((last - 1) >> 2) - ic.blk0 + 1 : 0;
+  if (n > kIdCache) n = kIdCache;
+  ic.n = (int)n;
+  for (int k = threadIdx.x; k < ic.n; k += blockDim.x) ids_s[k] = __ldg(c.sel_row + ic.blk0 + k);
+  return ic;
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -132,31 +160,41 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// ------------------------------------------------------------------ split merge (step 5, in-cluster)
-// Each CTA of a cluster holds the partial of one split of the same (row, KV
-// group): unnormalised output o_s[16][D] (fp32), running max m_s[16] of the
-// base-2 logits and running sum l_s[16].  After a cluster barrier, CTA c
-// merges the 4-channel groups c, c+S, ... of every head across the cluster
-// through
-// distributed shared memory:
+// ------------------------------------------------------------------ split merge (step 5)
+// The CTAs of one cluster hold the partials of consecutive splits of the same
+// (row, KV group): unnormalised output o_s[16][D] (fp32), running max m_s[16]
+// of the base-2 logits and running sum l_s[16].  After a cluster barrier,
+// CTA c merges the 4-channel groups c, c+CS, ... of every head across the
+// cluster through distributed shared memory:
 //   M = max_q m_q,  w_q = 2^(m_q - M),  out = sum_q w_q o_q / sum_q w_q l_q,
 //   lse = (M + log2 sum_q w_q l_q) * ln 2,
 // and a head whose splits saw no key gets out = 0 and lse = -inf.
+// With several clusters per (row, KV group), each cluster writes its merged,
+// normalised partial and lse to the workspace; the cluster that takes the
+// last ticket merges all of them by the same rule (natural-log lse) and
+// returns the ticket counter to zero.
+constexpr int kMaxClusters = 32;   // clusters per (row, KV group)
+
 struct MergeSmem {
   float mq[16][kMaxSplits];
   float lq[16][kMaxSplits];
   float w[16][kMaxSplits];
   float inv[16];
   float lse[16];
+  float cw[16][kMaxClusters];
+  float cinv[16];
+  float clse[16];
+  int last;
 };
 
 template <int NSEQ>
-__device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, int D, float* o_s, float* m_s,
+__device__ void merge_store(const AttnParams<NSEQ>& p, int r, int g, int G, int D, float* o_s, float* m_s,
                             float* l_s, MergeSmem* ms) {
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)cluster.num_blocks();
   const int c = (int)cluster.block_rank();
   const int tid = threadIdx.x, nt = blockDim.x;
+  const int head0 = g * G;
   cluster.sync();
   // Every split's running max and sum, one (head, split) pair per thread.
   for (int t = tid; t < G * S; t += nt) {
@@ -179,6 +217,9 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
     ms->lse[tid] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
   }
   __syncthreads();
+  const int NC = p.n_clusters;
+  const int64_t pair = (int64_t)r * (p.n_q_heads / G) + g;
+  const int64_t cid = blockIdx.x / S;
   // 4-channel groups c, c + S, c + 2S, ... of every head belong to this CTA
   // (any S <= 16; D / 4 >= 32 groups, so every CTA has at least one).
   const int nq = (D / 4 - c + S - 1) / S;
@@ -201,6 +242,77 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
       }
     }
     const float inv = ms->inv[h];
+    const float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (NC > 1) {
+      *reinterpret_cast<float4*>(p.part_o + ((pair * NC + cid) * G + h) * D + d) = res;
+    } else {
+      const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
+      if (p.out_dtype == QSA_F32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = res;
+      } else {
+        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
+        o2[0] = __floats2bfloat162_rn(res.x, res.y);
+        o2[1] = __floats2bfloat162_rn(res.z, res.w);
+      }
+    }
+  }
+  if (NC == 1) {
+    if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->lse[tid];
+    cluster.sync();  // keep this CTA's partial alive until every peer has read it
+    return;
+  }
+  if (c == 0 && tid < G) p.part_lse[(pair * NC + cid) * G + tid] = ms->lse[tid];
+  __threadfence();
+  cluster.sync();    // this cluster's partial is written; peers are done reading o_s
+  if (c == 0 && tid == 0) {
+    const unsigned t = atomicAdd(p.counters + pair, 1u);
+    const int last = t == (unsigned)(NC - 1);
+    if (last) p.counters[pair] = 0u;   // every ticket is taken: ready for the next call
+    for (int q = 0; q < S; ++q) cluster.map_shared_rank(ms, q)->last = last;
+  }
+  cluster.sync();
+  if (!ms->last) return;
+  __threadfence();
+  // The last cluster merges the clusters' partials (natural-log lse).
+  for (int t = tid; t < G * NC; t += nt) {
+    const int h = t / NC, q = t % NC;
+    ms->cw[h][q] = __ldcg(p.part_lse + (pair * NC + q) * G + h);
+  }
+  __syncthreads();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int q = 0; q < NC; ++q) M = fmaxf(M, ms->cw[tid][q]);
+    float Wsum = 0.f;
+    for (int q = 0; q < NC; ++q) {
+      const float lq = ms->cw[tid][q];
+      const float w = lq == -INFINITY ? 0.f : expf(lq - M);
+      ms->cw[tid][q] = w;
+      Wsum += w;
+    }
+    ms->cinv[tid] = Wsum > 0.f ? 1.f / Wsum : 0.f;
+    ms->clse[tid] = Wsum > 0.f ? M + logf(Wsum) : -INFINITY;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * nq; idx += nt) {
+    const int h = idx / nq;
+    const int d = 4 * (c + (idx % nq) * S);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < NC; q0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = q0 + j < NC ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((pair * NC + q0 + j) * G + h) * D + d))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = q0 + j < NC ? ms->cw[h][q0 + j] : 0.f;
+        acc.x = fmaf(w, v[j].x, acc.x);
+        acc.y = fmaf(w, v[j].y, acc.y);
+        acc.z = fmaf(w, v[j].z, acc.z);
+        acc.w = fmaf(w, v[j].w, acc.w);
+      }
+    }
+    const float inv = ms->cinv[h];
     const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
     if (p.out_dtype == QSA_F32) {
       *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) =
@@ -211,8 +323,7 @@ __device__ void merge_store(const AttnParams<NSEQ>& p, int r, int head0, int G, 
       o2[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     }
   }
-  if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->lse[tid];
-  cluster.sync();  // keep this CTA's partial alive until every peer has read it
+  if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->clse[tid];
 }
 
 // ------------------------------------------------------------------ tensor-pipe kernel (bf16 K/V)
@@ -225,9 +336,8 @@ constexpr int kPStride = 40;   // bf16 per P row: 80-byte rows keep ldmatrix con
 constexpr int kSStride = kTT + 4;
 constexpr int kAttnThreads = 256;
 
-template <int D>
+template <int D, int STAGES>
 struct MmaSmem {
-  static constexpr int STAGES = D == 256 ? 2 : 4;     // two CTAs per SM either way
   static constexpr int CH = D / 8;                     // 16-byte chunks per K/V/Q row
   static constexpr size_t q = 16 * D * 2;
   static constexpr size_t kv_tile = kTT * D * 2;       // one K or V tile
@@ -238,15 +348,19 @@ struct MmaSmem {
   static constexpr size_t off_p = off_s + s;
   static constexpr size_t off_m = off_p + pm;          // m, l, alpha: 3 x 16 floats
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
-  static constexpr size_t off_merge = off_valid + STAGES * kTT * 4;
-  static constexpr size_t bytes = off_merge + sizeof(MergeSmem);
-  static_assert(16 * D * 4 <= STAGES * 2 * kv_tile, "merge partial must fit the K/V stages");
+  static constexpr size_t off_ids = off_valid + STAGES * kTT * 4;
+  static constexpr size_t bytes = off_ids + kIdCache * 4;
+  // After the token loop the K/V stages hold the partial [16][D] fp32 and the
+  // merge scratch.
+  static constexpr size_t off_merge = off_kv + 16 * D * 4;
+  static_assert(16 * D * 4 + sizeof(MergeSmem) <= STAGES * 2 * kv_tile, "merge data must fit the K/V stages");
+  // Three stages keep two CTAs per SM (228 KB per SM, 1 KB reserved per CTA).
+  static_assert(STAGES != 3 || 2 * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
-template <int D, int NSEQ>
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnParams<NSEQ> p) {
-  using L = MmaSmem<D>;
-  constexpr int STAGES = L::STAGES;
+template <int D, int STAGES, int NSEQ>
+__global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_kernel(const AttnParams<NSEQ> p) {
+  using L = MmaSmem<D, STAGES>;
   constexpr int CH = L::CH;
   constexpr int KH = D / 32;   // k-steps (16 channels each) per channel half
   constexpr int NTD = D / 64;  // 8-channel n-tiles per warp in P.V
@@ -259,7 +373,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
   float* l_s = m_s + 16;
   float* a_s = m_s + 32;
   int* valid_s = reinterpret_cast<int*>(smem + L::off_valid);
+  int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L::off_ids);
   MergeSmem* msm = reinterpret_cast<MergeSmem*>(smem + L::off_merge);
+  grid_dependency_sync();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quarter = warp & 3, half = warp >> 2;
@@ -271,6 +387,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
   const int n_tiles = i1 > i0 ? (int)((i1 - i0 + kTT - 1) / kTT) : 0;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
 
+  // Q of the group's heads, read while the split's block ids are staged.
+  uint4 qv[(16 * CH + kAttnThreads - 1) / kAttnThreads];
+#pragma unroll
+  for (int k = 0; k < (16 * CH + kAttnThreads - 1) / kAttnThreads; ++k) {
+    const int idx = tid + k * kAttnThreads;
+    const int row = idx / CH, ch = idx % CH;
+    qv[k] = make_uint4(0u, 0u, 0u, 0u);
+    if (idx < 16 * CH && row < G) qv[k] = *reinterpret_cast<const uint4*>(qg + (int64_t)row * D + ch * 8);
+  }
+  const IdCache ic = stage_ids(c, i0, i1, ids_s);
+  __syncthreads();
+
   // Gather of one tile into a stage: thread -> token slot tid/8, chunks (tid&7) + 8j,
   // swizzled: chunk c of token row t lands at c ^ (t & 7).
   auto load_tile = [&](int it, int stage) {
@@ -278,14 +406,15 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
     const int64_t i = i0 + (int64_t)it * kTT + tk;
     int seg = 0;
     int64_t off = 0;
-    const bool ok = i < i1 && locate(p, c, i, g, seg, off);
+    const bool ok = i < i1 && locate(p, c, ic, i, g, seg, off);
     const __nv_bfloat16* ks = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].k) + off : qg;
     const __nv_bfloat16* vs = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].v) + off : qg;
     __nv_bfloat16* kd = kv_s + (size_t)stage * 2 * kTT * D + tk * D;
     __nv_bfloat16* vd = kd + kTT * D;
+    // The four tokens of a warp write different 128-byte segments (bank-conflict free).
 #pragma unroll
     for (int j = 0; j < CH / 8; ++j) {
-      const int ch = q8 + 8 * j;
+      const int ch = 8 * ((j + tk) % (CH / 8)) + q8;
       const int pc = ch ^ (tk & 7);
       cp_async16(kd + pc * 8, ks + (ok ? ch * 8 : 0), ok);
       cp_async16(vd + pc * 8, vs + (ok ? ch * 8 : 0), ok);
@@ -301,11 +430,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
   }
 
   // Q of the group's heads (rows >= G zero), swizzled like the K/V tiles.
-  for (int idx = tid; idx < 16 * CH; idx += kAttnThreads) {
+#pragma unroll
+  for (int k = 0; k < (16 * CH + kAttnThreads - 1) / kAttnThreads; ++k) {
+    const int idx = tid + k * kAttnThreads;
     const int row = idx / CH, ch = idx % CH;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (row < G) v = *reinterpret_cast<const uint4*>(qg + (int64_t)row * D + ch * 8);
-    *reinterpret_cast<uint4*>(q_s + (row * CH + (ch ^ (row & 7))) * 8) = v;
+    if (idx < 16 * CH) *reinterpret_cast<uint4*>(q_s + (row * CH + (ch ^ (row & 7))) * 8) = qv[k];
   }
   for (int idx = tid; idx < 16 * kPStride; idx += kAttnThreads) p_s[idx] = __float2bfloat16(0.f);
   if (tid < 16) {
@@ -328,10 +457,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
   const float zscale = p.scale * kLog2e;
   const int gq = lane >> 2, t4 = lane & 3;
 
+  // Commit groups: tile t < STAGES is group t (prologue); iteration j >= 1
+  // commits group STAGES + j - 1 holding tile STAGES + j - 1.  So tile t is
+  // group t, and at the top of iteration it the groups after it that may
+  // still be pending number STAGES - 1 (it = 0) or STAGES - 2 (it >= 1).
   for (int it = 0; it < n_tiles; ++it) {
     const int stage = it % STAGES;
-    cp_async_wait<STAGES - 1>();
+    if (it == 0) cp_async_wait<STAGES - 1>();
+    else cp_async_wait<STAGES - 2>();
     __syncthreads();
+    // Every thread is past tile it-1: its stage takes tile it-1+STAGES.
+    if (it >= 1) {
+      if (it - 1 + STAGES < n_tiles) load_tile(it - 1 + STAGES, (it - 1) % STAGES);
+      cp_async_commit();
+    }
     const __nv_bfloat16* kt = kv_s + (size_t)stage * 2 * kTT * D;
     const __nv_bfloat16* vt = kt + kTT * D;
     // Partial logits of tokens 8*quarter.. over this warp's channel half, two chains.
@@ -430,9 +569,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
         }
       }
     }
-    __syncthreads();
-    if (it + STAGES < n_tiles) load_tile(it + STAGES, stage);
-    cp_async_commit();
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -448,7 +584,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_mma_kernel(const AttnPar
       *reinterpret_cast<float2*>(o_s + row * D + d) = make_float2(o[j][2 * hf], o[j][2 * hf + 1]);
     }
   }
-  merge_store(p, r, head0, G, D, o_s, m_s, l_s, msm);
+  merge_store(p, r, g, G, D, o_s, m_s, l_s, msm);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel (fp32 K/V)
@@ -462,7 +598,7 @@ struct SimtSmem {
   static constexpr size_t v = kSimtTT * D;
   static constexpr size_t z = 16 * 33;
   static constexpr size_t floats = q + k + v + z + 3 * 16;
-  static constexpr size_t bytes = floats * 4 + kSimtTT * 4 + sizeof(MergeSmem);
+  static constexpr size_t bytes = floats * 4 + kSimtTT * 4 + kIdCache * 4 + sizeof(MergeSmem);
   static_assert(16 * D <= k + v, "merge partial must fit the K/V tiles");
 };
 
@@ -480,7 +616,9 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
   float* l_s = m_s + 16;
   float* a_s = l_s + 16;
   int* ok_s = reinterpret_cast<int*>(a_s + 16);
-  MergeSmem* msm = reinterpret_cast<MergeSmem*>(ok_s + kSimtTT);
+  int32_t* ids_s = ok_s + kSimtTT;
+  MergeSmem* msm = reinterpret_cast<MergeSmem*>(ids_s + kIdCache);
+  grid_dependency_sync();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
@@ -489,6 +627,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
   const int64_t i0 = (int64_t)split * p.split_tokens;
   const int64_t i1 = min(c.n_list, i0 + p.split_tokens);
   const float zscale = p.scale * kLog2e;
+  const IdCache ic = stage_ids(c, i0, i1, ids_s);
 
   const float* qg = static_cast<const float*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
   for (int idx = tid; idx < G * D; idx += 256) q_s[idx] = qg[idx];
@@ -507,7 +646,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
     for (int tk = warp; tk < kSimtTT; tk += 8) {
       int seg = 0;
       int64_t off = 0;
-      const bool ok = tk < nt && locate(p, c, base + tk, g, seg, off);
+      const bool ok = tk < nt && locate(p, c, ic, base + tk, g, seg, off);
       const float* ks = ok ? static_cast<const float*>(p.seg[seg].k) + off : nullptr;
       const float* vs = ok ? static_cast<const float*>(p.seg[seg].v) + off : nullptr;
       for (int dd = lane; dd < D; dd += 32) {
@@ -556,7 +695,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
     const int hh = hs + j * HS;
     if (hh < 16) o_s[hh * D + d] = hh < G ? acc[j] : 0.f;
   }
-  merge_store(p, r, head0, G, D, o_s, m_s, l_s, msm);
+  merge_store(p, r, g, G, D, o_s, m_s, l_s, msm);
 }
 
 
@@ -567,6 +706,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
                                                      const float* __restrict__ lse_parts, int n_parts,
                                                      int64_t n_rows, int head_dim, void* __restrict__ out,
                                                      int out_dtype, float* __restrict__ lse_out) {
+  grid_dependency_sync();
   const int q = head_dim / 4;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_rows * q) return;
@@ -622,70 +762,163 @@ cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_row
                                cudaStream_t st) {
   cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);
   if (e != cudaSuccess) return e;
-  const int S = p.n_splits;
-  if (S > 8) {
+  const int cs = p.cluster_size;
+  if (cs > 8) {
     e = allow_cluster16((const void*)kernel, threads, smem);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)S, (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows);
-  cfg.blockDim = dim3((unsigned)threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, p);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_kernel(kernel, dim3((unsigned)(cs * p.n_clusters), (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows),
+                       dim3((unsigned)threads), smem, st, (unsigned)cs, p);
 }
 
 }  // namespace
 
-int attn_max_splits(qsa_dtype kv_dtype, int head_dim) {
-  const void* k;
-  size_t smem;
+// The kernel variant a plan runs, with its block size and shared memory.
+struct AttnVariant {
+  const void* fn;
   int threads;
+  size_t smem;
+};
+
+static AttnVariant attn_variant(qsa_dtype kv_dtype, int head_dim, int stages) {
   if (kv_dtype == QSA_BF16) {
-    threads = kAttnThreads;
-    k = head_dim == 256 ? (const void*)attn_mma_kernel<256, 1> : (const void*)attn_mma_kernel<128, 1>;
-    smem = head_dim == 256 ? MmaSmem<256>::bytes : MmaSmem<128>::bytes;
-  } else {
-    threads = 256;
-    k = head_dim == 256 ? (const void*)attn_simt_kernel<256, 1> : (const void*)attn_simt_kernel<128, 1>;
-    smem = head_dim == 256 ? SimtSmem<256>::bytes : SimtSmem<128>::bytes;
+    if (head_dim == 256)
+      return stages == 5 ? AttnVariant{(const void*)attn_mma_kernel<256, 5, 1>, kAttnThreads, MmaSmem<256, 5>::bytes}
+                         : AttnVariant{(const void*)attn_mma_kernel<256, 3, 1>, kAttnThreads, MmaSmem<256, 3>::bytes};
+    return stages == 5 ? AttnVariant{(const void*)attn_mma_kernel<128, 5, 1>, kAttnThreads, MmaSmem<128, 5>::bytes}
+                       : AttnVariant{(const void*)attn_mma_kernel<128, 3, 1>, kAttnThreads, MmaSmem<128, 3>::bytes};
   }
-  if (allow_dynamic_smem(k, smem) != cudaSuccess) return 8;
-  return allow_cluster16(k, threads, smem) == cudaSuccess ? kMaxSplits : 8;
+  return head_dim == 256 ? AttnVariant{(const void*)attn_simt_kernel<256, 1>, 256, SimtSmem<256>::bytes}
+                         : AttnVariant{(const void*)attn_simt_kernel<128, 1>, 256, SimtSmem<128>::bytes};
+}
+
+// Clusters of `cs` CTAs of this variant that can be resident at once.
+static int max_active_clusters(const AttnVariant& v, int cs) {
+  struct Entry {
+    int dev;
+    const void* fn;
+    int cs;
+    int n;
+  };
+  static std::vector<Entry> cache;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const Entry& e : cache)
+    if (e.dev == dev && e.fn == v.fn && e.cs == cs) return e.n;
+  int n = 0;
+  if (allow_dynamic_smem(v.fn, v.smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cs, 1, 1);
+    cfg.blockDim = dim3((unsigned)v.threads, 1, 1);
+    cfg.dynamicSmemBytes = v.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, v.fn, &cfg) != cudaSuccess) n = 0;
+  }
+  cache.push_back(Entry{dev, v.fn, cs, n});
+  return n;
+}
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Splits of each (row, KV group): `total` CTAs in n_clusters clusters of
+// cluster_size, each split at most 5 tiles of 32 selected rows when the GPU
+// has room for one CTA per SM, all of them resident at once.
+AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_list, int user_splits) {
+  const int64_t sms = device_sm_count();
+  const int64_t max_total = std::min<int64_t>(ceil_div(n_list, kTT), (int64_t)kMaxSplits * kMaxClusters);
+  int64_t total;
+  if (user_splits > 0) {
+    total = std::min<int64_t>(user_splits, max_total);
+  } else {
+    total = std::max<int64_t>(1, sms / pairs);
+    if (ceil_div(ceil_div(n_list, std::min(total, max_total)), kTT) > 5) total = std::max<int64_t>(1, 2 * sms / pairs);
+    total = std::min(total, max_total);
+    // Fewer CTAs when that keeps the tiles per CTA.
+    const int64_t tiles = ceil_div(ceil_div(n_list, total), kTT);
+    while (total > 1 && ceil_div(ceil_div(n_list, total - 1), kTT) == tiles) --total;
+  }
+  total = std::max<int64_t>(1, total);
+  const int64_t tiles = ceil_div(ceil_div(n_list, total), kTT);
+  const int stages = (tiles <= 5 && pairs * total <= sms) ? 5 : 3;
+  const AttnVariant v = attn_variant(kv_dtype, head_dim, stages);
+  AttnPlan best{1, 1, (int32_t)n_list, stages};
+  bool found = false;
+  // Cluster sizes to try, largest first: min(total, 8), then 6, 4, 3, 2, 1.
+  const int first = (int)std::min<int64_t>(total, 8);
+  const int sizes[6] = {first, 6, 4, 3, 2, 1};
+  for (int k = 0; k < 6; ++k) {
+    const int cs = sizes[k];
+    if (k > 0 && cs >= first) continue;
+    const int64_t nc = ceil_div(total, cs);
+    if (nc > kMaxClusters) continue;
+    const int64_t cs_b = ceil_div(total, nc);           // balance the clusters
+    const int active = max_active_clusters(v, (int)cs_b);
+    if (user_splits <= 0 && active > 0 && pairs * nc > active) continue;   // keep every cluster resident
+    best = AttnPlan{(int32_t)cs_b, (int32_t)nc, (int32_t)ceil_div(n_list, cs_b * nc), stages};
+    found = true;
+    break;
+  }
+  if (!found) {
+    const int64_t cs = std::min<int64_t>(total, 8);
+    const int64_t nc = std::min<int64_t>(ceil_div(total, cs), kMaxClusters);
+    best = AttnPlan{(int32_t)cs, (int32_t)nc, (int32_t)ceil_div(n_list, cs * nc), stages};
+  }
+  return best;
+}
+
+size_t attn_workspace_bytes(const AttnPlan& pl, int64_t pairs, int group, int head_dim) {
+  if (pl.n_clusters <= 1) return 0;
+  const size_t parts = (size_t)pairs * pl.n_clusters * group;
+  return 256 * ceil_div(pairs * 4, 256) + 256 * ceil_div((int64_t)parts * 4, 256) + parts * head_dim * 4;
+}
+
+void attn_workspace_layout(const AttnPlan& pl, int64_t pairs, int group, void* ws, uint32_t** counters,
+                           float** part_lse, float** part_o) {
+  char* b = static_cast<char*>(ws);
+  const size_t parts = (size_t)pairs * pl.n_clusters * group;
+  *counters = reinterpret_cast<uint32_t*>(b);
+  b += 256 * ceil_div(pairs * 4, 256);
+  *part_lse = reinterpret_cast<float*>(b);
+  b += 256 * ceil_div((int64_t)parts * 4, 256);
+  *part_o = reinterpret_cast<float*>(b);
 }
 
 template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st) {
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
   if (kv_dtype == QSA_BF16) {
-    if (p.head_dim == 256)
-      return launch_attn_kernel(attn_mma_kernel<256, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256>::bytes, st);
-    return launch_attn_kernel(attn_mma_kernel<128, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128>::bytes, st);
+    if (p.head_dim == 256) {
+      if (stages == 5)
+        return launch_attn_kernel(attn_mma_kernel<256, 5, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256, 5>::bytes, st);
+      return launch_attn_kernel(attn_mma_kernel<256, 3, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256, 3>::bytes, st);
+    }
+    if (stages == 5)
+      return launch_attn_kernel(attn_mma_kernel<128, 5, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128, 5>::bytes, st);
+    return launch_attn_kernel(attn_mma_kernel<128, 3, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128, 3>::bytes, st);
   }
   if (p.head_dim == 256)
     return launch_attn_kernel(attn_simt_kernel<256, NSEQ>, p, n_rows, 256, SimtSmem<256>::bytes, st);
   return launch_attn_kernel(attn_simt_kernel<128, NSEQ>, p, n_rows, 256, SimtSmem<128>::bytes, st);
 }
 
-template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, cudaStream_t);
-template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, cudaStream_t);
+template cudaError_t launch_attn<1>(const AttnParams<1>&, int, qsa_dtype, int, cudaStream_t);
+template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, qsa_dtype, int, cudaStream_t);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows, int head_dim,
                          void* out, int out_dtype, float* lse_out, cudaStream_t st) {
   const int64_t threads = n_rows * (head_dim / 4);
   if (threads == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((threads + 255) / 256);
-  merge_kernel<<<grid, 256, 0, st>>>(o_parts, lse_parts, n_parts, n_rows, head_dim, out, out_dtype, lse_out);
-  return cudaGetLastError();
+  return launch_kernel(merge_kernel, dim3(grid), dim3(256), 0, st, 0, o_parts, lse_parts, n_parts, n_rows, head_dim,
+                       out, out_dtype, lse_out);
 }
 
 }  // namespace qsa

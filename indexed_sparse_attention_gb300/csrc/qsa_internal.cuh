@@ -91,10 +91,14 @@ struct AttnParams {
   int32_t group;           // query heads per KV head
   int32_t head_dim;
   float scale;             // logit scale
-  int32_t n_splits;        // CTAs (one cluster) per (row, KV group), <= 16
+  int32_t cluster_size;    // CTAs per cluster (splits merged in distributed shared memory)
+  int32_t n_clusters;      // clusters per (row, KV group); > 1 merges through the workspace
   int32_t split_tokens;    // selected-list entries per split
   void* out;               // [rows, Hq, D]
   float* lse;              // [rows, Hq] or null
+  uint32_t* counters;      // [rows * Hkv] tickets, zero between calls (n_clusters > 1)
+  float* part_lse;         // [rows * Hkv, n_clusters, G]
+  float* part_o;           // [rows * Hkv, n_clusters, G, D]
   int32_t out_dtype;
 };
 
@@ -109,11 +113,22 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 
-template <int NSEQ>
-cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, cudaStream_t st);
+struct AttnPlan {
+  int32_t cluster_size;
+  int32_t n_clusters;
+  int32_t split_tokens;
+  int32_t stages;
+};
 
-// Largest split count (cluster size) the attention kernel can launch with.
-int attn_max_splits(qsa_dtype kv_dtype, int head_dim);
+// Split plan for pairs = rows * Hkv (row, KV group) pairs whose selected lists
+// are at most n_list entries; user_splits > 0 fixes the splits per pair.
+AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_list, int user_splits);
+size_t attn_workspace_bytes(const AttnPlan& pl, int64_t pairs, int group, int head_dim);
+void attn_workspace_layout(const AttnPlan& pl, int64_t pairs, int group, void* ws, uint32_t** counters,
+                           float** part_lse, float** part_o);
+
+template <int NSEQ>
+cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st);
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows,
                          int head_dim, void* out, int out_dtype, float* lse_out, cudaStream_t st);
@@ -130,7 +145,45 @@ cudaError_t allow_cluster16(const void* kernel, int threads, size_t smem);
 // Blocks per scoring work item for the kernel that serves q_dtype.
 int score_tile_blocks(qsa_dtype q_dtype);
 
+// ---------------------------------------------------------------- launches
+// Every kernel is launched with programmatic stream serialization: it may
+// start while its predecessor on the stream finishes, and waits
+// (griddepcontrol.wait) before it touches any memory the predecessor writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // ---------------------------------------------------------------- device helpers
+// Wait until the grids this one depends on have completed and their writes
+// are visible; then let this grid's dependents be scheduled.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

@@ -46,6 +46,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 // ------------------------------------------------------------------ pooling
 __global__ void pool_kernel(const void* __restrict__ idx, int dtype, int64_t tok_stride, int64_t first_block,
                             int64_t n_blocks, float* __restrict__ pooled, int64_t pstride) {
+  grid_dependency_sync();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (block, 4-channel group)
   if (i >= n_blocks * (QSA_INDEX_DIM / 4)) return;
   const int64_t b = first_block + i / (QSA_INDEX_DIM / 4);
@@ -92,7 +93,7 @@ __device__ __forceinline__ int find_seq_by_work(const ScoreParams<NSEQ>& p, int6
 // (2t+8, 2t+9) <- channels (4t+2, 4t+3).  A and B use the same channel
 // permutation, so the dot products are unchanged and each thread reads one
 // float4 per row per k-step.
-constexpr int kScoreWarps = 8;
+constexpr int kScoreWarps = 12;
 constexpr int kScoreStages = 2;
 constexpr int kRowPitch = 144;   // floats per staged row: 576 bytes keep the float4 reads conflict-free
 constexpr int kStageFloats = kScoreTile * kRowPitch;
@@ -129,12 +130,13 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams<NSEQ>& p, int6
   if (!x.valid) return x;
   x.si = find_seq_by_work(p, item);
   const ScoreSeq& sq = p.seq[x.si];
-  const int64_t w = item - sq.work_begin;
-  const int64_t tile = w / sq.n_groups;
-  const int grp = (int)(w - tile * sq.n_groups);
+  // Items of one sequence number < 2^31 (<= 2^14 tiles x groups of 8 rows).
+  const int w = (int)(item - sq.work_begin);
+  const int tile = sq.n_groups == 1 ? w : w / sq.n_groups;
+  const int grp = w - tile * sq.n_groups;
   x.row0 = grp * kRowGroup;
   x.rows = min(kRowGroup, sq.n_rows - x.row0);
-  x.b0 = tile * kScoreTile;
+  x.b0 = (int64_t)tile * kScoreTile;
   x.nb_last = visible_blocks(row_position(sq.n_tokens, sq.n_rows, x.row0 + x.rows - 1));
   x.active = x.b0 < x.nb_last;
   return x;
@@ -143,6 +145,7 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams<NSEQ>& p, int6
 template <int NT, int NSEQ>
 __global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const ScoreParams<NSEQ> p) {
   extern __shared__ float4 score_smem4[];
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   float* my = reinterpret_cast<float*>(score_smem4) + warp * kScoreStages * kStageFloats;
@@ -198,9 +201,12 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const Sc
         bq_row0 = cur.row0;
       }
       const float* a = my + stage * kStageFloats;
-      float acc[NT][4];
+      // One accumulator per bf16 part keeps the MMA dependency chains short.
+      float acc[NT][4], accm[NT][4], accl[NT][4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] = accm[j][e] = accl[j][e] = 0.f;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const float4 ra = *reinterpret_cast<const float4*>(a + g * kRowPitch + 16 * s + 4 * t);
@@ -212,11 +218,15 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const Sc
         split3(rb.z, rb.w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-          mma_bf16(acc[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
-          mma_bf16(acc[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
+          mma_bf16(accl[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
+          mma_bf16(accm[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
           mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
         }
       }
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[j][e] += accm[j][e] + accl[j][e];
       // Epilogue: thread (g, t) holds columns 8j+2t, 8j+2t+1 = heads 2(t&1),
       // 2(t&1)+1 of row 2j + (t>>1); its neighbour t^1 holds the other two.
 #pragma unroll
@@ -255,6 +265,7 @@ template <int NSEQ>
 __global__ void __launch_bounds__(256) score_simt_kernel(const ScoreParams<NSEQ> p) {
   __shared__ float q_s[32][QSA_INDEX_DIM + 1];
   __shared__ float k_s[kSimtTile][QSA_INDEX_DIM + 1];
+  grid_dependency_sync();
   const int64_t item = blockIdx.x;
   if (item >= p.n_work) return;
   const int si = find_seq_by_work(p, item);
@@ -306,8 +317,8 @@ cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64
   const int64_t threads = n_blocks * (QSA_INDEX_DIM / 4);
   const int bs = 256;
   const int64_t grid = (threads + bs - 1) / bs;
-  pool_kernel<<<(unsigned)grid, bs, 0, st>>>(idx, (int)dt, tok_stride, first_block, n_blocks, pooled, pstride);
-  return cudaGetLastError();
+  return launch_kernel(pool_kernel, dim3((unsigned)grid), dim3(bs), 0, st, 0, idx, (int)dt, tok_stride, first_block,
+                       n_blocks, pooled, pstride);
 }
 
 // The work decomposition (tile size) differs between the two kernels; the host
@@ -318,8 +329,7 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
   if (p.n_work == 0) return cudaSuccess;
   if (q_dtype == QSA_F32) {
-    score_simt_kernel<NSEQ><<<(unsigned)p.n_work, 256, 0, st>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0, p);
   }
   const size_t smem = sizeof(float) * kScoreWarps * kScoreStages * kStageFloats;
   const int64_t need = (p.n_work + kScoreWarps - 1) / kScoreWarps;
@@ -329,13 +339,10 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
                                             : (const void*)score_mma_kernel<4, NSEQ>;
   cudaError_t e = allow_dynamic_smem(k, smem);
   if (e != cudaSuccess) return e;
-  if (max_rows_per_group <= 2)
-    score_mma_kernel<1, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
-  else if (max_rows_per_group <= 4)
-    score_mma_kernel<2, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
-  else
-    score_mma_kernel<4, NSEQ><<<grid, kScoreWarps * 32, smem, st>>>(p);
-  return cudaGetLastError();
+  const dim3 block(kScoreWarps * 32);
+  if (max_rows_per_group <= 2) return launch_kernel(score_mma_kernel<1, NSEQ>, dim3(grid), block, smem, st, 0, p);
+  if (max_rows_per_group <= 4) return launch_kernel(score_mma_kernel<2, NSEQ>, dim3(grid), block, smem, st, 0, p);
+  return launch_kernel(score_mma_kernel<4, NSEQ>, dim3(grid), block, smem, st, 0, p);
 }
 
 template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t s_cand;
   cg::cluster_group cluster = cg::this_cluster();
+  grid_dependency_sync();
   const int S = (int)cluster.num_blocks();
   const int c = (int)cluster.block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -185,10 +186,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int i = base + j * kThreads + lane;
-      const bool act = i < i1;
-      const uint32_t key = order_key(v[j]);
-      if (act && cache_keys) keys[i - i0] = key;
-      hist_add(own, act, key >> 20, lane);
+      if (i < i1) {
+        const uint32_t key = order_key(v[j]);
+        if (cache_keys) keys[i - i0] = key;
+        atomicAdd(&own[key >> 20], 1u);
+      }
     }
   }
   cluster.sync();
@@ -385,21 +387,8 @@ cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_n
   smem = select_smem_bytes(chunk, nw_max);
   if ((e = allow_dynamic_smem((const void*)select_kernel<NSEQ>, smem)) != cudaSuccess) return e;
   const int cache_keys = chunk <= kKeyCacheMax ? 1 : 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)S, (unsigned)n_rows, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)S;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, select_kernel<NSEQ>, p, chunk, nw_max, cache_keys);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_kernel(select_kernel<NSEQ>, dim3((unsigned)S, (unsigned)n_rows), dim3(kThreads), smem, st,
+                       (unsigned)S, p, chunk, nw_max, cache_keys);
 }
 
 template cudaError_t launch_select<1>(const SelectParams<1>&, int, int64_t, cudaStream_t);

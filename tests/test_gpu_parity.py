@@ -177,13 +177,41 @@ def _attn_gpu(x, sel, cnt, *, segments=None, out_dtype=torch.float32, n_splits=0
 
 @pytest.mark.parametrize("dtype,D", [(torch.float32, 256), (torch.bfloat16, 256), (torch.float32, 128),
                                      (torch.bfloat16, 128)])
-@pytest.mark.parametrize("n_splits", [0, 1, 3])
+@pytest.mark.parametrize("n_splits", [0, 1, 3, 16, 40])
 def test_attention_matches_oracle(dtype, D, n_splits):
     x = make_layer(L=4099, M=4, dtype=dtype, seed=3, head_dim=D)
     sel, cnt, _ = _oracle_selection(x)
     out, lse = _attn_gpu(x, sel, cnt, n_splits=n_splits)
     ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
     assert_attn_close(out, lse, ref_out, ref_lse, dtype == torch.bfloat16)
+
+
+def test_attention_multi_cluster_workspace_returns_to_zero():
+    # 40 splits per (row, KV group) span several clusters, which merge through
+    # the workspace; a second call on the same workspace gives the same result
+    # and the workspace is zero-filled again afterwards.
+    x = make_layer(L=9001, M=3, dtype=torch.bfloat16, seed=13)
+    sel, cnt, _ = _oracle_selection(x)
+    q, k, v = x.q.to(dev()), x.k.to(dev()), x.v.to(dev())
+    seqs = [qsa.Seq(x.L, x.M, segments=[qsa.Segment(k, v, 0)])]
+    seld, cntd = torch.from_numpy(sel).to(dev()), torch.from_numpy(cnt).to(dev())
+    cfg = qsa.attn_config(q, 2, torch.float32, 0.0, 40)
+    need = qsa.attn_workspace_size(seqs, cfg, sel.shape[1])
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev())
+    outs = []
+    for _ in range(2):
+        out = torch.full((x.M, 24, 256), float("nan"), device=dev())
+        lse = torch.full((x.M, 24), float("nan"), device=dev())
+        qsa.sparse_attn(seqs, q, seld, cntd, out, lse, workspace=ws, cfg=cfg)
+        torch.cuda.synchronize()
+        outs.append((to_np(out), to_np(lse)))
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    for o, l in outs:
+        assert_attn_close(o, l, ref_out, ref_lse, True)
+    np.testing.assert_array_equal(outs[0][0], outs[1][0])
+    n_pairs = x.M * 2
+    assert (ws[: 4 * n_pairs].view(torch.int32) == 0).all()
 
 
 def test_attention_bf16_output():
