@@ -233,6 +233,33 @@ qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_c
                            void* stream);
 
 /*
+ * qsa_sparse_attn without a workspace argument.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot give the
+ * library device memory -- for example a host framework that owns all device
+ * memory through its own pool and offers plugins no allocation, or a serving
+ * loop that must never call cudaMalloc because that call can synchronize the
+ * device.  It computes exactly what qsa_sparse_attn computes, with the
+ * scratch the split merge needs taken from one array of static device memory
+ * inside libqsa.so: QSA_NOALLOC_SCRATCH_BYTES (4 MiB), which every GPU that
+ * loads the library holds until the process exits.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - It allocates and frees nothing.  It clears the part of the array that
+ *    must start at zero on `stream` before the launch.
+ *  - Every call on a device shares the array: calls whose work overlaps on
+ *    the GPU (other streams, other threads) race and must not be issued.
+ *  - A call whose split plan needs more than QSA_NOALLOC_SCRATCH_BYTES of
+ *    scratch (qsa_attn_workspace_size) fails with QSA_ERR_UNSUPPORTED.
+ * Arguments, layouts and errors are otherwise those of qsa_sparse_attn.
+ */
+#define QSA_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+qsa_status qsa_sparse_attn_noalloc(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
+                                   const void* q, const int32_t* sel, const int32_t* cnt, int32_t sel_ld,
+                                   void* out, float* lse, void* stream);
+
+/*
  * Step 5 -- log-sum-exp merge of partial attention results (MTPLX pull
  * request #610: per-segment partials merged by their log-sum-exp equal
  * single-buffer attention; rows without a visible key merge to zeros, not

@@ -62,7 +62,8 @@ class AttnConfig(ctypes.Structure):
 _lib = None
 EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks",
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn",
-           "qsa_lse_merge")
+           "qsa_sparse_attn_noalloc", "qsa_lse_merge")
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 def lib() -> ctypes.CDLL:
@@ -88,8 +89,10 @@ def lib() -> ctypes.CDLL:
     L.qsa_attn_workspace_size.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), i32]
     L.qsa_attn_workspace_size.restype = sz
     L.qsa_sparse_attn.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
-    for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_sparse_attn", "qsa_lse_merge"):
+    for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_sparse_attn",
+                 "qsa_sparse_attn_noalloc", "qsa_lse_merge"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -227,6 +230,19 @@ def sparse_attn(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out
         arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
         out.data_ptr(), _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         _stream(stream)))
+
+
+def sparse_attn_noalloc(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out: torch.Tensor,
+                        lse: torch.Tensor | None = None, *, n_kv_heads: int = 2, scale: float = 0.0,
+                        n_splits: int = 0, stream=None, seq_array=None, cfg: AttnConfig | None = None):
+    """Step 4 for callers that cannot provide device scratch: the library's
+    own static scratch array is used (see qsa_sparse_attn_noalloc in qsa.h)."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    if cfg is None:
+        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
+    _check("qsa_sparse_attn_noalloc", lib().qsa_sparse_attn_noalloc(
+        arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
+        out.data_ptr(), _ptr(lse), _stream(stream)))
 
 
 def lse_merge(o_parts: torch.Tensor, lse_parts: torch.Tensor, out: torch.Tensor,

@@ -482,3 +482,62 @@ QSA_API qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, i
   return ok();
 }
 
+
+// ------------------------------------------------------------------ attention without a caller workspace
+// Some callers cannot give the library device memory: a host framework that
+// owns every byte of device memory through its own pool and offers plugins no
+// allocation, or a serving loop that must never call cudaMalloc because the
+// call can synchronize the device and stall every stream.  For them
+// qsa_sparse_attn_noalloc keeps the scratch the split merge needs in a fixed
+// array of static device memory, part of the loaded library itself.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = QSA_NOALLOC_SCRATCH_BYTES;   // held by every GPU that loads the library
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code must not pass the array's name to a kernel).
+qsa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn_noalloc");
+  if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_attn_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn_noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return QSA_OK;
+}
+
+}  // namespace
+
+QSA_API qsa_status qsa_sparse_attn_noalloc(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
+                                           const void* q, const int32_t* sel, const int32_t* cnt, int32_t sel_ld,
+                                           void* out, float* lse, void* stream) {
+  const char* fn = "qsa_sparse_attn_noalloc";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  if ((s = check_attn_config(cfg, fn)) != QSA_OK) return s;
+  if (sel_ld < 1) return fail(QSA_ERR_INVALID_ARG, "%s: sel_ld < 1", fn);
+  const size_t need = qsa_attn_workspace_size(seqs, n_seqs, cfg, sel_ld);
+  if (need > kNoAllocScratchBytes)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: this call needs %zu bytes of scratch; the built-in array holds %zu", fn,
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != QSA_OK) return s;
+  if (need > 0) {
+    // The split tickets must start at zero; they lead the scratch layout.
+    const size_t tickets = 256 * (size_t)((rows * cfg->n_kv_heads * 4 + 255) / 256);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, tickets, as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+  }
+  return qsa_sparse_attn(seqs, n_seqs, cfg, q, sel, cnt, sel_ld, out, lse, scratch, kNoAllocScratchBytes, stream);
+}
