@@ -451,7 +451,7 @@ def main():
 
 
 # Revision tag of the scoring kernel whose DRAM counters profiles/ holds.
-SCORE_KERNEL_REV = "score_mma_v1"
+SCORE_KERNEL_REV = "score_mma_v2"
 
 if __name__ == "__main__":
     main()
