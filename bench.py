@@ -197,26 +197,41 @@ def oracle_layer_steps(layers_host, n_threads, budget_s):
     return done, elapsed
 
 
-def host_layer(layer):
+def host_layer(layer, rows=None):
     """Host copies of one layer's inputs for the oracle; pooled keys of the
-    blocks before this step are state (pooled here, untimed)."""
+    blocks before this step are state (pooled here, untimed).  ``rows``
+    restricts the step to a sample of query rows (rows are independent)."""
     import oracle
     x = layer.x
     idxk = x.idxk.cpu()
     b0 = (x.L - x.M) // 4
-    return {"idxk": idxk, "q_idx": x.q_idx.cpu(), "q": x.q.cpu(), "k": x.k.cpu(), "v": x.v.cpu(),
-            "row_pos": x.row_pos, "b0": b0, "nb": x.L // 4, "pooled_old": oracle.pool(idxk, 0, b0)}
+    q_idx, q, pos = x.q_idx.cpu(), x.q.cpu(), x.row_pos
+    if rows is not None:
+        q_idx, q, pos = q_idx[rows], q[rows], [pos[r] for r in rows]
+    return {"idxk": idxk, "q_idx": q_idx, "q": q, "k": x.k.cpu(), "v": x.v.cpu(),
+            "row_pos": pos, "b0": b0, "nb": x.L // 4, "pooled_old": oracle.pool(idxk, 0, b0)}
 
 
-def cpu_baseline(layers, budget_s=20.0, max_layers=3):
+def cpu_baseline(layers, budget_s=20.0, max_layers=3, max_rows=64):
+    """The oracle on a bounded sample of the workload: whole layer-steps when
+    a layer has few rows; else max_rows sampled rows of one layer-step
+    (first and last included), timed and scaled linearly to all rows."""
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0))
-    hosts = [host_layer(l) for l in layers[:max_layers]]
-    n, secs = oracle_layer_steps(hosts, cores, budget_s)
-    return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} of the workload's layer-steps (pool new block, score all blocks, select, "
-                      f"attention over all rows and heads) in fp64 C with OpenMP, {secs:.2f} s"}
+    M = layers[0].x.M
+    if M <= max_rows:
+        hosts = [host_layer(l) for l in layers[:max_layers]]
+        n, secs = oracle_layer_steps(hosts, cores, budget_s)
+        return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+                "sample": f"{n} of the workload's layer-steps (pool new blocks, score all blocks, select, "
+                          f"attention over all rows and heads) in fp64 C with OpenMP, {secs:.2f} s"}
+    rows = sorted(set([0, M - 1] + [int(i * (M - 1) / (max_rows - 1)) for i in range(max_rows)]))
+    n, secs = oracle_layer_steps([host_layer(layers[0], rows)], cores, budget_s)
+    full = secs * M / len(rows)
+    return {"value": 1.0 / full, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows)} of the {M} rows of one layer-step in fp64 C with OpenMP ({secs:.2f} s), "
+                      f"extrapolated linearly in rows to {full:.1f} s per layer-step"}
 
 
 # ---------------------------------------------------------------------- main
@@ -257,7 +272,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="verify_m4_261k_bf16",
-                    choices=["verify_m4_261k_bf16", "decode_m1_65k_bf16"])
+                    choices=["verify_m4_261k_bf16", "decode_m1_65k_bf16", "prefill_t2048_100k_bf16",
+                             "tiny_verify_f32"])
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's 12)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
