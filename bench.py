@@ -65,7 +65,7 @@ def launches_per_layer(layer) -> int:
     st = layer.step
     n = len(st.pool_jobs) + 1 + 1 + 1            # pool, score, select, attention
     ws_needed = st.ws.numel() > 16
-    return n + (1 if ws_needed else 0)           # + split merge
+    return n + (1 if ws_needed else 0)           # + split merge (several splits per row)
 
 
 def algorithmic_bytes(layer) -> dict:
@@ -366,7 +366,8 @@ def main():
         return 1e3 * e0.elapsed_time(e1) / (args.kernel_reps * n_layers)
 
     kernel_us = {"pool": time_kind(lambda st: st.pool()), "score": time_kind(lambda st: st.score()),
-                 "select": time_kind(lambda st: st.select()), "attend": time_kind(lambda st: st.attend())}
+                 "select": time_kind(lambda st: st.select()),
+                 "score_select": time_kind(lambda st: st.score_select()), "attend": time_kind(lambda st: st.attend())}
     score_us = kernel_us["score"]
 
     # End to end through the public API with host buffers: per step, the new

@@ -186,13 +186,31 @@ qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* sco
                            size_t workspace_bytes, void* stream);
 
 /*
- * Scratch bytes qsa_sparse_attn needs for this call.  The splits of one
- * (row, KV group) run as thread-block clusters of up to 8 (16 when forced)
- * CTAs and merge inside a cluster through distributed shared memory; when a
- * (row, KV group) spans several clusters, each cluster leaves a merged
- * partial in the workspace and the last one to finish merges them.  Returns 0
- * when one cluster per (row, KV group) suffices.  sel_ld is the row stride of
- * sel (the top_k used for selection).
+ * Steps 2 and 3 in one call.  For one sequence of at most 4 rows with bf16
+ * index queries (decode and verify) the scoring kernel also counts every
+ * score in its row's histogram of the top 12 key bits, and the selection
+ * starts from that histogram instead of building its own; any other call
+ * runs qsa_score_blocks then qsa_select_topk.  Results are those of the two
+ * separate calls.
+ *   workspace      device scratch of >= qsa_score_select_workspace_size bytes
+ *                  (may be NULL when that size is 0).  It must be zero-filled
+ *                  before its first use; every call leaves it zero-filled.
+ *                  Two calls that share a workspace must not run
+ *                  concurrently.
+ * Other arguments as for qsa_score_blocks and qsa_select_topk.
+ */
+size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k);
+
+qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
+                                 qsa_dtype q_idx_dtype, float* scores, int64_t ld, int32_t top_k,
+                                 int32_t* sel, int32_t* cnt, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * Scratch bytes qsa_sparse_attn needs for this call: the normalised partial
+ * outputs and lse values of every split when a (row, KV group) is cut into
+ * several splits (0 when each has one).  sel_ld is the row stride of sel (the
+ * top_k used for selection).
  */
 size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
                                int32_t sel_ld);
@@ -218,12 +236,13 @@ size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, const qsa_at
  *   out            device [rows, Hq, head_dim], cfg->out_dtype
  *   lse            device [rows, Hq] f32 (natural log); may be NULL
  *   workspace      device scratch of >= qsa_attn_workspace_size bytes (may be
- *                  NULL when that size is 0).  It must be zero-filled before
- *                  its first use; every call leaves it zero-filled again.  Two
- *                  calls that share a workspace must not run concurrently.
- * Each row's selected list is cut into splits (cfg->n_splits, at most 256;
- * 0 = library's choice); splits merge by the log-sum-exp rule of
- * qsa_lse_merge, inside their cluster and then across clusters.
+ *                  NULL when that size is 0); its contents need no
+ *                  initialisation.  Two calls that share a workspace must
+ *                  not run concurrently.
+ * Each row's selected list is cut into cfg->n_splits splits per KV group
+ * (at most 256; 0 = library's choice, about two CTAs per SM); every split
+ * writes its normalised partial and lse, and a second launch merges them by
+ * the log-sum-exp rule of qsa_lse_merge.
  * Supported: head_dim 128 or 256; q and K/V both bf16 or both f32;
  * Hq / Hkv <= 16.
  */
@@ -245,8 +264,7 @@ qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_c
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any stream
  *    capture.
- *  - It allocates and frees nothing.  It clears the part of the array that
- *    must start at zero on `stream` before the launch.
+ *  - It allocates and frees nothing.
  *  - Every call on a device shares the array: calls whose work overlaps on
  *    the GPU (other streams, other threads) race and must not be issued.
  *  - A call whose split plan needs more than QSA_NOALLOC_SCRATCH_BYTES of

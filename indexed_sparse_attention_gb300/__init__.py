@@ -61,8 +61,9 @@ class AttnConfig(ctypes.Structure):
 
 _lib = None
 EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks",
-           "qsa_select_workspace_size", "qsa_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn",
-           "qsa_sparse_attn_noalloc", "qsa_lse_merge")
+           "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
+           "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
+           "qsa_lse_merge")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -86,13 +87,16 @@ def lib() -> ctypes.CDLL:
     L.qsa_select_workspace_size.argtypes = [seqp, i32, i32]
     L.qsa_select_workspace_size.restype = sz
     L.qsa_select_topk.argtypes = [seqp, i32, vp, i64, i32, vp, vp, vp, sz, vp]
+    L.qsa_score_select_workspace_size.argtypes = [seqp, i32, i32]
+    L.qsa_score_select_workspace_size.restype = sz
+    L.qsa_score_select_topk.argtypes = [seqp, i32, vp, i32, vp, i64, i32, vp, vp, vp, sz, vp]
     L.qsa_attn_workspace_size.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), i32]
     L.qsa_attn_workspace_size.restype = sz
     L.qsa_sparse_attn.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp, sz, vp]
     L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
-    for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_sparse_attn",
-                 "qsa_sparse_attn_noalloc", "qsa_lse_merge"):
+    for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_score_select_topk",
+                 "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -200,6 +204,20 @@ def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor
         _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
+def score_select_topk(seqs, q_idx: torch.Tensor, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor,
+                      top_k: int = TOP_K, workspace: torch.Tensor | None = None, stream=None, seq_array=None):
+    """Steps 2 and 3 in one call (fused scoring histogram for decode/verify).
+    The workspace must start zero-filled; the library leaves it zero-filled."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    need = lib().qsa_score_select_workspace_size(arr, len(arr), top_k)
+    if need and workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=scores.device)
+    _check("qsa_score_select_topk", lib().qsa_score_select_topk(
+        arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0), int(top_k),
+        sel.data_ptr(), cnt.data_ptr(), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)))
+
+
 def attn_config(q: torch.Tensor, n_kv_heads: int, out_dtype=None, scale: float = 0.0, n_splits: int = 0):
     cfg = AttnConfig()
     cfg.n_q_heads, cfg.head_dim = q.shape[1], q.shape[2]
@@ -225,7 +243,7 @@ def sparse_attn(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out
         cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
     need = lib().qsa_attn_workspace_size(arr, len(arr), ctypes.byref(cfg), sel.stride(0))
     if need and workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=q.device)   # zero-filled before first use
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check("qsa_sparse_attn", lib().qsa_sparse_attn(
         arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
         out.data_ptr(), _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -290,7 +308,7 @@ class LayerStep:
         self.cnt = torch.empty((rows,), dtype=torch.int32, device=dev)
         self.out = torch.empty((rows, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev)
         self.lse = torch.empty((rows, q.shape[1]), dtype=torch.float32, device=dev)
-        sel_ws = int(lib().qsa_select_workspace_size(self.arr, len(self.arr), self.top_k))
+        sel_ws = int(lib().qsa_score_select_workspace_size(self.arr, len(self.arr), self.top_k))
         attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
         # Workspaces start zero-filled; the library returns them zero-filled.
         self.sel_ws = torch.zeros(max(sel_ws, 16), dtype=torch.uint8, device=dev)
@@ -313,7 +331,11 @@ class LayerStep:
         score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr)
 
     def select(self, stream=None):
-        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, self.sel_ws, stream, seq_array=self.arr)
+        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr)
+
+    def score_select(self, stream=None):
+        score_select_topk(None, self.q_idx, self.scores, self.sel, self.cnt, self.top_k, self.sel_ws, stream,
+                          seq_array=self.arr)
 
     def attend(self, stream=None):
         sparse_attn(None, self.q, self.sel, self.cnt, self.out, self.lse, workspace=self.ws, stream=stream,
@@ -321,7 +343,6 @@ class LayerStep:
 
     def run(self, stream=None):
         self.pool(stream)
-        self.score(stream)
-        self.select(stream)
+        self.score_select(stream)
         self.attend(stream)
         return self.out, self.lse

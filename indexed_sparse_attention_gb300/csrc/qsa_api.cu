@@ -179,8 +179,9 @@ QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype
 // ------------------------------------------------------------------ step 2
 template <int NSEQ>
 static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const void* q_idx, qsa_dtype qd,
-                              float* scores, int64_t ld, cudaStream_t st) {
+                              float* scores, int64_t ld, cudaStream_t st, uint32_t* hist = nullptr) {
   ScoreParams<NSEQ> p{};
+  p.hist = hist;
   const int tile = score_tile_blocks(qd);
   int64_t work = 0;
   int max_rows = 1;
@@ -253,8 +254,9 @@ QSA_API size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, in
 
 template <int NSEQ>
 static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const float* scores, int64_t ld,
-                               int32_t top_k, int32_t* sel, int32_t* cnt, cudaStream_t st) {
+                               int32_t top_k, int32_t* sel, int32_t* cnt, cudaStream_t st, uint32_t* hist = nullptr) {
   SelectParams<NSEQ> p{};
+  p.hist = hist;
   int rows = 0;
   int64_t max_nb = 0;
   p.row_base = row_begin;
@@ -305,6 +307,58 @@ QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const fl
   return s == QSA_OK ? ok() : s;
 }
 
+// ------------------------------------------------------------------ steps 2 + 3 fused
+namespace {
+// The fused path: one sequence of <= kHistRows rows with bf16 index queries;
+// the scoring kernel leaves each row's first-level histogram in the workspace.
+bool fused_score_select(const qsa_seq* seqs, int32_t n_seqs) {
+  return n_seqs == 1 && seqs[0].n_rows <= kHistRows;
+}
+}  // namespace
+
+QSA_API size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k) {
+  (void)top_k;
+  if (!seqs || n_seqs < 1 || !fused_score_select(seqs, n_seqs)) return 0;
+  return sizeof(uint32_t) * (size_t)seqs[0].n_rows * kSelBins;
+}
+
+QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
+                                         qsa_dtype q_idx_dtype, float* scores, int64_t ld, int32_t top_k,
+                                         int32_t* sel, int32_t* cnt, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  const char* fn = "qsa_score_select_topk";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  const size_t need = qsa_score_select_workspace_size(seqs, n_seqs, top_k);
+  if (q_idx_dtype != QSA_BF16 || need == 0) {
+    // No fused path for this call: the two steps one after the other.
+    if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, stream)) != QSA_OK) return s;
+    return qsa_select_topk(seqs, n_seqs, scores, ld, top_k, sel, cnt, nullptr, 0, stream);
+  }
+  if (!workspace || workspace_bytes < need)
+    return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
+  // Validate both steps' arguments before the first launch.
+  if (top_k < 1 || top_k > QSA_MAX_TOP_K)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: top_k=%d outside 1..%d", fn, top_k, QSA_MAX_TOP_K);
+  if (!q_idx || !scores || !sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q_idx) || !aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx/scores not aligned", fn);
+  const qsa_seq& q = seqs[0];
+  if (max_visible_blocks(q) > ld) return fail(QSA_ERR_INVALID_ARG, "%s: ld smaller than the visible blocks", fn);
+  if (max_visible_blocks(q) > 0) {
+    if (!q.pooled || q.pooled_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: bad pooled keys", fn);
+    if (!aligned16(q.pooled) || q.pooled_stride % 4 != 0)
+      return fail(QSA_ERR_MISALIGNED, "%s: pooled keys not 16-byte aligned", fn);
+  }
+  cudaStream_t st = as_stream(stream);
+  uint32_t* hist = static_cast<uint32_t*>(workspace);
+  if ((s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, st, hist)) != QSA_OK) return s;
+  if ((s = select_chunk<1>(seqs, 1, 0, scores, ld, top_k, sel, cnt, st, hist)) != QSA_OK) return s;
+  return ok();
+}
+
 // ------------------------------------------------------------------ step 4
 namespace {
 
@@ -322,7 +376,7 @@ AttnPlan plan_splits(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config*
 }
 
 size_t attn_ws_bytes(const AttnPlan& sp, int64_t rows, const qsa_attn_config* cfg) {
-  return attn_workspace_bytes(sp, rows * cfg->n_kv_heads, cfg->n_q_heads / cfg->n_kv_heads, cfg->head_dim);
+  return attn_workspace_bytes(sp, rows, cfg->n_q_heads, cfg->head_dim);
 }
 
 qsa_status check_attn_config(const qsa_attn_config* cfg, const char* fn) {
@@ -370,8 +424,8 @@ qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_co
 
 template <int NSEQ>
 qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_attn_config* cfg, const void* q,
-                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const AttnPlan& sp, void* out,
-                      float* lse, uint32_t* counters, float* part_lse, float* part_o, cudaStream_t st) {
+                      const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const AttnPlan& sp, int64_t total_rows,
+                      void* out, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
   AttnParams<NSEQ> p{};
   int rows = 0, nseg = 0;
   p.row_base = row_begin;
@@ -403,12 +457,11 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.group = cfg->n_q_heads / cfg->n_kv_heads;
   p.head_dim = cfg->head_dim;
   p.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
-  p.cluster_size = sp.cluster_size;
-  p.n_clusters = sp.n_clusters;
+  p.n_splits = sp.n_splits;
   p.split_tokens = sp.split_tokens;
-  p.counters = counters;
-  p.part_lse = part_lse;
+  p.total_rows = (int32_t)total_rows;
   p.part_o = part_o;
+  p.part_lse = part_lse;
   p.out = out;
   p.lse = lse;
   p.out_dtype = cfg->out_dtype;
@@ -444,25 +497,28 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
     return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? workspace_bytes : (size_t)0);
   if (need > 0 && !aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
-  uint32_t* counters = nullptr;
-  float* part_lse = nullptr;
   float* part_o = nullptr;
-  if (need > 0)
-    attn_workspace_layout(sp, rows * cfg->n_kv_heads, cfg->n_q_heads / cfg->n_kv_heads, workspace, &counters,
-                          &part_lse, &part_o);
+  float* part_lse = nullptr;
+  if (need > 0) attn_workspace_layout(sp, rows, cfg->n_q_heads, cfg->head_dim, workspace, &part_o, &part_lse);
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, out, lse, counters, part_lse, part_o, st);
+    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o, part_lse, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, out, lse, counters,
-                                  part_lse, part_o, st);
+      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o,
+                                  part_lse, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
   if (s != QSA_OK) return s;
+  if (sp.n_splits > 1) {
+    // Step 5 on the splits' partials.
+    cudaError_t e = launch_merge(part_o, part_lse, sp.n_splits, rows * cfg->n_q_heads, cfg->head_dim, out,
+                                 cfg->out_dtype, lse, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+  }
   return ok();
 }
 
@@ -533,11 +589,5 @@ QSA_API qsa_status qsa_sparse_attn_noalloc(const qsa_seq* seqs, int32_t n_seqs, 
                 need, kNoAllocScratchBytes);
   void* scratch = nullptr;
   if ((s = noalloc_scratch(&scratch)) != QSA_OK) return s;
-  if (need > 0) {
-    // The split tickets must start at zero; they lead the scratch layout.
-    const size_t tickets = 256 * (size_t)((rows * cfg->n_kv_heads * 4 + 255) / 256);
-    cudaError_t e = cudaMemsetAsync(scratch, 0, tickets, as_stream(stream));
-    if (e != cudaSuccess) return cuda_fail(e, fn);
-  }
   return qsa_sparse_attn(seqs, n_seqs, cfg, q, sel, cnt, sel_ld, out, lse, scratch, kNoAllocScratchBytes, stream);
 }

@@ -9,24 +9,21 @@
 //   launch, partials merged by their log-sum-exp; rows with no visible key
 //   merge to zeros; fp32 partials rounded once).
 //
-// One CTA per (query row, KV group, split).  A split walks its share of the
+// One CTA per (query row, KV group, split): a split walks its share of the
 // row's selected list (the 4 tokens of each selected block, then the tail) in
 // tiles of 32 tokens; each token is located in the sequence's segment table
-// and its K and V rows are gathered into shared memory.  bf16 K/V run on the
-// tensor pipe (mma.sync m16n8k16: the 12 heads of a group padded to 16 rows
-// against 32 gathered tokens), with an fp32 online softmax; fp32 K/V take a
-// CUDA-core kernel.  Partials (normalised output, lse) of several splits are
-// merged by the step-5 kernel.
-#include <cooperative_groups.h>
+// and its K and V rows are gathered into shared memory with cp.async.  bf16
+// K/V run on the tensor pipe (mma.sync m16n8k16: the 12 heads of a group
+// padded to 16 rows against 32 gathered tokens) with an fp32 online softmax;
+// fp32 K/V take a CUDA-core kernel.  A split writes its normalised partial
+// output and lse; a second launch merges the splits by log-sum-exp (step 5,
+// the kernel behind qsa_lse_merge).  A row with a single split is written
+// directly.
 #include <math.h>
 
 #include <algorithm>
-#include <mutex>
-#include <vector>
 
 #include "qsa_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace qsa {
 
@@ -34,7 +31,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMaxSplits = 16;   // splits of one (row, KV group) = CTAs of one cluster
+constexpr int kMaxSplits = 256;  // splits of one (row, KV group)
 
 // Per-row context: position, visible blocks, selected list length.
 struct RowCtx {
@@ -160,170 +157,36 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// ------------------------------------------------------------------ split merge (step 5)
-// The CTAs of one cluster hold the partials of consecutive splits of the same
-// (row, KV group): unnormalised output o_s[16][D] (fp32), running max m_s[16]
-// of the base-2 logits and running sum l_s[16].  After a cluster barrier,
-// CTA c merges the 4-channel groups c, c+CS, ... of every head across the
-// cluster through distributed shared memory:
-//   M = max_q m_q,  w_q = 2^(m_q - M),  out = sum_q w_q o_q / sum_q w_q l_q,
-//   lse = (M + log2 sum_q w_q l_q) * ln 2,
-// and a head whose splits saw no key gets out = 0 and lse = -inf.
-// With several clusters per (row, KV group), each cluster writes its merged,
-// normalised partial and lse to the workspace; the cluster that takes the
-// last ticket merges all of them by the same rule (natural-log lse) and
-// returns the ticket counter to zero.
-constexpr int kMaxClusters = 32;   // clusters per (row, KV group)
-
-struct MergeSmem {
-  float mq[16][kMaxSplits];
-  float lq[16][kMaxSplits];
-  float w[16][kMaxSplits];
-  float inv[16];
-  float lse[16];
-  float cw[16][kMaxClusters];
-  float cinv[16];
-  float clse[16];
-  int last;
-};
+// ------------------------------------------------------------------ a split's result
+// Normalised output and natural-log lse of one (row, head): to the final
+// output when the row has a single split, else to the split's partial slot
+// ([split][row * Hq + head][D] and [split][row * Hq + head], the layout of
+// qsa_lse_merge's inputs).
+template <int NSEQ>
+__device__ __forceinline__ void store_result(const AttnParams<NSEQ>& p, int split, int r, int head, int d, float x0,
+                                             float x1) {
+  const int64_t rh = (int64_t)r * p.n_q_heads + head;
+  if (p.n_splits == 1) {
+    if (p.out_dtype == QSA_F32) {
+      *reinterpret_cast<float2*>(static_cast<float*>(p.out) + rh * p.head_dim + d) = make_float2(x0, x1);
+    } else {
+      *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + rh * p.head_dim + d) =
+          __floats2bfloat162_rn(x0, x1);
+    }
+  } else {
+    const int64_t R = (int64_t)p.total_rows * p.n_q_heads;
+    *reinterpret_cast<float2*>(p.part_o + ((int64_t)split * R + rh) * p.head_dim + d) = make_float2(x0, x1);
+  }
+}
 
 template <int NSEQ>
-__device__ void merge_store(const AttnParams<NSEQ>& p, int r, int g, int G, int D, float* o_s, float* m_s,
-                            float* l_s, MergeSmem* ms) {
-  cg::cluster_group cluster = cg::this_cluster();
-  const int S = (int)cluster.num_blocks();
-  const int c = (int)cluster.block_rank();
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int head0 = g * G;
-  cluster.sync();
-  // Every split's running max and sum, one (head, split) pair per thread.
-  for (int t = tid; t < G * S; t += nt) {
-    const int h = t / S, q = t % S;
-    ms->mq[h][q] = *cluster.map_shared_rank(m_s + h, q);
-    ms->lq[h][q] = *cluster.map_shared_rank(l_s + h, q);
+__device__ __forceinline__ void store_lse(const AttnParams<NSEQ>& p, int split, int r, int head, float lse) {
+  const int64_t rh = (int64_t)r * p.n_q_heads + head;
+  if (p.n_splits == 1) {
+    if (p.lse) p.lse[rh] = lse;
+  } else {
+    p.part_lse[(int64_t)split * p.total_rows * p.n_q_heads + rh] = lse;
   }
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int q = 0; q < S; ++q) M = fmaxf(M, ms->mq[tid][q]);
-    float Lsum = 0.f;
-    for (int q = 0; q < S; ++q) {
-      const float mq = ms->mq[tid][q];
-      const float w = mq == -INFINITY ? 0.f : exp2f(mq - M);
-      ms->w[tid][q] = w;
-      Lsum += w * ms->lq[tid][q];
-    }
-    ms->inv[tid] = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    ms->lse[tid] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
-  }
-  __syncthreads();
-  const int NC = p.n_clusters;
-  const int64_t pair = (int64_t)r * (p.n_q_heads / G) + g;
-  const int64_t cid = blockIdx.x / S;
-  // 4-channel groups c, c + S, c + 2S, ... of every head belong to this CTA
-  // (any S <= 16; D / 4 >= 32 groups, so every CTA has at least one).
-  const int nq = (D / 4 - c + S - 1) / S;
-  for (int idx = tid; idx < G * nq; idx += nt) {
-    const int h = idx / nq;
-    const int d = 4 * (c + (idx % nq) * S);
-    float4 v[kMaxSplits];
-#pragma unroll
-    for (int q = 0; q < kMaxSplits; ++q)
-      if (q < S) v[q] = *reinterpret_cast<const float4*>(cluster.map_shared_rank(o_s + h * D + d, q));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < kMaxSplits; ++q) {
-      if (q < S) {
-        const float w = ms->w[h][q];
-        acc.x = fmaf(w, v[q].x, acc.x);
-        acc.y = fmaf(w, v[q].y, acc.y);
-        acc.z = fmaf(w, v[q].z, acc.z);
-        acc.w = fmaf(w, v[q].w, acc.w);
-      }
-    }
-    const float inv = ms->inv[h];
-    const float4 res = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (NC > 1) {
-      *reinterpret_cast<float4*>(p.part_o + ((pair * NC + cid) * G + h) * D + d) = res;
-    } else {
-      const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
-      if (p.out_dtype == QSA_F32) {
-        *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = res;
-      } else {
-        __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
-        o2[0] = __floats2bfloat162_rn(res.x, res.y);
-        o2[1] = __floats2bfloat162_rn(res.z, res.w);
-      }
-    }
-  }
-  if (NC == 1) {
-    if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->lse[tid];
-    cluster.sync();  // keep this CTA's partial alive until every peer has read it
-    return;
-  }
-  if (c == 0 && tid < G) p.part_lse[(pair * NC + cid) * G + tid] = ms->lse[tid];
-  __threadfence();
-  cluster.sync();    // this cluster's partial is written; peers are done reading o_s
-  if (c == 0 && tid == 0) {
-    const unsigned t = atomicAdd(p.counters + pair, 1u);
-    const int last = t == (unsigned)(NC - 1);
-    if (last) p.counters[pair] = 0u;   // every ticket is taken: ready for the next call
-    for (int q = 0; q < S; ++q) cluster.map_shared_rank(ms, q)->last = last;
-  }
-  cluster.sync();
-  if (!ms->last) return;
-  __threadfence();
-  // The last cluster merges the clusters' partials (natural-log lse).
-  for (int t = tid; t < G * NC; t += nt) {
-    const int h = t / NC, q = t % NC;
-    ms->cw[h][q] = __ldcg(p.part_lse + (pair * NC + q) * G + h);
-  }
-  __syncthreads();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int q = 0; q < NC; ++q) M = fmaxf(M, ms->cw[tid][q]);
-    float Wsum = 0.f;
-    for (int q = 0; q < NC; ++q) {
-      const float lq = ms->cw[tid][q];
-      const float w = lq == -INFINITY ? 0.f : expf(lq - M);
-      ms->cw[tid][q] = w;
-      Wsum += w;
-    }
-    ms->cinv[tid] = Wsum > 0.f ? 1.f / Wsum : 0.f;
-    ms->clse[tid] = Wsum > 0.f ? M + logf(Wsum) : -INFINITY;
-  }
-  __syncthreads();
-  for (int idx = tid; idx < G * nq; idx += nt) {
-    const int h = idx / nq;
-    const int d = 4 * (c + (idx % nq) * S);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q0 = 0; q0 < NC; q0 += 8) {
-      float4 v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = q0 + j < NC ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((pair * NC + q0 + j) * G + h) * D + d))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float w = q0 + j < NC ? ms->cw[h][q0 + j] : 0.f;
-        acc.x = fmaf(w, v[j].x, acc.x);
-        acc.y = fmaf(w, v[j].y, acc.y);
-        acc.z = fmaf(w, v[j].z, acc.z);
-        acc.w = fmaf(w, v[j].w, acc.w);
-      }
-    }
-    const float inv = ms->cinv[h];
-    const int64_t o = ((int64_t)r * p.n_q_heads + head0 + h) * D + d;
-    if (p.out_dtype == QSA_F32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    } else {
-      __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
-      o2[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      o2[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    }
-  }
-  if (c == 0 && tid < G && p.lse) p.lse[(int64_t)r * p.n_q_heads + head0 + tid] = ms->clse[tid];
 }
 
 // ------------------------------------------------------------------ tensor-pipe kernel (bf16 K/V)
@@ -350,10 +213,6 @@ struct MmaSmem {
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
   static constexpr size_t off_ids = off_valid + STAGES * kTT * 4;
   static constexpr size_t bytes = off_ids + kIdCache * 4;
-  // After the token loop the K/V stages hold the partial [16][D] fp32 and the
-  // merge scratch.
-  static constexpr size_t off_merge = off_kv + 16 * D * 4;
-  static_assert(16 * D * 4 + sizeof(MergeSmem) <= STAGES * 2 * kv_tile, "merge data must fit the K/V stages");
   // Three stages keep two CTAs per SM (228 KB per SM, 1 KB reserved per CTA).
   static_assert(STAGES != 3 || 2 * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
@@ -374,7 +233,6 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   float* a_s = m_s + 32;
   int* valid_s = reinterpret_cast<int*>(smem + L::off_valid);
   int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L::off_ids);
-  MergeSmem* msm = reinterpret_cast<MergeSmem*>(smem + L::off_merge);
   grid_dependency_sync();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -573,18 +431,20 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   cp_async_wait<0>();
   __syncthreads();
 
-  // Unnormalised partial into shared memory (over the K/V stages), then merge.
-  float* o_s = reinterpret_cast<float*>(kv_s);
+  // Normalised result of heads gq and gq + 8 over this warp's channels.
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     const int row = gq + 8 * hf;
+    if (row >= G) continue;
+    const float l = l_s[row];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int j = 0; j < NTD; ++j) {
       const int d = warp * (D / 8) + j * 8 + 2 * t4;
-      *reinterpret_cast<float2*>(o_s + row * D + d) = make_float2(o[j][2 * hf], o[j][2 * hf + 1]);
+      store_result(p, split, r, head0 + row, d, o[j][2 * hf] * inv, o[j][2 * hf + 1] * inv);
     }
+    if (warp == 0 && t4 == 0) store_lse(p, split, r, head0 + row, l > 0.f ? (m_s[row] + log2f(l)) * kLn2 : -INFINITY);
   }
-  merge_store(p, r, g, G, D, o_s, m_s, l_s, msm);
 }
 
 // ------------------------------------------------------------------ CUDA-core kernel (fp32 K/V)
@@ -598,8 +458,7 @@ struct SimtSmem {
   static constexpr size_t v = kSimtTT * D;
   static constexpr size_t z = 16 * 33;
   static constexpr size_t floats = q + k + v + z + 3 * 16;
-  static constexpr size_t bytes = floats * 4 + kSimtTT * 4 + kIdCache * 4 + sizeof(MergeSmem);
-  static_assert(16 * D <= k + v, "merge partial must fit the K/V tiles");
+  static constexpr size_t bytes = floats * 4 + kSimtTT * 4 + kIdCache * 4;
 };
 
 template <int D, int NSEQ>
@@ -617,7 +476,6 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
   float* a_s = l_s + 16;
   int* ok_s = reinterpret_cast<int*>(a_s + 16);
   int32_t* ids_s = ok_s + kSimtTT;
-  MergeSmem* msm = reinterpret_cast<MergeSmem*>(ids_s + kIdCache);
   grid_dependency_sync();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -689,19 +547,119 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
     }
     __syncthreads();
   }
-  float* o_s = k_s;  // [16][D] over the K/V tiles
 #pragma unroll
   for (int j = 0; j < MAXH; ++j) {
     const int hh = hs + j * HS;
-    if (hh < 16) o_s[hh * D + d] = hh < G ? acc[j] : 0.f;
+    if (hh >= G) continue;
+    const float l = l_s[hh];
+    const float x = l > 0.f ? acc[j] / l : 0.f;
+    const int64_t rh = (int64_t)r * p.n_q_heads + head0 + hh;
+    if (p.n_splits == 1) {
+      if (p.out_dtype == QSA_F32) static_cast<float*>(p.out)[rh * D + d] = x;
+      else static_cast<__nv_bfloat16*>(p.out)[rh * D + d] = __float2bfloat16(x);
+    } else {
+      p.part_o[((int64_t)split * p.total_rows * p.n_q_heads + rh) * D + d] = x;
+    }
+    if (d == 0) store_lse(p, split, r, head0 + hh, l > 0.f ? (m_s[hh] + log2f(l)) * kLn2 : -INFINITY);
   }
-  merge_store(p, r, g, G, D, o_s, m_s, l_s, msm);
 }
 
+// ------------------------------------------------------------------ step 5: merge of split partials
+// One CTA of 8 warps per (row, head) when head_dim is 128 or 256: warp w
+// takes partials w, w + 8, ...; lane l accumulates channels [l*CPL, (l+1)*CPL)
+// of each, weighted by 2^(lse_s - m_w) against its own running maximum; the
+// warps then combine in shared memory by the same rule.  Every load of a warp
+// is independent of its other loads.
+constexpr int kMergeWarps = 8;
 
-// ------------------------------------------------------------------ step 5 entry point: merge of given partials
-// Thread -> (row, 4 channels).  The partials' lse values are read first in
-// batches, so each thread's loads are independent of one another.
+template <int CPL>   // channels per lane (4 or 8)
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_cta_kernel(const float* __restrict__ o_parts,
+                                                                     const float* __restrict__ lse_parts,
+                                                                     int n_parts, int64_t n_rows, int head_dim,
+                                                                     void* __restrict__ out, int out_dtype,
+                                                                     float* __restrict__ lse_out) {
+  __shared__ float acc_s[kMergeWarps][32 * CPL];
+  __shared__ float m_s[kMergeWarps], w_s[kMergeWarps];
+  grid_dependency_sync();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t row = blockIdx.x;
+  const int d0 = lane * CPL;
+  // This warp's partials: lse first (one per lane, up to 32 at a time).
+  float m = -INFINITY;
+  for (int s = warp + kMergeWarps * lane; s < n_parts; s += kMergeWarps * 32)
+    m = fmaxf(m, __ldg(lse_parts + (int64_t)s * n_rows + row));
+  m = warp_max(m);
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int s0 = warp; s0 < n_parts; s0 += kMergeWarps * 4) {
+      float w[4];
+      float4 v[4][CPL / 4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int s = s0 + k * kMergeWarps;
+        const float ls = s < n_parts ? __ldg(lse_parts + (int64_t)s * n_rows + row) : -INFINITY;
+        w[k] = ls == -INFINITY ? 0.f : exp2f((ls - m) * 1.4426950408889634f);
+#pragma unroll
+        for (int c = 0; c < CPL / 4; ++c)
+          v[k][c] = w[k] > 0.f ? __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * n_rows + row) * head_dim + d0) + c)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        wsum += w[k];
+#pragma unroll
+        for (int c = 0; c < CPL / 4; ++c) {
+          acc[4 * c + 0] = fmaf(w[k], v[k][c].x, acc[4 * c + 0]);
+          acc[4 * c + 1] = fmaf(w[k], v[k][c].y, acc[4 * c + 1]);
+          acc[4 * c + 2] = fmaf(w[k], v[k][c].z, acc[4 * c + 2]);
+          acc[4 * c + 3] = fmaf(w[k], v[k][c].w, acc[4 * c + 3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc_s[warp][d0 + c] = acc[c];
+  if (lane == 0) {
+    m_s[warp] = m;
+    w_s[warp] = wsum;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < kMergeWarps; ++k) M = fmaxf(M, m_s[k]);
+  float f[kMergeWarps], W = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMergeWarps; ++k) {
+    f[k] = m_s[k] == -INFINITY ? 0.f : expf(m_s[k] - M);
+    W += f[k] * w_s[k];
+  }
+  const float inv = W > 0.f ? 1.f / W : 0.f;
+  float r[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    float x = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMergeWarps; ++k) x = fmaf(f[k], acc_s[k][d0 + c], x);
+    r[c] = x * inv;
+  }
+  if (out_dtype == QSA_F32) {
+    float* o = static_cast<float*>(out) + row * head_dim + d0;
+#pragma unroll
+    for (int c = 0; c < CPL / 4; ++c)
+      reinterpret_cast<float4*>(o)[c] = make_float4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+  } else {
+    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(out) + row * head_dim + d0);
+#pragma unroll
+    for (int c = 0; c < CPL / 2; ++c) o[c] = __floats2bfloat162_rn(r[2 * c], r[2 * c + 1]);
+  }
+  if (lane == 0 && lse_out) lse_out[row] = W > 0.f ? M + logf(W) : -INFINITY;
+}
+
+// Thread -> (row, 4 channels), for any head_dim that is a multiple of 4.
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_parts,
                                                      const float* __restrict__ lse_parts, int n_parts,
                                                      int64_t n_rows, int head_dim, void* __restrict__ out,
@@ -757,151 +715,64 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ o_
   if (d == 0 && lse_out) lse_out[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
+}  // namespace
+
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Splits per (row, KV group): about two CTAs per SM over the whole call, each
+// split a whole number of 32-token tiles; one split for calls with enough
+// rows (prefill).
+AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_list, int user_splits) {
+  (void)kv_dtype;
+  (void)head_dim;
+  const int64_t sms = device_sm_count();
+  const int64_t max_splits = std::min<int64_t>(ceil_div(n_list, kTT), kMaxSplits);
+  int64_t n = user_splits > 0 ? user_splits : ceil_div(2 * sms, pairs);
+  n = std::max<int64_t>(1, std::min(n, max_splits));
+  int64_t per = ceil_div(n_list, n);
+  if (n > 1) per = ceil_div(per, kTT) * kTT;
+  n = ceil_div(n_list, per);
+  const int stages = per <= 2 * kTT ? 2 : 3;
+  return AttnPlan{(int32_t)n, (int32_t)per, stages};
+}
+
+size_t attn_workspace_bytes(const AttnPlan& pl, int64_t rows, int n_q_heads, int head_dim) {
+  if (pl.n_splits <= 1) return 0;
+  const int64_t R = rows * n_q_heads;
+  return 256 * (size_t)ceil_div(pl.n_splits * R * head_dim * 4, 256) + (size_t)pl.n_splits * R * 4;
+}
+
+void attn_workspace_layout(const AttnPlan& pl, int64_t rows, int n_q_heads, int head_dim, void* ws, float** part_o,
+                           float** part_lse) {
+  const int64_t R = rows * n_q_heads;
+  *part_o = static_cast<float*>(ws);
+  *part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + 256 * ceil_div(pl.n_splits * R * head_dim * 4, 256));
+}
+
+namespace {
+
 template <int NSEQ, typename Kern>
 cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_rows, int threads, size_t smem,
                                cudaStream_t st) {
   cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);
   if (e != cudaSuccess) return e;
-  const int cs = p.cluster_size;
-  if (cs > 8) {
-    e = allow_cluster16((const void*)kernel, threads, smem);
-    if (e != cudaSuccess) return e;
-  }
-  return launch_kernel(kernel, dim3((unsigned)(cs * p.n_clusters), (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows),
-                       dim3((unsigned)threads), smem, st, (unsigned)cs, p);
+  return launch_kernel(kernel, dim3((unsigned)p.n_splits, (unsigned)(p.n_q_heads / p.group), (unsigned)n_rows),
+                       dim3((unsigned)threads), smem, st, 0u, p);
 }
 
 }  // namespace
-
-// The kernel variant a plan runs, with its block size and shared memory.
-struct AttnVariant {
-  const void* fn;
-  int threads;
-  size_t smem;
-};
-
-static AttnVariant attn_variant(qsa_dtype kv_dtype, int head_dim, int stages) {
-  if (kv_dtype == QSA_BF16) {
-    if (head_dim == 256)
-      return stages == 5 ? AttnVariant{(const void*)attn_mma_kernel<256, 5, 1>, kAttnThreads, MmaSmem<256, 5>::bytes}
-                         : AttnVariant{(const void*)attn_mma_kernel<256, 3, 1>, kAttnThreads, MmaSmem<256, 3>::bytes};
-    return stages == 5 ? AttnVariant{(const void*)attn_mma_kernel<128, 5, 1>, kAttnThreads, MmaSmem<128, 5>::bytes}
-                       : AttnVariant{(const void*)attn_mma_kernel<128, 3, 1>, kAttnThreads, MmaSmem<128, 3>::bytes};
-  }
-  return head_dim == 256 ? AttnVariant{(const void*)attn_simt_kernel<256, 1>, 256, SimtSmem<256>::bytes}
-                         : AttnVariant{(const void*)attn_simt_kernel<128, 1>, 256, SimtSmem<128>::bytes};
-}
-
-// Clusters of `cs` CTAs of this variant that can be resident at once.
-static int max_active_clusters(const AttnVariant& v, int cs) {
-  struct Entry {
-    int dev;
-    const void* fn;
-    int cs;
-    int n;
-  };
-  static std::vector<Entry> cache;
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> lk(mu);
-  for (const Entry& e : cache)
-    if (e.dev == dev && e.fn == v.fn && e.cs == cs) return e.n;
-  int n = 0;
-  if (allow_dynamic_smem(v.fn, v.smem) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cs, 1, 1);
-    cfg.blockDim = dim3((unsigned)v.threads, 1, 1);
-    cfg.dynamicSmemBytes = v.smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, v.fn, &cfg) != cudaSuccess) n = 0;
-  }
-  cache.push_back(Entry{dev, v.fn, cs, n});
-  return n;
-}
-
-static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
-
-// Splits of each (row, KV group): `total` CTAs in n_clusters clusters of
-// cluster_size, each split at most 5 tiles of 32 selected rows when the GPU
-// has room for one CTA per SM, all of them resident at once.
-AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_list, int user_splits) {
-  const int64_t sms = device_sm_count();
-  const int64_t max_total = std::min<int64_t>(ceil_div(n_list, kTT), (int64_t)kMaxSplits * kMaxClusters);
-  int64_t total;
-  if (user_splits > 0) {
-    total = std::min<int64_t>(user_splits, max_total);
-  } else {
-    total = std::max<int64_t>(1, sms / pairs);
-    if (ceil_div(ceil_div(n_list, std::min(total, max_total)), kTT) > 5) total = std::max<int64_t>(1, 2 * sms / pairs);
-    total = std::min(total, max_total);
-    // Fewer CTAs when that keeps the tiles per CTA.
-    const int64_t tiles = ceil_div(ceil_div(n_list, total), kTT);
-    while (total > 1 && ceil_div(ceil_div(n_list, total - 1), kTT) == tiles) --total;
-  }
-  total = std::max<int64_t>(1, total);
-  const int64_t tiles = ceil_div(ceil_div(n_list, total), kTT);
-  const int stages = (tiles <= 5 && pairs * total <= sms) ? 5 : 3;
-  const AttnVariant v = attn_variant(kv_dtype, head_dim, stages);
-  AttnPlan best{1, 1, (int32_t)n_list, stages};
-  bool found = false;
-  // Cluster sizes to try, largest first: min(total, 8), then 6, 4, 3, 2, 1.
-  const int first = (int)std::min<int64_t>(total, 8);
-  const int sizes[6] = {first, 6, 4, 3, 2, 1};
-  for (int k = 0; k < 6; ++k) {
-    const int cs = sizes[k];
-    if (k > 0 && cs >= first) continue;
-    const int64_t nc = ceil_div(total, cs);
-    if (nc > kMaxClusters) continue;
-    const int64_t cs_b = ceil_div(total, nc);           // balance the clusters
-    const int active = max_active_clusters(v, (int)cs_b);
-    if (user_splits <= 0 && active > 0 && pairs * nc > active) continue;   // keep every cluster resident
-    best = AttnPlan{(int32_t)cs_b, (int32_t)nc, (int32_t)ceil_div(n_list, cs_b * nc), stages};
-    found = true;
-    break;
-  }
-  if (!found) {
-    const int64_t cs = std::min<int64_t>(total, 8);
-    const int64_t nc = std::min<int64_t>(ceil_div(total, cs), kMaxClusters);
-    best = AttnPlan{(int32_t)cs, (int32_t)nc, (int32_t)ceil_div(n_list, cs * nc), stages};
-  }
-  return best;
-}
-
-size_t attn_workspace_bytes(const AttnPlan& pl, int64_t pairs, int group, int head_dim) {
-  if (pl.n_clusters <= 1) return 0;
-  const size_t parts = (size_t)pairs * pl.n_clusters * group;
-  return 256 * ceil_div(pairs * 4, 256) + 256 * ceil_div((int64_t)parts * 4, 256) + parts * head_dim * 4;
-}
-
-void attn_workspace_layout(const AttnPlan& pl, int64_t pairs, int group, void* ws, uint32_t** counters,
-                           float** part_lse, float** part_o) {
-  char* b = static_cast<char*>(ws);
-  const size_t parts = (size_t)pairs * pl.n_clusters * group;
-  *counters = reinterpret_cast<uint32_t*>(b);
-  b += 256 * ceil_div(pairs * 4, 256);
-  *part_lse = reinterpret_cast<float*>(b);
-  b += 256 * ceil_div((int64_t)parts * 4, 256);
-  *part_o = reinterpret_cast<float*>(b);
-}
 
 template <int NSEQ>
 cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
   if (kv_dtype == QSA_BF16) {
     if (p.head_dim == 256) {
-      if (stages == 5)
-        return launch_attn_kernel(attn_mma_kernel<256, 5, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256, 5>::bytes, st);
+      if (stages == 2)
+        return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256, 2>::bytes, st);
       return launch_attn_kernel(attn_mma_kernel<256, 3, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<256, 3>::bytes, st);
     }
-    if (stages == 5)
-      return launch_attn_kernel(attn_mma_kernel<128, 5, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128, 5>::bytes, st);
+    if (stages == 2)
+      return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128, 2>::bytes, st);
     return launch_attn_kernel(attn_mma_kernel<128, 3, NSEQ>, p, n_rows, kAttnThreads, MmaSmem<128, 3>::bytes, st);
   }
   if (p.head_dim == 256)
@@ -914,10 +785,18 @@ template cudaError_t launch_attn<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, in
 
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows, int head_dim,
                          void* out, int out_dtype, float* lse_out, cudaStream_t st) {
+  if (n_rows == 0) return cudaSuccess;
+  if (head_dim == 256 || head_dim == 128) {
+    const dim3 grid((unsigned)n_rows), block(kMergeWarps * 32);
+    if (head_dim == 256)
+      return launch_kernel(merge_cta_kernel<8>, grid, block, 0, st, 0u, o_parts, lse_parts, n_parts, n_rows, head_dim,
+                           out, out_dtype, lse_out);
+    return launch_kernel(merge_cta_kernel<4>, grid, block, 0, st, 0u, o_parts, lse_parts, n_parts, n_rows, head_dim,
+                         out, out_dtype, lse_out);
+  }
   const int64_t threads = n_rows * (head_dim / 4);
-  if (threads == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((threads + 255) / 256);
-  return launch_kernel(merge_kernel, dim3(grid), dim3(256), 0, st, 0, o_parts, lse_parts, n_parts, n_rows, head_dim,
+  return launch_kernel(merge_kernel, dim3(grid), dim3(256), 0, st, 0u, o_parts, lse_parts, n_parts, n_rows, head_dim,
                        out, out_dtype, lse_out);
 }
 

@@ -38,7 +38,17 @@ struct ScoreParams {
   const void* q_idx;     // [rows, 4, 128]
   float* scores;
   int64_t ld;
+  uint32_t* hist;        // optional [rows, kSelBins] histogram of the scores' top key bits
 };
+
+// Bins of the selection's first radix level: the top 12 bits of a score's
+// order-preserving key.
+constexpr int kSelBins = 4096;
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;  // -0.0 ties with +0.0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // ---------------------------------------------------------------- selection
 struct RowSeq {
@@ -57,6 +67,8 @@ struct SelectParams {
   int32_t top_k;
   int32_t* sel;
   int32_t* cnt;
+  uint32_t* hist;        // optional [rows, kSelBins] first-level histogram made by the scoring
+                         // kernel; the selection returns it to zero
 };
 
 // ---------------------------------------------------------------- attention
@@ -91,14 +103,13 @@ struct AttnParams {
   int32_t group;           // query heads per KV head
   int32_t head_dim;
   float scale;             // logit scale
-  int32_t cluster_size;    // CTAs per cluster (splits merged in distributed shared memory)
-  int32_t n_clusters;      // clusters per (row, KV group); > 1 merges through the workspace
+  int32_t n_splits;        // splits per (row, KV group)
   int32_t split_tokens;    // selected-list entries per split
-  void* out;               // [rows, Hq, D]
-  float* lse;              // [rows, Hq] or null
-  uint32_t* counters;      // [rows * Hkv] tickets, zero between calls (n_clusters > 1)
-  float* part_lse;         // [rows * Hkv, n_clusters, G]
-  float* part_o;           // [rows * Hkv, n_clusters, G, D]
+  int32_t total_rows;      // rows of the whole call (partial buffer stride)
+  void* out;               // [rows, Hq, D] (single split)
+  float* lse;              // [rows, Hq] or null (single split)
+  float* part_o;           // [n_splits, rows * Hq, D] normalised partials (several splits)
+  float* part_lse;         // [n_splits, rows * Hq]
   int32_t out_dtype;
 };
 
@@ -110,12 +121,14 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group,
                          cudaStream_t st);
 
+// Rows a scoring launch can also histogram (p.hist) for the selection.
+constexpr int kHistRows = 4;
+
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 
 struct AttnPlan {
-  int32_t cluster_size;
-  int32_t n_clusters;
+  int32_t n_splits;
   int32_t split_tokens;
   int32_t stages;
 };
@@ -123,9 +136,9 @@ struct AttnPlan {
 // Split plan for pairs = rows * Hkv (row, KV group) pairs whose selected lists
 // are at most n_list entries; user_splits > 0 fixes the splits per pair.
 AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_list, int user_splits);
-size_t attn_workspace_bytes(const AttnPlan& pl, int64_t pairs, int group, int head_dim);
-void attn_workspace_layout(const AttnPlan& pl, int64_t pairs, int group, void* ws, uint32_t** counters,
-                           float** part_lse, float** part_o);
+size_t attn_workspace_bytes(const AttnPlan& pl, int64_t rows, int n_q_heads, int head_dim);
+void attn_workspace_layout(const AttnPlan& pl, int64_t rows, int n_q_heads, int head_dim, void* ws, float** part_o,
+                           float** part_lse);
 
 template <int NSEQ>
 cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st);

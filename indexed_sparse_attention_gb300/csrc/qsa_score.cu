@@ -93,7 +93,6 @@ __device__ __forceinline__ int find_seq_by_work(const ScoreParams<NSEQ>& p, int6
 // (2t+8, 2t+9) <- channels (4t+2, 4t+3).  A and B use the same channel
 // permutation, so the dot products are unchanged and each thread reads one
 // float4 per row per k-step.
-constexpr int kScoreWarps = 12;
 constexpr int kScoreStages = 2;
 constexpr int kRowPitch = 144;   // floats per staged row: 576 bytes keep the float4 reads conflict-free
 constexpr int kStageFloats = kScoreTile * kRowPitch;
@@ -142,9 +141,18 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams<NSEQ>& p, int6
   return x;
 }
 
-template <int NT, int NSEQ>
-__global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const ScoreParams<NSEQ> p) {
+// HIST: the launch also counts every score it writes in its row's histogram
+// of the top 12 key bits (one sequence, one group of <= 4 rows): per-CTA
+// counts in shared memory, added to p.hist once at the end.
+template <int NT, int NSEQ, int WARPS, bool HIST>
+__global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScoreParams<NSEQ> p) {
   extern __shared__ float4 score_smem4[];
+  constexpr int kScoreWarps = WARPS;
+  uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(score_smem4) + WARPS * kScoreStages * kStageFloats);
+  if (HIST) {
+    for (int i = threadIdx.x; i < kHistRows * kSelBins; i += WARPS * 32) hist_s[i] = 0u;
+    __syncthreads();
+  }
   grid_dependency_sync();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -239,8 +247,14 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const Sc
         if ((t & 1) == 0 && r < cur.rows) {
           const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, cur.row0 + r));
           float* dst = p.scores + (int64_t)(sq.row_begin + cur.row0 + r) * p.ld;
-          if (cur.b0 + g < nb) dst[cur.b0 + g] = v0 * kScoreScale;
-          if (cur.b0 + g + 8 < nb) dst[cur.b0 + g + 8] = v1 * kScoreScale;
+          if (cur.b0 + g < nb) {
+            dst[cur.b0 + g] = v0 * kScoreScale;
+            if (HIST) atomicAdd(&hist_s[r * kSelBins + (order_key(v0 * kScoreScale) >> 20)], 1u);
+          }
+          if (cur.b0 + g + 8 < nb) {
+            dst[cur.b0 + g + 8] = v1 * kScoreScale;
+            if (HIST) atomicAdd(&hist_s[r * kSelBins + (order_key(v1 * kScoreScale) >> 20)], 1u);
+          }
         }
       }
     }
@@ -254,6 +268,13 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) score_mma_kernel(const Sc
     stage ^= 1;
   }
   cp_async_wait<0>();
+  if (HIST) {
+    __syncthreads();
+    const ScoreSeq& sq = p.seq[0];
+    const int rows = min(kHistRows, sq.n_rows);
+    for (int i = threadIdx.x; i < rows * kSelBins; i += WARPS * 32)
+      if (hist_s[i]) atomicAdd(p.hist + (int64_t)(sq.row_begin + i / kSelBins) * kSelBins + i % kSelBins, hist_s[i]);
+  }
 }
 
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
@@ -329,20 +350,36 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
   if (p.n_work == 0) return cudaSuccess;
   if (q_dtype == QSA_F32) {
-    return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0, p);
+    return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0u, p);
   }
-  const size_t smem = sizeof(float) * kScoreWarps * kScoreStages * kStageFloats;
-  const int64_t need = (p.n_work + kScoreWarps - 1) / kScoreWarps;
-  const unsigned grid = (unsigned)(need < device_sm_count() ? need : device_sm_count());
-  const void* k = max_rows_per_group <= 2   ? (const void*)score_mma_kernel<1, NSEQ>
-                  : max_rows_per_group <= 4 ? (const void*)score_mma_kernel<2, NSEQ>
-                                            : (const void*)score_mma_kernel<4, NSEQ>;
+  const int sms = device_sm_count();
+  if (p.hist) {
+    // 8 warps: their stages (147 KB) and the 4 rows' histograms (64 KB) share the CTA.
+    constexpr int Wh = 8;
+    const size_t smem = sizeof(float) * Wh * kScoreStages * kStageFloats + sizeof(uint32_t) * kHistRows * kSelBins;
+    const int64_t need = (p.n_work + Wh - 1) / Wh;
+    const unsigned grid = (unsigned)(need < sms ? need : sms);
+    const void* k = max_rows_per_group <= 2 ? (const void*)score_mma_kernel<1, NSEQ, Wh, true>
+                                            : (const void*)score_mma_kernel<2, NSEQ, Wh, true>;
+    cudaError_t e = allow_dynamic_smem(k, smem);
+    if (e != cudaSuccess) return e;
+    if (max_rows_per_group <= 2)
+      return launch_kernel(score_mma_kernel<1, NSEQ, Wh, true>, dim3(grid), dim3(Wh * 32), smem, st, 0u, p);
+    return launch_kernel(score_mma_kernel<2, NSEQ, Wh, true>, dim3(grid), dim3(Wh * 32), smem, st, 0u, p);
+  }
+  constexpr int Ws = 12;
+  const size_t smem = sizeof(float) * Ws * kScoreStages * kStageFloats;
+  const int64_t need = (p.n_work + Ws - 1) / Ws;
+  const unsigned grid = (unsigned)(need < sms ? need : sms);
+  const void* k = max_rows_per_group <= 2   ? (const void*)score_mma_kernel<1, NSEQ, Ws, false>
+                  : max_rows_per_group <= 4 ? (const void*)score_mma_kernel<2, NSEQ, Ws, false>
+                                            : (const void*)score_mma_kernel<4, NSEQ, Ws, false>;
   cudaError_t e = allow_dynamic_smem(k, smem);
   if (e != cudaSuccess) return e;
-  const dim3 block(kScoreWarps * 32);
-  if (max_rows_per_group <= 2) return launch_kernel(score_mma_kernel<1, NSEQ>, dim3(grid), block, smem, st, 0, p);
-  if (max_rows_per_group <= 4) return launch_kernel(score_mma_kernel<2, NSEQ>, dim3(grid), block, smem, st, 0, p);
-  return launch_kernel(score_mma_kernel<4, NSEQ>, dim3(grid), block, smem, st, 0, p);
+  const dim3 block(Ws * 32);
+  if (max_rows_per_group <= 2) return launch_kernel(score_mma_kernel<1, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
+  if (max_rows_per_group <= 4) return launch_kernel(score_mma_kernel<2, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
+  return launch_kernel(score_mma_kernel<4, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
 }
 
 template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);

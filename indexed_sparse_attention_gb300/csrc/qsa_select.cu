@@ -30,16 +30,10 @@ namespace qsa {
 
 namespace {
 
-constexpr int kBins = 4096;          // top 12 key bits
+constexpr int kBins = kSelBins;      // top 12 key bits
 constexpr int kCandCap = 2048;       // candidates kept by CTA 0
 constexpr int kThreads = 512;
 constexpr int kMaxCluster = 16;
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;  // -0.0 ties with +0.0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Exclusive prefix sum of v over the CTA; *total gets the sum of all v.
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
@@ -115,9 +109,11 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool act, uint32_t bin,
   if (act && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
 }
 
+constexpr int kSubCap = 256;        // candidates sharing the k-th key's top 24 bits, resolved by rank
+
 struct SelSmem {
   // offsets in 32-bit words
-  int own, merged, keys, selw, eqw, ck, ci, total;
+  int own, merged, keys, selw, eqw, ck, ci, h2, subk, subi, total;
   __host__ __device__ SelSmem(int chunk, int nw) {
     own = 0;
     merged = own + kBins;
@@ -126,7 +122,10 @@ struct SelSmem {
     eqw = selw + nw;
     ck = eqw + nw;
     ci = ck + kCandCap;
-    total = ci + kCandCap;
+    h2 = ci + kCandCap;      // second-level histogram (key bits 19..8) of the candidates, in CTA 0
+    subk = h2 + kBins;
+    subi = subk + kSubCap;
+    total = subi + kSubCap;
   }
 };
 
@@ -136,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
   extern __shared__ uint32_t sm[];
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_res[2];
-  __shared__ uint32_t s_cand;
+  __shared__ uint32_t s_cand, s_sub;
   cg::cluster_group cluster = cg::this_cluster();
   grid_dependency_sync();
   const int S = (int)cluster.num_blocks();
@@ -168,65 +167,82 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
   const int i0 = c * chunk;
   const int i1 = min(n, i0 + chunk);
 
-  // 1. Histogram of this CTA's keys (kept in shared memory for step 3).
-  for (int b = tid; b < kBins; b += kThreads) own[b] = 0u;
   if (c == 0) {
     for (int i = tid; i < nw; i += kThreads) sm[L.eqw + i] = 0u;
-    if (tid == 0) s_cand = 0u;
-  }
-  __syncthreads();
-  // Loads are issued 8 per thread at a time, then counted.
-  for (int base = i0 + warp * 32; base < i0 + chunk; base += 8 * kThreads) {
-    float v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = base + j * kThreads + lane;
-      v[j] = i < i1 ? __ldg(srow + i) : 0.f;
+    for (int b = tid; b < kBins; b += kThreads) sm[L.h2 + b] = 0u;
+    if (tid == 0) {
+      s_cand = 0u;
+      s_sub = 0u;
     }
+  }
+  if (tid == 0) {   // a histogram that cannot hold the k-th key leaves bin 0
+    s_res[0] = 0u;
+    s_res[1] = 0u;
+  }
+  const uint32_t* hrow = p.hist ? p.hist + (int64_t)r * kBins : nullptr;
+  if (hrow) {
+    // The scoring kernel left the row's histogram: every CTA reads it.
+    cluster.sync();   // peers are running and CTA 0's candidate state is zeroed
+    find_bin([&](int b) { return __ldcg(hrow + b); }, kBins, (uint32_t)k, warp_sums, s_res);
+  } else {
+    // 1. Histogram of this CTA's keys (kept in shared memory for step 3).
+    for (int b = tid; b < kBins; b += kThreads) own[b] = 0u;
+    __syncthreads();
+    // Loads are issued 8 per thread at a time, then counted.
+    for (int base = i0 + warp * 32; base < i0 + chunk; base += 8 * kThreads) {
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = base + j * kThreads + lane;
-      if (i < i1) {
-        const uint32_t key = order_key(v[j]);
-        if (cache_keys) keys[i - i0] = key;
-        atomicAdd(&own[key >> 20], 1u);
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * kThreads + lane;
+        v[j] = i < i1 ? __ldg(srow + i) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = base + j * kThreads + lane;
+        if (i < i1) {
+          const uint32_t key = order_key(v[j]);
+          if (cache_keys) keys[i - i0] = key;
+          atomicAdd(&own[key >> 20], 1u);
+        }
       }
     }
-  }
-  cluster.sync();
+    cluster.sync();
 
-  // 2. Sum bin slice c over the cluster and broadcast it to every CTA.
-  {
-    const int per = kBins / S;
-    for (int b = c * per + tid; b < (c + 1) * per; b += kThreads) {
-      uint32_t h[kMaxCluster];
+    // 2. Sum bin slice c over the cluster and broadcast it to every CTA.
+    {
+      const int per = kBins / S;
+      for (int b = c * per + tid; b < (c + 1) * per; b += kThreads) {
+        uint32_t h[kMaxCluster];
 #pragma unroll
-      for (int q = 0; q < kMaxCluster; ++q) h[q] = q < S ? *cluster.map_shared_rank(own + b, q) : 0u;
-      uint32_t sum = 0u;
+        for (int q = 0; q < kMaxCluster; ++q) h[q] = q < S ? *cluster.map_shared_rank(own + b, q) : 0u;
+        uint32_t sum = 0u;
 #pragma unroll
-      for (int q = 0; q < kMaxCluster; ++q) sum += h[q];
+        for (int q = 0; q < kMaxCluster; ++q) sum += h[q];
 #pragma unroll
-      for (int q = 0; q < kMaxCluster; ++q)
-        if (q < S) *cluster.map_shared_rank(merged + b, q) = sum;
+        for (int q = 0; q < kMaxCluster; ++q)
+          if (q < S) *cluster.map_shared_rank(merged + b, q) = sum;
+      }
     }
+    cluster.sync();
+    find_bin([&](int b) { return merged[b]; }, kBins, (uint32_t)k, warp_sums, s_res);
   }
-  cluster.sync();
-  find_bin([&](int b) { return merged[b]; }, kBins, (uint32_t)k, warp_sums, s_res);
   const uint32_t B = s_res[0];
   uint32_t need = (uint32_t)k - s_res[1];
-  const bool overflow = merged[B] > (uint32_t)kCandCap;
+  const bool overflow = (hrow ? __ldcg(hrow + B) : merged[B]) > (uint32_t)kCandCap;
+  const bool cached = cache_keys && !hrow;
 
   // 3. Bitmap words (bin above B) and candidates (bin B) into CTA 0.
   uint32_t* selw0 = cluster.map_shared_rank(sm + L.selw, 0);
   uint32_t* ck0 = cluster.map_shared_rank(sm + L.ck, 0);
   uint32_t* ci0 = cluster.map_shared_rank(sm + L.ci, 0);
   uint32_t* cand0 = cluster.map_shared_rank(&s_cand, 0);
+  uint32_t* h20 = cluster.map_shared_rank(sm + L.h2, 0);
   if (i0 < i1) {
     const int w0 = i0 >> 5, w1 = (i1 + 31) >> 5;
     for (int word = w0 + warp; word < w1; word += kThreads / 32) {
       const int i = word * 32 + lane;
       const bool in = i < i1;
-      const uint32_t key = in ? (cache_keys ? keys[i - i0] : order_key(srow[i])) : 0u;
+      const uint32_t key = in ? (cached ? keys[i - i0] : order_key(srow[i])) : 0u;
       const uint32_t bin = key >> 20;
       const uint32_t gt = __ballot_sync(0xffffffffu, in && bin > B);
       const uint32_t eq = __ballot_sync(0xffffffffu, in && bin == B);
@@ -239,6 +255,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
           const uint32_t at = base + __popc(eq & ((1u << lane) - 1u));
           ck0[at] = key;
           ci0[at] = (uint32_t)i;
+          atomicAdd(h20 + ((key >> 8) & (kBins - 1)), 1u);
         }
       }
     }
@@ -252,28 +269,61 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
   uint32_t* hist = own;                 // free again: reused as radix scratch
   uint32_t prefix = B << 20;
   uint32_t pmask = 0xfff00000u;
+  bool ranked = false;   // candidates resolved by rank: no "equal key" bitmap to apply
   if (!overflow) {
     const int C = (int)s_cand;
     const uint32_t* ck = sm + L.ck;
     const uint32_t* ci = sm + L.ci;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = pass == 0 ? 10 : 0;
-      for (int b = tid; b < 1024; b += kThreads) hist[b] = 0u;
+    uint32_t* subk = sm + L.subk;
+    uint32_t* subi = sm + L.subi;
+    // Second level: the bin of key bits 19..8 holding the k-th key.
+    find_bin([&](int b) { return sm[L.h2 + b]; }, kBins, need, warp_sums, s_res);
+    const uint32_t need2 = need - s_res[1];
+    const uint32_t p24 = (B << 12) | s_res[0];
+    for (int i = tid; i < C; i += kThreads) {
+      const uint32_t key = ck[i], id = ci[i], k24 = key >> 8;
+      if (k24 > p24) {
+        atomicOr(&selw[id >> 5], 1u << (id & 31));
+      } else if (k24 == p24) {
+        const uint32_t j = atomicAdd(&s_sub, 1u);
+        if (j < (uint32_t)kSubCap) {
+          subk[j] = key;
+          subi[j] = id;
+        }
+      }
+    }
+    __syncthreads();
+    const int n_sub = (int)s_sub;
+    if (n_sub <= kSubCap) {
+      // Keep the need2 best of the few candidates left, by (key desc, id asc).
+      for (int j = tid; j < n_sub; j += kThreads) {
+        const uint32_t kj = subk[j], ij = subi[j];
+        uint32_t rank = 0u;
+        for (int i = 0; i < n_sub; ++i) rank += (subk[i] > kj) || (subk[i] == kj && subi[i] < ij);
+        if (rank < need2) atomicOr(&selw[ij >> 5], 1u << (ij & 31));
+      }
+      ranked = true;
+    } else {
+      // Too many near-ties: a last radix pass over key bits 7..0.
+      need = need2;
+      prefix = p24 << 8;
+      pmask = 0xffffff00u;
+      for (int b = tid; b < 256; b += kThreads) hist[b] = 0u;
       __syncthreads();
       for (int i = tid; i < C; i += kThreads)
-        if ((ck[i] & pmask) == prefix) atomicAdd(&hist[(ck[i] >> shift) & 1023u], 1u);
+        if ((ck[i] & pmask) == prefix) atomicAdd(&hist[ck[i] & 255u], 1u);
       __syncthreads();
-      find_bin([&](int b) { return hist[b]; }, 1024, need, warp_sums, s_res);
+      find_bin([&](int b) { return hist[b]; }, 256, need, warp_sums, s_res);
       need -= s_res[1];
-      prefix |= s_res[0] << shift;
-      pmask |= 1023u << shift;
+      prefix |= s_res[0];
       __syncthreads();
-    }
-    for (int i = tid; i < C; i += kThreads) {
-      const uint32_t key = ck[i], id = ci[i];
-      if (key > prefix) atomicOr(&selw[id >> 5], 1u << (id & 31));
-      else if (key == prefix) atomicOr(&eqw[id >> 5], 1u << (id & 31));
+      for (int i = tid; i < C; i += kThreads) {
+        const uint32_t key = ck[i], id = ci[i];
+        if ((key >> 8) == p24) {
+          if (key > prefix) atomicOr(&selw[id >> 5], 1u << (id & 31));
+          else if (key == prefix) atomicOr(&eqw[id >> 5], 1u << (id & 31));
+        }
+      }
     }
   } else {
 #pragma unroll 1
@@ -312,23 +362,27 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
     }
   }
   __syncthreads();
-  // Keep the `need` lowest ids among keys equal to the k-th key, then write
-  // every chosen id in ascending order.
+  // Keep the `need` lowest ids among keys equal to the k-th key (unless the
+  // candidates were ranked), then write every chosen id in ascending order.
   const int wp = (nw + kThreads - 1) / kThreads;
   const int a0 = tid * wp, a1 = min(nw, a0 + wp);
   uint32_t local = 0u, total;
-  for (int i = a0; i < a1; ++i) local += __popc(eqw[i]);
-  uint32_t cpos = block_exclusive_scan(local, warp_sums, &total);
-  local = 0u;
-  for (int i = a0; i < a1; ++i) {
-    uint32_t e = eqw[i];
-    const uint32_t pc = __popc(e);
-    if (cpos >= need) e = 0u;
-    else if (cpos + pc > need) e = lowest_bits(e, need - cpos);
-    cpos += pc;
-    e |= selw[i];
-    selw[i] = e;
-    local += __popc(e);
+  if (!ranked) {
+    for (int i = a0; i < a1; ++i) local += __popc(eqw[i]);
+    uint32_t cpos = block_exclusive_scan(local, warp_sums, &total);
+    local = 0u;
+    for (int i = a0; i < a1; ++i) {
+      uint32_t e = eqw[i];
+      const uint32_t pc = __popc(e);
+      if (cpos >= need) e = 0u;
+      else if (cpos + pc > need) e = lowest_bits(e, need - cpos);
+      cpos += pc;
+      e |= selw[i];
+      selw[i] = e;
+      local += __popc(e);
+    }
+  } else {
+    for (int i = a0; i < a1; ++i) local += __popc(selw[i]);
   }
   uint32_t at = block_exclusive_scan(local, warp_sums, &total);
   for (int i = a0; i < a1; ++i) {
@@ -341,6 +395,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
     }
   }
   if (tid == 0) p.cnt[r] = k;
+  // Every CTA of the row read the histogram before the last cluster barrier:
+  // return it to zero for the next call.
+  if (hrow)
+    for (int b = tid; b < kBins; b += kThreads) p.hist[(int64_t)r * kBins + b] = 0u;
 }
 
 }  // namespace

@@ -186,10 +186,9 @@ def test_attention_matches_oracle(dtype, D, n_splits):
     assert_attn_close(out, lse, ref_out, ref_lse, dtype == torch.bfloat16)
 
 
-def test_attention_multi_cluster_workspace_returns_to_zero():
-    # 40 splits per (row, KV group) span several clusters, which merge through
-    # the workspace; a second call on the same workspace gives the same result
-    # and the workspace is zero-filled again afterwards.
+def test_attention_many_splits_reuse_workspace():
+    # 40 splits per (row, KV group) merge through the workspace; a second call
+    # on the same (now dirty) workspace gives the same result.
     x = make_layer(L=9001, M=3, dtype=torch.bfloat16, seed=13)
     sel, cnt, _ = _oracle_selection(x)
     q, k, v = x.q.to(dev()), x.k.to(dev()), x.v.to(dev())
@@ -198,7 +197,7 @@ def test_attention_multi_cluster_workspace_returns_to_zero():
     cfg = qsa.attn_config(q, 2, torch.float32, 0.0, 40)
     need = qsa.attn_workspace_size(seqs, cfg, sel.shape[1])
     assert need > 0
-    ws = torch.zeros(need, dtype=torch.uint8, device=dev())
+    ws = torch.full((need,), 0x7F, dtype=torch.uint8, device=dev())
     outs = []
     for _ in range(2):
         out = torch.full((x.M, 24, 256), float("nan"), device=dev())
@@ -210,8 +209,6 @@ def test_attention_multi_cluster_workspace_returns_to_zero():
     for o, l in outs:
         assert_attn_close(o, l, ref_out, ref_lse, True)
     np.testing.assert_array_equal(outs[0][0], outs[1][0])
-    n_pairs = x.M * 2
-    assert (ws[: 4 * n_pairs].view(torch.int32) == 0).all()
 
 
 def test_attention_bf16_output():
