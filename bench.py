@@ -468,7 +468,7 @@ def main():
 
 
 # Revision tag of the scoring kernel whose DRAM counters profiles/ holds.
-SCORE_KERNEL_REV = "score_mma_v2"
+SCORE_KERNEL_REV = "score_mma_tf32_gmax_v3"
 
 if __name__ == "__main__":
     main()

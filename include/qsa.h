@@ -62,6 +62,7 @@ extern "C" {
 #define QSA_MAX_SEGMENTS 12        /* KV segments per sequence */
 #define QSA_MAX_FEW_ROWS 8         /* rows per sequence on the few-row scoring path */
 #define QSA_MAX_BLOCKS (1 << 18)   /* complete blocks per sequence (1,048,576 tokens) */
+#define QSA_SCORE_GROUP 16         /* blocks per group of the group maxima (qsa_score_blocks) */
 
 typedef enum qsa_status {
   QSA_OK = 0,
@@ -145,21 +146,30 @@ qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_
  * every pooled block; section 03: a few-row variant for decode and verify
  * and a wide variant for prefill).
  *   scores[r * ld + b] = (1/sqrt(128)) * sum_{h<4} max(0, q_idx[r][h] . pooled_s[b])
- * for every b < nb(p_r); entries b >= nb(p_r) are left unwritten.
+ * for every b < nb(p_r); entries b >= nb(p_r) are left unwritten.  With
+ * group_max given, also the maximum score of every group of QSA_SCORE_GROUP
+ * consecutive blocks:
+ *   group_max[r * group_ld + g] = max { scores[r * ld + b] : 16g <= b < min(16g + 16, nb(p_r)) }
+ * for g < ceil(nb(p_r) / 16); other entries are left unwritten.
  *   seqs, n_seqs   host descriptors; uses n_tokens, n_rows, pooled, pooled_stride
  *   q_idx          device [rows, 4, 128], q_idx_dtype
  *   scores         device [rows, ld] f32, ld >= max_r nb(p_r)
- * Arithmetic: fp32-exact products (bf16 index queries against the fp32
- * pooled key split into three bf16 parts on the tensor pipe; fp32 index
- * queries on the CUDA cores) with fp32 accumulation.
+ *   group_max      device [rows, group_ld] f32, group_ld >= max_r ceil(nb(p_r) / 16)
+ *                  and a multiple of 4; may be NULL (not written)
+ * Arithmetic: fp32 accumulation of products that lose nothing of the fp32
+ * pooled key beyond one fp32 ulp (bf16 index queries on the tensor pipe:
+ * for groups of <= 4 rows per sequence the key is split into two tf32
+ * parts, otherwise into three bf16 parts that sum to it exactly; fp32 index
+ * queries on the CUDA cores).
  */
 qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
-                            qsa_dtype q_idx_dtype, float* scores, int64_t ld, void* stream);
+                            qsa_dtype q_idx_dtype, float* scores, int64_t ld, float* group_max,
+                            int64_t group_ld, void* stream);
 
 /*
- * Scratch bytes qsa_select_topk needs for these sequences.  The current
- * kernels keep all selection state in shared memory and return 0; the
- * workspace arguments are kept so that variants needing scratch keep the ABI.
+ * Scratch bytes qsa_select_topk needs for these sequences.  The kernel keeps
+ * all selection state in shared memory and this returns 0; the workspace
+ * arguments are kept so that variants needing scratch keep the ABI.
  */
 size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k);
 
@@ -175,28 +185,27 @@ size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t to
  * The tail block (tokens 4*nb(p_r)..p_r) is not listed; qsa_sparse_attn adds
  * it.  Scores must not be NaN.  top_k in 1..QSA_MAX_TOP_K.
  *   scores         device [rows, ld] f32 (as written by qsa_score_blocks)
+ *   group_max      device [rows, group_ld] f32, the group maxima of exactly
+ *                  these scores as qsa_score_blocks writes them; may be NULL,
+ *                  and then the kernel takes the maxima from the scores
  *   sel, cnt       device int32 [rows, top_k], [rows]
  *   workspace      device scratch of >= qsa_select_workspace_size bytes
  *                  (may be NULL when that size is 0)
- * One thread-block cluster of up to 16 CTAs handles a row: per-CTA histograms
- * of the top 12 key bits are summed through distributed shared memory.
+ * One CTA per row: the group maxima bound the k-th score from below, so
+ * only groups whose maximum can reach the top k are read again, and an
+ * exact radix select runs over their blocks.
  */
 qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld,
-                           int32_t top_k, int32_t* sel, int32_t* cnt, void* workspace,
-                           size_t workspace_bytes, void* stream);
+                           const float* group_max, int64_t group_ld, int32_t top_k, int32_t* sel,
+                           int32_t* cnt, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Steps 2 and 3 in one call.  For one sequence of at most 4 rows with bf16
- * index queries (decode and verify) the scoring kernel also counts every
- * score in its row's histogram of the top 12 key bits, and the selection
- * starts from that histogram instead of building its own; any other call
- * runs qsa_score_blocks then qsa_select_topk.  Results are those of the two
- * separate calls.
- *   workspace      device scratch of >= qsa_score_select_workspace_size bytes
- *                  (may be NULL when that size is 0).  It must be zero-filled
- *                  before its first use; every call leaves it zero-filled.
- *                  Two calls that share a workspace must not run
- *                  concurrently.
+ * Steps 2 and 3 in one call: qsa_score_blocks writes the group maxima into
+ * the workspace and qsa_select_topk starts from them.  Results are those of
+ * the two separate calls.
+ *   workspace      device scratch of >= qsa_score_select_workspace_size bytes;
+ *                  its contents need no initialisation.  Two calls that share
+ *                  a workspace must not run concurrently.
  * Other arguments as for qsa_score_blocks and qsa_select_topk.
  */
 size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k);

@@ -29,6 +29,7 @@ INDEX_HEADS = 4
 TOP_K = 512
 MAX_TOP_K = 1024
 MAX_SEGMENTS = 12
+SCORE_GROUP = 16
 
 STATUS = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_MISALIGNED",
           4: "QSA_ERR_WORKSPACE", 5: "QSA_ERR_CUDA"}
@@ -83,10 +84,10 @@ def lib() -> ctypes.CDLL:
     L.qsa_last_error.restype = ctypes.c_char_p
     L.qsa_version.restype = i32
     L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
-    L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp]
+    L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp]
     L.qsa_select_workspace_size.argtypes = [seqp, i32, i32]
     L.qsa_select_workspace_size.restype = sz
-    L.qsa_select_topk.argtypes = [seqp, i32, vp, i64, i32, vp, vp, vp, sz, vp]
+    L.qsa_select_topk.argtypes = [seqp, i32, vp, i64, vp, i64, i32, vp, vp, vp, sz, vp]
     L.qsa_score_select_workspace_size.argtypes = [seqp, i32, i32]
     L.qsa_score_select_workspace_size.restype = sz
     L.qsa_score_select_topk.argtypes = [seqp, i32, vp, i32, vp, i64, i32, vp, vp, vp, sz, vp]
@@ -184,34 +185,43 @@ def pool_index_keys(idx_keys: torch.Tensor, pooled: torch.Tensor, first_block: i
         pooled.data_ptr(), pooled.stride(0), _stream(stream)))
 
 
-def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None):
-    """Step 2: scores[r, b] for every complete block row r sees."""
+def n_groups(n_tokens: int) -> int:
+    """Groups of SCORE_GROUP blocks covering the complete blocks of n_tokens."""
+    return (n_tokens // 4 + SCORE_GROUP - 1) // SCORE_GROUP
+
+
+def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None,
+                 group_max: torch.Tensor | None = None):
+    """Step 2: scores[r, b] for every complete block row r sees; with
+    group_max, also each row's maximum over every group of 16 blocks."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     _check("qsa_score_blocks", lib().qsa_score_blocks(
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0),
-        _stream(stream)))
+        _ptr(group_max), 0 if group_max is None else group_max.stride(0), _stream(stream)))
 
 
 def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, top_k: int = TOP_K,
-                workspace: torch.Tensor | None = None, stream=None, seq_array=None):
-    """Step 3: the top_k best blocks per row, ascending ids, -1 padded."""
+                workspace: torch.Tensor | None = None, stream=None, seq_array=None,
+                group_max: torch.Tensor | None = None):
+    """Step 3: the top_k best blocks per row, ascending ids, -1 padded.
+    group_max: the group maxima score_blocks wrote for these scores, or None."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     need = lib().qsa_select_workspace_size(arr, len(arr), top_k)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
     _check("qsa_select_topk", lib().qsa_select_topk(
-        arr, len(arr), scores.data_ptr(), scores.stride(0), int(top_k), sel.data_ptr(), cnt.data_ptr(),
+        arr, len(arr), scores.data_ptr(), scores.stride(0), _ptr(group_max),
+        0 if group_max is None else group_max.stride(0), int(top_k), sel.data_ptr(), cnt.data_ptr(),
         _ptr(workspace), 0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def score_select_topk(seqs, q_idx: torch.Tensor, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor,
                       top_k: int = TOP_K, workspace: torch.Tensor | None = None, stream=None, seq_array=None):
-    """Steps 2 and 3 in one call (fused scoring histogram for decode/verify).
-    The workspace must start zero-filled; the library leaves it zero-filled."""
+    """Steps 2 and 3 in one call; the workspace holds the group maxima."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     need = lib().qsa_score_select_workspace_size(arr, len(arr), top_k)
     if need and workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=scores.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
     _check("qsa_score_select_topk", lib().qsa_score_select_topk(
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0), int(top_k),
         sel.data_ptr(), cnt.data_ptr(), _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -304,15 +314,16 @@ class LayerStep:
         self.arr = make_seq_array(self.seqs)
         self.cfg = attn_config(q, n_kv_heads, out_dtype, scale, n_splits)
         self.scores = torch.empty((rows, self.ld), dtype=torch.float32, device=dev)
+        gld = max(1, max(n_groups(s.n_tokens) for s in self.seqs))
+        self.group_max = torch.empty((rows, (gld + 3) // 4 * 4), dtype=torch.float32, device=dev)
         self.sel = torch.empty((rows, self.top_k), dtype=torch.int32, device=dev)
         self.cnt = torch.empty((rows,), dtype=torch.int32, device=dev)
         self.out = torch.empty((rows, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev)
         self.lse = torch.empty((rows, q.shape[1]), dtype=torch.float32, device=dev)
         sel_ws = int(lib().qsa_score_select_workspace_size(self.arr, len(self.arr), self.top_k))
         attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
-        # Workspaces start zero-filled; the library returns them zero-filled.
-        self.sel_ws = torch.zeros(max(sel_ws, 16), dtype=torch.uint8, device=dev)
-        self.ws = torch.zeros(max(attn_ws, 16), dtype=torch.uint8, device=dev)
+        self.sel_ws = torch.empty(max(sel_ws, 16), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(max(attn_ws, 16), dtype=torch.uint8, device=dev)
         # Blocks completed by each sequence's new rows: [first, last] of nb(p) over its rows.
         self.pool_jobs = []
         for s in self.seqs:
@@ -328,10 +339,11 @@ class LayerStep:
             pool_index_keys(idxk, pooled, b0, n, stream)
 
     def score(self, stream=None):
-        score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr)
+        score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr, group_max=self.group_max)
 
     def select(self, stream=None):
-        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr)
+        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr,
+                    group_max=self.group_max)
 
     def score_select(self, stream=None):
         score_select_topk(None, self.q_idx, self.scores, self.sel, self.cnt, self.top_k, self.sel_ws, stream,
@@ -343,6 +355,7 @@ class LayerStep:
 
     def run(self, stream=None):
         self.pool(stream)
-        self.score_select(stream)
+        self.score(stream)
+        self.select(stream)
         self.attend(stream)
         return self.out, self.lse

@@ -43,6 +43,7 @@ bool valid_dtype(int d) { return d == QSA_F32 || d == QSA_BF16; }
 
 // Complete blocks the last (furthest) row of a sequence sees: floor(L / 4).
 int64_t max_visible_blocks(const qsa_seq& s) { return s.n_tokens / 4; }
+int64_t n_groups(int64_t blocks) { return (blocks + QSA_SCORE_GROUP - 1) / QSA_SCORE_GROUP; }
 
 qsa_status check_rows(const qsa_seq* seqs, int32_t n_seqs, const char* fn, int64_t* total_rows) {
   if (!seqs || n_seqs < 1) return fail(QSA_ERR_INVALID_ARG, "%s: need at least one sequence", fn);
@@ -86,41 +87,6 @@ cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes) {
     if (x.dev == dev && x.kernel == kernel && x.bytes >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) done.push_back(Entry{dev, kernel, bytes});
-  return e;
-}
-
-cudaError_t allow_cluster16(const void* kernel, int threads, size_t smem) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  struct Entry {
-    int dev;
-    const void* kernel;
-    size_t smem;
-    cudaError_t result;
-  };
-  static std::vector<Entry> done;
-  std::lock_guard<std::mutex> lk(g_dev_mu);
-  for (const Entry& x : done)
-    if (x.dev == dev && x.kernel == kernel && x.smem == smem) return x.result;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
-    cfg.blockDim = dim3((unsigned)threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-    if (e == cudaSuccess && n < 1) e = cudaErrorNotSupported;
-  }
-  done.push_back(Entry{dev, kernel, smem, e});
   return e;
 }
 
@@ -179,9 +145,10 @@ QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype
 // ------------------------------------------------------------------ step 2
 template <int NSEQ>
 static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const void* q_idx, qsa_dtype qd,
-                              float* scores, int64_t ld, cudaStream_t st, uint32_t* hist = nullptr) {
+                              float* scores, int64_t ld, float* gmax, int64_t gld, cudaStream_t st) {
   ScoreParams<NSEQ> p{};
-  p.hist = hist;
+  p.gmax = gmax;
+  p.gld = gld;
   const int tile = score_tile_blocks(qd);
   int64_t work = 0;
   int max_rows = 1;
@@ -210,7 +177,7 @@ static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, con
 }
 
 QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
-                            float* scores, int64_t ld, void* stream) {
+                            float* scores, int64_t ld, float* group_max, int64_t group_ld, void* stream) {
   const char* fn = "qsa_score_blocks";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -218,8 +185,13 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
   if (!valid_dtype(q_idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: q_idx_dtype %d", fn, (int)q_idx_dtype);
   if (!q_idx || !scores) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (!aligned16(q_idx) || !aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx/scores not aligned", fn);
+  if (group_max && (!aligned16(group_max) || group_ld % 4 != 0))
+    return fail(QSA_ERR_MISALIGNED, "%s: group_max or group_ld not 16-byte aligned", fn);
   for (int i = 0; i < n_seqs; ++i) {
     const qsa_seq& q = seqs[i];
+    if (group_max && n_groups(max_visible_blocks(q)) > group_ld)
+      return fail(QSA_ERR_INVALID_ARG, "%s: group_ld=%lld < %lld groups of sequence %d", fn, (long long)group_ld,
+                  (long long)n_groups(max_visible_blocks(q)), i);
     if (max_visible_blocks(q) > ld)
       return fail(QSA_ERR_INVALID_ARG, "%s: ld=%lld < %lld visible blocks of sequence %d", fn, (long long)ld,
                   (long long)max_visible_blocks(q), i);
@@ -232,12 +204,12 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
   }
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, st);
+    s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = score_chunk<kLaunchSeqs>(seqs + c, n, row_begin, q_idx, q_idx_dtype, scores, ld, st);
+      s = score_chunk<kLaunchSeqs>(seqs + c, n, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
@@ -254,9 +226,11 @@ QSA_API size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, in
 
 template <int NSEQ>
 static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const float* scores, int64_t ld,
-                               int32_t top_k, int32_t* sel, int32_t* cnt, cudaStream_t st, uint32_t* hist = nullptr) {
+                               const float* gmax, int64_t gld, int32_t top_k, int32_t* sel, int32_t* cnt,
+                               cudaStream_t st) {
   SelectParams<NSEQ> p{};
-  p.hist = hist;
+  p.gmax = gmax;
+  p.gld = gld;
   int rows = 0;
   int64_t max_nb = 0;
   p.row_base = row_begin;
@@ -278,8 +252,9 @@ static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, co
   return QSA_OK;
 }
 
-QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld, int32_t top_k,
-                           int32_t* sel, int32_t* cnt, void* workspace, size_t workspace_bytes, void* stream) {
+QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld,
+                                   const float* group_max, int64_t group_ld, int32_t top_k, int32_t* sel, int32_t* cnt,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
   const char* fn = "qsa_select_topk";
   (void)workspace;
   (void)workspace_bytes;
@@ -289,18 +264,23 @@ QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const fl
   if (top_k < 1 || top_k > QSA_MAX_TOP_K)
     return fail(QSA_ERR_UNSUPPORTED, "%s: top_k=%d outside 1..%d", fn, top_k, QSA_MAX_TOP_K);
   if (!scores || !sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
-  if (!aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: scores not aligned", fn);
-  for (int i = 0; i < n_seqs; ++i)
+  if (!aligned16(scores) || ld % 4 != 0) return fail(QSA_ERR_MISALIGNED, "%s: scores or ld not 16-byte aligned", fn);
+  if (group_max && (!aligned16(group_max) || group_ld % 4 != 0))
+    return fail(QSA_ERR_MISALIGNED, "%s: group_max or group_ld not 16-byte aligned", fn);
+  for (int i = 0; i < n_seqs; ++i) {
     if (max_visible_blocks(seqs[i]) > ld)
       return fail(QSA_ERR_INVALID_ARG, "%s: ld smaller than the visible blocks of sequence %d", fn, i);
+    if (group_max && n_groups(max_visible_blocks(seqs[i])) > group_ld)
+      return fail(QSA_ERR_INVALID_ARG, "%s: group_ld smaller than the groups of sequence %d", fn, i);
+  }
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = select_chunk<1>(seqs, 1, 0, scores, ld, top_k, sel, cnt, st);
+    s = select_chunk<1>(seqs, 1, 0, scores, ld, group_max, group_ld, top_k, sel, cnt, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = select_chunk<kLaunchSeqs>(seqs + c, n, row_begin, scores, ld, top_k, sel, cnt, st);
+      s = select_chunk<kLaunchSeqs>(seqs + c, n, row_begin, scores, ld, group_max, group_ld, top_k, sel, cnt, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
@@ -309,17 +289,20 @@ QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const fl
 
 // ------------------------------------------------------------------ steps 2 + 3 fused
 namespace {
-// The fused path: one sequence of <= kHistRows rows with bf16 index queries;
-// the scoring kernel leaves each row's first-level histogram in the workspace.
-bool fused_score_select(const qsa_seq* seqs, int32_t n_seqs) {
-  return n_seqs == 1 && seqs[0].n_rows <= kHistRows;
+// Row stride of the group maxima a fused call keeps in its workspace.
+int64_t fused_group_ld(const qsa_seq* seqs, int32_t n_seqs) {
+  int64_t g = 0;
+  for (int i = 0; i < n_seqs; ++i) g = std::max(g, n_groups(max_visible_blocks(seqs[i])));
+  return std::max<int64_t>(4, (g + 3) / 4 * 4);
 }
 }  // namespace
 
 QSA_API size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k) {
   (void)top_k;
-  if (!seqs || n_seqs < 1 || !fused_score_select(seqs, n_seqs)) return 0;
-  return sizeof(uint32_t) * (size_t)seqs[0].n_rows * kSelBins;
+  if (!seqs || n_seqs < 1) return 0;
+  int64_t rows = 0;
+  for (int i = 0; i < n_seqs; ++i) rows += std::max(0, seqs[i].n_rows);
+  return sizeof(float) * (size_t)rows * (size_t)fused_group_ld(seqs, n_seqs);
 }
 
 QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
@@ -331,32 +314,18 @@ QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, co
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
   if (s != QSA_OK) return s;
   const size_t need = qsa_score_select_workspace_size(seqs, n_seqs, top_k);
-  if (q_idx_dtype != QSA_BF16 || need == 0) {
-    // No fused path for this call: the two steps one after the other.
-    if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, stream)) != QSA_OK) return s;
-    return qsa_select_topk(seqs, n_seqs, scores, ld, top_k, sel, cnt, nullptr, 0, stream);
-  }
   if (!workspace || workspace_bytes < need)
     return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need,
                 workspace ? workspace_bytes : (size_t)0);
   if (!aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
-  // Validate both steps' arguments before the first launch.
+  // Check the selection's own arguments before the scoring launch.
   if (top_k < 1 || top_k > QSA_MAX_TOP_K)
     return fail(QSA_ERR_UNSUPPORTED, "%s: top_k=%d outside 1..%d", fn, top_k, QSA_MAX_TOP_K);
-  if (!q_idx || !scores || !sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
-  if (!aligned16(q_idx) || !aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx/scores not aligned", fn);
-  const qsa_seq& q = seqs[0];
-  if (max_visible_blocks(q) > ld) return fail(QSA_ERR_INVALID_ARG, "%s: ld smaller than the visible blocks", fn);
-  if (max_visible_blocks(q) > 0) {
-    if (!q.pooled || q.pooled_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: bad pooled keys", fn);
-    if (!aligned16(q.pooled) || q.pooled_stride % 4 != 0)
-      return fail(QSA_ERR_MISALIGNED, "%s: pooled keys not 16-byte aligned", fn);
-  }
-  cudaStream_t st = as_stream(stream);
-  uint32_t* hist = static_cast<uint32_t*>(workspace);
-  if ((s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, st, hist)) != QSA_OK) return s;
-  if ((s = select_chunk<1>(seqs, 1, 0, scores, ld, top_k, sel, cnt, st, hist)) != QSA_OK) return s;
-  return ok();
+  if (!sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  float* gmax = static_cast<float*>(workspace);
+  const int64_t gld = fused_group_ld(seqs, n_seqs);
+  if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, gmax, gld, stream)) != QSA_OK) return s;
+  return qsa_select_topk(seqs, n_seqs, scores, ld, gmax, gld, top_k, sel, cnt, nullptr, 0, stream);
 }
 
 // ------------------------------------------------------------------ step 4

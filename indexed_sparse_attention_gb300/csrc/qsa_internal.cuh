@@ -38,12 +38,12 @@ struct ScoreParams {
   const void* q_idx;     // [rows, 4, 128]
   float* scores;
   int64_t ld;
-  uint32_t* hist;        // optional [rows, kSelBins] histogram of the scores' top key bits
+  float* gmax;           // optional [rows, gld]: max score of each group of QSA_SCORE_GROUP blocks
+  int64_t gld;
 };
 
-// Bins of the selection's first radix level: the top 12 bits of a score's
-// order-preserving key.
-constexpr int kSelBins = 4096;
+static_assert(kScoreTile == QSA_SCORE_GROUP, "a scoring tile is one group of the group maxima");
+
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;  // -0.0 ties with +0.0
@@ -64,11 +64,11 @@ struct SelectParams {
   int32_t row_base;      // global index of this launch's first row
   const float* scores;
   int64_t ld;
+  const float* gmax;     // optional group maxima [rows, gld] (from the scoring kernel)
+  int64_t gld;
   int32_t top_k;
   int32_t* sel;
   int32_t* cnt;
-  uint32_t* hist;        // optional [rows, kSelBins] first-level histogram made by the scoring
-                         // kernel; the selection returns it to zero
 };
 
 // ---------------------------------------------------------------- attention
@@ -121,11 +121,9 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group,
                          cudaStream_t st);
 
-// Rows a scoring launch can also histogram (p.hist) for the selection.
-constexpr int kHistRows = 4;
-
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
+size_t select_smem_bytes(int64_t max_nb);
 
 struct AttnPlan {
   int32_t n_splits;
@@ -150,10 +148,6 @@ int device_sm_count();
 
 // Raise a kernel's dynamic shared-memory limit (once per device and size).
 cudaError_t allow_dynamic_smem(const void* kernel, size_t bytes);
-
-// Allow 16-CTA clusters for a kernel (once per device); cudaErrorNotSupported
-// when no 16-CTA cluster of that shape can be resident.
-cudaError_t allow_cluster16(const void* kernel, int threads, size_t smem);
 
 // Blocks per scoring work item for the kernel that serves q_dtype.
 int score_tile_blocks(qsa_dtype q_dtype);

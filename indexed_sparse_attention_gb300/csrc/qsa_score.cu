@@ -5,10 +5,17 @@
 //
 // Scoring is a streaming pass over the pooled keys: every 512-byte pooled
 // block is read once per row-group of <= 8 query rows.  For bf16 index
-// queries the dot products run on the tensor pipe (mma.sync m16n8k16): the
-// fp32 pooled key is split into three bf16 parts hi + mid + lo that sum to it
-// exactly, and bf16 x bf16 products are exact in fp32, so the result carries
-// fp32-accumulation error only.  fp32 index queries take a CUDA-core kernel.
+// queries the dot products run on the tensor pipe with fp32 accumulation,
+// and the fp32 pooled key is split so that no product loses precision:
+//  - rows groups of <= 4 rows (decode, verify): tf32 MMAs (m16n8k8) on two
+//    planes, hi = the key rounded to tf32 and lo = key - hi (exact; the MMA
+//    keeps at least its top 11 bits, so hi + lo is the key to within one
+//    fp32 ulp); 3 integer/fp32 ops per key element;
+//  - wider groups (prefill): bf16 MMAs (m16n8k16) on three planes hi + mid +
+//    lo that sum to the key exactly.
+// bf16 queries are exact in both formats.  Every tile of 16 blocks is one
+// group of the group maxima the selection starts from.  fp32 index queries
+// take a CUDA-core kernel.
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -41,6 +48,24 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// x = hi + lo: hi is x rounded to 11 significant bits (to nearest, ties away
+// from zero, by integer add and mask on the bit pattern), lo = x - hi exactly
+// (|lo| <= 2^-12 |x|, a multiple of x's fp32 ulp, so it has <= 12 bits).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  const uint32_t h = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
+  hi = h;
+  lo = __float_as_uint(x - __uint_as_float(h));
 }
 
 // ------------------------------------------------------------------ pooling
@@ -141,24 +166,21 @@ __device__ __forceinline__ ScoreItem score_item(const ScoreParams<NSEQ>& p, int6
   return x;
 }
 
-// HIST: the launch also counts every score it writes in its row's histogram
-// of the top 12 key bits (one sequence, one group of <= 4 rows): per-CTA
-// counts in shared memory, added to p.hist once at the end.
-template <int NT, int NSEQ, int WARPS, bool HIST>
+// tf32 planes (rows groups of <= 4 rows): in every 16-channel k-step above,
+// thread t's float4 of channels 4t..4t+3 feeds two m16n8k8 steps -- channels
+// 4t, 4t+1 are fragment k = t, t+4 of the first, channels 4t+2, 4t+3 those of
+// the second -- and the queries take the same mapping.
+template <int NT, int NSEQ, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScoreParams<NSEQ> p) {
+  constexpr bool kTf32 = NT <= 2;
+  constexpr int kBq = kTf32 ? 4 : 2;
   extern __shared__ float4 score_smem4[];
-  constexpr int kScoreWarps = WARPS;
-  uint32_t* hist_s = reinterpret_cast<uint32_t*>(reinterpret_cast<float*>(score_smem4) + WARPS * kScoreStages * kStageFloats);
-  if (HIST) {
-    for (int i = threadIdx.x; i < kHistRows * kSelBins; i += WARPS * 32) hist_s[i] = 0u;
-    __syncthreads();
-  }
   grid_dependency_sync();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   float* my = reinterpret_cast<float*>(score_smem4) + warp * kScoreStages * kStageFloats;
-  const int64_t W = (int64_t)gridDim.x * kScoreWarps;
-  int64_t item = (int64_t)blockIdx.x * kScoreWarps + warp;
+  const int64_t W = (int64_t)gridDim.x * WARPS;
+  int64_t item = (int64_t)blockIdx.x * WARPS + warp;
 
   // 16 rows x 32 chunks of 16 bytes; lane takes chunks lane, lane + 32, ...
   auto issue = [&](const ScoreItem& x, int stage) {
@@ -181,7 +203,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
   issue(nxt, 1);
   cp_async_commit();
 
-  uint32_t bq[NT][8][2];
+  // B operand, the group's index queries: per n-tile and 16-channel step,
+  // tf32 words (channels 4t, 4t+1, 4t+2, 4t+3) or packed bf16 pairs.
+  uint32_t bq[NT][8][kBq];
   int bq_si = -1, bq_row0 = -1;
   int stage = 0;
   while (cur.valid) {
@@ -190,7 +214,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
     if (cur.active) {
       const ScoreSeq& sq = p.seq[cur.si];
       if (cur.si != bq_si || cur.row0 != bq_row0) {
-        // B operand: the group's index queries, bf16 [rows, 4, 128].
         const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -201,60 +224,115 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
           for (int s = 0; s < 8; ++s) {
             uint2 v = make_uint2(0u, 0u);
             if (r < cur.rows) v = *reinterpret_cast<const uint2*>(src + 16 * s);
-            bq[j][s][0] = v.x;
-            bq[j][s][1] = v.y;
+            if constexpr (kTf32) {
+              bq[j][s][0] = v.x << 16;
+              bq[j][s][1] = v.x & 0xffff0000u;
+              bq[j][s][kBq - 2] = v.y << 16;
+              bq[j][s][kBq - 1] = v.y & 0xffff0000u;
+            } else {
+              bq[j][s][0] = v.x;
+              bq[j][s][1] = v.y;
+            }
           }
         }
         bq_si = cur.si;
         bq_row0 = cur.row0;
       }
       const float* a = my + stage * kStageFloats;
-      // One accumulator per bf16 part keeps the MMA dependency chains short.
-      float acc[NT][4], accm[NT][4], accl[NT][4];
+      float acc[NT][4];
+      if constexpr (kTf32) {
+        // Separate accumulators per plane and k-step parity keep the MMA
+        // dependency chains short.
+        float ah[2][NT][4], al[2][NT][4];
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] = accm[j][e] = accl[j][e] = 0.f;
+          for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const float4 ra = *reinterpret_cast<const float4*>(a + g * kRowPitch + 16 * s + 4 * t);
-        const float4 rb = *reinterpret_cast<const float4*>(a + (g + 8) * kRowPitch + 16 * s + 4 * t);
-        uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
-        split3(ra.x, ra.y, h0, m0, l0);  // row g,   columns 2t, 2t+1
-        split3(rb.x, rb.y, h1, m1, l1);  // row g+8, columns 2t, 2t+1
-        split3(ra.z, ra.w, h2, m2, l2);  // row g,   columns 2t+8, 2t+9
-        split3(rb.z, rb.w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
+            for (int e = 0; e < 4; ++e) ah[q][j][e] = al[q][j][e] = 0.f;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          mma_bf16(accl[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
-          mma_bf16(accm[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
-          mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
+        for (int s = 0; s < 8; ++s) {
+          const float4 ra = *reinterpret_cast<const float4*>(a + g * kRowPitch + 16 * s + 4 * t);
+          const float4 rb = *reinterpret_cast<const float4*>(a + (g + 8) * kRowPitch + 16 * s + 4 * t);
+          uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+          split_tf32(ra.x, h0, l0);  // row g,   k = t     (channel 4t)
+          split_tf32(rb.x, h1, l1);  // row g+8, k = t
+          split_tf32(ra.y, h2, l2);  // row g,   k = t + 4 (channel 4t+1)
+          split_tf32(rb.y, h3, l3);  // row g+8, k = t + 4
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            mma_tf32(al[0][j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
+            mma_tf32(ah[0][j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
+          }
+          split_tf32(ra.z, h0, l0);  // channel 4t+2
+          split_tf32(rb.z, h1, l1);
+          split_tf32(ra.w, h2, l2);  // channel 4t+3
+          split_tf32(rb.w, h3, l3);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            mma_tf32(al[1][j], l0, l1, l2, l3, bq[j][s][kBq - 2], bq[j][s][kBq - 1]);
+            mma_tf32(ah[1][j], h0, h1, h2, h3, bq[j][s][kBq - 2], bq[j][s][kBq - 1]);
+          }
         }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] = (ah[0][j][e] + ah[1][j][e]) + (al[0][j][e] + al[1][j][e]);
+      } else {
+        // One accumulator per bf16 part keeps the MMA dependency chains short.
+        float accm[NT][4], accl[NT][4];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] = accm[j][e] = accl[j][e] = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const float4 ra = *reinterpret_cast<const float4*>(a + g * kRowPitch + 16 * s + 4 * t);
+          const float4 rb = *reinterpret_cast<const float4*>(a + (g + 8) * kRowPitch + 16 * s + 4 * t);
+          uint32_t h0, m0, l0, h1, m1, l1, h2, m2, l2, h3, m3, l3;
+          split3(ra.x, ra.y, h0, m0, l0);  // row g,   columns 2t, 2t+1
+          split3(rb.x, rb.y, h1, m1, l1);  // row g+8, columns 2t, 2t+1
+          split3(ra.z, ra.w, h2, m2, l2);  // row g,   columns 2t+8, 2t+9
+          split3(rb.z, rb.w, h3, m3, l3);  // row g+8, columns 2t+8, 2t+9
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            mma_bf16(accl[j], l0, l1, l2, l3, bq[j][s][0], bq[j][s][1]);
+            mma_bf16(accm[j], m0, m1, m2, m3, bq[j][s][0], bq[j][s][1]);
+            mma_bf16(acc[j], h0, h1, h2, h3, bq[j][s][0], bq[j][s][1]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] += accm[j][e] + accl[j][e];
       }
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] += accm[j][e] + accl[j][e];
       // Epilogue: thread (g, t) holds columns 8j+2t, 8j+2t+1 = heads 2(t&1),
-      // 2(t&1)+1 of row 2j + (t>>1); its neighbour t^1 holds the other two.
+      // 2(t&1)+1 of row 2j + (t>>1) for blocks b0+g and b0+g+8; its
+      // neighbour t^1 holds the other two heads.  The tile's maximum per row
+      // is its group maximum.
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         float v0 = fmaxf(acc[j][0], 0.f) + fmaxf(acc[j][1], 0.f);
         float v1 = fmaxf(acc[j][2], 0.f) + fmaxf(acc[j][3], 0.f);
         v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
         v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+        v0 *= kScoreScale;
+        v1 *= kScoreScale;
         const int r = 2 * j + (t >> 1);
+        const int64_t nb = r < cur.rows ? visible_blocks(row_position(sq.n_tokens, sq.n_rows, cur.row0 + r)) : 0;
+        const bool ok0 = cur.b0 + g < nb, ok1 = cur.b0 + g + 8 < nb;
+        const int64_t grow = sq.row_begin + cur.row0 + r;
         if ((t & 1) == 0 && r < cur.rows) {
-          const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, cur.row0 + r));
-          float* dst = p.scores + (int64_t)(sq.row_begin + cur.row0 + r) * p.ld;
-          if (cur.b0 + g < nb) {
-            dst[cur.b0 + g] = v0 * kScoreScale;
-            if (HIST) atomicAdd(&hist_s[r * kSelBins + (order_key(v0 * kScoreScale) >> 20)], 1u);
-          }
-          if (cur.b0 + g + 8 < nb) {
-            dst[cur.b0 + g + 8] = v1 * kScoreScale;
-            if (HIST) atomicAdd(&hist_s[r * kSelBins + (order_key(v1 * kScoreScale) >> 20)], 1u);
-          }
+          float* dst = p.scores + grow * p.ld;
+          if (ok0) dst[cur.b0 + g] = v0;
+          if (ok1) dst[cur.b0 + g + 8] = v1;
+        }
+        if (p.gmax) {
+          float m = fmaxf(ok0 ? v0 : -INFINITY, ok1 ? v1 : -INFINITY);
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          if (g == 0 && (t & 1) == 0 && cur.b0 < nb) p.gmax[grow * p.gld + cur.b0 / kScoreTile] = m;
         }
       }
     }
@@ -268,13 +346,6 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
     stage ^= 1;
   }
   cp_async_wait<0>();
-  if (HIST) {
-    __syncthreads();
-    const ScoreSeq& sq = p.seq[0];
-    const int rows = min(kHistRows, sq.n_rows);
-    for (int i = threadIdx.x; i < rows * kSelBins; i += WARPS * 32)
-      if (hist_s[i]) atomicAdd(p.hist + (int64_t)(sq.row_begin + i / kSelBins) * kSelBins + i % kSelBins, hist_s[i]);
-  }
 }
 
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
@@ -286,6 +357,7 @@ template <int NSEQ>
 __global__ void __launch_bounds__(256) score_simt_kernel(const ScoreParams<NSEQ> p) {
   __shared__ float q_s[32][QSA_INDEX_DIM + 1];
   __shared__ float k_s[kSimtTile][QSA_INDEX_DIM + 1];
+  __shared__ float m_s[kRowGroup][kSimtTile];
   grid_dependency_sync();
   const int64_t item = blockIdx.x;
   if (item >= p.n_work) return;
@@ -318,15 +390,30 @@ __global__ void __launch_bounds__(256) score_simt_kernel(const ScoreParams<NSEQ>
     for (int j = 0; j < 4; ++j) acc[j] = fmaf(qv, k_s[4 * warp + j][d], acc[j]);
   }
   const int r = lane >> 2;
+  const int64_t nb = r < rows ? visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + r)) : 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     float v = fmaxf(acc[j], 0.f);
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v *= kScoreScale;
     const int64_t b = b0 + 4 * warp + j;
-    if ((lane & 3) == 0 && r < rows) {
-      const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + r));
-      if (b < nb) p.scores[(int64_t)(sq.row_begin + row0 + r) * p.ld + b] = v * kScoreScale;
+    if ((lane & 3) == 0) {
+      if (b < nb) p.scores[(int64_t)(sq.row_begin + row0 + r) * p.ld + b] = v;
+      m_s[r][4 * warp + j] = b < nb ? v : -INFINITY;
+    }
+  }
+  if (!p.gmax) return;
+  // The tile's two groups of 16 blocks: their maxima per row.
+  __syncthreads();
+  if (threadIdx.x < 2 * kRowGroup) {
+    const int rr = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int64_t nbr = rr < rows ? visible_blocks(row_position(sq.n_tokens, sq.n_rows, row0 + rr)) : 0;
+    const int64_t gb0 = b0 + 16 * half;
+    if (gb0 < nbr) {
+      float m = -INFINITY;
+      for (int i = 0; i < 16; ++i) m = fmaxf(m, m_s[rr][16 * half + i]);
+      p.gmax[(int64_t)(sq.row_begin + row0 + rr) * p.gld + gb0 / QSA_SCORE_GROUP] = m;
     }
   }
 }
@@ -353,33 +440,19 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
     return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0u, p);
   }
   const int sms = device_sm_count();
-  if (p.hist) {
-    // 8 warps: their stages (147 KB) and the 4 rows' histograms (64 KB) share the CTA.
-    constexpr int Wh = 8;
-    const size_t smem = sizeof(float) * Wh * kScoreStages * kStageFloats + sizeof(uint32_t) * kHistRows * kSelBins;
-    const int64_t need = (p.n_work + Wh - 1) / Wh;
-    const unsigned grid = (unsigned)(need < sms ? need : sms);
-    const void* k = max_rows_per_group <= 2 ? (const void*)score_mma_kernel<1, NSEQ, Wh, true>
-                                            : (const void*)score_mma_kernel<2, NSEQ, Wh, true>;
-    cudaError_t e = allow_dynamic_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    if (max_rows_per_group <= 2)
-      return launch_kernel(score_mma_kernel<1, NSEQ, Wh, true>, dim3(grid), dim3(Wh * 32), smem, st, 0u, p);
-    return launch_kernel(score_mma_kernel<2, NSEQ, Wh, true>, dim3(grid), dim3(Wh * 32), smem, st, 0u, p);
-  }
   constexpr int Ws = 12;
   const size_t smem = sizeof(float) * Ws * kScoreStages * kStageFloats;
   const int64_t need = (p.n_work + Ws - 1) / Ws;
   const unsigned grid = (unsigned)(need < sms ? need : sms);
-  const void* k = max_rows_per_group <= 2   ? (const void*)score_mma_kernel<1, NSEQ, Ws, false>
-                  : max_rows_per_group <= 4 ? (const void*)score_mma_kernel<2, NSEQ, Ws, false>
-                                            : (const void*)score_mma_kernel<4, NSEQ, Ws, false>;
+  const void* k = max_rows_per_group <= 2   ? (const void*)score_mma_kernel<1, NSEQ, Ws>
+                  : max_rows_per_group <= 4 ? (const void*)score_mma_kernel<2, NSEQ, Ws>
+                                            : (const void*)score_mma_kernel<4, NSEQ, Ws>;
   cudaError_t e = allow_dynamic_smem(k, smem);
   if (e != cudaSuccess) return e;
   const dim3 block(Ws * 32);
-  if (max_rows_per_group <= 2) return launch_kernel(score_mma_kernel<1, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
-  if (max_rows_per_group <= 4) return launch_kernel(score_mma_kernel<2, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
-  return launch_kernel(score_mma_kernel<4, NSEQ, Ws, false>, dim3(grid), block, smem, st, 0u, p);
+  if (max_rows_per_group <= 2) return launch_kernel(score_mma_kernel<1, NSEQ, Ws>, dim3(grid), block, smem, st, 0u, p);
+  if (max_rows_per_group <= 4) return launch_kernel(score_mma_kernel<2, NSEQ, Ws>, dim3(grid), block, smem, st, 0u, p);
+  return launch_kernel(score_mma_kernel<4, NSEQ, Ws>, dim3(grid), block, smem, st, 0u, p);
 }
 
 template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);

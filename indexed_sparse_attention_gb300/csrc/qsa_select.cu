@@ -1,452 +1,479 @@
-// Step 3 of the QSA layer step: per query row, keep the top-k complete
-// blocks by score, lower block id winning ties (hipfire, "QSA sparse
-// attention and the VMM KV backend", section 02: the top-scoring blocks
-// within a 2,048-token budget of 512 blocks; section 03: a radix select from
-// the scores).
+// Step 3 of the QSA layer step: per query row, the top-k pooled blocks by
+// score, the lower block id first among equal scores, listed in ascending id
+// order (hipfire, "QSA sparse attention and the VMM KV backend", section 02:
+// a budget of 512 blocks = 2,048 tokens; section 03: selection by a radix
+// select over the scores).
 //
-// Scores map to order-preserving uint32 keys (-0.0 folded onto +0.0).  One
-// thread-block cluster of S CTAs handles one row; CTA c owns a chunk of the
-// row's blocks and keeps its keys in shared memory.  In one launch:
-//   1. each CTA histograms its keys over the top 12 key bits (4096 bins);
-//   2. the histograms are summed across the cluster through distributed
-//      shared memory (CTA c sums bin slice c of every peer and broadcasts it),
-//      and every CTA finds the bin B holding the row's k-th best key;
-//   3. each CTA writes one bitmap word per 32 of its ids -- ids whose bin is
-//      above B -- into CTA 0, and appends the ids in bin B (the candidates)
-//      to CTA 0's candidate list;
-//   4. CTA 0 resolves the candidates with two more radix passes over the low
-//      20 key bits, keeps the lowest ids among keys equal to the k-th key,
-//      and writes the row's ids in ascending order by a prefix popcount over
-//      the bitmap.
-// If bin B holds more candidates than the list takes (massive ties), CTA 0
-// runs the remaining radix passes over the row's scores instead.
-#include <cooperative_groups.h>
-
+// One CTA per row runs an exact radix select over order-preserving 32-bit
+// keys of the fp32 scores (-0.0 folded onto +0.0), restricted to candidate
+// groups.  A group is QSA_SCORE_GROUP = 16 consecutive blocks; its maximum
+// comes from the scoring kernel or is computed here from the scores.
+//  1. Histogram the G group maxima on their top 12 key bits and find the bin
+//     B of the k-th largest.  The k largest group maxima are the scores of k
+//     different blocks, so the k-th best block score is at least the k-th
+//     largest group maximum, whose key lies in bin B or above: every block of
+//     the top k has a key in a bin >= B and sits in a group whose maximum is
+//     in a bin >= B.  With fewer than k groups nothing is pruned.
+//  2. Read the blocks of the candidate groups (maximum in a bin >= B) and
+//     keep those whose own key is in a bin >= B as a (key, id) list.
+//  3. Radix select over the list (12 + 12 + 8 key bits, stopping early when
+//     a bin is taken whole) gives the k-th key K and how many entries equal
+//     to K to keep -- the lowest ids.
+//  4. The kept ids are marked in a bitmap over the row's blocks, which one
+//     prefix scan turns into the ascending id list.
+// A row whose candidates exceed the shared-memory capacity (many equal or
+// nearly equal scores) runs steps 3 and 4 over its whole score row in
+// global memory instead.
 #include "qsa_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace qsa {
 
 namespace {
 
-constexpr int kBins = kSelBins;      // top 12 key bits
-constexpr int kCandCap = 2048;       // candidates kept by CTA 0
-constexpr int kThreads = 512;
-constexpr int kMaxCluster = 16;
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+constexpr int kGroup = QSA_SCORE_GROUP;
+constexpr int kBins = 4096;                        // radix levels 1 and 2: 12 key bits each
+constexpr int kBins3 = 256;                        // radix level 3: the last 8 key bits
+constexpr int kGroupCap = 1024;                    // candidate groups read back (16,384 blocks)
+constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
+constexpr int kMaxGroups = QSA_MAX_BLOCKS / kGroup;
+constexpr int kGroupsPerThread = kMaxGroups / kThreads;
+constexpr int kChunksPerThread = kGroupCap * (kGroup / 4) / kThreads;   // float4 chunks of candidate groups
 
-// Exclusive prefix sum of v over the CTA; *total gets the sum of all v.
-__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n_warps = blockDim.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t s = lane < n_warps ? warp_sums[lane] : 0u;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, s, off);
-      if (lane >= off) s += y;
-    }
-    warp_sums[lane] = s;
-  }
-  __syncthreads();
-  const uint32_t before = warp == 0 ? 0u : warp_sums[warp - 1];
-  *total = warp_sums[n_warps - 1];
-  __syncthreads();
-  return before + x - v;
-}
-
-// Keep the n lowest set bits of w.
-__device__ __forceinline__ uint32_t lowest_bits(uint32_t w, uint32_t n) {
-  uint32_t out = 0;
-  for (uint32_t i = 0; i < n && w; ++i) {
-    const uint32_t b = w & (0u - w);
-    out |= b;
-    w ^= b;
-  }
-  return out;
-}
-
-// Bin of a histogram (nbins bins, read through hist(b)) that holds the
-// need-th largest element counting from the top bin.  s_out[0] = bin,
-// s_out[1] = elements in higher bins.
-template <typename H>
-__device__ __forceinline__ void find_bin(H hist, int nbins, uint32_t need, uint32_t* warp_sums, uint32_t* s_out) {
-  const int nt = blockDim.x;
-  const int per = nbins >= nt ? nbins / nt : 1;
-  const int hi = nbins - (int)threadIdx.x * per;
-  uint32_t local = 0u;
-  if (hi > 0)
-    for (int b = hi - 1; b >= hi - per; --b) local += hist(b);
-  uint32_t total;
-  const uint32_t above = block_exclusive_scan(local, warp_sums, &total);
-  if (hi > 0 && above < need && above + local >= need) {
-    uint32_t c = above;
-    for (int b = hi - 1; b >= hi - per; --b) {
-      const uint32_t h = hist(b);
-      if (c + h >= need) {
-        s_out[0] = (uint32_t)b;
-        s_out[1] = c;
-        break;
-      }
-      c += h;
-    }
-  }
-  __syncthreads();
-}
-
-// Warp-aggregated shared-memory histogram increment (one atomic per
-// distinct bin in the warp); all 32 lanes must call it.
-__device__ __forceinline__ void hist_add(uint32_t* hist, bool act, uint32_t bin, int lane) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, act ? bin : 0xffffffffu);
-  if (act && (__ffs(peers) - 1) == lane) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
-
-constexpr int kSubCap = 256;        // candidates sharing the k-th key's top 24 bits, resolved by rank
-
-struct SelSmem {
-  // offsets in 32-bit words
-  int own, merged, keys, selw, eqw, ck, ci, h2, subk, subi, total;
-  __host__ __device__ SelSmem(int chunk, int nw) {
-    own = 0;
-    merged = own + kBins;
-    keys = merged + kBins;
-    selw = keys + chunk;
-    eqw = selw + nw;
-    ck = eqw + nw;
-    ci = ck + kCandCap;
-    h2 = ci + kCandCap;      // second-level histogram (key bits 19..8) of the candidates, in CTA 0
-    subk = h2 + kBins;
-    subi = subk + kSubCap;
-    total = subi + kSubCap;
+// Shared-memory layout (32-bit words); R1 holds the group-maximum keys, then
+// the list keys.
+struct SelLayout {
+  int h1, h2, h3, cg, r1, r2, selw, eqw, total;
+  __host__ __device__ SelLayout(int64_t max_nb) {
+    const int groups = (int)((max_nb + kGroup - 1) / kGroup);
+    const int nw = (int)((max_nb + 31) / 32);
+    h1 = 0;                                        // group-maximum histogram, then radix level 2
+    h2 = h1 + kBins;                               // radix level 1
+    h3 = h2 + kBins;                               // radix level 3
+    cg = h3 + kBins3;                              // candidate group ids
+    r1 = cg + kGroupCap;
+    r2 = r1 + (groups > kListCap ? groups : kListCap);   // list ids
+    selw = r2 + kListCap;                          // kept ids, one bit per block
+    eqw = selw + (nw + 3) / 4 * 4;                 // entries equal to the k-th key
+    total = eqw + (nw + 3) / 4 * 4;
   }
 };
 
-template <int NSEQ>
-__global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSEQ> p, int chunk, int nw_max,
-                                                            int cache_keys) {
-  extern __shared__ uint32_t sm[];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ uint32_t s_res[2];
-  __shared__ uint32_t s_cand, s_sub;
-  cg::cluster_group cluster = cg::this_cluster();
-  grid_dependency_sync();
-  const int S = (int)cluster.num_blocks();
-  const int c = (int)cluster.block_rank();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = p.row_base + blockIdx.y;
-  int si = 0;
-#pragma unroll
-  for (int i = 1; i < NSEQ; ++i)
-    if (i < p.n_seqs && r >= p.seq[i].row_begin) si = i;
-  const RowSeq sq = p.seq[si];
-  const int n = (int)visible_blocks(row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin));
-  const int k = p.top_k;
-  int32_t* out = p.sel + (int64_t)r * k;
-  // Uniform across the cluster: every CTA of the row takes the same branch.
-  if (n <= k) {
-    if (c == 0) {
-      for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
-      if (tid == 0) p.cnt[r] = n;
-    }
-    return;
-  }
-  const int nw = (n + 31) >> 5;
-  const SelSmem L(cache_keys ? chunk : 0, nw_max);
-  uint32_t* own = sm + L.own;
-  uint32_t* merged = sm + L.merged;
-  uint32_t* keys = sm + L.keys;
-  const float* srow = p.scores + (int64_t)r * p.ld;
-  const int i0 = c * chunk;
-  const int i1 = min(n, i0 + chunk);
+__device__ __forceinline__ uint32_t lanes_below() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
 
-  if (c == 0) {
-    for (int i = tid; i < nw; i += kThreads) sm[L.eqw + i] = 0u;
-    for (int b = tid; b < kBins; b += kThreads) sm[L.h2 + b] = 0u;
-    if (tid == 0) {
-      s_cand = 0u;
-      s_sub = 0u;
-    }
+// Exclusive prefix sum of v over the warps of the CTA (v uniform within each
+// warp, warp order); *total = the sum over warps.  wt (kWarps words) must not
+// be touched again before the next __syncthreads() after this call.
+__device__ __forceinline__ uint32_t warp_prefix(uint32_t v, uint32_t* wt, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) wt[warp] = v;
+  __syncthreads();
+  const uint32_t w = wt[lane];   // kWarps == 32
+  uint32_t before = lane < warp ? w : 0u;
+  uint32_t all = w;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    all += __shfl_xor_sync(0xffffffffu, all, o);
   }
-  if (tid == 0) {   // a histogram that cannot hold the k-th key leaves bin 0
-    s_res[0] = 0u;
-    s_res[1] = 0u;
+  *total = all;
+  return before;
+}
+
+// Exclusive prefix sum of v over the CTA in thread order (same contract on wt).
+__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
+  const int lane = threadIdx.x & 31;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  const uint32_t* hrow = p.hist ? p.hist + (int64_t)r * kBins : nullptr;
-  if (hrow) {
-    // The scoring kernel left the row's histogram: every CTA reads it.
-    cluster.sync();   // peers are running and CTA 0's candidate state is zeroed
-    find_bin([&](int b) { return __ldcg(hrow + b); }, kBins, (uint32_t)k, warp_sums, s_res);
+  return warp_prefix(__shfl_sync(0xffffffffu, x, 31), wt, total) + x - v;
+}
+
+// Bin (of nbins = kBins or kBins3) holding the need-th largest key counted in
+// hist: s_res[0] = the bin, s_res[1] = keys in higher bins.  The histogram
+// holds at least need >= 1 keys.  Ends with a barrier.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t* wt,
+                                         uint32_t* s_res) {
+  const int tid = threadIdx.x;
+  uint32_t c[4];   // c[j] = count of bin top - 1 - j
+  int per, top;
+  if (nbins == kBins) {
+    per = 4;
+    top = kBins - 4 * tid;
+    const uint4 u = *reinterpret_cast<const uint4*>(hist + top - 4);
+    c[0] = u.w; c[1] = u.z; c[2] = u.y; c[3] = u.x;
   } else {
-    // 1. Histogram of this CTA's keys (kept in shared memory for step 3).
-    for (int b = tid; b < kBins; b += kThreads) own[b] = 0u;
-    __syncthreads();
-    // Loads are issued 8 per thread at a time, then counted.
-    for (int base = i0 + warp * 32; base < i0 + chunk; base += 8 * kThreads) {
-      float v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * kThreads + lane;
-        v[j] = i < i1 ? __ldg(srow + i) : 0.f;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = base + j * kThreads + lane;
-        if (i < i1) {
-          const uint32_t key = order_key(v[j]);
-          if (cache_keys) keys[i - i0] = key;
-          atomicAdd(&own[key >> 20], 1u);
-        }
-      }
-    }
-    cluster.sync();
-
-    // 2. Sum bin slice c over the cluster and broadcast it to every CTA.
-    {
-      const int per = kBins / S;
-      for (int b = c * per + tid; b < (c + 1) * per; b += kThreads) {
-        uint32_t h[kMaxCluster];
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q) h[q] = q < S ? *cluster.map_shared_rank(own + b, q) : 0u;
-        uint32_t sum = 0u;
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q) sum += h[q];
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q)
-          if (q < S) *cluster.map_shared_rank(merged + b, q) = sum;
-      }
-    }
-    cluster.sync();
-    find_bin([&](int b) { return merged[b]; }, kBins, (uint32_t)k, warp_sums, s_res);
+    per = tid < nbins ? 1 : 0;
+    top = nbins - tid;
+    c[0] = per ? hist[top - 1] : 0u;
+    c[1] = c[2] = c[3] = 0u;
   }
-  const uint32_t B = s_res[0];
-  uint32_t need = (uint32_t)k - s_res[1];
-  const bool overflow = (hrow ? __ldcg(hrow + B) : merged[B]) > (uint32_t)kCandCap;
-  const bool cached = cache_keys && !hrow;
-
-  // 3. Bitmap words (bin above B) and candidates (bin B) into CTA 0.
-  uint32_t* selw0 = cluster.map_shared_rank(sm + L.selw, 0);
-  uint32_t* ck0 = cluster.map_shared_rank(sm + L.ck, 0);
-  uint32_t* ci0 = cluster.map_shared_rank(sm + L.ci, 0);
-  uint32_t* cand0 = cluster.map_shared_rank(&s_cand, 0);
-  uint32_t* h20 = cluster.map_shared_rank(sm + L.h2, 0);
-  if (i0 < i1) {
-    const int w0 = i0 >> 5, w1 = (i1 + 31) >> 5;
-    for (int word = w0 + warp; word < w1; word += kThreads / 32) {
-      const int i = word * 32 + lane;
-      const bool in = i < i1;
-      const uint32_t key = in ? (cached ? keys[i - i0] : order_key(srow[i])) : 0u;
-      const uint32_t bin = key >> 20;
-      const uint32_t gt = __ballot_sync(0xffffffffu, in && bin > B);
-      const uint32_t eq = __ballot_sync(0xffffffffu, in && bin == B);
-      if (lane == 0) selw0[word] = gt;
-      if (!overflow && eq) {
-        uint32_t base = 0u;
-        if (lane == 0) base = atomicAdd(cand0, (uint32_t)__popc(eq));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (eq & (1u << lane)) {
-          const uint32_t at = base + __popc(eq & ((1u << lane) - 1u));
-          ck0[at] = key;
-          ci0[at] = (uint32_t)i;
-          atomicAdd(h20 + ((key >> 8) & (kBins - 1)), 1u);
+  const uint32_t local = (c[0] + c[1]) + (c[2] + c[3]);
+  uint32_t total;
+  const uint32_t above = block_scan(local, wt, &total);
+  if (above < need && above + local >= need) {
+    uint32_t acc = above;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j < per) {
+        if (acc + c[j] >= need) {
+          s_res[0] = (uint32_t)(top - 1 - j);
+          s_res[1] = acc;
+          break;
         }
-      }
-    }
-  }
-  cluster.sync();
-  if (c != 0) return;
-
-  // 4. CTA 0 finishes the row.
-  uint32_t* selw = sm + L.selw;
-  uint32_t* eqw = sm + L.eqw;
-  uint32_t* hist = own;                 // free again: reused as radix scratch
-  uint32_t prefix = B << 20;
-  uint32_t pmask = 0xfff00000u;
-  bool ranked = false;   // candidates resolved by rank: no "equal key" bitmap to apply
-  if (!overflow) {
-    const int C = (int)s_cand;
-    const uint32_t* ck = sm + L.ck;
-    const uint32_t* ci = sm + L.ci;
-    uint32_t* subk = sm + L.subk;
-    uint32_t* subi = sm + L.subi;
-    // Second level: the bin of key bits 19..8 holding the k-th key.
-    find_bin([&](int b) { return sm[L.h2 + b]; }, kBins, need, warp_sums, s_res);
-    const uint32_t need2 = need - s_res[1];
-    const uint32_t p24 = (B << 12) | s_res[0];
-    for (int i = tid; i < C; i += kThreads) {
-      const uint32_t key = ck[i], id = ci[i], k24 = key >> 8;
-      if (k24 > p24) {
-        atomicOr(&selw[id >> 5], 1u << (id & 31));
-      } else if (k24 == p24) {
-        const uint32_t j = atomicAdd(&s_sub, 1u);
-        if (j < (uint32_t)kSubCap) {
-          subk[j] = key;
-          subi[j] = id;
-        }
-      }
-    }
-    __syncthreads();
-    const int n_sub = (int)s_sub;
-    if (n_sub <= kSubCap) {
-      // Keep the need2 best of the few candidates left, by (key desc, id asc).
-      for (int j = tid; j < n_sub; j += kThreads) {
-        const uint32_t kj = subk[j], ij = subi[j];
-        uint32_t rank = 0u;
-        for (int i = 0; i < n_sub; ++i) rank += (subk[i] > kj) || (subk[i] == kj && subi[i] < ij);
-        if (rank < need2) atomicOr(&selw[ij >> 5], 1u << (ij & 31));
-      }
-      ranked = true;
-    } else {
-      // Too many near-ties: a last radix pass over key bits 7..0.
-      need = need2;
-      prefix = p24 << 8;
-      pmask = 0xffffff00u;
-      for (int b = tid; b < 256; b += kThreads) hist[b] = 0u;
-      __syncthreads();
-      for (int i = tid; i < C; i += kThreads)
-        if ((ck[i] & pmask) == prefix) atomicAdd(&hist[ck[i] & 255u], 1u);
-      __syncthreads();
-      find_bin([&](int b) { return hist[b]; }, 256, need, warp_sums, s_res);
-      need -= s_res[1];
-      prefix |= s_res[0];
-      __syncthreads();
-      for (int i = tid; i < C; i += kThreads) {
-        const uint32_t key = ck[i], id = ci[i];
-        if ((key >> 8) == p24) {
-          if (key > prefix) atomicOr(&selw[id >> 5], 1u << (id & 31));
-          else if (key == prefix) atomicOr(&eqw[id >> 5], 1u << (id & 31));
-        }
-      }
-    }
-  } else {
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int shift = pass == 0 ? 8 : 0;
-      const int nbins = pass == 0 ? 4096 : 256;
-      for (int b = tid; b < nbins; b += kThreads) hist[b] = 0u;
-      __syncthreads();
-      for (int base = warp * 32; base < n; base += kThreads) {
-        const int i = base + lane;
-        bool act = false;
-        uint32_t bin = 0u;
-        if (i < n) {
-          const uint32_t key = order_key(srow[i]);
-          act = (key & pmask) == prefix;
-          bin = (key >> shift) & (uint32_t)(nbins - 1);
-        }
-        hist_add(hist, act, bin, lane);
-      }
-      __syncthreads();
-      find_bin([&](int b) { return hist[b]; }, nbins, need, warp_sums, s_res);
-      need -= s_res[1];
-      prefix |= s_res[0] << shift;
-      pmask |= (uint32_t)(nbins - 1) << shift;
-      __syncthreads();
-    }
-    for (int word = warp; word < nw; word += kThreads / 32) {
-      const int i = word * 32 + lane;
-      const uint32_t key = i < n ? order_key(srow[i]) : 0u;
-      const uint32_t gt = __ballot_sync(0xffffffffu, i < n && key > prefix);
-      const uint32_t eq = __ballot_sync(0xffffffffu, i < n && key == prefix);
-      if (lane == 0) {
-        selw[word] = gt;
-        eqw[word] = eq;
+        acc += c[j];
       }
     }
   }
   __syncthreads();
-  // Keep the `need` lowest ids among keys equal to the k-th key (unless the
-  // candidates were ranked), then write every chosen id in ascending order.
-  const int wp = (nw + kThreads - 1) / kThreads;
-  const int a0 = tid * wp, a1 = min(nw, a0 + wp);
-  uint32_t local = 0u, total;
-  if (!ranked) {
-    for (int i = a0; i < a1; ++i) local += __popc(eqw[i]);
-    uint32_t cpos = block_exclusive_scan(local, warp_sums, &total);
-    local = 0u;
+}
+
+// Warp-aggregated shared-memory histogram increment (one atomic per distinct
+// bin among the active lanes); all 32 lanes of the warp must call it.  Used
+// where many keys can share a bin.
+__device__ __forceinline__ void hist_add(uint32_t* hist, bool act, uint32_t bin) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, act ? bin : 0xffffffffu);
+  if (act && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Maximum of the scores of blocks 16g .. min(16g + 16, nb) - 1 (the row's
+// stride keeps every group start 16-byte aligned).
+__device__ __forceinline__ float group_max_of(const float* srow, int64_t g, int64_t nb) {
+  const int64_t b0 = g * kGroup;
+  float m = -INFINITY;
+  if (b0 + kGroup <= nb) {
+    const float4* v = reinterpret_cast<const float4*>(srow + b0);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 x = __ldg(v + j);
+      m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+    }
+  } else {
+    for (int64_t b = b0; b < nb; ++b) m = fmaxf(m, __ldg(srow + b));
+  }
+  return m;
+}
+
+// Steps 3 and 4 over the candidates: for_each(f) calls f(key, id) for every
+// candidate (key != 0), each exactly once over the CTA's threads, and
+// for_each_warp(f) does the same with all 32 lanes of every warp calling f
+// the same number of times (f(key, id, active)).  level1_done: the caller
+// already filled the level-1 histogram.
+template <typename ForEach, typename ForEachWarp>
+__device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_each, ForEachWarp for_each_warp,
+                                                uint32_t* sm, const SelLayout& L, bool level1_done,
+                                                uint32_t (*wt)[kWarps], uint32_t* s_res, int32_t* out) {
+  const int tid = threadIdx.x;
+  uint32_t* h1 = sm + L.h1;
+  uint32_t* h2 = sm + L.h2;
+  uint32_t* h3 = sm + L.h3;
+  uint32_t* selw = sm + L.selw;
+  uint32_t* eqw = sm + L.eqw;
+  if (!level1_done) {
+    for_each_warp([&](uint32_t key, int32_t, bool act) { hist_add(h2, act, key >> 20); });
+    __syncthreads();
+  }
+  uint32_t need = k;
+  find_bin(h2, kBins, need, wt[0], s_res);
+  const uint32_t b1 = s_res[0];
+  need -= s_res[1];
+  uint32_t K = b1 << 20, mask = 0xfff00000u;
+  uint32_t n_eq = h2[b1];   // entries whose masked key equals K
+  if (n_eq != need) {
+    // Level 2: key bits 19..8 of the keys in bin b1.
+    for_each_warp([&](uint32_t key, int32_t, bool act) {
+      hist_add(h1, act && (key & 0xfff00000u) == K, (key >> 8) & (kBins - 1));
+    });
+    __syncthreads();
+    find_bin(h1, kBins, need, wt[1], s_res);
+    const uint32_t b2 = s_res[0];
+    need -= s_res[1];
+    K |= b2 << 8;
+    mask = 0xffffff00u;
+    n_eq = h1[b2];
+    if (n_eq != need) {
+      // Level 3: the last 8 key bits.
+      for_each_warp([&](uint32_t key, int32_t, bool act) {
+        hist_add(h3, act && (key & 0xffffff00u) == K, key & (kBins3 - 1));
+      });
+      __syncthreads();
+      find_bin(h3, kBins3, need, wt[0], s_res);
+      K |= s_res[0];
+      mask = 0xffffffffu;
+      need -= s_res[1];
+      n_eq = h3[s_res[0]];
+    }
+  }
+  // Step 4: mark the kept ids.  Entries above K are kept; so are those equal
+  // to K when all of them fit, else the `need` lowest ids among them.
+  const bool all_eq = n_eq == need;
+  for_each([&](uint32_t key, int32_t id) {
+    const uint32_t m = key & mask;
+    if (m > K || (all_eq && m == K)) atomicOr(&selw[id >> 5], 1u << (id & 31));
+    else if (m == K) atomicOr(&eqw[id >> 5], 1u << (id & 31));
+  });
+  __syncthreads();
+  const int wpt = (nw + kThreads - 1) / kThreads;
+  const int a0 = min(nw, tid * wpt), a1 = min(nw, a0 + wpt);
+  uint32_t total;
+  if (!all_eq) {
+    uint32_t c = 0u;
+    for (int i = a0; i < a1; ++i) c += __popc(eqw[i]);
+    uint32_t before = block_scan(c, wt[1], &total);
     for (int i = a0; i < a1; ++i) {
       uint32_t e = eqw[i];
       const uint32_t pc = __popc(e);
-      if (cpos >= need) e = 0u;
-      else if (cpos + pc > need) e = lowest_bits(e, need - cpos);
-      cpos += pc;
-      e |= selw[i];
-      selw[i] = e;
-      local += __popc(e);
+      if (before >= need) {
+        e = 0u;
+      } else if (before + pc > need) {   // keep the lowest need - before bits
+        uint32_t keep = 0u;
+        for (uint32_t j = 0; j < need - before; ++j) {
+          keep |= e & (0u - e);
+          e &= e - 1u;
+        }
+        e = keep;
+      }
+      before += pc;
+      selw[i] |= e;
     }
-  } else {
-    for (int i = a0; i < a1; ++i) local += __popc(selw[i]);
+    __syncthreads();
   }
-  uint32_t at = block_exclusive_scan(local, warp_sums, &total);
+  uint32_t c = 0u;
+  for (int i = a0; i < a1; ++i) c += __popc(selw[i]);
+  uint32_t at = block_scan(c, wt[0], &total);
   for (int i = a0; i < a1; ++i) {
     uint32_t e = selw[i];
     while (e) {
       const int b = __ffs(e) - 1;
       e &= e - 1u;
-      if (at < (uint32_t)k) out[at] = i * 32 + b;
+      // (Positions stay below k for scores that obey the contract; the bound
+      // also keeps NaN keys from writing outside the row.)
+      if (at < k) out[at] = i * 32 + b;
       ++at;
     }
   }
+}
+
+template <int NSEQ>
+__global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ uint32_t wt[2][kWarps];
+  __shared__ uint32_t s_res[2];
+  __shared__ uint32_t s_cnt;
+  const SelLayout L(max_nb);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < L.cg; i += kThreads) sm[i] = 0u;          // the three histograms
+  for (int i = L.selw + tid; i < L.total; i += kThreads) sm[i] = 0u;   // the two bitmaps
+  if (tid == 0) {
+    s_res[0] = 0u;
+    s_res[1] = 0u;
+    s_cnt = 0u;
+  }
+  grid_dependency_sync();
+  const int r = p.row_base + (int)blockIdx.x;
+  int si = 0;
+#pragma unroll
+  for (int i = 1; i < NSEQ; ++i)
+    if (i < p.n_seqs && r >= p.seq[i].row_begin) si = i;
+  const RowSeq sq = p.seq[si];
+  const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin));
+  const int k = p.top_k;
+  int32_t* out = p.sel + (int64_t)r * k;
+  if (nb <= k) {
+    for (int i = tid; i < k; i += kThreads) out[i] = i < nb ? i : -1;
+    if (tid == 0) p.cnt[r] = (int32_t)nb;
+    return;
+  }
+  const float* srow = p.scores + (int64_t)r * p.ld;
+  const int G = (int)((nb + kGroup - 1) / kGroup);   // <= kMaxGroups
+  const int nw = (int)((nb + 31) / 32);
+  uint32_t* r1 = sm + L.r1;
+  uint32_t* r2 = sm + L.r2;
+  uint32_t* cg = sm + L.cg;
+  uint32_t* h1 = sm + L.h1;
+  uint32_t* h2 = sm + L.h2;
+  __syncthreads();   // histograms and bitmaps cleared
+
+  // 1. Keys of the group maxima (all loads in flight at once) and their
+  // top-12-bit histogram.
+  {
+    const float* grow = p.gmax ? p.gmax + (int64_t)r * p.gld : nullptr;
+    float v[kGroupsPerThread];
+#pragma unroll
+    for (int j = 0; j < kGroupsPerThread; ++j) {
+      const int g = tid + j * kThreads;
+      v[j] = 0.f;
+      if (g < G) v[j] = grow ? __ldg(grow + g) : group_max_of(srow, g, nb);
+    }
+#pragma unroll
+    for (int j = 0; j < kGroupsPerThread; ++j) {
+      const int g = tid + j * kThreads;
+      if (g < G) {
+        const uint32_t key = order_key(v[j]);
+        r1[g] = key;
+        atomicAdd(&h1[key >> 20], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  const bool prune = G >= k;
+  uint32_t B = 0u;
+  if (prune) {
+    find_bin(h1, kBins, (uint32_t)k, wt[0], s_res);
+    B = s_res[0];
+  }
+
+  // 2a. Candidate groups: warp w owns a contiguous run of groups, 32 per round.
+  const int gpw = (G + kWarps * 32 - 1) / (kWarps * 32) * 32;
+  const int ga = min(G, warp * gpw), gb = min(G, ga + gpw);
+  uint32_t c = 0u;
+  for (int g0 = ga; g0 < gb; g0 += 32) {
+    const int g = g0 + lane;
+    c += __popc(__ballot_sync(0xffffffffu, g < gb && (r1[g] >> 20) >= B));
+  }
+  uint32_t n_cg;
+  uint32_t q = warp_prefix(c, wt[1], &n_cg);
+  bool overflow = n_cg > (uint32_t)kGroupCap;
+  if (!overflow) {
+    const uint32_t below = lanes_below();
+    for (int g0 = ga; g0 < gb; g0 += 32) {
+      const int g = g0 + lane;
+      const bool in = g < gb && (r1[g] >> 20) >= B;
+      const uint32_t bal = __ballot_sync(0xffffffffu, in);
+      if (in) cg[q + __popc(bal & below)] = (uint32_t)g;
+      q += __popc(bal);
+    }
+  }
+  for (int i = tid; i < kBins; i += kThreads) h1[i] = 0u;   // reused by radix level 2
+  __syncthreads();
+
+  uint32_t n_list = 0u;
+  if (!overflow) {
+    // 2b. The candidate groups' blocks, 4 per float4 chunk, all loads in
+    // flight at once; keys in a bin >= B join the list and its level-1
+    // histogram.
+    const int n_ch = (int)n_cg * (kGroup / 4);
+    float4 v[kChunksPerThread];
+#pragma unroll
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int ch = tid + j * kThreads;
+      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ch < n_ch) {
+        const int64_t b0 = (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3);
+        if (b0 + 4 <= nb) {
+          v[j] = __ldg(reinterpret_cast<const float4*>(srow + b0));
+        } else {
+          v[j].x = b0 < nb ? __ldg(srow + b0) : 0.f;
+          v[j].y = b0 + 1 < nb ? __ldg(srow + b0 + 1) : 0.f;
+          v[j].z = b0 + 2 < nb ? __ldg(srow + b0 + 2) : 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kChunksPerThread; ++j) {
+      const int ch = tid + j * kThreads;
+      if (ch < n_ch) {
+        const int64_t b0 = (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3);
+        const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t key[4];
+        int n = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          key[e] = order_key(x[e]);
+          if (b0 + e >= nb || (key[e] >> 20) < B) key[e] = 0u;
+          n += key[e] != 0u;
+        }
+        if (n) {
+          uint32_t at = atomicAdd(&s_cnt, (uint32_t)n);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (key[e] != 0u) {
+              if (at < (uint32_t)kListCap) {
+                r1[at] = key[e];
+                r2[at] = (uint32_t)(b0 + e);
+              }
+              ++at;
+              atomicAdd(&h2[key[e] >> 20], 1u);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    n_list = s_cnt;
+    overflow = n_list > (uint32_t)kListCap;
+  }
+  if (!overflow) {
+    const int n = (int)n_list;
+    radix_and_write(
+        (uint32_t)k, nw,
+        [&](auto f) {
+          for (int i = tid; i < n; i += kThreads) f(r1[i], (int32_t)r2[i]);
+        },
+        [&](auto f) {
+          const int n_pad = (n + 31) / 32 * 32;
+          for (int i = tid; i < n_pad; i += kThreads) f(i < n ? r1[i] : 0u, i < n ? (int32_t)r2[i] : 0, i < n);
+        },
+        sm, L, true, wt, s_res, out);
+  } else {
+    // The whole row from global memory (the level-1 histogram is rebuilt).
+    if (n_list) {
+      for (int i = tid; i < kBins; i += kThreads) h2[i] = 0u;
+      __syncthreads();
+    }
+    const int nbi = (int)nb;
+    radix_and_write(
+        (uint32_t)k, nw,
+        [&](auto f) {
+          for (int b0 = tid; b0 < nbi; b0 += 8 * kThreads) {   // 8 loads in flight
+            uint32_t kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int b = b0 + j * kThreads;
+              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (b0 + j * kThreads < nbi) f(kk[j], (int32_t)(b0 + j * kThreads));
+          }
+        },
+        [&](auto f) {
+          const int n_pad = (nbi + 31) / 32 * 32;   // warp-uniform trip counts
+          for (int b0 = tid; b0 < n_pad; b0 += 8 * kThreads) {
+            uint32_t kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int b = b0 + j * kThreads;
+              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f(kk[j], (int32_t)(b0 + j * kThreads), b0 + j * kThreads < nbi);
+          }
+        },
+        sm, L, false, wt, s_res, out);
+  }
   if (tid == 0) p.cnt[r] = k;
-  // Every CTA of the row read the histogram before the last cluster barrier:
-  // return it to zero for the next call.
-  if (hrow)
-    for (int b = tid; b < kBins; b += kThreads) p.hist[(int64_t)r * kBins + b] = 0u;
 }
 
 }  // namespace
 
-// Cluster size and chunk for rows of up to max_nb blocks: chunks of at most
-// 2,048 keys when the cluster allows it, fewer CTAs per row when there are
-// many rows.
-void select_plan(int64_t rows, int64_t max_nb, int* cluster, int* chunk) {
-  int s = 1;
-  while (s < kMaxCluster && (max_nb + s - 1) / s > 2048) s <<= 1;
-  const int64_t cap = 8 * (int64_t)device_sm_count();
-  while (s > 1 && rows * s > cap) s >>= 1;
-  int64_t ch = (max_nb + s - 1) / s;
-  ch = (ch + 31) / 32 * 32;
-  if (ch < 32) ch = 32;
-  *cluster = s;
-  *chunk = (int)ch;
-}
-
-constexpr int kKeyCacheMax = 16384;   // keys a CTA keeps in shared memory
-
-size_t select_smem_bytes(int chunk, int nw_max) {
-  return sizeof(uint32_t) * (size_t)SelSmem(chunk <= kKeyCacheMax ? chunk : 0, nw_max).total;
-}
+size_t select_smem_bytes(int64_t max_nb) { return sizeof(uint32_t) * (size_t)SelLayout(max_nb).total; }
 
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
-  int S = 1, chunk = 32;
-  select_plan(n_rows, max_nb, &S, &chunk);
-  const int nw_max = (int)((max_nb + 31) / 32);
-  size_t smem = select_smem_bytes(chunk, nw_max);
+  const size_t smem = select_smem_bytes(max_nb);
   cudaError_t e = allow_dynamic_smem((const void*)select_kernel<NSEQ>, smem);
   if (e != cudaSuccess) return e;
-  if (S > 8) {
-    e = allow_cluster16((const void*)select_kernel<NSEQ>, kThreads, smem);
-    if (e == cudaErrorNotSupported) {   // no 16-CTA cluster fits: use 8
-      S = 8;
-      chunk = (int)(((max_nb + 7) / 8 + 31) / 32 * 32);
-    } else if (e != cudaSuccess) {
-      return e;
-    }
-  }
-  smem = select_smem_bytes(chunk, nw_max);
-  if ((e = allow_dynamic_smem((const void*)select_kernel<NSEQ>, smem)) != cudaSuccess) return e;
-  const int cache_keys = chunk <= kKeyCacheMax ? 1 : 0;
-  return launch_kernel(select_kernel<NSEQ>, dim3((unsigned)S, (unsigned)n_rows), dim3(kThreads), smem, st,
-                       (unsigned)S, p, chunk, nw_max, cache_keys);
+  return launch_kernel(select_kernel<NSEQ>, dim3((unsigned)n_rows), dim3(kThreads), smem, st, 0u, p, max_nb);
 }
 
 template cudaError_t launch_select<1>(const SelectParams<1>&, int, int64_t, cudaStream_t);

@@ -59,14 +59,24 @@ def test_scores_match_oracle(dtype, L, M):
     q_idx = x.q_idx.to(dev())
     ld = (L // 4 + 7) // 8 * 8
     scores = torch.full((M, ld), float("nan"), device=dev())
+    gld = (qsa.n_groups(L) + 3) // 4 * 4
+    gmax = torch.full((M, gld), float("nan"), device=dev())
     seq = qsa.Seq(L, M, pooled)
-    qsa.score_blocks([seq], q_idx, scores)
+    qsa.score_blocks([seq], q_idx, scores, group_max=gmax)
     ref = oracle.score(x.q_idx, pooled_ref.astype(np.float32).astype(np.float64), x.row_pos, ld=ld)
     bound = score_bound(x.q_idx, pooled_ref, x.row_pos)
     got = to_np(scores)
     assert_scores_close(got, ref, bound, x.row_pos)
     for r, p in enumerate(x.row_pos):                       # blocks a row cannot see stay unwritten
         assert np.isnan(got[r, oracle.visible_blocks(p):]).all()
+    # Group maxima: exactly the maximum of the written scores of each group.
+    gm = to_np(gmax)
+    for r, p in enumerate(x.row_pos):
+        nb = oracle.visible_blocks(p)
+        G = (nb + 15) // 16
+        want = np.array([got[r, 16 * g:min(16 * g + 16, nb)].max() for g in range(G)], dtype=np.float32)
+        np.testing.assert_array_equal(gm[r, :G], want)
+        assert np.isnan(gm[r, G:]).all()
     # ... and the chained GPU pool gives scores within the same bound.
     gp = pooled_buffer(L, dev())
     pool_all(x.idxk.to(dev()), gp, L)
@@ -89,28 +99,45 @@ def test_scores_zero_query_and_nonnegative():
 
 
 # ------------------------------------------------------------------ step 3
-def _select_gpu(scores_f32: np.ndarray, row_pos, L, top_k=512):
+def group_maxima(scores_f32: np.ndarray, row_pos) -> np.ndarray:
+    """Per row, the maximum score of every group of 16 visible blocks (the
+    layout qsa_score_blocks writes), NaN elsewhere."""
+    G = max((oracle.visible_blocks(p) + 15) // 16 for p in row_pos)
+    out = np.full((len(row_pos), (G + 3) // 4 * 4), np.nan, dtype=np.float32)
+    for r, p in enumerate(row_pos):
+        nb = oracle.visible_blocks(p)
+        for g in range((nb + 15) // 16):
+            out[r, g] = scores_f32[r, 16 * g:min(16 * g + 16, nb)].max()
+    return out
+
+
+def _select_gpu(scores_f32: np.ndarray, row_pos, L, top_k=512, with_group_max=False):
     M, ld = scores_f32.shape
     n_rows = len(row_pos)
     s = torch.from_numpy(np.ascontiguousarray(scores_f32)).to(dev())
     sel = torch.full((M, top_k), -7, dtype=torch.int32, device=dev())
     cnt = torch.full((M,), -7, dtype=torch.int32, device=dev())
-    qsa.select_topk([qsa.Seq(L, n_rows)], s, sel, cnt, top_k)
+    gm = torch.from_numpy(group_maxima(scores_f32, row_pos)).to(dev()) if with_group_max else None
+    qsa.select_topk([qsa.Seq(L, n_rows)], s, sel, cnt, top_k, group_max=gm)
     return to_np(sel), to_np(cnt)
 
 
 def _select_case(scores_f32, L, M, top_k=512):
     row_pos = [L - M + j for j in range(M)]
-    sel, cnt = _select_gpu(scores_f32, row_pos, L, top_k)
     rs, rc, _ = oracle.select(scores_f32.astype(np.float64), row_pos, top_k)
-    np.testing.assert_array_equal(cnt, rc)
-    np.testing.assert_array_equal(sel, rs)
+    # Without group maxima (the kernel derives them) and with them.
+    for with_gm in (False, True):
+        sel, cnt = _select_gpu(scores_f32, row_pos, L, top_k, with_gm)
+        np.testing.assert_array_equal(cnt, rc)
+        np.testing.assert_array_equal(sel, rs)
 
 
 @pytest.mark.parametrize("L,M,kind", [(4099, 4, "normal"), (261_120, 4, "normal"), (65_536, 1, "normal"),
                                       (9001, 3, "coarse"), (9001, 3, "zeros"), (9001, 2, "signed_zeros"),
                                       (9001, 2, "increasing"), (2051, 4, "normal"), (2052, 1, "normal"),
-                                      (2049, 2, "normal"), (13, 4, "normal"), (1 << 20, 1, "coarse")])
+                                      (2049, 2, "normal"), (13, 4, "normal"), (1 << 20, 1, "coarse"),
+                                      (262_144, 2, "zeros"), (100_003, 3, "planted_ties"),
+                                      (40_000, 2, "negative")])
 def test_select_bit_exact_on_fp32_scores(L, M, kind):
     rng = np.random.default_rng(L + M)
     nb = L // 4
@@ -125,6 +152,13 @@ def test_select_bit_exact_on_fp32_scores(L, M, kind):
         s[:, 7::97] = 1.5
     elif kind == "increasing":
         s[:, :nb] = np.arange(nb, dtype=np.float32)[None]
+    elif kind == "planted_ties":
+        # 600 blocks share the top score: the 512 lowest ids among them win.
+        s[:, :nb] = np.abs(rng.standard_normal((M, nb))).astype(np.float32)
+        for r in range(M):
+            s[r, rng.choice(nb - M, 600, replace=False)] = 9.0
+    elif kind == "negative":
+        s[:, :nb] = rng.standard_normal((M, nb)).astype(np.float32) - 4
     _select_case(s, L, M)
 
 
@@ -132,14 +166,15 @@ def test_select_bit_exact_on_fp32_scores(L, M, kind):
 def test_select_other_budgets(top_k):
     rng = np.random.default_rng(top_k)
     L, M = 20_011, 2
-    s = (rng.integers(0, 300, size=(M, L // 4)) * 0.5).astype(np.float32)
+    s = np.zeros((M, (L // 4 + 3) // 4 * 4), dtype=np.float32)     # row stride: a multiple of 16 bytes
+    s[:, :L // 4] = rng.integers(0, 300, size=(M, L // 4)) * 0.5
     _select_case(s, L, M, top_k)
 
 
 def test_select_ragged_sequences():
     rng = np.random.default_rng(5)
     Ls, Ms = [4099, 700, 30_000, 9, 2052, 65_540, 5000, 8001, 12_345], [4, 1, 2, 3, 1, 4, 8, 1, 2]
-    ld = max(L // 4 for L in Ls)
+    ld = (max(L // 4 for L in Ls) + 3) // 4 * 4
     rows = sum(Ms)
     s = np.abs(rng.standard_normal((rows, ld))).astype(np.float32)
     s[3] = np.round(s[3] * 4) / 4   # ties
@@ -358,6 +393,13 @@ def test_layer_step_ragged_batch_small():
     step = qsa.LayerStep(seqs, q_idx, q)
     step.run()
     torch.cuda.synchronize()
+    # The fused scoring + selection entry point gives the same selection.
+    sel0, cnt0 = step.sel.clone(), step.cnt.clone()
+    step.sel.fill_(-5)
+    step.cnt.fill_(-5)
+    step.score_select()
+    torch.cuda.synchronize()
+    assert torch.equal(step.sel, sel0) and torch.equal(step.cnt, cnt0)
     row = 0
     for x in xs:
         ref = oracle_layer(x)
