@@ -16,6 +16,11 @@
 // bf16 queries are exact in both formats.  Every tile of 16 blocks is one
 // group of the group maxima the selection starts from.  fp32 index queries
 // take a CUDA-core kernel.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -348,6 +353,251 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
   cp_async_wait<0>();
 }
 
+// ------------------------------------------------------------------ scoring, tensor pipe, TMA-fed
+// The few-row path (<= 4 rows per sequence, bf16 queries): persistent CTAs,
+// each owning a contiguous range of items; an item is 2 tiles (32 blocks) of
+// one sequence.  Warp 0 is the producer: lane L < kTmaItems loads the items
+// of ring slot L, each with four 2-D tensor copies of 32 blocks x 32 channels
+// (4 KB, 128-byte swizzle) completing on the slot's barrier, so a CTA keeps
+// kTmaItems x 16 KB of pooled keys in flight and refills each slot as soon
+// as it is consumed (the tensor-copy engine spends a fixed time per copy and
+// per barrier transaction, so copies are issued from several lanes, and a
+// steady ring keeps HBM busier than requesting a CTA's whole range at once).
+// kTmaConsumers consumer warps run the tf32 MMAs of the kernel above, one
+// tile at a time: tile j of the item in slot q belongs to consumer
+// (kItemTiles q + j) % kTmaConsumers, so each consumer waits on a slot's
+// barrier phases in order.  With the swizzle, the 16-byte chunk c of box row
+// r (4 of its 32 channels) sits at chunk c ^ (r & 7).  In 16-channel step s,
+// thread t reads chunk 2t + (s & 1) of box s / 2 -- channels
+// 32 (s / 2) + 8t + 4 (s & 1) .. +3, split over the two m16n8k8 steps as above
+// -- so the 8 lanes of one shared-memory phase (rows g, g ^ 1, t = 0..3)
+// cover all 8 chunks of a bank row.  The queries take the same channel
+// mapping.
+constexpr int kItemTiles = 2;
+constexpr int kItemBlocks = kItemTiles * kScoreTile;          // 32
+constexpr int kTmaItems = 8;                                  // ring slots: 128 KB in flight
+constexpr int kTmaConsumers = 8;
+constexpr int kTmaCtasPerSm = 1;
+constexpr int kBoxRows = kItemBlocks;
+constexpr int kBoxBytes = kBoxRows * 128;                     // 32 rows x 32 fp32 = 4 KB
+constexpr int kItemBytes = 4 * kBoxBytes;                     // 16 KB
+static_assert((kTmaItems * kItemTiles) % kTmaConsumers == 0, "tile slots split evenly over consumers");
+static_assert(kTmaItems <= 32, "one producer lane per ring slot");
+constexpr size_t kTmaSmem = (size_t)kTmaItems * kItemBytes + 1024;   // + alignment slack
+
+__device__ int g_score_wait_timeouts;   // waits that gave up (never expected)
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of the given parity to complete; gives up after about
+// two seconds (counted in g_score_wait_timeouts) instead of hanging.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > 2000000000ull) {
+      atomicAdd(&g_score_wait_timeouts, 1);
+      return false;
+    }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+template <int NSEQ>
+struct ScoreTmaParams {
+  CUtensorMap tmap[NSEQ];      // pooled keys of sequence i: [n_tokens / 4 rows, 128] fp32
+  int64_t item_begin[NSEQ];    // first item of sequence i
+  int64_t n_items;
+  ScoreParams<NSEQ> p;
+};
+
+template <int NSEQ>
+__device__ __forceinline__ int find_seq_by_item(const ScoreTmaParams<NSEQ>& P, int64_t item) {
+  int s = 0;
+#pragma unroll
+  for (int i = 1; i < NSEQ; ++i)
+    if (i < P.p.n_seqs && item >= P.item_begin[i]) s = i;
+  return s;
+}
+
+template <int NT, int NSEQ>
+__global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
+    score_tma_kernel(const __grid_constant__ ScoreTmaParams<NSEQ> P) {
+  static_assert(NT <= 2, "the TMA path serves groups of <= 4 rows");
+  extern __shared__ unsigned char tma_smem_raw[];
+  __shared__ uint64_t full_bar[kTmaItems], empty_bar[kTmaItems];
+  const ScoreParams<NSEQ>& p = P.p;
+  unsigned char* items = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(tma_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTmaItems; ++i) {
+      mbar_init((uint32_t)__cvta_generic_to_shared(&full_bar[i]), 1);
+      mbar_init((uint32_t)__cvta_generic_to_shared(&empty_bar[i]), kItemTiles);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  grid_dependency_sync();
+  const int64_t i0 = P.n_items * blockIdx.x / gridDim.x;
+  const int64_t i1 = P.n_items * (blockIdx.x + 1) / gridDim.x;
+  const int n_items = (int)(i1 - i0);
+
+  if (warp == 0) {
+    // Producer: lane q issues the items of slot q, in order.
+    if (lane < kTmaItems) {
+      const uint32_t fb = (uint32_t)__cvta_generic_to_shared(&full_bar[lane]);
+      const uint32_t eb = (uint32_t)__cvta_generic_to_shared(&empty_bar[lane]);
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(items + (size_t)lane * kItemBytes);
+      for (int n = lane; n < n_items; n += kTmaItems) {
+        if (n >= kTmaItems && !mbar_wait(eb, (uint32_t)((n / kTmaItems - 1) & 1))) break;
+        const int si = find_seq_by_item(P, i0 + n);
+        const int y = (int)((i0 + n - P.item_begin[si]) * kItemBlocks);
+        mbar_expect_tx(fb, kItemBytes);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kBoxBytes, &P.tmap[si], 32 * c, y, fb);
+      }
+    }
+    return;
+  }
+
+  // Consumers.
+  const int cw = warp - 1;
+  const int g = lane >> 2, t = lane & 3;
+  uint32_t bq[NT][8][2];   // packed bf16 pairs (channels +0, +1) and (+2, +3)
+  int bq_si = -1;
+  for (int n = 0; n < n_items; ++n) {
+    const int q = n % kTmaItems;
+    const int j = ((cw - kItemTiles * q) % kTmaConsumers + kTmaConsumers) % kTmaConsumers;
+    if (j >= kItemTiles) continue;   // no tile of this item is ours
+    const int64_t item = i0 + n;
+    const int si = find_seq_by_item(P, item);
+    const ScoreSeq& sq = p.seq[si];
+    const int64_t tile = (item - P.item_begin[si]) * kItemTiles + j;
+    const bool valid = tile < sq.n_tiles;
+    const int64_t b0 = tile * kScoreTile;
+    const int rows = sq.n_rows;   // one row group on this path
+    if (valid && si != bq_si) {
+      const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
+#pragma unroll
+      for (int jj = 0; jj < NT; ++jj) {
+        const int nn = 8 * jj + g, r = nn >> 2, h = nn & 3;
+        const __nv_bfloat16* src = qb + ((int64_t)(sq.row_begin + r) * QSA_INDEX_HEADS + h) * QSA_INDEX_DIM + 8 * t;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          uint2 v = make_uint2(0u, 0u);
+          if (r < rows) v = *reinterpret_cast<const uint2*>(src + 32 * (s >> 1) + 4 * (s & 1));
+          bq[jj][s][0] = v.x;
+          bq[jj][s][1] = v.y;
+        }
+      }
+      bq_si = si;
+    }
+    if (!mbar_wait((uint32_t)__cvta_generic_to_shared(&full_bar[q]), (uint32_t)((n / kTmaItems) & 1))) break;
+    float acc[NT][4];
+    if (valid) {
+      const unsigned char* tl = items + (size_t)q * kItemBytes + j * (kScoreTile * 128);
+      float ah[2][NT][4], al[2][NT][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ah[u][jj][e] = al[u][jj][e] = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        // Rows g and g + 8 of the tile (same swizzle: g & 7), chunk 2t + (s & 1) of box s / 2.
+        const unsigned char* box = tl + (s >> 1) * kBoxBytes;
+        const int chunk = (2 * t + (s & 1)) ^ g;
+        const float4 ra = *reinterpret_cast<const float4*>(box + g * 128 + 16 * chunk);
+        const float4 rb = *reinterpret_cast<const float4*>(box + (g + 8) * 128 + 16 * chunk);
+        uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
+        split_tf32(ra.x, h0, l0);  // row g,   k = t     (first channel of the chunk)
+        split_tf32(rb.x, h1, l1);  // row g+8, k = t
+        split_tf32(ra.y, h2, l2);  // row g,   k = t + 4 (second channel)
+        split_tf32(rb.y, h3, l3);  // row g+8, k = t + 4
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj) {
+          const uint32_t b0 = bq[jj][s][0] << 16, b1 = bq[jj][s][0] & 0xffff0000u;
+          mma_tf32(al[0][jj], l0, l1, l2, l3, b0, b1);
+          mma_tf32(ah[0][jj], h0, h1, h2, h3, b0, b1);
+        }
+        split_tf32(ra.z, h0, l0);  // third and fourth channels: the second k-step
+        split_tf32(rb.z, h1, l1);
+        split_tf32(ra.w, h2, l2);
+        split_tf32(rb.w, h3, l3);
+#pragma unroll
+        for (int jj = 0; jj < NT; ++jj) {
+          const uint32_t b0 = bq[jj][s][1] << 16, b1 = bq[jj][s][1] & 0xffff0000u;
+          mma_tf32(al[1][jj], l0, l1, l2, l3, b0, b1);
+          mma_tf32(ah[1][jj], h0, h1, h2, h3, b0, b1);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < NT; ++jj)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[jj][e] = (ah[0][jj][e] + ah[1][jj][e]) + (al[0][jj][e] + al[1][jj][e]);
+    }
+    // The tile is free once every lane has read it.
+    __syncwarp();
+    if (lane == 0) mbar_arrive((uint32_t)__cvta_generic_to_shared(&empty_bar[q]));
+    if (!valid) continue;
+    // Epilogue as in score_mma_kernel: scores and the tile's group maximum.
+#pragma unroll
+    for (int jj = 0; jj < NT; ++jj) {
+      float v0 = fmaxf(acc[jj][0], 0.f) + fmaxf(acc[jj][1], 0.f);
+      float v1 = fmaxf(acc[jj][2], 0.f) + fmaxf(acc[jj][3], 0.f);
+      v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+      v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+      v0 *= kScoreScale;
+      v1 *= kScoreScale;
+      const int r = 2 * jj + (t >> 1);
+      const int64_t nb = r < rows ? visible_blocks(row_position(sq.n_tokens, sq.n_rows, r)) : 0;
+      const bool ok0 = b0 + g < nb, ok1 = b0 + g + 8 < nb;
+      const int64_t grow = sq.row_begin + r;
+      if ((t & 1) == 0 && r < rows) {
+        float* dst = p.scores + grow * p.ld;
+        if (ok0) dst[b0 + g] = v0;
+        if (ok1) dst[b0 + g + 8] = v1;
+      }
+      if (p.gmax) {
+        float m = fmaxf(ok0 ? v0 : -INFINITY, ok1 ? v1 : -INFINITY);
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (g == 0 && (t & 1) == 0 && b0 < nb) p.gmax[grow * p.gld + b0 / kScoreTile] = m;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
 // One CTA per (32-block tile, group of <= 8 rows); lane = (row, head) pair,
 // warp w = blocks 4w..4w+3 of the tile.
@@ -433,6 +683,61 @@ cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64
 // fills n_tiles / work_begin for kScoreTile (bf16) or kSimtTile (fp32).
 int score_tile_blocks(qsa_dtype q_dtype) { return q_dtype == QSA_BF16 ? kScoreTile : kSimtTile; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// cudaErrorNotSupported: the TMA path does not apply (no encoder, a tensor
+// map the driver refuses); the caller then launches the cp.async kernel.
+template <int NSEQ>
+cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group, int sms, cudaStream_t st) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  ScoreTmaParams<NSEQ> P;
+  memset(&P, 0, sizeof(P));
+  P.p = p;
+  int64_t n_items = 0;
+  for (int i = 0; i < p.n_seqs; ++i) {
+    const ScoreSeq& q = p.seq[i];
+    if (q.n_groups > 1) return cudaErrorNotSupported;   // one row group per sequence on this path
+    P.item_begin[i] = n_items;
+    n_items += (q.n_tiles + kItemTiles - 1) / kItemTiles;
+    const int64_t rows = q.n_tokens / 4;
+    if (rows < 1 || !q.pooled) continue;   // no tile of this sequence is loaded
+    const cuuint64_t dims[2] = {(cuuint64_t)QSA_INDEX_DIM, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)q.pooled_stride * sizeof(float)};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kBoxRows};
+    const cuuint32_t elem[2] = {1, 1};
+    if (encode(&P.tmap[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(q.pooled), dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorNotSupported;
+  }
+  const void* k = max_rows_per_group <= 2 ? (const void*)score_tma_kernel<1, NSEQ> : (const void*)score_tma_kernel<2, NSEQ>;
+  cudaError_t e = allow_dynamic_smem(k, kTmaSmem);
+  if (e != cudaSuccess) return e;
+  P.n_items = n_items;
+  if (n_items == 0) return cudaSuccess;
+  const int64_t ctas = (int64_t)sms * kTmaCtasPerSm;
+  const unsigned grid = (unsigned)(n_items < ctas ? n_items : ctas);
+  const dim3 block(32 * (1 + kTmaConsumers));
+  if (max_rows_per_group <= 2) return launch_kernel(score_tma_kernel<1, NSEQ>, dim3(grid), block, kTmaSmem, st, 0u, P);
+  return launch_kernel(score_tma_kernel<2, NSEQ>, dim3(grid), block, kTmaSmem, st, 0u, P);
+}
+
+}  // namespace
+
 template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
   if (p.n_work == 0) return cudaSuccess;
@@ -440,6 +745,10 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
     return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0u, p);
   }
   const int sms = device_sm_count();
+  if (max_rows_per_group <= 4) {
+    cudaError_t e = launch_score_tma(p, max_rows_per_group, sms, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   constexpr int Ws = 12;
   const size_t smem = sizeof(float) * Ws * kScoreStages * kStageFloats;
   const int64_t need = (p.n_work + Ws - 1) / Ws;
