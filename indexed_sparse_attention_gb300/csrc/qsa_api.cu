@@ -427,7 +427,6 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.head_dim = cfg->head_dim;
   p.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
   p.n_splits = sp.n_splits;
-  p.split_tokens = sp.split_tokens;
   p.total_rows = (int32_t)total_rows;
   p.part_o = part_o;
   p.part_lse = part_lse;

@@ -11,7 +11,8 @@
 //
 // One CTA per (query row, KV group, split): a split walks its share of the
 // row's selected list (the 4 tokens of each selected block, then the tail) in
-// tiles of 32 tokens; each token is located in the sequence's segment table
+// tiles of 32 tokens -- split s of n takes tiles [s T / n, (s + 1) T / n) of
+// the T tiles of the row's longest possible list -- and each token is located in the sequence's segment table
 // and its K and V rows are gathered into shared memory with cp.async.  bf16
 // K/V run on the tensor pipe (mma.sync m16n8k16: the 12 heads of a group
 // padded to 16 rows against 32 gathered tokens) with an fp32 online softmax;
@@ -33,10 +34,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxSplits = 256;  // splits of one (row, KV group)
 
-// Per-row context: position, visible blocks, selected list length.
+// Per-row context: position, visible blocks, selected list length.  The
+// list's longest possible length (cnt = min(sel_ld, nb)) is known without
+// reading cnt, so the splits' ranges and id loads need not wait for it.
 struct RowCtx {
   int64_t nb;
-  int64_t n_list;
+  int64_t tail;       // tail tokens 4 nb .. p
+  int64_t n_list;     // 4 cnt + tail (set by set_count)
+  int64_t n_max;      // 4 min(sel_ld, nb) + tail
   const int32_t* sel_row;
   int32_t cnt;
   int32_t seg_begin;
@@ -53,15 +58,30 @@ __device__ __forceinline__ RowCtx make_row_ctx(const AttnParams<NSEQ>& p, int r)
   const int64_t pos = row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin);
   RowCtx c;
   c.nb = visible_blocks(pos);
-  int32_t cnt = p.cnt[r];
-  cnt = max(0, min(cnt, p.sel_ld));
-  if ((int64_t)cnt > c.nb) cnt = (int32_t)c.nb;
-  c.cnt = cnt;
-  c.n_list = 4 * (int64_t)cnt + (pos + 1 - 4 * c.nb);
+  c.tail = pos + 1 - 4 * c.nb;
+  c.n_max = 4 * min((int64_t)p.sel_ld, c.nb) + c.tail;
+  c.n_list = c.n_max;
+  c.cnt = 0;
   c.sel_row = p.sel + (int64_t)r * p.sel_ld;
   c.seg_begin = sq.seg_begin;
   c.n_segs = sq.n_segs;
   return c;
+}
+
+// The row's count as loaded (clamped to 0 .. min(sel_ld, nb)).
+__device__ __forceinline__ void set_count(RowCtx& c, int32_t cnt, int32_t sel_ld) {
+  cnt = max(0, min(cnt, sel_ld));
+  if ((int64_t)cnt > c.nb) cnt = (int32_t)c.nb;
+  c.cnt = cnt;
+  c.n_list = 4 * (int64_t)cnt + c.tail;
+}
+
+// Entries [i0, i1) of the longest possible list that split `split` of n
+// takes: whole 32-token tiles, balanced over the row.
+__device__ __forceinline__ void split_range(const RowCtx& c, int split, int n, int64_t& i0, int64_t& i1) {
+  const int64_t T = (c.n_max + 31) / 32;
+  i0 = 32 * (T * split / n);
+  i1 = min(c.n_max, 32 * (T * (split + 1) / n));
 }
 
 // The block ids a split needs, staged in shared memory once: entries
@@ -81,6 +101,7 @@ template <int NSEQ>
 __device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& c, const IdCache& ic, int64_t i,
                                        int g, int& seg, int64_t& off) {
   int64_t t;
+  if (i >= c.n_list) return false;
   if (i < 4 * (int64_t)c.cnt) {
     const int64_t k = (i >> 2) - ic.blk0;
     const int32_t b = (k >= 0 && k < ic.n) ? ic.ids[k] : __ldg(c.sel_row + (i >> 2));
@@ -105,7 +126,7 @@ __device__ __forceinline__ IdCache stage_ids(const RowCtx& c, int64_t i0, int64_
   IdCache ic;
   ic.ids = ids_s;
   ic.blk0 = i0 >> 2;
-  const int64_t last = min(i1, 4 * (int64_t)c.cnt);   // entries past 4*cnt are tail tokens
+  const int64_t last = min(i1, c.n_max - c.tail);   // entries past the selected part are tail tokens
   int64_t n = last > i0 ? ((last - 1) >> 2) - ic.blk0 + 1 : 0;
   if (n > kIdCache) n = kIdCache;
   ic.n = (int)n;
@@ -239,9 +260,10 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   const int quarter = warp & 3, half = warp >> 2;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
   const int G = p.group, head0 = g * G;
-  const RowCtx c = make_row_ctx(p, r);
-  const int64_t i0 = (int64_t)split * p.split_tokens;
-  const int64_t i1 = min(c.n_list, i0 + p.split_tokens);
+  RowCtx c = make_row_ctx(p, r);
+  const int32_t cnt_loaded = __ldg(p.cnt + r);   // in flight with the ids and Q below
+  int64_t i0, i1;
+  split_range(c, split, p.n_splits, i0, i1);
   const int n_tiles = i1 > i0 ? (int)((i1 - i0 + kTT - 1) / kTT) : 0;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
 
@@ -255,6 +277,7 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
     if (idx < 16 * CH && row < G) qv[k] = *reinterpret_cast<const uint4*>(qg + (int64_t)row * D + ch * 8);
   }
   const IdCache ic = stage_ids(c, i0, i1, ids_s);
+  set_count(c, cnt_loaded, p.sel_ld);
   __syncthreads();
 
   // Gather of one tile into a stage: thread -> token slot tid/8, chunks (tid&7) + 8j,
@@ -481,11 +504,13 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
   const int G = p.group, head0 = g * G;
-  const RowCtx c = make_row_ctx(p, r);
-  const int64_t i0 = (int64_t)split * p.split_tokens;
-  const int64_t i1 = min(c.n_list, i0 + p.split_tokens);
+  RowCtx c = make_row_ctx(p, r);
+  const int32_t cnt_loaded = __ldg(p.cnt + r);
+  int64_t i0, i1;
+  split_range(c, split, p.n_splits, i0, i1);
   const float zscale = p.scale * kLog2e;
   const IdCache ic = stage_ids(c, i0, i1, ids_s);
+  set_count(c, cnt_loaded, p.sel_ld);
 
   const float* qg = static_cast<const float*>(p.q) + ((int64_t)r * p.n_q_heads + head0) * D;
   for (int idx = tid; idx < G * D; idx += 256) q_s[idx] = qg[idx];
@@ -584,41 +609,46 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_cta_kernel(const float
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
   const int d0 = lane * CPL;
-  // This warp's partials: lse first (one per lane, up to 32 at a time).
-  float m = -INFINITY;
-  for (int s = warp + kMergeWarps * lane; s < n_parts; s += kMergeWarps * 32)
-    m = fmaxf(m, __ldg(lse_parts + (int64_t)s * n_rows + row));
-  m = warp_max(m);
+  // This warp's partials w, w + 8, ..., four per pass: their lse values and
+  // channels are loaded together (one round trip for up to 32 partials), then
+  // added with an online rescale to the warp's running maximum m.
+  float m = -INFINITY, wsum = 0.f;
   float acc[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  float wsum = 0.f;
-  if (m != -INFINITY) {
-    for (int s0 = warp; s0 < n_parts; s0 += kMergeWarps * 4) {
-      float w[4];
-      float4 v[4][CPL / 4];
+  for (int s0 = warp; s0 < n_parts; s0 += kMergeWarps * 4) {
+    float ls[4];
+    float4 v[4][CPL / 4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int s = s0 + k * kMergeWarps;
-        const float ls = s < n_parts ? __ldg(lse_parts + (int64_t)s * n_rows + row) : -INFINITY;
-        w[k] = ls == -INFINITY ? 0.f : exp2f((ls - m) * 1.4426950408889634f);
+    for (int k = 0; k < 4; ++k) {
+      const int s = s0 + k * kMergeWarps;
+      ls[k] = s < n_parts ? __ldg(lse_parts + (int64_t)s * n_rows + row) : -INFINITY;
 #pragma unroll
-        for (int c = 0; c < CPL / 4; ++c)
-          v[k][c] = w[k] > 0.f ? __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * n_rows + row) * head_dim + d0) + c)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      for (int c = 0; c < CPL / 4; ++c)
+        v[k][c] = s < n_parts
+                      ? __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * n_rows + row) * head_dim + d0) + c)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mn = fmaxf(m, fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3])));
+    if (mn == -INFINITY) continue;
+    const float rescale = m == -INFINITY ? 0.f : exp2f((m - mn) * kLog2e);
+    wsum *= rescale;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        wsum += w[k];
+    for (int c = 0; c < CPL; ++c) acc[c] *= rescale;
 #pragma unroll
-        for (int c = 0; c < CPL / 4; ++c) {
-          acc[4 * c + 0] = fmaf(w[k], v[k][c].x, acc[4 * c + 0]);
-          acc[4 * c + 1] = fmaf(w[k], v[k][c].y, acc[4 * c + 1]);
-          acc[4 * c + 2] = fmaf(w[k], v[k][c].z, acc[4 * c + 2]);
-          acc[4 * c + 3] = fmaf(w[k], v[k][c].w, acc[4 * c + 3]);
-        }
+    for (int k = 0; k < 4; ++k) {
+      if (ls[k] == -INFINITY) continue;   // drops the values of a partial without keys
+      const float w = exp2f((ls[k] - mn) * kLog2e);
+      wsum += w;
+#pragma unroll
+      for (int c = 0; c < CPL / 4; ++c) {
+        acc[4 * c + 0] = fmaf(w, v[k][c].x, acc[4 * c + 0]);
+        acc[4 * c + 1] = fmaf(w, v[k][c].y, acc[4 * c + 1]);
+        acc[4 * c + 2] = fmaf(w, v[k][c].z, acc[4 * c + 2]);
+        acc[4 * c + 3] = fmaf(w, v[k][c].w, acc[4 * c + 3]);
       }
     }
+    m = mn;
   }
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc_s[warp][d0 + c] = acc[c];

@@ -103,8 +103,8 @@ struct AttnParams {
   int32_t group;           // query heads per KV head
   int32_t head_dim;
   float scale;             // logit scale
-  int32_t n_splits;        // splits per (row, KV group)
-  int32_t split_tokens;    // selected-list entries per split
+  int32_t n_splits;        // splits per (row, KV group): split s takes tiles [s T / n, (s + 1) T / n)
+                           // of the T 32-token tiles of a row's longest possible list
   int32_t total_rows;      // rows of the whole call (partial buffer stride)
   void* out;               // [rows, Hq, D] (single split)
   float* lse;              // [rows, Hq] or null (single split)
