@@ -189,8 +189,8 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
   uint32_t n_eq = h2[b1];   // entries whose masked key equals K
   if (n_eq != need) {
     // Level 2: key bits 19..8 of the keys in bin b1.
-    for_each_warp([&](uint32_t key, int32_t, bool act) {
-      hist_add(h1, act && (key & 0xfff00000u) == K, (key >> 8) & (kBins - 1));
+    for_each([&](uint32_t key, int32_t) {
+      if ((key & 0xfff00000u) == K) atomicAdd(&h1[(key >> 8) & (kBins - 1)], 1u);
     });
     __syncthreads();
     find_bin(h1, kBins, need, wt[1], s_res);
@@ -201,8 +201,8 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
     n_eq = h1[b2];
     if (n_eq != need) {
       // Level 3: the last 8 key bits.
-      for_each_warp([&](uint32_t key, int32_t, bool act) {
-        hist_add(h3, act && (key & 0xffffff00u) == K, key & (kBins3 - 1));
+      for_each([&](uint32_t key, int32_t) {
+        if ((key & 0xffffff00u) == K) atomicAdd(&h3[key & (kBins3 - 1)], 1u);
       });
       __syncthreads();
       find_bin(h3, kBins3, need, wt[0], s_res);
@@ -304,14 +304,13 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
 
   // 1. Keys of the group maxima (all loads in flight at once) and their
   // top-12-bit histogram.
-  {
-    const float* grow = p.gmax ? p.gmax + (int64_t)r * p.gld : nullptr;
+  if (p.gmax) {
+    const float* grow = p.gmax + (int64_t)r * p.gld;
     float v[kGroupsPerThread];
 #pragma unroll
     for (int j = 0; j < kGroupsPerThread; ++j) {
       const int g = tid + j * kThreads;
-      v[j] = 0.f;
-      if (g < G) v[j] = grow ? __ldg(grow + g) : group_max_of(srow, g, nb);
+      v[j] = g < G ? __ldg(grow + g) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kGroupsPerThread; ++j) {
@@ -321,6 +320,13 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
         r1[g] = key;
         atomicAdd(&h1[key >> 20], 1u);
       }
+    }
+  } else {
+#pragma unroll 1
+    for (int g = tid; g < G; g += kThreads) {
+      const uint32_t key = order_key(group_max_of(srow, g, nb));
+      r1[g] = key;
+      atomicAdd(&h1[key >> 20], 1u);
     }
   }
   __syncthreads();
