@@ -425,8 +425,10 @@ def main():
     if os.path.exists(tf):
         try:
             t = json.load(open(tf))
-            if t.get("workload") == args.workload and t.get("kernel_rev") == SCORE_KERNEL_REV:
-                traffic = t["dram_bytes_per_launch"]
+            if t.get("kernel_rev") == SCORE_KERNEL_REV:
+                for e in t.get("entries", []):
+                    if e.get("workload") == args.workload:
+                        traffic = e["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):
             traffic = None
 
@@ -468,7 +470,7 @@ def main():
 
 
 # Revision tag of the scoring kernel whose DRAM counters profiles/ holds.
-SCORE_KERNEL_REV = "score_mma_tf32_gmax_v3"
+SCORE_KERNEL_REV = "score_tma_ring8_v4"
 
 if __name__ == "__main__":
     main()
