@@ -156,15 +156,28 @@ qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_
  *   scores         device [rows, ld] f32, ld >= max_r nb(p_r)
  *   group_max      device [rows, group_ld] f32, group_ld >= max_r ceil(nb(p_r) / 16)
  *                  and a multiple of 4; may be NULL (not written)
+ *   workspace      device scratch of >= qsa_score_workspace_size bytes, or NULL
+ *                  (then sequences of more than 4 rows use a slower
+ *                  warp-level tensor-pipe kernel); its contents need no
+ *                  initialisation; calls sharing it must not run concurrently
  * Arithmetic: fp32 accumulation of products that lose nothing of the fp32
  * pooled key beyond one fp32 ulp (bf16 index queries on the tensor pipe:
- * for groups of <= 4 rows per sequence the key is split into two tf32
- * parts, otherwise into three bf16 parts that sum to it exactly; fp32 index
- * queries on the CUDA cores).
+ * for <= 4 rows per sequence the key is split into two tf32 parts; for more
+ * rows into three bf16 parts that sum to it exactly; fp32 index queries on
+ * the CUDA cores).
  */
 qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
                             qsa_dtype q_idx_dtype, float* scores, int64_t ld, float* group_max,
-                            int64_t group_ld, void* stream);
+                            int64_t group_ld, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Scratch bytes qsa_score_blocks can use: with bf16 index queries, sequences
+ * of more than 4 rows (prefill chunks) are scored as one tensor-core product
+ * (tcgen05) against the pooled keys split into three bf16 planes, kept in the
+ * workspace (768 bytes per complete block of the largest such sequence).
+ * 0 when no sequence takes that path.
+ */
+size_t qsa_score_workspace_size(const qsa_seq* seqs, int32_t n_seqs, qsa_dtype q_idx_dtype);
 
 /*
  * Scratch bytes qsa_select_topk needs for these sequences.  The kernel keeps
@@ -201,7 +214,8 @@ qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* sco
 
 /*
  * Steps 2 and 3 in one call: qsa_score_blocks writes the group maxima into
- * the workspace and qsa_select_topk starts from them.  Results are those of
+ * the workspace (followed by its own scratch) and qsa_select_topk starts
+ * from them.  Results are those of
  * the two separate calls.
  *   workspace      device scratch of >= qsa_score_select_workspace_size bytes;
  *                  its contents need no initialisation.  Two calls that share

@@ -61,7 +61,7 @@ class AttnConfig(ctypes.Structure):
 
 
 _lib = None
-EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks",
+EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks", "qsa_score_workspace_size",
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
            "qsa_lse_merge")
@@ -84,7 +84,9 @@ def lib() -> ctypes.CDLL:
     L.qsa_last_error.restype = ctypes.c_char_p
     L.qsa_version.restype = i32
     L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
-    L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp]
+    L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp, sz, vp]
+    L.qsa_score_workspace_size.argtypes = [seqp, i32, i32]
+    L.qsa_score_workspace_size.restype = sz
     L.qsa_select_workspace_size.argtypes = [seqp, i32, i32]
     L.qsa_select_workspace_size.restype = sz
     L.qsa_select_topk.argtypes = [seqp, i32, vp, i64, vp, i64, i32, vp, vp, vp, sz, vp]
@@ -190,14 +192,26 @@ def n_groups(n_tokens: int) -> int:
     return (n_tokens // 4 + SCORE_GROUP - 1) // SCORE_GROUP
 
 
-def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None,
-                 group_max: torch.Tensor | None = None):
-    """Step 2: scores[r, b] for every complete block row r sees; with
-    group_max, also each row's maximum over every group of 16 blocks."""
+def score_workspace_size(seqs, q_idx: torch.Tensor, seq_array=None) -> int:
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    return int(lib().qsa_score_workspace_size(arr, len(arr), _dtype_code(q_idx)))
+
+
+def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None,
+                 group_max: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Step 2: scores[r, b] for every complete block row r sees; with
+    group_max, also each row's maximum over every group of 16 blocks.  A
+    workspace is allocated when the call has a tensor-core (prefill) part and
+    none is given."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    if workspace is None:
+        need = score_workspace_size(None, q_idx, seq_array=arr)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
     _check("qsa_score_blocks", lib().qsa_score_blocks(
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0),
-        _ptr(group_max), 0 if group_max is None else group_max.stride(0), _stream(stream)))
+        _ptr(group_max), 0 if group_max is None else group_max.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
 def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, top_k: int = TOP_K,
@@ -320,6 +334,8 @@ class LayerStep:
         self.cnt = torch.empty((rows,), dtype=torch.int32, device=dev)
         self.out = torch.empty((rows, q.shape[1], q.shape[2]), dtype=out_dtype, device=dev)
         self.lse = torch.empty((rows, q.shape[1]), dtype=torch.float32, device=dev)
+        score_ws = score_workspace_size(None, q_idx, seq_array=self.arr)
+        self.score_ws = torch.empty(max(score_ws, 16), dtype=torch.uint8, device=dev) if score_ws else None
         sel_ws = int(lib().qsa_score_select_workspace_size(self.arr, len(self.arr), self.top_k))
         attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
         self.sel_ws = torch.empty(max(sel_ws, 16), dtype=torch.uint8, device=dev)
@@ -339,7 +355,8 @@ class LayerStep:
             pool_index_keys(idxk, pooled, b0, n, stream)
 
     def score(self, stream=None):
-        score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr, group_max=self.group_max)
+        score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr, group_max=self.group_max,
+                     workspace=self.score_ws)
 
     def select(self, stream=None):
         select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr,

@@ -176,8 +176,23 @@ static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, con
   return QSA_OK;
 }
 
+namespace {
+// Sequences that take the tensor-core path: bf16 index queries, more rows
+// than the few-row path serves.
+bool wide_seq(const qsa_seq& q, qsa_dtype qd) { return qd == QSA_BF16 && q.n_rows > 4 && q.n_tokens / 4 > 0; }
+}  // namespace
+
+QSA_API size_t qsa_score_workspace_size(const qsa_seq* seqs, int32_t n_seqs, qsa_dtype q_idx_dtype) {
+  if (!seqs || n_seqs < 1) return 0;
+  size_t need = 0;
+  for (int i = 0; i < n_seqs; ++i)
+    if (wide_seq(seqs[i], q_idx_dtype)) need = std::max(need, score_tc_workspace_bytes(max_visible_blocks(seqs[i])));
+  return need;
+}
+
 QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
-                            float* scores, int64_t ld, float* group_max, int64_t group_ld, void* stream) {
+                            float* scores, int64_t ld, float* group_max, int64_t group_ld, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   const char* fn = "qsa_score_blocks";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -203,7 +218,27 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
     }
   }
   cudaStream_t st = as_stream(stream);
-  if (n_seqs == 1) {
+  const size_t tc_need = qsa_score_workspace_size(seqs, n_seqs, q_idx_dtype);
+  if (tc_need > 0 && workspace && workspace_bytes >= tc_need) {
+    if (!aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
+    // Wide sequences on the tensor cores, one after the other (they share the
+    // workspace in stream order); the others on the few-row path.
+    int32_t row_begin = 0;
+    for (int i = 0; i < n_seqs && s == QSA_OK; ++i) {
+      const qsa_seq& q = seqs[i];
+      if (wide_seq(q, q_idx_dtype)) {
+        cudaError_t e = launch_score_tc(q_idx, row_begin, q.n_rows, q.n_tokens, q.pooled, q.pooled_stride, scores,
+                                        ld, group_max, group_ld, workspace, st);
+        if (e == cudaErrorNotSupported)
+          s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+        else if (e != cudaSuccess)
+          s = cuda_fail(e, fn);
+      } else {
+        s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+      }
+      row_begin += q.n_rows;
+    }
+  } else if (n_seqs == 1) {
     s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
   } else {
     int32_t row_begin = 0;
@@ -297,12 +332,20 @@ int64_t fused_group_ld(const qsa_seq* seqs, int32_t n_seqs) {
 }
 }  // namespace
 
+// Bytes of group maxima a fused call keeps at the start of its workspace
+// (256-byte multiple); the key planes of the tensor-core path follow.
+size_t fused_gmax_bytes(const qsa_seq* seqs, int32_t n_seqs) {
+  int64_t rows = 0;
+  for (int i = 0; i < n_seqs; ++i) rows += std::max(0, seqs[i].n_rows);
+  return (sizeof(float) * (size_t)rows * (size_t)fused_group_ld(seqs, n_seqs) + 255) / 256 * 256;
+}
+
 QSA_API size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k) {
   (void)top_k;
   if (!seqs || n_seqs < 1) return 0;
-  int64_t rows = 0;
-  for (int i = 0; i < n_seqs; ++i) rows += std::max(0, seqs[i].n_rows);
-  return sizeof(float) * (size_t)rows * (size_t)fused_group_ld(seqs, n_seqs);
+  // (bf16 queries assumed: the tensor-core planes are counted whenever a
+  // sequence is wide.)
+  return fused_gmax_bytes(seqs, n_seqs) + qsa_score_workspace_size(seqs, n_seqs, QSA_BF16);
 }
 
 QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
@@ -324,7 +367,12 @@ QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, co
   if (!sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
   float* gmax = static_cast<float*>(workspace);
   const int64_t gld = fused_group_ld(seqs, n_seqs);
-  if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, gmax, gld, stream)) != QSA_OK) return s;
+  const size_t gb = fused_gmax_bytes(seqs, n_seqs);
+  void* planes = static_cast<char*>(workspace) + gb;
+  const size_t planes_bytes = workspace_bytes - gb;
+  if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, gmax, gld, planes, planes_bytes, stream)) !=
+      QSA_OK)
+    return s;
   return qsa_select_topk(seqs, n_seqs, scores, ld, gmax, gld, top_k, sel, cnt, nullptr, 0, stream);
 }
 

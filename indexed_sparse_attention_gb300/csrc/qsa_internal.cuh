@@ -121,6 +121,12 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group,
                          cudaStream_t st);
 
+// Wide scoring on the tensor cores (one sequence; see qsa_score_tc.cu).
+size_t score_tc_workspace_bytes(int64_t n_blocks);
+cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows, int64_t n_tokens,
+                            const float* pooled, int64_t pooled_stride, float* scores, int64_t ld, float* gmax,
+                            int64_t gld, void* workspace, cudaStream_t st);
+
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 size_t select_smem_bytes(int64_t max_nb);

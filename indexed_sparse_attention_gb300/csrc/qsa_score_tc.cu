@@ -1,0 +1,356 @@
+// Step 2 for many query rows (chunked prefill): block scoring as one dense
+// contraction on the 5th-generation tensor cores (hipfire, "QSA sparse
+// attention and the VMM KV backend", section 03: the wide scoring variant for
+// prefill; section 02 for the score itself).
+//
+// For one sequence with R rows, the logits of index head h of row r against
+// block b form the product of A = the index queries as an (4R x 128) bf16
+// matrix (m = 4r + h) and the pooled keys.  The pooled keys are fp32; they are
+// split once per call into three bf16 planes hi + mid + lo that sum to them
+// exactly (each residual is the exact rounding error of the previous plane),
+// laid out as one (blocks x 384) bf16 matrix B = [hi | mid | lo].  Against
+// A' = [Q | Q | Q] (the same query tile reused for each plane) one product
+// with K = 384 gives sum_c q_c (hi_c + mid_c + lo_c) = q . k exactly up to fp32
+// accumulation: bf16 x bf16 products are exact in fp32.
+//
+// score_tc_kernel: one CTA per (128 blocks, 128 row-heads = 32 rows) tile.
+//   warp 0, lane 0  loads the query tile once (two 64-channel boxes) and the
+//                   six 64-wide K slices of the key planes through a 4-stage
+//                   ring, with 2-D tensor copies (128-byte swizzle);
+//   warp 1          allocates 128 TMEM columns; lane 0 issues
+//                   tcgen05.mma (kind::f16, M = 128, N = 128, K = 16) into the
+//                   fp32 accumulator in TMEM and commits each stage back to
+//                   the producer and the finished accumulator to the epilogue;
+//   warps 2..5      read the accumulator with tcgen05.ld (warp w reads TMEM
+//                   lanes 32 (w % 4) ..), apply ReLU per head, add the four
+//                   heads of a row across lanes, scale, mask blocks the row
+//                   cannot see, and write the scores and group maxima.
+// Every wait on an mbarrier gives up after about two seconds instead of
+// hanging (counted in a device counter).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+namespace {
+
+constexpr float kScale = 0.08838834764831845f;   // 1/sqrt(128)
+constexpr int kTcM = 128;                        // row-heads per tile (32 rows)
+constexpr int kTcN = 128;                        // blocks per tile
+constexpr int kTcK = 64;                         // bf16 per 128-byte swizzled row
+constexpr int kPlanesK = 3 * QSA_INDEX_DIM;      // 384
+constexpr int kKSlices = kPlanesK / kTcK;        // 6
+constexpr int kStages = 4;
+constexpr int kSliceBytes = kTcN * kTcK * 2;     // 16 KB of B per slice
+constexpr int kABytes = kTcM * QSA_INDEX_DIM * 2;  // 32 KB query tile
+constexpr size_t kTcSmem = kABytes + (size_t)kStages * kSliceBytes + 1024;
+constexpr int kTcThreads = 192;
+
+__device__ int g_tc_wait_timeouts;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity) {
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!bar_try(b, parity))
+    if (now_ns() - t0 > 2000000000ull) {
+      atomicAdd(&g_tc_wait_timeouts, 1);
+      return false;
+    }
+  return true;
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored as the
+// 128-byte swizzle writes it: rows of 128 bytes (64 bf16 of K), 8-row groups
+// 1,024 bytes apart.  Fields: start address >> 4 (bits 0-13), leading byte
+// offset >> 4 (16-29; unused for this layout), stride byte offset >> 4
+// (32-45), the fixed value 1 at bit 46, base offset 0 (49-51), swizzle mode
+// 2 = 128-byte (61-63).
+__device__ __forceinline__ uint64_t umma_desc(const void* p) {
+  const uint64_t a = (smem_addr(p) & 0x3FFFFu) >> 4;
+  return a | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
+// A and B (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+                            ((uint32_t)(kTcM >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ key planes
+// planes[b][p * 128 + c], p = 0, 1, 2: bf16 hi, mid, lo of pooled[b][c].
+__global__ void split_planes_kernel(const float* __restrict__ pooled, int64_t pstride, int64_t n_blocks,
+                                    __nv_bfloat16* __restrict__ planes) {
+  grid_dependency_sync();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // (block, 4-channel group)
+  if (i >= n_blocks * (QSA_INDEX_DIM / 4)) return;
+  const int64_t b = i / (QSA_INDEX_DIM / 4);
+  const int c = (int)(i % (QSA_INDEX_DIM / 4)) * 4;
+  const float4 x = *reinterpret_cast<const float4*>(pooled + b * pstride + c);
+  const float v[4] = {x.x, x.y, x.z, x.w};
+  __nv_bfloat16 h[4], m[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    h[j] = __float2bfloat16_rn(v[j]);
+    const float r1 = v[j] - __bfloat162float(h[j]);
+    m[j] = __float2bfloat16_rn(r1);
+    l[j] = __float2bfloat16_rn(r1 - __bfloat162float(m[j]));
+  }
+  __nv_bfloat16* row = planes + b * kPlanesK + c;
+  *reinterpret_cast<uint2*>(row) = *reinterpret_cast<const uint2*>(h);
+  *reinterpret_cast<uint2*>(row + QSA_INDEX_DIM) = *reinterpret_cast<const uint2*>(m);
+  *reinterpret_cast<uint2*>(row + 2 * QSA_INDEX_DIM) = *reinterpret_cast<const uint2*>(l);
+}
+
+// ------------------------------------------------------------------ scoring
+struct ScoreTcParams {
+  CUtensorMap tmap_q;       // index queries of the sequence: [4 R, 128] bf16
+  CUtensorMap tmap_k;       // key planes: [blocks, 384] bf16
+  float* scores;
+  int64_t ld;
+  float* gmax;
+  int64_t gld;
+  int64_t n_tokens;
+  int32_t n_rows;
+  int32_t row_begin;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(const __grid_constant__ ScoreTcParams P) {
+  extern __shared__ uint8_t tc_raw[];
+  __shared__ uint64_t a_full, full[kStages], empty[kStages], acc_full;
+  __shared__ uint32_t tmem_slot;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* smA = base;             // two boxes [128 row-heads][64 channels]
+  uint8_t* smB = base + kABytes;   // kStages boxes [128 blocks][64 of K]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kTcN;
+  const int m0 = blockIdx.y * kTcM;
+  const int r_last = min(P.n_rows - 1, m0 / 4 + kTcM / 4 - 1);
+  const int64_t nb_last = visible_blocks(row_position(P.n_tokens, P.n_rows, r_last));
+  if (n0 >= nb_last) return;   // no row of the tile sees these blocks
+
+  if (tid == 0) {
+    bar_init(&a_full, 1);
+    bar_init(&acc_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      bar_init(&full[s], 1);
+      bar_init(&empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&tmem_slot)),
+                 "r"(kTcN)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  grid_dependency_sync();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bar_expect_tx(&a_full, kABytes);
+      tma_2d(smA, &P.tmap_q, 0, m0, &a_full);
+      tma_2d(smA + kABytes / 2, &P.tmap_q, kTcK, m0, &a_full);
+      for (int kc = 0; kc < kKSlices; ++kc) {
+        const int s = kc % kStages;
+        if (kc >= kStages && !bar_wait(&empty[s], (uint32_t)((kc / kStages - 1) & 1))) break;
+        bar_expect_tx(&full[s], kSliceBytes);
+        tma_2d(smB + s * kSliceBytes, &P.tmap_k, kc * kTcK, n0, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && bar_wait(&a_full, 0)) {
+      bool ok = true;
+      for (int kc = 0; kc < kKSlices && ok; ++kc) {
+        const int s = kc % kStages;
+        if (!(ok = bar_wait(&full[s], (uint32_t)((kc / kStages) & 1)))) break;
+        tc_fence_after();
+        // Slice kc is plane kc / 2, channels 64 (kc % 2) ..: the query half kc % 2.
+        const uint8_t* a = smA + (kc % 2) * (kABytes / 2);
+        const uint8_t* b = smB + s * kSliceBytes;
+#pragma unroll
+        for (int j = 0; j < kTcK / 16; ++j)
+          umma_f16(tmem, umma_desc(a + 32 * j), umma_desc(b + 32 * j), (kc | j) != 0 ? 1u : 0u);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(&acc_full);
+    }
+  } else {
+    // Epilogue: TMEM lanes 32 (warp % 4) .. +31 = row-heads m of the tile.
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const int r = m0 / 4 + m / 4;   // row within the sequence
+    const bool row_ok = r < P.n_rows;
+    const int64_t nb = row_ok ? visible_blocks(row_position(P.n_tokens, P.n_rows, r)) : 0;
+    if (bar_wait(&acc_full, 0)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c0 = 0; c0 < kTcN; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float x = fmaxf(v[i], 0.f);
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          v[i] = x * kScale;
+        }
+        if ((lane & 3) == 0 && row_ok) {
+          const int64_t b0 = n0 + c0;
+          float* dst = P.scores + (int64_t)(P.row_begin + r) * P.ld + b0;
+          if (b0 + 32 <= nb) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (b0 + i < nb) dst[i] = v[i];
+          }
+          if (P.gmax) {
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              if (b0 + 16 * g >= nb) continue;
+              float mx = -INFINITY;
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (b0 + 16 * g + i < nb) mx = fmaxf(mx, v[16 * g + i]);
+              P.gmax[(int64_t)(P.row_begin + r) * P.gld + b0 / 16 + g] = mx;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTcN) : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t score_tc_workspace_bytes(int64_t n_blocks) {
+  return n_blocks > 0 ? (size_t)n_blocks * kPlanesK * 2 : 0;
+}
+
+cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows, int64_t n_tokens,
+                            const float* pooled, int64_t pooled_stride, float* scores, int64_t ld, float* gmax,
+                            int64_t gld, void* workspace, cudaStream_t st) {
+  const int64_t nb = n_tokens / 4;
+  if (nb <= 0 || n_rows <= 0) return cudaSuccess;
+  __nv_bfloat16* planes = static_cast<__nv_bfloat16*>(workspace);
+  const int64_t threads = nb * (QSA_INDEX_DIM / 4);
+  cudaError_t e = launch_kernel(split_planes_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, 0u,
+                                pooled, pooled_stride, nb, planes);
+  if (e != cudaSuccess) return e;
+  ScoreTcParams P;
+  memset(&P, 0, sizeof(P));
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(q_idx) + (int64_t)row_begin * QSA_INDEX_HEADS * QSA_INDEX_DIM;
+  if (!encode_bf16_2d(&P.tmap_q, q, QSA_INDEX_DIM, (uint64_t)n_rows * QSA_INDEX_HEADS, QSA_INDEX_DIM * 2, kTcK, kTcM) ||
+      !encode_bf16_2d(&P.tmap_k, planes, kPlanesK, (uint64_t)nb, kPlanesK * 2, kTcK, kTcN))
+    return cudaErrorNotSupported;
+  P.scores = scores;
+  P.ld = ld;
+  P.gmax = gmax;
+  P.gld = gld;
+  P.n_tokens = n_tokens;
+  P.n_rows = n_rows;
+  P.row_begin = row_begin;
+  if ((e = allow_dynamic_smem((const void*)score_tc_kernel, kTcSmem)) != cudaSuccess) return e;
+  const dim3 grid((unsigned)((nb + kTcN - 1) / kTcN), (unsigned)(((int64_t)n_rows * 4 + kTcM - 1) / kTcM));
+  return launch_kernel(score_tc_kernel, grid, dim3(kTcThreads), kTcSmem, st, 0u, P);
+}
+
+}  // namespace qsa

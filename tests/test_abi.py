@@ -88,21 +88,21 @@ def test_pool_validation(L):
 
 def test_score_validation(L):
     seq = _seq()
-    assert L.qsa_score_blocks(seq, 0, FAKE, qsa.BF16, FAKE, 1024, None, 0, None) == 1
-    assert L.qsa_score_blocks(seq, 1, FAKE, 9, FAKE, 1024, None, 0, None) == 2
-    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1023, None, 0, None) == 1       # ld < 1,024 blocks
-    assert L.qsa_score_blocks(seq, 1, FAKE_MIS, qsa.BF16, FAKE, 1024, None, 0, None) == 3
-    assert L.qsa_score_blocks(_seq(pooled=None), 1, FAKE, qsa.BF16, FAKE, 1024, None, 0, None) == 1
-    assert L.qsa_score_blocks(_seq(n_rows=5000), 1, FAKE, qsa.BF16, FAKE, 1024, None, 0, None) == 1
-    assert L.qsa_score_blocks(_seq(n_tokens=4 * (1 << 18) + 4), 1, FAKE, qsa.BF16, FAKE, 1 << 20, None, 0, None) == 2
+    assert L.qsa_score_blocks(seq, 0, FAKE, qsa.BF16, FAKE, 1024, None, 0, None, 0, None) == 1
+    assert L.qsa_score_blocks(seq, 1, FAKE, 9, FAKE, 1024, None, 0, None, 0, None) == 2
+    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1023, None, 0, None, 0, None) == 1       # ld < 1,024 blocks
+    assert L.qsa_score_blocks(seq, 1, FAKE_MIS, qsa.BF16, FAKE, 1024, None, 0, None, 0, None) == 3
+    assert L.qsa_score_blocks(_seq(pooled=None), 1, FAKE, qsa.BF16, FAKE, 1024, None, 0, None, 0, None) == 1
+    assert L.qsa_score_blocks(_seq(n_rows=5000), 1, FAKE, qsa.BF16, FAKE, 1024, None, 0, None, 0, None) == 1
+    assert L.qsa_score_blocks(_seq(n_tokens=4 * (1 << 18) + 4), 1, FAKE, qsa.BF16, FAKE, 1 << 20, None, 0, None, 0, None) == 2
 
 
 def test_group_max_validation(L):
     seq = _seq()   # 4,099 tokens: 1,024 blocks = 64 groups
-    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE, 60, None) == 1
+    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE, 60, None, 0, None) == 1
     assert "group_ld" in L.qsa_last_error().decode()
-    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE, 66, None) == 3
-    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE_MIS, 64, None) == 3
+    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE, 66, None, 0, None) == 3
+    assert L.qsa_score_blocks(seq, 1, FAKE, qsa.BF16, FAKE, 1024, FAKE_MIS, 64, None, 0, None) == 3
     assert L.qsa_select_topk(seq, 1, FAKE, 1024, FAKE, 60, 512, FAKE, FAKE, None, 0, None) == 1
     assert L.qsa_select_topk(seq, 1, FAKE, 1024, FAKE_MIS, 64, 512, FAKE, FAKE, None, 0, None) == 3
     assert L.qsa_select_topk(seq, 1, FAKE, 1022, None, 0, 512, FAKE, FAKE, None, 0, None) == 3   # ld % 4
