@@ -13,18 +13,29 @@
 // with K = 384 gives sum_c q_c (hi_c + mid_c + lo_c) = q . k exactly up to fp32
 // accumulation: bf16 x bf16 products are exact in fp32.
 //
-// score_tc_kernel: one CTA per (128 blocks, 128 row-heads = 32 rows) tile.
-//   warp 0, lane 0  loads the query tile once (two 64-channel boxes) and the
-//                   six 64-wide K slices of the key planes through a 4-stage
-//                   ring, with 2-D tensor copies (128-byte swizzle);
-//   warp 1          allocates 128 TMEM columns; lane 0 issues
-//                   tcgen05.mma (kind::f16, M = 128, N = 128, K = 16) into the
-//                   fp32 accumulator in TMEM and commits each stage back to
-//                   the producer and the finished accumulator to the epilogue;
-//   warps 2..5      read the accumulator with tcgen05.ld (warp w reads TMEM
-//                   lanes 32 (w % 4) ..), apply ReLU per head, add the four
-//                   heads of a row across lanes, scale, mask blocks the row
-//                   cannot see, and write the scores and group maxima.
+// score_tc_kernel: persistent, one CTA per SM; CTA c takes a contiguous run of
+// output tiles (128 row-heads = 32 rows x 128 blocks), block tile major, so
+// one tile of key planes (128 blocks x 384 = 96 KB) stays in shared memory
+// while the query tiles (32 KB) stream past it.
+//   warp 0, lane 0  loads the key-plane tile (six 64-wide K slices) when the
+//                   block tile changes, and each output tile's query tile as
+//                   two 64-channel boxes through a 4-box ring, with 2-D
+//                   tensor copies (128-byte swizzle);
+//   warp 1          allocates 256 TMEM columns (two fp32 accumulators of
+//                   128 columns); lane 0 issues tcgen05.mma (kind::f16,
+//                   M = 128, N = 128, K = 16) into the accumulator the
+//                   epilogue has released -- K slice kc pairs query half
+//                   kc % 2 with key plane kc / 2 -- and commits the query
+//                   boxes and, at a block-tile change, the key tile back to
+//                   the producer, and each finished accumulator to the
+//                   epilogue;
+//   warps 2..9      read an accumulator with tcgen05.ld (warp w reads TMEM
+//                   lanes 32 (w % 4) .., columns 64 ((w - 2) / 4) ..), release
+//                   it, apply ReLU per head,
+//                   add the four heads of a row across lanes, scale, mask
+//                   blocks the row cannot see, and write the scores and group
+//                   maxima -- while the MMAs of the next tile run.
+// Tiles whose blocks no row of the tile can see are skipped by every role.
 // Every wait on an mbarrier gives up after about two seconds instead of
 // hanging (counted in a device counter).
 #include <cuda.h>
@@ -44,11 +55,14 @@ constexpr int kTcN = 128;                        // blocks per tile
 constexpr int kTcK = 64;                         // bf16 per 128-byte swizzled row
 constexpr int kPlanesK = 3 * QSA_INDEX_DIM;      // 384
 constexpr int kKSlices = kPlanesK / kTcK;        // 6
-constexpr int kStages = 4;
+constexpr int kABoxes = 4;                       // query-box ring (two per output tile)
 constexpr int kSliceBytes = kTcN * kTcK * 2;     // 16 KB of B per slice
-constexpr int kABytes = kTcM * QSA_INDEX_DIM * 2;  // 32 KB query tile
-constexpr size_t kTcSmem = kABytes + (size_t)kStages * kSliceBytes + 1024;
-constexpr int kTcThreads = 192;
+constexpr int kBBytes = kKSlices * kSliceBytes;  // 96 KB key-plane tile
+constexpr int kABoxBytes = kTcM * kTcK * 2;      // 16 KB: 128 row-heads x 64 channels
+constexpr size_t kTcSmem = (size_t)kBBytes + (size_t)kABoxes * kABoxBytes + 1024;
+constexpr int kEpiWarps = 8;                     // two per TMEM lane quarter, each half the columns
+constexpr int kTcThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 
 __device__ int g_tc_wait_timeouts;
 
@@ -175,32 +189,49 @@ struct ScoreTcParams {
   int32_t row_begin;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(const __grid_constant__ ScoreTcParams P) {
+struct TcTile {
+  int m0, n0;
+  bool live;   // some row of the tile sees some of its blocks
+};
+
+__device__ __forceinline__ TcTile tc_tile(const ScoreTcParams& P, int n_tiles_m, int t) {
+  TcTile x;
+  x.n0 = (t / n_tiles_m) * kTcN;
+  x.m0 = (t % n_tiles_m) * kTcM;
+  const int r_last = min(P.n_rows - 1, x.m0 / 4 + kTcM / 4 - 1);
+  x.live = x.n0 < visible_blocks(row_position(P.n_tokens, P.n_rows, r_last));
+  return x;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_constant__ ScoreTcParams P) {
   extern __shared__ uint8_t tc_raw[];
-  __shared__ uint64_t a_full, full[kStages], empty[kStages], acc_full;
+  __shared__ uint64_t b_full, b_empty, a_full[kABoxes], a_empty[kABoxes], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_slot;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* smA = base;             // two boxes [128 row-heads][64 channels]
-  uint8_t* smB = base + kABytes;   // kStages boxes [128 blocks][64 of K]
+  uint8_t* smB = base;              // six boxes [128 blocks][64 of K]
+  uint8_t* smA = base + kBBytes;    // kABoxes boxes [128 row-heads][64 channels]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kTcN;
-  const int m0 = blockIdx.y * kTcM;
-  const int r_last = min(P.n_rows - 1, m0 / 4 + kTcM / 4 - 1);
-  const int64_t nb_last = visible_blocks(row_position(P.n_tokens, P.n_rows, r_last));
-  if (n0 >= nb_last) return;   // no row of the tile sees these blocks
+  const int n_tiles_m = (int)(((int64_t)P.n_rows * 4 + kTcM - 1) / kTcM);
+  const int n_tiles = n_tiles_m * (int)((P.n_tokens / 4 + kTcN - 1) / kTcN);
+  const int t0 = (int)((int64_t)n_tiles * blockIdx.x / gridDim.x);
+  const int t1 = (int)((int64_t)n_tiles * (blockIdx.x + 1) / gridDim.x);
 
   if (tid == 0) {
-    bar_init(&a_full, 1);
-    bar_init(&acc_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      bar_init(&full[s], 1);
-      bar_init(&empty[s], 1);
+    bar_init(&b_full, 1);
+    bar_init(&b_empty, 1);
+    for (int i = 0; i < kABoxes; ++i) {
+      bar_init(&a_full[i], 1);
+      bar_init(&a_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      bar_init(&acc_full[i], 1);
+      bar_init(&acc_empty[i], kEpiThreads);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&tmem_slot)),
-                 "r"(kTcN)
+                 "r"(2 * kTcN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
@@ -212,63 +243,106 @@ __global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(const __grid_co
 
   if (warp == 0) {
     if (lane == 0) {
-      bar_expect_tx(&a_full, kABytes);
-      tma_2d(smA, &P.tmap_q, 0, m0, &a_full);
-      tma_2d(smA + kABytes / 2, &P.tmap_q, kTcK, m0, &a_full);
-      for (int kc = 0; kc < kKSlices; ++kc) {
-        const int s = kc % kStages;
-        if (kc >= kStages && !bar_wait(&empty[s], (uint32_t)((kc / kStages - 1) & 1))) break;
-        bar_expect_tx(&full[s], kSliceBytes);
-        tma_2d(smB + s * kSliceBytes, &P.tmap_k, kc * kTcK, n0, &full[s]);
+      int b_loads = 0, boxes = 0, n_prev = -1;
+      bool ok = true;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const TcTile x = tc_tile(P, n_tiles_m, t);
+        if (!x.live) continue;
+        if (x.n0 != n_prev) {   // a new key-plane tile, once the MMAs are done with the last
+          if (b_loads >= 1 && !(ok = bar_wait(&b_empty, (uint32_t)((b_loads - 1) & 1)))) break;
+          bar_expect_tx(&b_full, kBBytes);
+          for (int kc = 0; kc < kKSlices; ++kc) tma_2d(smB + kc * kSliceBytes, &P.tmap_k, kc * kTcK, x.n0, &b_full);
+          ++b_loads;
+          n_prev = x.n0;
+        }
+        for (int h = 0; h < 2; ++h, ++boxes) {
+          const int q = boxes % kABoxes;
+          if (boxes >= kABoxes && !(ok = bar_wait(&a_empty[q], (uint32_t)((boxes / kABoxes - 1) & 1)))) break;
+          bar_expect_tx(&a_full[q], kABoxBytes);
+          tma_2d(smA + q * kABoxBytes, &P.tmap_q, h * kTcK, x.m0, &a_full[q]);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && bar_wait(&a_full, 0)) {
+    if (lane == 0) {
+      int b_loads = 0, boxes = 0, tiles = 0, n_prev = -1;
       bool ok = true;
-      for (int kc = 0; kc < kKSlices && ok; ++kc) {
-        const int s = kc % kStages;
-        if (!(ok = bar_wait(&full[s], (uint32_t)((kc / kStages) & 1)))) break;
+      for (int t = t0; t < t1 && ok; ++t) {
+        const TcTile x = tc_tile(P, n_tiles_m, t);
+        if (!x.live) continue;
+        if (x.n0 != n_prev) {
+          if (b_loads > 0) umma_commit(&b_empty);   // the previous key tile is done once these MMAs finish
+          if (!(ok = bar_wait(&b_full, (uint32_t)(b_loads & 1)))) break;
+          ++b_loads;
+          n_prev = x.n0;
+        }
+        const int acc = tiles & 1;
+        if (tiles >= 2 && !(ok = bar_wait(&acc_empty[acc], (uint32_t)((tiles / 2 - 1) & 1)))) break;
+        const int q0 = boxes % kABoxes, q1 = (boxes + 1) % kABoxes;
+        if (!(ok = bar_wait(&a_full[q0], (uint32_t)((boxes / kABoxes) & 1)))) break;
+        if (!(ok = bar_wait(&a_full[q1], (uint32_t)(((boxes + 1) / kABoxes) & 1)))) break;
         tc_fence_after();
-        // Slice kc is plane kc / 2, channels 64 (kc % 2) ..: the query half kc % 2.
-        const uint8_t* a = smA + (kc % 2) * (kABytes / 2);
-        const uint8_t* b = smB + s * kSliceBytes;
+        const uint32_t d = tmem + (uint32_t)(acc * kTcN);
+        for (int kc = 0; kc < kKSlices; ++kc) {
+          // Slice kc is plane kc / 2, channels 64 (kc % 2) ..: the query half kc % 2.
+          const uint8_t* a = smA + ((kc % 2) ? q1 : q0) * kABoxBytes;
+          const uint8_t* b = smB + kc * kSliceBytes;
 #pragma unroll
-        for (int j = 0; j < kTcK / 16; ++j)
-          umma_f16(tmem, umma_desc(a + 32 * j), umma_desc(b + 32 * j), (kc | j) != 0 ? 1u : 0u);
-        umma_commit(&empty[s]);
+          for (int j = 0; j < kTcK / 16; ++j)
+            umma_f16(d, umma_desc(a + 32 * j), umma_desc(b + 32 * j), (kc | j) != 0 ? 1u : 0u);
+        }
+        umma_commit(&a_empty[q0]);
+        umma_commit(&a_empty[q1]);
+        umma_commit(&acc_full[acc]);
+        boxes += 2;
+        ++tiles;
       }
-      umma_commit(&acc_full);
     }
   } else {
     // Epilogue: TMEM lanes 32 (warp % 4) .. +31 = row-heads m of the tile.
     const int quarter = warp & 3;
+    constexpr int kColGroups = kEpiWarps / 4;
+    constexpr int kGroupCols = kTcN / kColGroups;
+    const int cgrp = (warp - 2) / 4;   // columns [kGroupCols cgrp, + kGroupCols)
     const int m = quarter * 32 + lane;
-    const int r = m0 / 4 + m / 4;   // row within the sequence
-    const bool row_ok = r < P.n_rows;
-    const int64_t nb = row_ok ? visible_blocks(row_position(P.n_tokens, P.n_rows, r)) : 0;
-    if (bar_wait(&acc_full, 0)) {
+    int tiles = 0;
+    for (int t = t0; t < t1; ++t) {
+      const TcTile x = tc_tile(P, n_tiles_m, t);
+      if (!x.live) continue;
+      const int acc = tiles & 1;
+      if (!bar_wait(&acc_full[acc], (uint32_t)((tiles / 2) & 1))) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int c0 = 0; c0 < kTcN; c0 += 32) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+      const int r = x.m0 / 4 + m / 4;   // row within the sequence
+      const bool row_ok = r < P.n_rows;
+      const int64_t nb = row_ok ? visible_blocks(row_position(P.n_tokens, P.n_rows, r)) : 0;
+      constexpr int kChunks = kGroupCols / 32;
+      float v[kChunks][32];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kTcN + kGroupCols * cgrp + 32 * c), v[c]);
+      // The accumulator is in registers: the MMAs of a later tile may reuse it.
+      tc_fence_before();
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(&acc_empty[acc])) : "memory");
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float x = fmaxf(v[i], 0.f);
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          v[i] = x * kScale;
+          float y = fmaxf(v[c][i], 0.f);
+          y += __shfl_xor_sync(0xffffffffu, y, 1);
+          y += __shfl_xor_sync(0xffffffffu, y, 2);
+          v[c][i] = y * kScale;
         }
         if ((lane & 3) == 0 && row_ok) {
-          const int64_t b0 = n0 + c0;
+          const int64_t b0 = x.n0 + kGroupCols * cgrp + 32 * c;
           float* dst = P.scores + (int64_t)(P.row_begin + r) * P.ld + b0;
           if (b0 + 32 <= nb) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v[c][i], v[c][i + 1], v[c][i + 2], v[c][i + 3]);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (b0 + i < nb) dst[i] = v[i];
+              if (b0 + i < nb) dst[i] = v[c][i];
           }
           if (P.gmax) {
 #pragma unroll
@@ -277,19 +351,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) score_tc_kernel(const __grid_co
               float mx = -INFINITY;
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                if (b0 + 16 * g + i < nb) mx = fmaxf(mx, v[16 * g + i]);
+                if (b0 + 16 * g + i < nb) mx = fmaxf(mx, v[c][16 * g + i]);
               P.gmax[(int64_t)(P.row_begin + r) * P.gld + b0 / 16 + g] = mx;
             }
           }
         }
       }
+      ++tiles;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTcN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(2 * kTcN) : "memory");
   }
 }
 
@@ -349,8 +424,10 @@ cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows
   P.n_rows = n_rows;
   P.row_begin = row_begin;
   if ((e = allow_dynamic_smem((const void*)score_tc_kernel, kTcSmem)) != cudaSuccess) return e;
-  const dim3 grid((unsigned)((nb + kTcN - 1) / kTcN), (unsigned)(((int64_t)n_rows * 4 + kTcM - 1) / kTcM));
-  return launch_kernel(score_tc_kernel, grid, dim3(kTcThreads), kTcSmem, st, 0u, P);
+  const int64_t tiles = ((nb + kTcN - 1) / kTcN) * (((int64_t)n_rows * 4 + kTcM - 1) / kTcM);
+  const int sms = device_sm_count();
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  return launch_kernel(score_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, 0u, P);
 }
 
 }  // namespace qsa
