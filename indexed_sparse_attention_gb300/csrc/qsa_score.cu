@@ -76,7 +76,10 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
 // ------------------------------------------------------------------ pooling
 __global__ void pool_kernel(const void* __restrict__ idx, int dtype, int64_t tok_stride, int64_t first_block,
                             int64_t n_blocks, float* __restrict__ pooled, int64_t pstride) {
-  grid_dependency_sync();
+  // The scoring launch after this one may start at once: it reads blocks this
+  // launch writes only after its own dependency wait.
+  grid_dependency_release();
+  grid_dependency_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // (block, 4-channel group)
   if (i >= n_blocks * (QSA_INDEX_DIM / 4)) return;
   const int64_t b = first_block + i / (QSA_INDEX_DIM / 4);
@@ -465,28 +468,41 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-  grid_dependency_sync();
   const int64_t i0 = P.n_items * blockIdx.x / gridDim.x;
   const int64_t i1 = P.n_items * (blockIdx.x + 1) / gridDim.x;
   const int n_items = (int)(i1 - i0);
 
   if (warp == 0) {
-    // Producer: lane q issues the items of slot q, in order.
+    // Producer: lane q issues the items of slot q, in order.  Pooled blocks
+    // before the ones this step's rows complete are state from earlier steps
+    // that no launch of this step writes: a slot's first item is requested
+    // before the dependency wait when it holds only such blocks.
+    bool waited = false;
     if (lane < kTmaItems) {
       const uint32_t fb = (uint32_t)__cvta_generic_to_shared(&full_bar[lane]);
       const uint32_t eb = (uint32_t)__cvta_generic_to_shared(&empty_bar[lane]);
       const uint32_t dst = (uint32_t)__cvta_generic_to_shared(items + (size_t)lane * kItemBytes);
       for (int n = lane; n < n_items; n += kTmaItems) {
-        if (n >= kTmaItems && !mbar_wait(eb, (uint32_t)((n / kTmaItems - 1) & 1))) break;
         const int si = find_seq_by_item(P, i0 + n);
-        const int y = (int)((i0 + n - P.item_begin[si]) * kItemBlocks);
+        const int64_t y = (i0 + n - P.item_begin[si]) * kItemBlocks;
+        const ScoreSeq& sq = p.seq[si];
+        const bool old_blocks = y + kItemBlocks <= (sq.n_tokens - sq.n_rows) / 4;
+        if (!waited && !(n < kTmaItems && old_blocks)) {
+          grid_dependency_wait();
+          waited = true;
+        }
+        if (n >= kTmaItems && !mbar_wait(eb, (uint32_t)((n / kTmaItems - 1) & 1))) break;
         mbar_expect_tx(fb, kItemBytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kBoxBytes, &P.tmap[si], 32 * c, y, fb);
+        for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kBoxBytes, &P.tmap[si], 32 * c, (int)y, fb);
       }
     }
+    if (!waited) grid_dependency_wait();
+    grid_dependency_release();
     return;
   }
+  grid_dependency_wait();
+  grid_dependency_release();
 
   // Consumers.
   const int cw = warp - 1;
