@@ -254,14 +254,12 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   float* a_s = m_s + 32;
   int* valid_s = reinterpret_cast<int*>(smem + L::off_valid);
   int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L::off_ids);
-  grid_dependency_sync();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quarter = warp & 3, half = warp >> 2;
   const int split = blockIdx.x, g = blockIdx.y, r = p.row_base + blockIdx.z;
   const int G = p.group, head0 = g * G;
   RowCtx c = make_row_ctx(p, r);
-  const int32_t cnt_loaded = __ldg(p.cnt + r);   // in flight with the ids and Q below
   int64_t i0, i1;
   split_range(c, split, p.n_splits, i0, i1);
   const int n_tiles = i1 > i0 ? (int)((i1 - i0 + kTT - 1) / kTT) : 0;
@@ -276,6 +274,11 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
     qv[k] = make_uint4(0u, 0u, 0u, 0u);
     if (idx < 16 * CH && row < G) qv[k] = *reinterpret_cast<const uint4*>(qg + (int64_t)row * D + ch * 8);
   }
+  // Q is an input of the step that no earlier launch of the step writes: its
+  // loads above are issued before the wait for the selection.
+  grid_dependency_wait();
+  grid_dependency_release();
+  const int32_t cnt_loaded = __ldg(p.cnt + r);   // in flight with the ids
   const IdCache ic = stage_ids(c, i0, i1, ids_s);
   set_count(c, cnt_loaded, p.sel_ld);
   __syncthreads();
