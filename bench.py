@@ -469,6 +469,27 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers)
 
+    roofline = {"kernel": "score_blocks", "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
+                "unit": "GB/s", "frac": score_gbs / peak_gbs, "traffic": traffic,
+                "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
+                "timing": "graph of 12 launches each followed by a one-element non-PDL kernel, minus a graph "
+                          "of those kernels alone (no overlap with neighbours)",
+                "algorithmic_bytes_per_launch": ab["score"]}
+    if M > 4:
+        # Many rows: scoring is a dense contraction on the tensor cores.  The
+        # algorithmic flops are 2 x rows x 4 heads x blocks x 128; the kernel
+        # executes three times as many (three bf16 planes of the fp32 keys).
+        flops = 2.0 * M * 4 * (L // 4) * 128
+        try:
+            peak_tf, tf_src = float(peaks["bf16_tflops"]), "measured (bf16_tflops, burst)"
+        except (KeyError, ValueError, TypeError):
+            peak_tf, tf_src = 1900.0, "fallback"
+        achieved = flops / (score_us * 1e-6) / 1e12
+        roofline.update({"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tf, "traffic": None, "peak_source": tf_src,
+                         "algorithmic_flops_per_launch": flops, "executed_flops_per_launch": 3 * flops})
+        roofline.pop("algorithmic_bytes_per_launch")
+
     launches = sum(launches_per_layer(l) for l in layers) * args.steps
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -484,11 +505,7 @@ def main():
         "algorithmic_bytes_per_layer_step": ab["total"],
         "step_hbm_gbs": step_gbs,
         "step_frac_of_peak": step_gbs / peak_gbs,
-        "roofline": {"kernel": "score_blocks", "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
-                     "unit": "GB/s", "frac": score_gbs / peak_gbs, "traffic": traffic,
-                     "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
-                     "timing": "graph of 12 launches each followed by a one-element non-PDL kernel, minus a graph of those kernels alone (no overlap with neighbours)",
-                     "algorithmic_bytes_per_launch": ab["score"]},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
