@@ -166,6 +166,12 @@ def barrier(world):
         dist.barrier()
 
 
+def whole_job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Units every rank processed, over the slowest rank's time (ms): the
+    whole-job throughput of N weak-scaled replicas."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
 def max_over_ranks(x: float, world) -> float:
     if world == 1:
         return x
@@ -197,12 +203,12 @@ def oracle_layer_steps(layers_host, n_threads, budget_s):
     return done, elapsed
 
 
-def host_layer(layer, rows=None):
-    """Host copies of one layer's inputs for the oracle; pooled keys of the
-    blocks before this step are state (pooled here, untimed).  ``rows``
-    restricts the step to a sample of query rows (rows are independent)."""
+def host_layer(x, rows=None):
+    """Host copies of one layer's inputs (``make_layer`` output) for the
+    oracle; pooled keys of the blocks before this step are state (pooled here
+    by the oracle, untimed).  ``rows`` restricts the step to a sample of query
+    rows (rows are independent)."""
     import oracle
-    x = layer.x
     idxk = x.idxk.cpu()
     b0 = (x.L - x.M) // 4
     q_idx, q, pos = x.q_idx.cpu(), x.q.cpu(), x.row_pos
@@ -221,13 +227,13 @@ def cpu_baseline(layers, budget_s=20.0, max_layers=3, max_rows=64):
     cores = len(os.sched_getaffinity(0))
     M = layers[0].x.M
     if M <= max_rows:
-        hosts = [host_layer(l) for l in layers[:max_layers]]
+        hosts = [host_layer(l.x) for l in layers[:max_layers]]
         n, secs = oracle_layer_steps(hosts, cores, budget_s)
         return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
                 "sample": f"{n} of the workload's layer-steps (pool new blocks, score all blocks, select, "
                           f"attention over all rows and heads) in fp64 C with OpenMP, {secs:.2f} s"}
     rows = sorted(set([0, M - 1] + [int(i * (M - 1) / (max_rows - 1)) for i in range(max_rows)]))
-    n, secs = oracle_layer_steps([host_layer(layers[0], rows)], cores, budget_s)
+    n, secs = oracle_layer_steps([host_layer(layers[0].x, rows)], cores, budget_s)
     full = secs * M / len(rows)
     return {"value": 1.0 / full, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{len(rows)} of the {M} rows of one layer-step in fp64 C with OpenMP ({secs:.2f} s), "
@@ -242,10 +248,11 @@ def run_reference(args, spec, world, rank):
         return
     import oracle
     oracle.build()
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
     n_layers = min(args.layers or spec["layers"], 2)
-    layers = build_layers(spec, n_layers, dev)
-    hosts = [host_layer(l) for l in layers]
+    # Inputs drawn on the host: nothing of the CUDA library runs on this arm.
+    hosts = [host_layer(make_layer(L=spec["L"], M=spec["M"], dtype=spec["dtype"], seed=0, layer=l,
+                                   n_planted=spec["n_planted"], head_dim=spec["head_dim"], device="cpu"))
+             for l in range(n_layers)]
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
     for i in range(args.warmup):
@@ -343,8 +350,7 @@ def main():
     barrier(world)
     ms = max_over_ranks(ms, world)
     ms_per_step = ms / args.steps
-    layer_steps = n_layers * args.steps * world
-    value = layer_steps / (ms / 1e3)
+    value = whole_job_rate(n_layers * args.steps, world, ms)
 
     # Each step kind on its own: a graph of its 12 back-to-back launches (one
     # per layer), timed live.  Scoring is the dominant kernel (the roofline
@@ -452,7 +458,7 @@ def main():
         e1.record(stream)
     e1.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = n_layers * e2e_steps * world / (e2e_ms / 1e3)
+    e2e_value = whole_job_rate(n_layers * e2e_steps, world, e2e_ms)
 
     ab = algorithmic_bytes(layers[0])
     peaks = {}
