@@ -126,6 +126,16 @@ const char* qsa_last_error(void);
 int32_t qsa_version(void);
 
 /*
+ * Device-side waits that gave up since the library was loaded, summed over
+ * its kernels.  The pipelined kernels wait on shared-memory barriers for
+ * their own copies and tensor-core operations; each wait gives up after about
+ * two seconds instead of hanging the GPU, and the kernel then runs to its end
+ * with an invalid result.  0 in normal operation; -1 if the counters could
+ * not be read.  Reads device memory: waits for the device to be idle.
+ */
+int32_t qsa_wait_timeouts(void);
+
+/*
  * Step 1 -- pooling (hipfire, section 02: every 4 consecutive index keys are
  * averaged into one pooled block key).
  *   pooled[b * pooled_stride + d] = ((k[4b][d] + k[4b+1][d]) + k[4b+2][d] + k[4b+3][d]) / 4

@@ -64,7 +64,7 @@ _lib = None
 EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks", "qsa_score_workspace_size",
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
-           "qsa_lse_merge")
+           "qsa_lse_merge", "qsa_wait_timeouts")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -83,6 +83,7 @@ def lib() -> ctypes.CDLL:
     L.qsa_status_string.restype = ctypes.c_char_p
     L.qsa_last_error.restype = ctypes.c_char_p
     L.qsa_version.restype = i32
+    L.qsa_wait_timeouts.restype = i32
     L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
     L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp, sz, vp]
     L.qsa_score_workspace_size.argtypes = [seqp, i32, i32]
@@ -103,6 +104,11 @@ def lib() -> ctypes.CDLL:
         getattr(L, name).restype = i32
     _lib = L
     return L
+
+
+def wait_timeouts() -> int:
+    """Device-side barrier waits that gave up (0 in normal operation)."""
+    return int(lib().qsa_wait_timeouts())
 
 
 def _check(fn: str, status: int):

@@ -123,6 +123,12 @@ QSA_API const char* qsa_last_error(void) { return g_last_error.c_str(); }
 
 QSA_API int32_t qsa_version(void) { return QSA_VERSION; }
 
+QSA_API int32_t qsa_wait_timeouts(void) {
+  const int a = score_wait_timeouts(), b = score_tc_wait_timeouts(), c = attn_tc_wait_timeouts();
+  if (a < 0 || b < 0 || c < 0) return -1;
+  return a + b + c;
+}
+
 // ------------------------------------------------------------------ step 1
 QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_t tok_stride, int64_t first_block,
                                int64_t n_blocks, float* pooled, int64_t pooled_stride, void* stream) {
@@ -442,7 +448,7 @@ qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_co
 template <int NSEQ>
 qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_attn_config* cfg, const void* q,
                       const int32_t* sel, const int32_t* cnt, int32_t sel_ld, const AttnPlan& sp, int64_t total_rows,
-                      void* out, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
+                      bool tensor_cores, void* out, float* lse, float* part_o, float* part_lse, cudaStream_t st) {
   AttnParams<NSEQ> p{};
   int rows = 0, nseg = 0;
   p.row_base = row_begin;
@@ -481,7 +487,7 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
   p.out = out;
   p.lse = lse;
   p.out_dtype = cfg->out_dtype;
-  cudaError_t e = launch_attn<NSEQ>(p, rows, cfg->kv_dtype, sp.stages, st);
+  cudaError_t e = tensor_cores ? launch_attn_tc<NSEQ>(p, rows, st) : launch_attn<NSEQ>(p, rows, cfg->kv_dtype, sp.stages, st);
   if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn");
   return QSA_OK;
 }
@@ -517,14 +523,18 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
   float* part_lse = nullptr;
   if (need > 0) attn_workspace_layout(sp, rows, cfg->n_q_heads, cfg->head_dim, workspace, &part_o, &part_lse);
   cudaStream_t st = as_stream(stream);
+  // Calls with many rows and a single split run on the tensor cores.
+  const bool tensor_cores = sp.n_splits == 1 &&
+                            attn_tc_eligible(cfg->kv_dtype, cfg->head_dim, cfg->n_q_heads / cfg->n_kv_heads,
+                                             max_list(seqs, n_seqs, sel_ld), rows);
   if (n_seqs == 1) {
-    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o, part_lse, st);
+    s = attn_chunk<1>(seqs, 1, 0, cfg, q, sel, cnt, sel_ld, sp, rows, tensor_cores, out, lse, part_o, part_lse, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, rows, out, lse, part_o,
-                                  part_lse, st);
+      s = attn_chunk<kLaunchSeqs>(seqs + c, n, row_begin, cfg, q, sel, cnt, sel_ld, sp, rows, tensor_cores, out, lse,
+                                  part_o, part_lse, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }

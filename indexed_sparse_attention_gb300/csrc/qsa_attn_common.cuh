@@ -1,0 +1,128 @@
+// Row bookkeeping and K/V gathers shared by the attention kernels: the
+// selected list of a query row (hipfire, "QSA sparse attention and the VMM KV
+// backend", section 02: the 4 tokens of every selected block, then the
+// incomplete tail block) and the lookup of a list entry in the sequence's KV
+// segment table (MTPLX pull request #610).
+#pragma once
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+namespace attn {
+
+// Per-row context: position, visible blocks, selected list length.  The
+// list's longest possible length (cnt = min(sel_ld, nb)) is known without
+// reading cnt, so the splits' ranges and id loads need not wait for it.
+struct RowCtx {
+  int64_t nb;
+  int64_t tail;       // tail tokens 4 nb .. p
+  int64_t n_list;     // 4 cnt + tail (set by set_count)
+  int64_t n_max;      // 4 min(sel_ld, nb) + tail
+  const int32_t* sel_row;
+  int32_t cnt;
+  int32_t seg_begin;
+  int32_t n_segs;
+};
+
+template <int NSEQ>
+__device__ __forceinline__ RowCtx make_row_ctx(const AttnParams<NSEQ>& p, int r) {
+  int si = 0;
+#pragma unroll
+  for (int i = 1; i < NSEQ; ++i)
+    if (i < p.n_seqs && r >= p.seq[i].row_begin) si = i;
+  const AttnSeq sq = p.seq[si];
+  const int64_t pos = row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin);
+  RowCtx c;
+  c.nb = visible_blocks(pos);
+  c.tail = pos + 1 - 4 * c.nb;
+  c.n_max = 4 * min((int64_t)p.sel_ld, c.nb) + c.tail;
+  c.n_list = c.n_max;
+  c.cnt = 0;
+  c.sel_row = p.sel + (int64_t)r * p.sel_ld;
+  c.seg_begin = sq.seg_begin;
+  c.n_segs = sq.n_segs;
+  return c;
+}
+
+// The row's count as loaded (clamped to 0 .. min(sel_ld, nb)).
+__device__ __forceinline__ void set_count(RowCtx& c, int32_t cnt, int32_t sel_ld) {
+  cnt = max(0, min(cnt, sel_ld));
+  if ((int64_t)cnt > c.nb) cnt = (int32_t)c.nb;
+  c.cnt = cnt;
+  c.n_list = 4 * (int64_t)cnt + c.tail;
+}
+
+// Entries [i0, i1) of the longest possible list that split `split` of n
+// takes: whole 32-token tiles, balanced over the row.
+__device__ __forceinline__ void split_range(const RowCtx& c, int split, int n, int64_t& i0, int64_t& i1) {
+  const int64_t T = (c.n_max + 31) / 32;
+  i0 = 32 * (T * split / n);
+  i1 = min(c.n_max, 32 * (T * (split + 1) / n));
+}
+
+// The block ids a split needs, staged in shared memory once: entries
+// [blk0, blk0 + n) of the row's selection (n <= kIdCache).
+constexpr int kIdCache = 512;
+
+struct IdCache {
+  const int32_t* ids;   // shared memory
+  int64_t blk0;
+  int n;
+};
+
+// Entry i of the row's selected list -> element offset of (KV head g, token)
+// in its segment, and the segment.  False when the entry names an invalid
+// block id or a token no segment covers.
+template <int NSEQ>
+__device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& c, const IdCache& ic, int64_t i,
+                                       int g, int& seg, int64_t& off) {
+  int64_t t;
+  if (i >= c.n_list) return false;
+  if (i < 4 * (int64_t)c.cnt) {
+    const int64_t k = (i >> 2) - ic.blk0;
+    const int32_t b = (k >= 0 && k < ic.n) ? ic.ids[k] : __ldg(c.sel_row + (i >> 2));
+    if (b < 0 || (int64_t)b >= c.nb) return false;
+    t = 4 * (int64_t)b + (i & 3);
+  } else {
+    t = 4 * c.nb + (i - 4 * (int64_t)c.cnt);
+  }
+  for (int s = 0; s < c.n_segs; ++s) {
+    const Segment& sg = p.seg[c.seg_begin + s];
+    if (t >= sg.first && t < sg.first + sg.n) {
+      seg = c.seg_begin + s;
+      off = (int64_t)g * sg.head_stride + (t - sg.first) * sg.tok_stride;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Stage the ids of list entries [i0, i1) into ids_s (all threads call).
+__device__ __forceinline__ IdCache stage_ids(const RowCtx& c, int64_t i0, int64_t i1, int32_t* ids_s) {
+  IdCache ic;
+  ic.ids = ids_s;
+  ic.blk0 = i0 >> 2;
+  const int64_t last = min(i1, c.n_max - c.tail);   // entries past the selected part are tail tokens
+  int64_t n = last > i0 ? ((last - 1) >> 2) - ic.blk0 + 1 : 0;
+  if (n > kIdCache) n = kIdCache;
+  ic.n = (int)n;
+  for (int k = threadIdx.x; k < ic.n; k += blockDim.x) ids_s[k] = __ldg(c.sel_row + ic.blk0 + k);
+  return ic;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+}  // namespace attn
+}  // namespace qsa

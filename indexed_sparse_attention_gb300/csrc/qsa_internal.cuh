@@ -150,6 +150,19 @@ cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtyp
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_parts, int64_t n_rows,
                          int head_dim, void* out, int out_dtype, float* lse_out, cudaStream_t st);
 
+// Attention on the tensor cores (see qsa_attn_tc.cu): bf16 K/V, head_dim 128
+// or 256, at most 16 query heads per KV head, lists of at most 3,840 entries,
+// one split, calls with at least kAttnTcMinRows query rows.
+constexpr int kAttnTcMinRows = 512;
+bool attn_tc_eligible(qsa_dtype kv_dtype, int head_dim, int group, int64_t max_list, int64_t rows);
+template <int NSEQ>
+cudaError_t launch_attn_tc(const AttnParams<NSEQ>& p, int n_rows, cudaStream_t st);
+
+// Device-side waits that gave up after their time limit, per translation unit.
+int score_wait_timeouts();
+int score_tc_wait_timeouts();
+int attn_tc_wait_timeouts();
+
 int device_sm_count();
 
 // Raise a kernel's dynamic shared-memory limit (once per device and size).

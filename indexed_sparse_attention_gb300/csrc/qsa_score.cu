@@ -783,4 +783,9 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
 template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);
 template cudaError_t launch_score<kLaunchSeqs>(const ScoreParams<kLaunchSeqs>&, qsa_dtype, int, cudaStream_t);
 
+int score_wait_timeouts() {
+  int v = 0;
+  return cudaMemcpyFromSymbol(&v, g_score_wait_timeouts, sizeof(int)) == cudaSuccess ? v : -1;
+}
+
 }  // namespace qsa

@@ -43,7 +43,7 @@
 
 #include <mutex>
 
-#include "qsa_internal.cuh"
+#include "qsa_tc.cuh"
 
 namespace qsa {
 
@@ -66,90 +66,16 @@ constexpr int kEpiThreads = 32 * kEpiWarps;
 
 __device__ int g_tc_wait_timeouts;
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(b)), "r"(count));
-}
-__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity) {
-  if (bar_try(b, parity)) return true;
-  const uint64_t t0 = now_ns();
-  while (!bar_try(b, parity))
-    if (now_ns() - t0 > 2000000000ull) {
-      atomicAdd(&g_tc_wait_timeouts, 1);
-      return false;
-    }
-  return true;
-}
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
-          "r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
+using namespace tc;
+
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity) {
+  return bar_wait(b, parity, &g_tc_wait_timeouts);
 }
 
-// Shared-memory matrix descriptor of a K-major operand tile stored as the
-// 128-byte swizzle writes it: rows of 128 bytes (64 bf16 of K), 8-row groups
-// 1,024 bytes apart.  Fields: start address >> 4 (bits 0-13), leading byte
-// offset >> 4 (16-29; unused for this layout), stride byte offset >> 4
-// (32-45), the fixed value 1 at bit 46, base offset 0 (49-51), swizzle mode
-// 2 = 128-byte (61-63).
-__device__ __forceinline__ uint64_t umma_desc(const void* p) {
-  const uint64_t a = (smem_addr(p) & 0x3FFFFu) >> 4;
-  return a | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
+// Both operands K-major with the 128-byte swizzle: 8-row groups 1,024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc(const void* p) { return desc_sw128(p, 16, 1024); }
 
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16
-// A and B (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
-                            ((uint32_t)(kTcM >> 4) << 24);
-
-__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
+constexpr uint32_t kIdesc = idesc_bf16(kTcM, kTcN, false, false);
 
 // ------------------------------------------------------------------ key planes
 // planes[b][p * 128 + c], p = 0, 1, 2: bf16 hi, mid, lo of pooled[b][c].
@@ -227,17 +153,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       bar_init(&acc_full[i], 1);
       bar_init(&acc_empty[i], kEpiThreads);
     }
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    bar_init_fence();
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&tmem_slot)),
-                 "r"(2 * kTcN)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    tmem_alloc(&tmem_slot, 2 * kTcN);
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
-  tc_fence_after();
+  fence_after();
   const uint32_t tmem = tmem_slot;
   grid_dependency_sync();
 
@@ -249,7 +172,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
         const TcTile x = tc_tile(P, n_tiles_m, t);
         if (!x.live) continue;
         if (x.n0 != n_prev) {   // a new key-plane tile, once the MMAs are done with the last
-          if (b_loads >= 1 && !(ok = bar_wait(&b_empty, (uint32_t)((b_loads - 1) & 1)))) break;
+          if (b_loads >= 1 && !(ok = wait_bar(&b_empty, (uint32_t)((b_loads - 1) & 1)))) break;
           bar_expect_tx(&b_full, kBBytes);
           for (int kc = 0; kc < kKSlices; ++kc) tma_2d(smB + kc * kSliceBytes, &P.tmap_k, kc * kTcK, x.n0, &b_full);
           ++b_loads;
@@ -257,7 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
         }
         for (int h = 0; h < 2; ++h, ++boxes) {
           const int q = boxes % kABoxes;
-          if (boxes >= kABoxes && !(ok = bar_wait(&a_empty[q], (uint32_t)((boxes / kABoxes - 1) & 1)))) break;
+          if (boxes >= kABoxes && !(ok = wait_bar(&a_empty[q], (uint32_t)((boxes / kABoxes - 1) & 1)))) break;
           bar_expect_tx(&a_full[q], kABoxBytes);
           tma_2d(smA + q * kABoxBytes, &P.tmap_q, h * kTcK, x.m0, &a_full[q]);
         }
@@ -271,17 +194,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
         const TcTile x = tc_tile(P, n_tiles_m, t);
         if (!x.live) continue;
         if (x.n0 != n_prev) {
-          if (b_loads > 0) umma_commit(&b_empty);   // the previous key tile is done once these MMAs finish
-          if (!(ok = bar_wait(&b_full, (uint32_t)(b_loads & 1)))) break;
+          if (b_loads > 0) commit(&b_empty);   // the previous key tile is done once these MMAs finish
+          if (!(ok = wait_bar(&b_full, (uint32_t)(b_loads & 1)))) break;
           ++b_loads;
           n_prev = x.n0;
         }
         const int acc = tiles & 1;
-        if (tiles >= 2 && !(ok = bar_wait(&acc_empty[acc], (uint32_t)((tiles / 2 - 1) & 1)))) break;
+        if (tiles >= 2 && !(ok = wait_bar(&acc_empty[acc], (uint32_t)((tiles / 2 - 1) & 1)))) break;
         const int q0 = boxes % kABoxes, q1 = (boxes + 1) % kABoxes;
-        if (!(ok = bar_wait(&a_full[q0], (uint32_t)((boxes / kABoxes) & 1)))) break;
-        if (!(ok = bar_wait(&a_full[q1], (uint32_t)(((boxes + 1) / kABoxes) & 1)))) break;
-        tc_fence_after();
+        if (!(ok = wait_bar(&a_full[q0], (uint32_t)((boxes / kABoxes) & 1)))) break;
+        if (!(ok = wait_bar(&a_full[q1], (uint32_t)(((boxes + 1) / kABoxes) & 1)))) break;
+        fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * kTcN);
         for (int kc = 0; kc < kKSlices; ++kc) {
           // Slice kc is plane kc / 2, channels 64 (kc % 2) ..: the query half kc % 2.
@@ -289,11 +212,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
           const uint8_t* b = smB + kc * kSliceBytes;
 #pragma unroll
           for (int j = 0; j < kTcK / 16; ++j)
-            umma_f16(d, umma_desc(a + 32 * j), umma_desc(b + 32 * j), (kc | j) != 0 ? 1u : 0u);
+            mma_bf16(d, umma_desc(a + 32 * j), umma_desc(b + 32 * j), kIdesc, (kc | j) != 0 ? 1u : 0u);
         }
-        umma_commit(&a_empty[q0]);
-        umma_commit(&a_empty[q1]);
-        umma_commit(&acc_full[acc]);
+        commit(&a_empty[q0]);
+        commit(&a_empty[q1]);
+        commit(&acc_full[acc]);
         boxes += 2;
         ++tiles;
       }
@@ -310,8 +233,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       const TcTile x = tc_tile(P, n_tiles_m, t);
       if (!x.live) continue;
       const int acc = tiles & 1;
-      if (!bar_wait(&acc_full[acc], (uint32_t)((tiles / 2) & 1))) break;
-      tc_fence_after();
+      if (!wait_bar(&acc_full[acc], (uint32_t)((tiles / 2) & 1))) break;
+      fence_after();
       const int r = x.m0 / 4 + m / 4;   // row within the sequence
       const bool row_ok = r < P.n_rows;
       const int64_t nb = row_ok ? visible_blocks(row_position(P.n_tokens, P.n_rows, r)) : 0;
@@ -321,8 +244,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       for (int c = 0; c < kChunks; ++c)
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kTcN + kGroupCols * cgrp + 32 * c), v[c]);
       // The accumulator is in registers: the MMAs of a later tile may reuse it.
-      tc_fence_before();
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(&acc_empty[acc])) : "memory");
+      fence_before();
+      bar_arrive(&acc_empty[acc]);
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
 #pragma unroll
@@ -360,11 +283,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       ++tiles;
     }
   }
-  tc_fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(2 * kTcN) : "memory");
+    fence_after();
+    tmem_dealloc(tmem, 2 * kTcN);
   }
 }
 
@@ -428,6 +351,11 @@ cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows
   const int sms = device_sm_count();
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
   return launch_kernel(score_tc_kernel, dim3(grid), dim3(kTcThreads), kTcSmem, st, 0u, P);
+}
+
+int score_tc_wait_timeouts() {
+  int v = 0;
+  return cudaMemcpyFromSymbol(&v, g_tc_wait_timeouts, sizeof(int)) == cudaSuccess ? v : -1;
 }
 
 }  // namespace qsa

@@ -283,6 +283,52 @@ def test_attention_skips_invalid_ids():
     assert_attn_close(out, lse, ref_out, ref_lse, True)
 
 
+# ------------------------------------------------------------------ step 4 on the tensor cores
+# Calls with at least 512 query rows and a single split (chunked prefill) run
+# on tcgen05; two forced splits take the mma.sync kernel and the merge on the
+# same inputs.  Rows at small positions give short, ragged lists (2 to 10
+# tiles of 128 tokens); the 6,000-token case gives full 2,051-entry lists.
+@pytest.mark.parametrize("L,M,D", [(1200, 1000, 256), (6000, 600, 256), (1200, 700, 128)])
+def test_attention_tensor_cores_matches_oracle(L, M, D):
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + M, head_dim=D)
+    sel, cnt, _ = _oracle_selection(x)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    out, lse = _attn_gpu(x, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+    out2, lse2 = _attn_gpu(x, sel, cnt, n_splits=2)
+    assert_attn_close(out2, lse2, ref_out, ref_lse, True)
+    assert qsa.wait_timeouts() == 0
+
+
+def test_attention_tensor_cores_edge_cases():
+    # Out-of-range ids (skipped), a row with an empty list (count 0, no tail:
+    # zeros and lse = -inf), KV segments with a hole, bf16 output.
+    x = make_layer(L=2600, M=560, dtype=torch.bfloat16, seed=21)
+    sel, cnt, _ = _oracle_selection(x)
+    bad, bad_cnt = sel.copy(), cnt.copy()
+    bad[1, 3] = 10_000_000
+    bad[2, 5] = -5
+    assert (x.row_pos[3] + 1) % 4 == 0
+    bad_cnt[3] = 0
+    ref_sel, ref_cnt = sel.copy(), cnt.copy()
+    for r, j in ((1, 3), (2, 5)):
+        keep = np.delete(sel[r, :cnt[r]], j)
+        ref_sel[r] = -1
+        ref_sel[r, :len(keep)] = keep
+        ref_cnt[r] = len(keep)
+    ref_cnt[3] = 0
+    cuts = segment_cuts(x.L, 5, seed=3)
+    kept = cuts[:2] + cuts[3:]
+    vis = np.zeros(x.L, dtype=bool)
+    for f, n in kept:
+        vis[f:f + n] = True
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, ref_sel, ref_cnt, visible=vis)
+    out, lse = _attn_gpu(x, bad, bad_cnt, segments=_segment_views(kept), out_dtype=torch.bfloat16)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+    assert (out[3] == 0).all() and np.isneginf(lse[3]).all()
+    assert qsa.wait_timeouts() == 0
+
+
 # ------------------------------------------------------------------ segments and step 5
 def _segment_views(cuts):
     def make(k, v):
