@@ -63,7 +63,10 @@ def build_layers(spec, n_layers, device, seed=0):
 
 def launches_per_layer(layer) -> int:
     st = layer.step
+    x = layer.x
     n = len(st.pool_jobs) + 1 + 1 + 1            # pool, score, select, attention
+    if x.M > 4 and x.q_idx.dtype == torch.bfloat16:
+        n += 1                                   # scoring on the tensor cores: + the key-plane split
     ws_needed = st.ws.numel() > 16
     return n + (1 if ws_needed else 0)           # + split merge (several splits per row)
 
@@ -408,6 +411,7 @@ def main():
         return out[0] - out[1]
 
     score_us = time_isolated(lambda st: st.score())
+    attn_us = time_isolated(lambda st: st.attend()) if spec["M"] > 4 else None
 
     # End to end through the public API with host buffers: per step, the new
     # rows' q, index queries, K/V and index keys of every layer go host ->
@@ -469,42 +473,57 @@ def main():
         peak_gbs, peak_src = 6800.0, "fallback"
     score_gbs = ab["score"] / (score_us * 1e-6) / 1e9
     step_gbs = ab["total"] * n_layers / (ms_per_step * 1e-3) / 1e9
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
-    if os.path.exists(tf):
+
+    def traffic_of(kernel):
+        """DRAM bytes per launch from the committed ncu counters, if they were
+        taken on the kernel revision built now."""
         try:
-            t = json.load(open(tf))
-            if t.get("kernel_rev") == SCORE_KERNEL_REV:
-                for e in t.get("entries", []):
-                    if e.get("workload") == args.workload:
-                        traffic = e["dram_bytes_per_launch"]
+            t = json.load(open(os.path.join(ROOT, "profiles", "kernel_traffic.json")))
+            for e in t.get("entries", []):
+                if (e.get("kernel") == kernel and e.get("rev") == KERNEL_REVS[kernel]
+                        and e.get("workload") == args.workload):
+                    return e["dram_bytes_per_launch"]
         except (OSError, ValueError, KeyError):
-            traffic = None
+            pass
+        return None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers)
 
     roofline = {"kernel": "score_blocks", "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
-                "unit": "GB/s", "frac": score_gbs / peak_gbs, "traffic": traffic,
+                "unit": "GB/s", "frac": score_gbs / peak_gbs, "traffic": traffic_of("score_tma_kernel"),
                 "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
                 "timing": "graph of 12 launches each followed by a one-element non-PDL kernel, minus a graph "
                           "of those kernels alone (no overlap with neighbours)",
                 "algorithmic_bytes_per_launch": ab["score"]}
+    roofline_scoring = None
     if M > 4:
-        # Many rows: scoring is a dense contraction on the tensor cores.  The
-        # algorithmic flops are 2 x rows x 4 heads x blocks x 128; the kernel
-        # executes three times as many (three bf16 planes of the fp32 keys).
+        # Many rows (prefill).  Scoring is a dense contraction on the tensor
+        # cores: algorithmic flops 2 x rows x 4 heads x blocks x 128; the
+        # kernel executes three times as many (three bf16 planes of the fp32
+        # keys).
         flops = 2.0 * M * 4 * (L // 4) * 128
         try:
             peak_tf, tf_src = float(peaks["bf16_tflops"]), "measured (bf16_tflops, burst)"
         except (KeyError, ValueError, TypeError):
             peak_tf, tf_src = 1900.0, "fallback"
         achieved = flops / (score_us * 1e-6) / 1e12
-        roofline.update({"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                         "frac": achieved / peak_tf, "traffic": None, "peak_source": tf_src,
-                         "algorithmic_flops_per_launch": flops, "executed_flops_per_launch": 3 * flops})
-        roofline.pop("algorithmic_bytes_per_launch")
+        roofline_scoring = dict(roofline)
+        roofline_scoring.update({"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                                 "frac": achieved / peak_tf, "traffic": None, "peak_source": tf_src,
+                                 "algorithmic_flops_per_launch": flops, "executed_flops_per_launch": 3 * flops})
+        roofline_scoring.pop("algorithmic_bytes_per_launch")
+        # The dominant kernel is the gathered attention (tcgen05): every row
+        # moves its selected K and V rows of both KV groups into the SMs.  Most
+        # of those bytes come from L2 (rows overlap across the 2,048 queries),
+        # so the DRAM traffic is well below the algorithmic bytes.
+        attn_gbs = ab["attn"] / (attn_us * 1e-6) / 1e9
+        roofline = {"kernel": "sparse_attn (tcgen05 path)", "bound": "hbm", "achieved": attn_gbs,
+                    "peak": peak_gbs, "unit": "GB/s", "frac": attn_gbs / peak_gbs,
+                    "traffic": traffic_of("attn_tc_kernel"), "peak_source": f"{peak_src} (hbm_gbs, burst)",
+                    "us_per_launch": attn_us, "timing": roofline["timing"],
+                    "algorithmic_bytes_per_launch": ab["attn"]}
 
     launches = sum(launches_per_layer(l) for l in layers) * args.steps
     line = {
@@ -522,6 +541,7 @@ def main():
         "step_hbm_gbs": step_gbs,
         "step_frac_of_peak": step_gbs / peak_gbs,
         "roofline": roofline,
+        **({"roofline_scoring": roofline_scoring} if roofline_scoring else {}),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "one CUDA graph per step: pinned host->device input copies, the layer chain through "
@@ -538,8 +558,9 @@ def main():
         dist.destroy_process_group()
 
 
-# Revision tag of the scoring kernel whose DRAM counters profiles/ holds.
-SCORE_KERNEL_REV = "score_tma_ring8_v4"
+# Revision tags of the kernels as built now; DRAM counters in
+# profiles/kernel_traffic.json count only for the revision they were taken on.
+KERNEL_REVS = {"score_tma_kernel": "score_tma_ring8_v4", "attn_tc_kernel": "attn_tc_ring3_v1"}
 
 if __name__ == "__main__":
     main()
