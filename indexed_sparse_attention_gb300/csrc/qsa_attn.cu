@@ -487,6 +487,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const AttnParams<NSEQ> p
 // warps then combine in shared memory by the same rule.  Every load of a warp
 // is independent of its other loads.
 constexpr int kMergeWarps = 8;
+constexpr int kMergeBatch = 8;   // partials a warp loads per pass
 
 template <int CPL>   // channels per lane (4 or 8)
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_cta_kernel(const float* __restrict__ o_parts,
@@ -500,18 +501,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_cta_kernel(const float
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
   const int d0 = lane * CPL;
-  // This warp's partials w, w + 8, ..., four per pass: their lse values and
-  // channels are loaded together (one round trip for up to 32 partials), then
+  // This warp's partials w, w + 8, ..., eight per pass: their lse values and
+  // channels are loaded together (one round trip for up to 64 partials), then
   // added with an online rescale to the warp's running maximum m.
   float m = -INFINITY, wsum = 0.f;
   float acc[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  for (int s0 = warp; s0 < n_parts; s0 += kMergeWarps * 4) {
-    float ls[4];
-    float4 v[4][CPL / 4];
+  for (int s0 = warp; s0 < n_parts; s0 += kMergeWarps * kMergeBatch) {
+    float ls[kMergeBatch];
+    float4 v[kMergeBatch][CPL / 4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kMergeBatch; ++k) {
       const int s = s0 + k * kMergeWarps;
       ls[k] = s < n_parts ? __ldg(lse_parts + (int64_t)s * n_rows + row) : -INFINITY;
 #pragma unroll
@@ -520,14 +521,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_cta_kernel(const float
                       ? __ldg(reinterpret_cast<const float4*>(o_parts + ((int64_t)s * n_rows + row) * head_dim + d0) + c)
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float mn = fmaxf(m, fmaxf(fmaxf(ls[0], ls[1]), fmaxf(ls[2], ls[3])));
+    float mn = m;
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) mn = fmaxf(mn, ls[k]);
     if (mn == -INFINITY) continue;
     const float rescale = m == -INFINITY ? 0.f : exp2f((m - mn) * kLog2e);
     wsum *= rescale;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) acc[c] *= rescale;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kMergeBatch; ++k) {
       if (ls[k] == -INFINITY) continue;   // drops the values of a partial without keys
       const float w = exp2f((ls[k] - mn) * kLog2e);
       wsum += w;
@@ -647,13 +650,15 @@ AttnPlan attn_plan(qsa_dtype kv_dtype, int head_dim, int64_t pairs, int64_t n_li
   (void)kv_dtype;
   (void)head_dim;
   const int64_t sms = device_sm_count();
-  const int64_t max_splits = std::min<int64_t>(ceil_div(n_list, kTT), kMaxSplits);
+  // n_list counts up to 3 tail entries, which ride with the last split.
+  const int64_t blocks_part = std::max<int64_t>(n_list - 3, 1);
+  const int64_t max_splits = std::min<int64_t>(ceil_div(blocks_part, kTT), kMaxSplits);
   int64_t n = user_splits > 0 ? user_splits : ceil_div(2 * sms, pairs);
   n = std::max<int64_t>(1, std::min(n, max_splits));
-  int64_t per = ceil_div(n_list, n);
+  int64_t per = ceil_div(blocks_part, n);
   if (n > 1) per = ceil_div(per, kTT) * kTT;
-  n = ceil_div(n_list, per);
-  const int stages = per <= 2 * kTT ? 2 : 3;
+  n = ceil_div(blocks_part, per);
+  const int stages = per + 3 <= 2 * kTT ? 2 : 3;
   return AttnPlan{(int32_t)n, (int32_t)per, stages};
 }
 

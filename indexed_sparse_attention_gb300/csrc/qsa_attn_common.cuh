@@ -53,11 +53,13 @@ __device__ __forceinline__ void set_count(RowCtx& c, int32_t cnt, int32_t sel_ld
 }
 
 // Entries [i0, i1) of the longest possible list that split `split` of n
-// takes: whole 32-token tiles, balanced over the row.
+// takes: whole 32-token tiles of the selected blocks' entries, balanced over
+// the row; the last split also takes the tail tokens (at most 3), so they
+// cost no split of their own.
 __device__ __forceinline__ void split_range(const RowCtx& c, int split, int n, int64_t& i0, int64_t& i1) {
-  const int64_t T = (c.n_max + 31) / 32;
+  const int64_t T = max((c.n_max - c.tail + 31) / 32, (int64_t)1);
   i0 = 32 * (T * split / n);
-  i1 = min(c.n_max, 32 * (T * (split + 1) / n));
+  i1 = split == n - 1 ? c.n_max : min(c.n_max, 32 * (T * (split + 1) / n));
 }
 
 // The block ids a split needs, staged in shared memory once: entries
