@@ -240,6 +240,36 @@ qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void
                                  void* stream);
 
 /*
+ * Steps 2 and 3 over the key axis in chunks, with memory flat in the context
+ * length (the SGLang launcher notes, section 2.3: score the rows against key
+ * blocks of B_k, keep each part's top-k with ids, take the top-k of the
+ * kept candidates; the top-k of a union equals the top-k of the per-part
+ * top-k lists, so the result is exact).  Per sequence, blocks
+ * [c * block_keys, (c + 1) * block_keys) are scored on the tensor cores into
+ * a chunk buffer and merged into each row's running top-k (keys and ids in
+ * ascending id order, so the lowest id still wins among equal scores).
+ * Output: sel and cnt exactly as qsa_select_topk writes them for the
+ * scores qsa_score_blocks would write; no [rows, blocks] score buffer.
+ *   q_idx_dtype    QSA_BF16 (the tensor-core scoring); else QSA_ERR_UNSUPPORTED
+ *   top_k          1..QSA_MAX_TOP_K
+ *   block_keys     blocks per chunk: a multiple of 128, at least 128, and
+ *                  top_k + block_keys <= 8192
+ *   workspace      device scratch of >= qsa_score_select_blocked_workspace_size
+ *                  bytes (chunk scores, key planes and two running lists,
+ *                  sized by the largest sequence's rows and block_keys, not
+ *                  by the context); contents need no initialisation; calls
+ *                  that share it must not run concurrently
+ * Other arguments as for qsa_score_blocks and qsa_select_topk.  One scoring
+ * and one merge launch per chunk of each sequence.
+ */
+size_t qsa_score_select_blocked_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k,
+                                               int32_t block_keys);
+
+qsa_status qsa_score_select_topk_blocked(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
+                                         qsa_dtype q_idx_dtype, int32_t top_k, int32_t block_keys, int32_t* sel,
+                                         int32_t* cnt, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Scratch bytes qsa_sparse_attn needs for this call: the normalised partial
  * outputs and lse values of every split when a (row, KV group) is cut into
  * several splits (0 when each has one).  sel_ld is the row stride of sel (the

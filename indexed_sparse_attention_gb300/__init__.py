@@ -64,7 +64,8 @@ _lib = None
 EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index_keys", "qsa_score_blocks", "qsa_score_workspace_size",
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
-           "qsa_lse_merge", "qsa_wait_timeouts")
+           "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
+           "qsa_score_select_topk_blocked")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -99,8 +100,11 @@ def lib() -> ctypes.CDLL:
     L.qsa_sparse_attn.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp, sz, vp]
     L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
+    L.qsa_score_select_blocked_workspace_size.argtypes = [seqp, i32, i32, i32]
+    L.qsa_score_select_blocked_workspace_size.restype = sz
+    L.qsa_score_select_topk_blocked.argtypes = [seqp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_score_select_topk",
-                 "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge"):
+                 "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge", "qsa_score_select_topk_blocked"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -246,6 +250,24 @@ def score_select_topk(seqs, q_idx: torch.Tensor, scores: torch.Tensor, sel: torc
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0), int(top_k),
         sel.data_ptr(), cnt.data_ptr(), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         _stream(stream)))
+
+
+def score_select_blocked_workspace_size(seqs, top_k: int = TOP_K, block_keys: int = 4096, seq_array=None) -> int:
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    return int(lib().qsa_score_select_blocked_workspace_size(arr, len(arr), int(top_k), int(block_keys)))
+
+
+def score_select_topk_blocked(seqs, q_idx: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, top_k: int = TOP_K,
+                              block_keys: int = 4096, workspace: torch.Tensor | None = None, stream=None,
+                              seq_array=None):
+    """Steps 2 and 3 over key-axis chunks of block_keys blocks (no score buffer)."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    need = score_select_blocked_workspace_size(None, top_k, block_keys, seq_array=arr)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_idx.device)
+    _check("qsa_score_select_topk_blocked", lib().qsa_score_select_topk_blocked(
+        arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), int(top_k), int(block_keys), sel.data_ptr(),
+        cnt.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
 
 
 def attn_config(q: torch.Tensor, n_kv_heads: int, out_dtype=None, scale: float = 0.0, n_splits: int = 0):

@@ -233,8 +233,8 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
     for (int i = 0; i < n_seqs && s == QSA_OK; ++i) {
       const qsa_seq& q = seqs[i];
       if (wide_seq(q, q_idx_dtype)) {
-        cudaError_t e = launch_score_tc(q_idx, row_begin, q.n_rows, q.n_tokens, q.pooled, q.pooled_stride, scores,
-                                        ld, group_max, group_ld, workspace, st);
+        cudaError_t e = launch_score_tc(q_idx, row_begin, q.n_rows, q.n_tokens, q.pooled, q.pooled_stride, 0,
+                                        q.n_tokens / 4, scores, ld, group_max, group_ld, workspace, st);
         if (e == cudaErrorNotSupported)
           s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
         else if (e != cudaSuccess)
@@ -380,6 +380,118 @@ QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, co
       QSA_OK)
     return s;
   return qsa_select_topk(seqs, n_seqs, scores, ld, gmax, gld, top_k, sel, cnt, nullptr, 0, stream);
+}
+
+// ------------------------------------------------------------------ steps 2 + 3 over key-axis chunks
+namespace {
+
+struct BlockedLayout {
+  size_t chunk, planes, keys, ids, cnts, total;   // byte offsets of the parts
+  int64_t ld_chunk;
+};
+
+BlockedLayout blocked_layout(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k, int32_t block_keys) {
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  int64_t rows = 0;
+  for (int i = 0; i < n_seqs; ++i) rows = std::max<int64_t>(rows, seqs[i].n_rows);
+  BlockedLayout L;
+  L.ld_chunk = block_keys;
+  const size_t chunk_b = up(sizeof(float) * (size_t)rows * (size_t)block_keys);
+  const size_t planes_b = up(score_tc_workspace_bytes(block_keys));
+  const size_t list_b = up(sizeof(uint32_t) * (size_t)rows * (size_t)top_k);
+  const size_t cnt_b = up(sizeof(int32_t) * (size_t)std::max<int64_t>(rows, 1));
+  L.chunk = 0;
+  L.planes = chunk_b;
+  L.keys = L.planes + planes_b;      // two running lists: keys[2], ids[2], counts[2]
+  L.ids = L.keys + 2 * list_b;
+  L.cnts = L.ids + 2 * list_b;
+  L.total = L.cnts + 2 * cnt_b;
+  return L;
+}
+
+}  // namespace
+
+QSA_API size_t qsa_score_select_blocked_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k,
+                                                       int32_t block_keys) {
+  if (!seqs || n_seqs < 1 || top_k < 1 || block_keys < 1) return 0;
+  return blocked_layout(seqs, n_seqs, top_k, block_keys).total;
+}
+
+QSA_API qsa_status qsa_score_select_topk_blocked(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
+                                                 qsa_dtype q_idx_dtype, int32_t top_k, int32_t block_keys,
+                                                 int32_t* sel, int32_t* cnt, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+  const char* fn = "qsa_score_select_topk_blocked";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
+  if (s != QSA_OK) return s;
+  if (q_idx_dtype != QSA_BF16)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: q_idx_dtype must be bf16 (tensor-core scoring)", fn);
+  if (top_k < 1 || top_k > QSA_MAX_TOP_K)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: top_k=%d outside 1..%d", fn, top_k, QSA_MAX_TOP_K);
+  if (block_keys < 128 || block_keys % 128 != 0 || top_k + block_keys > merge_select_max_union())
+    return fail(QSA_ERR_UNSUPPORTED, "%s: block_keys=%d (a multiple of 128, top_k + block_keys <= %d)", fn,
+                block_keys, merge_select_max_union());
+  if (!q_idx || !sel || !cnt) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q_idx)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx not 16-byte aligned", fn);
+  for (int i = 0; i < n_seqs; ++i) {
+    const qsa_seq& q = seqs[i];
+    if (max_visible_blocks(q) > QSA_MAX_BLOCKS)
+      return fail(QSA_ERR_UNSUPPORTED, "%s: sequence %d has more than %d blocks", fn, i, QSA_MAX_BLOCKS);
+    if (max_visible_blocks(q) > 0) {
+      if (!q.pooled) return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has no pooled keys", fn, i);
+      if (q.pooled_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: pooled_stride < 128", fn);
+      if (!aligned16(q.pooled) || q.pooled_stride % 4 != 0)
+        return fail(QSA_ERR_MISALIGNED, "%s: pooled keys of sequence %d not 16-byte aligned", fn, i);
+    }
+  }
+  const BlockedLayout L = blocked_layout(seqs, n_seqs, top_k, block_keys);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+                workspace ? workspace_bytes : (size_t)0);
+  if (!aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
+  char* ws = static_cast<char*>(workspace);
+  const size_t list_b = (L.ids - L.keys) / 2, cnt_b = (L.total - L.cnts) / 2;
+  float* chunk = reinterpret_cast<float*>(ws + L.chunk);
+  void* planes = ws + L.planes;
+  cudaStream_t st = as_stream(stream);
+  int32_t row_begin = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const qsa_seq& q = seqs[i];
+    const int64_t nbmax = max_visible_blocks(q);   // n_tokens / 4 (the last row sees the most)
+    const int64_t n_chunks = std::max<int64_t>(1, (nbmax + block_keys - 1) / block_keys);
+    const void* qi = static_cast<const char*>(q_idx) + (size_t)row_begin * QSA_INDEX_HEADS * QSA_INDEX_DIM * 2;
+    for (int64_t c = 0; c < n_chunks; ++c) {
+      const int64_t lo = c * block_keys;
+      const int64_t n = std::max<int64_t>(0, std::min<int64_t>(block_keys, nbmax - lo));
+      cudaError_t e = launch_score_tc(qi, 0, q.n_rows, q.n_tokens, q.pooled, q.pooled_stride, lo, n, chunk,
+                                      L.ld_chunk, nullptr, 0, planes, st);
+      if (e != cudaSuccess) return cuda_fail(e, fn);
+      const int in = (int)(c & 1), out = 1 - in;
+      MergeSelectParams m{};
+      m.n_tokens = q.n_tokens;
+      m.n_rows = q.n_rows;
+      m.row_begin = row_begin;
+      m.chunk = chunk;
+      m.ld_chunk = L.ld_chunk;
+      m.block_lo = lo;
+      m.n_blocks = (int32_t)n;
+      m.top_k = top_k;
+      m.run_key_in = reinterpret_cast<const uint32_t*>(ws + L.keys + in * list_b);
+      m.run_id_in = reinterpret_cast<const int32_t*>(ws + L.ids + in * list_b);
+      m.run_cnt_in = reinterpret_cast<const int32_t*>(ws + L.cnts + in * cnt_b);
+      m.run_key_out = reinterpret_cast<uint32_t*>(ws + L.keys + out * list_b);
+      m.run_id_out = reinterpret_cast<int32_t*>(ws + L.ids + out * list_b);
+      m.run_cnt_out = reinterpret_cast<int32_t*>(ws + L.cnts + out * cnt_b);
+      m.first = c == 0;
+      m.last = c == n_chunks - 1;
+      m.sel = sel;
+      m.cnt = cnt;
+      if ((e = launch_merge_select(m, st)) != cudaSuccess) return cuda_fail(e, fn);
+    }
+    row_begin += q.n_rows;
+  }
+  return ok();
 }
 
 // ------------------------------------------------------------------ step 4

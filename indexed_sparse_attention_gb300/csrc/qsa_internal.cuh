@@ -123,13 +123,40 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_
 
 // Wide scoring on the tensor cores (one sequence; see qsa_score_tc.cu).
 size_t score_tc_workspace_bytes(int64_t n_blocks);
+// Scores blocks [block_lo, block_lo + n_blocks) into columns 0 .. n_blocks - 1.
 cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows, int64_t n_tokens,
-                            const float* pooled, int64_t pooled_stride, float* scores, int64_t ld, float* gmax,
-                            int64_t gld, void* workspace, cudaStream_t st);
+                            const float* pooled, int64_t pooled_stride, int64_t block_lo, int64_t n_blocks,
+                            float* scores, int64_t ld, float* gmax, int64_t gld, void* workspace, cudaStream_t st);
 
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st);
 size_t select_smem_bytes(int64_t max_nb);
+
+// Selection over key-axis chunks: merge one chunk's scores into each row's
+// running top-k (see qsa_select.cu).
+struct MergeSelectParams {
+  int64_t n_tokens;             // the sequence
+  int32_t n_rows;
+  int32_t row_begin;            // global index of its first row (sel, cnt)
+  const float* chunk;           // [n_rows, ld_chunk] scores of blocks block_lo .. block_lo + n_blocks - 1
+  int64_t ld_chunk;
+  int64_t block_lo;
+  int32_t n_blocks;
+  int32_t top_k;
+  const uint32_t* run_key_in;   // [n_rows, top_k] order keys of the running top-k (ascending ids)
+  const int32_t* run_id_in;     // [n_rows, top_k]
+  const int32_t* run_cnt_in;    // [n_rows]
+  uint32_t* run_key_out;
+  int32_t* run_id_out;
+  int32_t* run_cnt_out;
+  int32_t first;                // no running list yet
+  int32_t last;                 // write sel and cnt instead of the running list
+  int32_t* sel;
+  int32_t* cnt;
+};
+cudaError_t launch_merge_select(const MergeSelectParams& p, cudaStream_t st);
+// Largest top_k + chunk width the merge holds in shared memory.
+int merge_select_max_union();
 
 struct AttnPlan {
   int32_t n_splits;

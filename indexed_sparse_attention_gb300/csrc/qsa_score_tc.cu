@@ -111,6 +111,8 @@ struct ScoreTcParams {
   float* gmax;
   int64_t gld;
   int64_t n_tokens;
+  int64_t block_lo;         // absolute id of the first block scored (column 0 of scores)
+  int64_t n_blocks;         // blocks scored: block_lo .. block_lo + n_blocks - 1
   int32_t n_rows;
   int32_t row_begin;
 };
@@ -125,7 +127,7 @@ __device__ __forceinline__ TcTile tc_tile(const ScoreTcParams& P, int n_tiles_m,
   x.n0 = (t / n_tiles_m) * kTcN;
   x.m0 = (t % n_tiles_m) * kTcM;
   const int r_last = min(P.n_rows - 1, x.m0 / 4 + kTcM / 4 - 1);
-  x.live = x.n0 < visible_blocks(row_position(P.n_tokens, P.n_rows, r_last));
+  x.live = P.block_lo + x.n0 < visible_blocks(row_position(P.n_tokens, P.n_rows, r_last));
   return x;
 }
 
@@ -138,7 +140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
   uint8_t* smA = base + kBBytes;    // kABoxes boxes [128 row-heads][64 channels]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_tiles_m = (int)(((int64_t)P.n_rows * 4 + kTcM - 1) / kTcM);
-  const int n_tiles = n_tiles_m * (int)((P.n_tokens / 4 + kTcN - 1) / kTcN);
+  const int n_tiles = n_tiles_m * (int)((P.n_blocks + kTcN - 1) / kTcN);
   const int t0 = (int)((int64_t)n_tiles * blockIdx.x / gridDim.x);
   const int t1 = (int)((int64_t)n_tiles * (blockIdx.x + 1) / gridDim.x);
 
@@ -237,7 +239,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) score_tc_kernel(const __grid_co
       fence_after();
       const int r = x.m0 / 4 + m / 4;   // row within the sequence
       const bool row_ok = r < P.n_rows;
-      const int64_t nb = row_ok ? visible_blocks(row_position(P.n_tokens, P.n_rows, r)) : 0;
+      // Blocks of this launch's range the row can see (column index limit).
+      const int64_t nb =
+          row_ok ? min(P.n_blocks, visible_blocks(row_position(P.n_tokens, P.n_rows, r)) - P.block_lo) : 0;
       constexpr int kChunks = kGroupCols / 32;
       float v[kChunks][32];
 #pragma unroll
@@ -324,14 +328,14 @@ size_t score_tc_workspace_bytes(int64_t n_blocks) {
 }
 
 cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows, int64_t n_tokens,
-                            const float* pooled, int64_t pooled_stride, float* scores, int64_t ld, float* gmax,
-                            int64_t gld, void* workspace, cudaStream_t st) {
-  const int64_t nb = n_tokens / 4;
+                            const float* pooled, int64_t pooled_stride, int64_t block_lo, int64_t n_blocks,
+                            float* scores, int64_t ld, float* gmax, int64_t gld, void* workspace, cudaStream_t st) {
+  const int64_t nb = n_blocks;
   if (nb <= 0 || n_rows <= 0) return cudaSuccess;
   __nv_bfloat16* planes = static_cast<__nv_bfloat16*>(workspace);
   const int64_t threads = nb * (QSA_INDEX_DIM / 4);
   cudaError_t e = launch_kernel(split_planes_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, 0u,
-                                pooled, pooled_stride, nb, planes);
+                                pooled + block_lo * pooled_stride, pooled_stride, nb, planes);
   if (e != cudaSuccess) return e;
   ScoreTcParams P;
   memset(&P, 0, sizeof(P));
@@ -344,6 +348,8 @@ cudaError_t launch_score_tc(const void* q_idx, int32_t row_begin, int32_t n_rows
   P.gmax = gmax;
   P.gld = gld;
   P.n_tokens = n_tokens;
+  P.block_lo = block_lo;
+  P.n_blocks = n_blocks;
   P.n_rows = n_rows;
   P.row_begin = row_begin;
   if ((e = allow_dynamic_smem((const void*)score_tc_kernel, kTcSmem)) != cudaSuccess) return e;

@@ -469,9 +469,129 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSE
   if (tid == 0) p.cnt[r] = k;
 }
 
+// ------------------------------------------------------------------ selection over key-axis chunks
+// One CTA per row merges the row's running top-k (keys and ids, ascending
+// ids) with the scores of one chunk of blocks [block_lo, block_lo + n_blocks):
+// the top-k of the union equals the top-k over the whole row once every chunk
+// has been merged (the SGLang launcher notes, section 2.3: top-k of a union
+// equals the top-k of the per-part top-k lists).  The union is laid out in
+// ascending id order -- the running entries, whose ids precede the chunk's,
+// then the chunk's blocks the row can see -- so the radix select's rule
+// "lowest index among keys equal to the k-th" is the method's lowest-id rule.
+// Once the running list holds k entries, a chunk block enters the union only
+// with a key above the list's smallest (it cannot displace an entry of equal
+// key and lower id), which leaves few chunk entries after the first chunks.
+__global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelectParams p, int64_t max_union) {
+  extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ uint32_t wt[2][kWarps];
+  __shared__ uint32_t s_res[2];
+  __shared__ int32_t out_s[QSA_MAX_TOP_K];
+  const SelLayout L(max_union);
+  const int tid = threadIdx.x;
+  for (int i = tid; i < L.cg; i += kThreads) sm[i] = 0u;          // the three histograms
+  for (int i = L.selw + tid; i < L.total; i += kThreads) sm[i] = 0u;   // the two bitmaps
+  if (tid == 0) {
+    s_res[0] = 0u;
+    s_res[1] = 0u;
+  }
+  grid_dependency_sync();
+  const int r = (int)blockIdx.x;
+  const int k = p.top_k;
+  const int64_t nb = visible_blocks(row_position(p.n_tokens, p.n_rows, r));
+  const int n_run = p.first ? 0 : max(0, min(k, p.run_cnt_in[r]));
+  const int vis = (int)max((int64_t)0, min((int64_t)p.n_blocks, nb - p.block_lo));
+  uint32_t* keys = sm + L.r1;
+  uint32_t* ids = sm + L.r2;
+  // The running entries, and their smallest key when they are k: a chunk
+  // block can only enter with a larger key (on an equal key the running
+  // entry's lower id wins).
+  uint32_t run_min = 0xffffffffu;
+  for (int u = tid; u < n_run; u += kThreads) {
+    const uint32_t key = p.run_key_in[(int64_t)r * k + u];
+    keys[u] = key;
+    ids[u] = (uint32_t)p.run_id_in[(int64_t)r * k + u];
+    run_min = min(run_min, key);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) run_min = min(run_min, __shfl_xor_sync(0xffffffffu, run_min, o));
+  if ((tid & 31) == 0) wt[0][tid >> 5] = run_min;
+  __syncthreads();
+  run_min = wt[0][tid & 31];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) run_min = min(run_min, __shfl_xor_sync(0xffffffffu, run_min, o));
+  const uint32_t floor_key = n_run == k ? run_min : 0u;   // chunk keys must exceed this
+  // The chunk's blocks above the floor, appended in id order: thread t takes
+  // a contiguous run, a block-wide scan places it.
+  const float* crow = p.chunk + (int64_t)r * p.ld_chunk;
+  const int per = (vis + kThreads - 1) / kThreads;
+  const int j0 = min(vis, tid * per), j1 = min(vis, j0 + per);
+  uint32_t c = 0u;
+  for (int j = j0; j < j1; ++j) c += order_key(__ldg(crow + j)) > floor_key;
+  uint32_t total;
+  uint32_t at = (uint32_t)n_run + block_scan(c, wt[1], &total);
+  for (int j = j0; j < j1; ++j) {
+    const uint32_t key = order_key(__ldg(crow + j));
+    if (key > floor_key) {
+      keys[at] = key;
+      ids[at] = (uint32_t)(p.block_lo + j);
+      ++at;
+    }
+  }
+  const int n_union = n_run + (int)total;
+  __syncthreads();
+  int n_sel;
+  if (n_union <= k) {
+    n_sel = n_union;
+    for (int i = tid; i < n_union; i += kThreads) out_s[i] = i;
+  } else {
+    n_sel = k;
+    radix_and_write(
+        (uint32_t)k, (n_union + 31) / 32,
+        [&](auto f) {
+          for (int i = tid; i < n_union; i += kThreads) f(keys[i], (int32_t)i);
+        },
+        [&](auto f) {
+          const int n_pad = (n_union + 31) / 32 * 32;
+          for (int i = tid; i < n_pad; i += kThreads) f(i < n_union ? keys[i] : 0u, (int32_t)i, i < n_union);
+        },
+        sm, L, false, wt, s_res, out_s);
+  }
+  __syncthreads();
+  // The kept entries in ascending union index = ascending id order.
+  const int64_t grow = (int64_t)p.row_begin + r;
+  for (int i = tid; i < n_sel; i += kThreads) {
+    const int u = out_s[i];
+    const int32_t id = (int32_t)ids[u];
+    if (p.last) {
+      p.sel[grow * k + i] = id;
+    } else {
+      p.run_key_out[(int64_t)r * k + i] = keys[u];
+      p.run_id_out[(int64_t)r * k + i] = id;
+    }
+  }
+  if (p.last) {
+    for (int i = n_sel + tid; i < k; i += kThreads) p.sel[grow * k + i] = -1;
+    if (tid == 0) p.cnt[grow] = n_sel;
+  } else if (tid == 0) {
+    p.run_cnt_out[r] = n_sel;
+  }
+}
+
 }  // namespace
 
 size_t select_smem_bytes(int64_t max_nb) { return sizeof(uint32_t) * (size_t)SelLayout(max_nb).total; }
+
+int merge_select_max_union() { return kListCap; }
+
+cudaError_t launch_merge_select(const MergeSelectParams& p, cudaStream_t st) {
+  if (p.n_rows == 0) return cudaSuccess;
+  const int64_t max_union = (int64_t)p.top_k + p.n_blocks;
+  if (max_union > kListCap || p.top_k > QSA_MAX_TOP_K) return cudaErrorInvalidValue;
+  const size_t smem = select_smem_bytes(max_union);
+  cudaError_t e = allow_dynamic_smem((const void*)merge_select_kernel, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(merge_select_kernel, dim3((unsigned)p.n_rows), dim3(kThreads), smem, st, 0u, p, max_union);
+}
 
 template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st) {

@@ -29,7 +29,7 @@ def L():
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?(qsa_[a-z_]+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\*?\s+\*?(qsa_[a-z_0-9]+)\(", text, re.M)))
 
 
 def test_header_declares_the_five_steps():
@@ -146,6 +146,21 @@ def test_attn_validation(L):
     assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c16), FAKE, FAKE, FAKE, 512, FAKE, None, FAKE, need - 1,
                              None) == 4
     assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c16), FAKE, FAKE, FAKE, 512, FAKE, None, None, 0, None) == 4
+
+
+def test_blocked_score_select_validation(L):
+    seq = _seq(n_tokens=40_000, n_rows=600)
+    need = L.qsa_score_select_blocked_workspace_size(seq, 1, 512, 1024)
+    assert need > 0
+    # Flat in the context: the same rows at 10x the context need the same workspace.
+    assert L.qsa_score_select_blocked_workspace_size(_seq(n_tokens=400_000, n_rows=600), 1, 512, 1024) == need
+    args = lambda dt, k, bk, ws=need: (seq, 1, FAKE, dt, k, bk, FAKE, FAKE, FAKE, ws, None)
+    assert L.qsa_score_select_topk_blocked(*args(qsa.F32, 512, 1024)) == 2       # bf16 queries only
+    assert L.qsa_score_select_topk_blocked(*args(qsa.BF16, 512, 1000)) == 2      # not a multiple of 128
+    assert L.qsa_score_select_topk_blocked(*args(qsa.BF16, 1024, 7424)) == 2     # top_k + block_keys > 8192
+    assert L.qsa_score_select_topk_blocked(*args(qsa.BF16, 0, 1024)) == 2
+    assert L.qsa_score_select_topk_blocked(*args(qsa.BF16, 512, 1024, need - 1)) == 4
+    assert L.qsa_score_select_topk_blocked(seq, 1, FAKE, qsa.BF16, 512, 1024, None, FAKE, FAKE, need, None) == 1
 
 
 def test_merge_validation(L):

@@ -102,6 +102,21 @@ def test_prefill_chunk_sampled_rows():
     assert_attn_close(to_np(out)[rows], to_np(lse)[rows], out_ref, lse_ref, True)
 
 
+def test_prefill_chunk_blocked_selection_equals_one_pass():
+    # The 2,048-row chunk at a 100,352-token prefix: key-axis chunks of 4,096
+    # blocks give the same selection as the [2,048, 25,600] score buffer.
+    T, prefix = 2048, 100_352
+    x = make_layer(L=prefix + T, M=T, dtype=torch.bfloat16, seed=4, n_planted=256, device=dev())
+    step, _ = _gpu_step(x)
+    sel = torch.empty_like(step.sel)
+    cnt = torch.empty_like(step.cnt)
+    seqs = [qsa.Seq(x.L, T, step.seqs[0].pooled)]
+    qsa.score_select_topk_blocked(seqs, x.q_idx, sel, cnt, 512, 4096)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(cnt), to_np(step.cnt))
+    np.testing.assert_array_equal(to_np(sel), to_np(step.sel))
+
+
 @pytest.mark.parametrize("D", [256, 128])
 def test_ragged_segmented_batch_full_size(D):
     # 16 sequences, 8 decoding one row and 8 verifying four, contexts

@@ -189,6 +189,84 @@ def test_select_ragged_sequences():
     np.testing.assert_array_equal(to_np(sel), rs)
 
 
+# ------------------------------------------------------------------ steps 2 + 3 over key-axis chunks
+def _blocked_vs_one_pass(seqs, q_idx, block_keys, top_k=512):
+    """Selections of the chunked path and of score_blocks + select_topk."""
+    rows = sum(sq.n_rows for sq in seqs)
+    ld = max(1, max(sq.n_tokens // 4 for sq in seqs))
+    ld = (ld + 3) // 4 * 4
+    scores = torch.empty((rows, ld), dtype=torch.float32, device=dev())
+    gm = torch.empty((rows, (qsa.n_groups(max(sq.n_tokens for sq in seqs)) + 3) // 4 * 4), device=dev())
+    sel1 = torch.empty((rows, top_k), dtype=torch.int32, device=dev())
+    cnt1 = torch.empty((rows,), dtype=torch.int32, device=dev())
+    qsa.score_blocks(seqs, q_idx, scores, group_max=gm)
+    qsa.select_topk(seqs, scores, sel1, cnt1, top_k, group_max=gm)
+    sel2 = torch.full((rows, top_k), 12345, dtype=torch.int32, device=dev())
+    cnt2 = torch.full((rows,), -7, dtype=torch.int32, device=dev())
+    ws = torch.full((qsa.score_select_blocked_workspace_size(seqs, top_k, block_keys),), 0x7F, dtype=torch.uint8,
+                    device=dev())
+    qsa.score_select_topk_blocked(seqs, q_idx, sel2, cnt2, top_k, block_keys, workspace=ws)
+    torch.cuda.synchronize()
+    return to_np(sel1), to_np(cnt1), to_np(sel2), to_np(cnt2), scores
+
+
+@pytest.mark.parametrize("L,M,block_keys", [(12_000, 600, 1024), (2500, 600, 128), (20_000, 520, 4096),
+                                            (4099, 512, 256)])
+def test_blocked_selection_equals_one_pass(L, M, block_keys):
+    # Many rows score on the tensor cores in both paths, so the scores are the
+    # same numbers and the selections must be identical.  Rows at small
+    # positions see fewer than 512 blocks; the last chunk is ragged.
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + block_keys, device=dev())
+    pooled = pooled_buffer(L, dev())
+    pool_all(x.idxk, pooled, L)
+    seqs = [qsa.Seq(L, M, pooled)]
+    sel1, cnt1, sel2, cnt2, _ = _blocked_vs_one_pass(seqs, x.q_idx, block_keys)
+    np.testing.assert_array_equal(cnt2, cnt1)
+    np.testing.assert_array_equal(sel2, sel1)
+    assert qsa.wait_timeouts() == 0
+
+
+def test_blocked_selection_matches_oracle_and_ties():
+    # A ragged batch (a prefill chunk and an 8-row verify); rows 0-2 of the
+    # chunk have all-zero index queries, so every block ties at 0 and the
+    # lowest ids must win.  Sampled rows against the oracle.
+    xa = make_layer(L=9000, M=600, dtype=torch.bfloat16, seed=31, device=dev())
+    xb = make_layer(L=5003, M=8, dtype=torch.bfloat16, seed=32, device=dev())
+    xa.q_idx[:3] = 0
+    pa, pb = pooled_buffer(9000, dev()), pooled_buffer(5003, dev())
+    pool_all(xa.idxk, pa, 9000)
+    pool_all(xb.idxk, pb, 5003)
+    seqs = [qsa.Seq(9000, 600, pa), qsa.Seq(5003, 8, pb)]
+    q_idx = torch.cat([xa.q_idx, xb.q_idx])
+    sel1, cnt1, sel2, cnt2, _ = _blocked_vs_one_pass(seqs, q_idx, 1024)
+    np.testing.assert_array_equal(cnt2, cnt1)
+    np.testing.assert_array_equal(sel2, sel1)
+    np.testing.assert_array_equal(sel2[0], np.arange(512))
+    rows = [0, 1, 5, 300, 599]
+    for x, sel, cnt, rr in ((xa, sel2[:600], cnt2[:600], rows), (xb, sel2[600:], cnt2[600:], list(range(8)))):
+        h_idxk, h_q = x.idxk.cpu(), x.q_idx.cpu()
+        pos = [x.row_pos[r] for r in rr]
+        pooled_ref = oracle.pool(h_idxk)
+        s_ref = oracle.score(h_q[rr], pooled_ref, pos)
+        sel_ref, cnt_ref, tau = oracle.select(s_ref, pos)
+        assert_selection_close(sel[rr], cnt[rr], sel_ref, cnt_ref, tau, s_ref, pos)
+
+
+def test_blocked_selection_few_rows_matches_oracle():
+    # Four rows: the one-pass path scores them on the few-row kernel (tf32
+    # planes), the chunked path on the tensor cores; both against the oracle.
+    L, M = 30_001, 4
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=33, device=dev())
+    pooled = pooled_buffer(L, dev())
+    pool_all(x.idxk, pooled, L)
+    seqs = [qsa.Seq(L, M, pooled)]
+    _, _, sel2, cnt2, _ = _blocked_vs_one_pass(seqs, x.q_idx, 2048)
+    pooled_ref = oracle.pool(x.idxk.cpu())
+    s_ref = oracle.score(x.q_idx.cpu(), pooled_ref, x.row_pos)
+    sel_ref, cnt_ref, tau = oracle.select(s_ref, x.row_pos)
+    assert_selection_close(sel2, cnt2, sel_ref, cnt_ref, tau, s_ref, x.row_pos)
+
+
 # ------------------------------------------------------------------ step 4 (given the oracle's selection)
 def _oracle_selection(x):
     pooled = oracle.pool(x.idxk)
