@@ -152,6 +152,37 @@ qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_
                                int64_t pooled_stride, void* stream);
 
 /*
+ * Appending tokens with in-place pooling (step 1 and the cache writes either
+ * side of it: hipfire, section 02 -- a QSA layer writes K/V and an index key
+ * for every token, and every 4 index keys are averaged into a pooled block
+ * key; MTPLX pull request #482, optimisation 1 -- the new rows' K/V are
+ * written into the existing cache).  For the n = seq->n_rows newest tokens
+ * t = L - n .. L - 1 (L = seq->n_tokens, the cache length after the append):
+ *   K/V:  head h of token t -> the segment s covering t, at
+ *         s.k[h * s.head_stride + (t - s.first_token) * s.tok_stride + d]
+ *         (s.v likewise), from k_new[(h * n + (t - L + n)) * D + d];
+ *   index keys: idx_keys[t * idx_tok_stride + c] = idx_new[(t - L + n) * 128 + c];
+ *   pooled keys of every block the new tokens complete (floor((L - n) / 4)
+ *   <= b < floor(L / 4)), exactly as qsa_pool_index_keys computes them,
+ *   reading earlier tokens' index keys from idx_keys.
+ * One launch.  The library writes into the caller's caches here (and only
+ * here): the segments' K/V and seq->pooled are written through their
+ * pointers, which the descriptor declares const for the read-only calls.
+ *   seq            host descriptor: n_tokens, n_rows (= n), n_segments,
+ *                  segments, pooled, pooled_stride
+ *   cfg            n_kv_heads, head_dim, kv_dtype (other fields checked as
+ *                  for qsa_sparse_attn)
+ *   k_new, v_new   device [Hkv, n, D] kv_dtype, contiguous
+ *   idx_new        device [n, 128] idx_dtype, contiguous
+ *   idx_keys       device index-key cache, [>= L, idx_tok_stride] idx_dtype
+ * Errors: QSA_ERR_INVALID_ARG (a new token in no segment, null pointers,
+ * n > L), QSA_ERR_MISALIGNED, QSA_ERR_UNSUPPORTED (dtypes, head_dim).
+ */
+qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* cfg, const void* k_new, const void* v_new,
+                             const void* idx_new, void* idx_keys, int64_t idx_tok_stride, qsa_dtype idx_dtype,
+                             void* stream);
+
+/*
  * Step 2 -- block scoring (hipfire, section 02: four index-query heads score
  * every pooled block; section 03: a few-row variant for decode and verify
  * and a wide variant for prefill).

@@ -65,7 +65,7 @@ EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
            "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
-           "qsa_score_select_topk_blocked")
+           "qsa_score_select_topk_blocked", "qsa_append_tokens")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -100,11 +100,13 @@ def lib() -> ctypes.CDLL:
     L.qsa_sparse_attn.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp, sz, vp]
     L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
+    L.qsa_append_tokens.argtypes = [seqp, ctypes.POINTER(AttnConfig), vp, vp, vp, vp, i64, i32, vp]
     L.qsa_score_select_blocked_workspace_size.argtypes = [seqp, i32, i32, i32]
     L.qsa_score_select_blocked_workspace_size.restype = sz
     L.qsa_score_select_topk_blocked.argtypes = [seqp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_score_select_topk",
-                 "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge", "qsa_score_select_topk_blocked"):
+                 "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge", "qsa_score_select_topk_blocked",
+                 "qsa_append_tokens"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -250,6 +252,23 @@ def score_select_topk(seqs, q_idx: torch.Tensor, scores: torch.Tensor, sel: torc
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0), int(top_k),
         sel.data_ptr(), cnt.data_ptr(), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         _stream(stream)))
+
+
+def append_tokens(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: torch.Tensor, stream=None,
+                  cfg=None):
+    """Write the seq.n_rows newest tokens' K/V ([Hkv, n, D]) and index keys
+    ([n, 128]) into seq's segments and seq.idx_keys, and pool the blocks they
+    complete into seq.pooled, in one launch."""
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and idx_new.is_contiguous()):
+        raise ValueError("append_tokens: k_new, v_new and idx_new must be contiguous")
+    arr = make_seq_array([seq])
+    if cfg is None:   # only the KV heads, head_dim and dtype matter here
+        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], _dtype_code(k_new), _dtype_code(k_new),
+                         F32, 0.0, 0)
+    idxk = seq.idx_keys
+    _check("qsa_append_tokens", lib().qsa_append_tokens(
+        arr, ctypes.byref(cfg), k_new.data_ptr(), v_new.data_ptr(), idx_new.data_ptr(), idxk.data_ptr(),
+        idxk.stride(0), _dtype_code(idxk), _stream(stream)))
 
 
 def score_select_blocked_workspace_size(seqs, top_k: int = TOP_K, block_keys: int = 4096, seq_array=None) -> int:
@@ -398,8 +417,20 @@ class LayerStep:
         sparse_attn(None, self.q, self.sel, self.cnt, self.out, self.lse, workspace=self.ws, stream=stream,
                     seq_array=self.arr, cfg=self.cfg)
 
-    def run(self, stream=None):
-        self.pool(stream)
+    def append(self, new_tokens, stream=None):
+        """Append each sequence's n_rows newest tokens (a (k_new, v_new,
+        idx_new) triple per sequence) and pool the blocks they complete:
+        replaces pool() when the caller hands the new tokens to the library."""
+        for sq, (k_new, v_new, idx_new) in zip(self.seqs, new_tokens):
+            append_tokens(sq, k_new, v_new, idx_new, stream, cfg=self.cfg)
+
+    def run(self, stream=None, new_tokens=None):
+        """One layer step: pool (or append new_tokens and pool), score,
+        select, attend."""
+        if new_tokens is None:
+            self.pool(stream)
+        else:
+            self.append(new_tokens, stream)
         self.score(stream)
         self.select(stream)
         self.attend(stream)

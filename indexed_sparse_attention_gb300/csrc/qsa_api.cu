@@ -660,6 +660,73 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
   return ok();
 }
 
+// ------------------------------------------------------------------ appending tokens (step 1 in place)
+QSA_API qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* cfg, const void* k_new,
+                                     const void* v_new, const void* idx_new, void* idx_keys, int64_t idx_tok_stride,
+                                     qsa_dtype idx_dtype, void* stream) {
+  const char* fn = "qsa_append_tokens";
+  int64_t rows = 0;
+  qsa_status s = check_rows(seq, 1, fn, &rows);
+  if (s != QSA_OK) return s;
+  if ((s = check_attn_config(cfg, fn)) != QSA_OK) return s;
+  if (!valid_dtype(idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: idx_dtype %d", fn, (int)idx_dtype);
+  if (!k_new || !v_new || !idx_new || !idx_keys) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  const int64_t idx_es = (int64_t)dtype_size(idx_dtype), kv_es = (int64_t)dtype_size(cfg->kv_dtype);
+  if (idx_tok_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: idx_tok_stride < 128", fn);
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(idx_new) || !aligned16(idx_keys) ||
+      (idx_tok_stride * idx_es) % 16 != 0)
+    return fail(QSA_ERR_MISALIGNED, "%s: pointers and strides must be 16-byte aligned", fn);
+  if ((s = check_segments(seq, 1, cfg, fn)) != QSA_OK) return s;
+  const int64_t L = seq->n_tokens, n_new = seq->n_rows;
+  // Every new token must land in a segment (segments do not overlap).
+  {
+    std::vector<std::pair<int64_t, int64_t>> r;
+    for (int j = 0; j < seq->n_segments; ++j)
+      r.emplace_back(seq->segments[j].first_token, seq->segments[j].first_token + seq->segments[j].n_tokens);
+    std::sort(r.begin(), r.end());
+    int64_t t = L - n_new;
+    for (const auto& e : r)
+      if (e.first <= t && e.second > t) t = e.second;
+    if (t < L) return fail(QSA_ERR_INVALID_ARG, "%s: token %lld is in no KV segment", fn, (long long)t);
+  }
+  const int64_t b0 = (L - n_new) / 4, b1 = L / 4;   // blocks the new tokens complete
+  if (b1 > b0) {
+    if (!seq->pooled) return fail(QSA_ERR_INVALID_ARG, "%s: no pooled keys to write", fn);
+    if (seq->pooled_stride < QSA_INDEX_DIM || seq->pooled_stride % 4 != 0 || !aligned16(seq->pooled))
+      return fail(QSA_ERR_MISALIGNED, "%s: pooled keys must be 16-byte aligned, stride >= 128", fn);
+  }
+  AppendParams p{};
+  for (int j = 0; j < seq->n_segments; ++j) {
+    const qsa_kv_segment& g = seq->segments[j];
+    p.seg[j] = AppendSeg{const_cast<void*>(g.k), const_cast<void*>(g.v), g.first_token, g.n_tokens, g.head_stride,
+                         g.tok_stride};
+  }
+  p.n_segs = seq->n_segments;
+  p.n_kv_heads = cfg->n_kv_heads;
+  p.n_tokens = L;
+  p.n_new = n_new;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.kv_es = (int32_t)kv_es;
+  p.row_bytes = cfg->head_dim * kv_es;
+  p.row_chunks = p.row_bytes / 16;
+  p.idx_new = idx_new;
+  p.idx_keys = idx_keys;
+  p.idx_stride = idx_tok_stride;
+  p.idx_dtype = idx_dtype;
+  p.idx_es = (int32_t)idx_es;
+  p.idx_chunks = QSA_INDEX_DIM * idx_es / 16;
+  p.pooled = const_cast<float*>(seq->pooled);
+  p.pooled_stride = seq->pooled_stride;
+  p.first_block = b0;
+  p.kv_items = 2 * (int64_t)cfg->n_kv_heads * n_new * p.row_chunks;
+  p.idx_items = n_new * p.idx_chunks;
+  p.pool_items = std::max<int64_t>(0, b1 - b0) * (QSA_INDEX_DIM / 4);
+  cudaError_t e = launch_append(p, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 // ------------------------------------------------------------------ step 5
 QSA_API qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t n_rows,
                          int32_t head_dim, void* out, qsa_dtype out_dtype, float* lse_out, void* stream) {

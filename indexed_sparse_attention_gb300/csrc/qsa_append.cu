@@ -1,0 +1,94 @@
+// Appending a sequence's newest tokens to its caches in place, with the
+// pooling of the blocks they complete (step 1) in the same launch: the step
+// either side of the pooling in a QSA layer (hipfire, "QSA sparse attention
+// and the VMM KV backend", section 02: a QSA layer writes an index key for
+// every token besides its K/V, and every 4 consecutive index keys are
+// averaged into one pooled block key; MTPLX pull request #482, optimisation
+// 1: the new rows' K/V are written into the existing cache, not into a copy).
+//
+// One launch, three kinds of 16-byte work item (thread = item):
+//   K and V rows of the new tokens -> the KV segment that covers each token;
+//   index keys of the new tokens  -> the index-key cache;
+//   pooled keys of every block a new token completes -> pooled, averaging
+//   the block's four index keys in the order ((k0 + k1) + k2) + k3, x 0.25
+//   (the pooling kernel's arithmetic), reading the keys of new tokens from
+//   the input and those of earlier tokens from the cache, so no item reads
+//   what another item of the launch writes.
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+namespace {
+
+__device__ __forceinline__ float4 load_key4(const void* base, int dtype, int64_t row, int64_t stride, int d) {
+  if (dtype == QSA_F32) return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * stride + d);
+  const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + row * stride + d);
+  return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+}
+
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  // Writes what earlier launches of the stream may read: wait for them first.
+  grid_dependency_wait();
+  grid_dependency_release();
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t first_new = p.n_tokens - p.n_new;
+  if (i < p.kv_items) {
+    // (K or V, KV head, new token, 16-byte chunk of the row)
+    const int64_t per_row = p.row_chunks;
+    const int64_t row = i / per_row, c = i % per_row;
+    const int which = (int)(row / ((int64_t)p.n_kv_heads * p.n_new));   // 0: K, 1: V
+    const int64_t hr = row % ((int64_t)p.n_kv_heads * p.n_new);
+    const int h = (int)(hr / p.n_new);
+    const int64_t j = hr % p.n_new;
+    const int64_t t = first_new + j;
+    const char* src = static_cast<const char*>(which ? p.v_new : p.k_new) +
+                      ((int64_t)h * p.n_new + j) * p.row_bytes + c * 16;
+    for (int s = 0; s < p.n_segs; ++s) {
+      const AppendSeg& sg = p.seg[s];
+      if (t >= sg.first && t < sg.first + sg.n) {
+        char* dst = static_cast<char*>(which ? sg.v : sg.k) +
+                    ((int64_t)h * sg.head_stride + (t - sg.first) * sg.tok_stride) * p.kv_es + c * 16;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        break;
+      }
+    }
+    return;
+  }
+  const int64_t i2 = i - p.kv_items;
+  if (i2 < p.idx_items) {
+    const int64_t j = i2 / p.idx_chunks, c = i2 % p.idx_chunks;
+    const char* src = static_cast<const char*>(p.idx_new) + j * QSA_INDEX_DIM * p.idx_es + c * 16;
+    char* dst = static_cast<char*>(p.idx_keys) + (first_new + j) * p.idx_stride * p.idx_es + c * 16;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    return;
+  }
+  const int64_t i3 = i2 - p.idx_items;
+  if (i3 < p.pool_items) {
+    const int64_t b = p.first_block + i3 / (QSA_INDEX_DIM / 4);
+    const int d = (int)(i3 % (QSA_INDEX_DIM / 4)) * 4;
+    float4 k[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t t = 4 * b + q;
+      k[q] = t >= first_new ? load_key4(p.idx_new, p.idx_dtype, t - first_new, QSA_INDEX_DIM, d)
+                            : load_key4(p.idx_keys, p.idx_dtype, t, p.idx_stride, d);
+    }
+    float4 m;
+    m.x = (((k[0].x + k[1].x) + k[2].x) + k[3].x) * 0.25f;
+    m.y = (((k[0].y + k[1].y) + k[2].y) + k[3].y) * 0.25f;
+    m.z = (((k[0].z + k[1].z) + k[2].z) + k[3].z) * 0.25f;
+    m.w = (((k[0].w + k[1].w) + k[2].w) + k[3].w) * 0.25f;
+    *reinterpret_cast<float4*>(p.pooled + b * p.pooled_stride + d) = m;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st) {
+  const int64_t items = p.kv_items + p.idx_items + p.pool_items;
+  if (items == 0) return cudaSuccess;
+  const int64_t grid = (items + 255) / 256;
+  return launch_kernel(append_kernel, dim3((unsigned)grid), dim3(256), 0, st, 0u, p);
+}
+
+}  // namespace qsa

@@ -113,6 +113,38 @@ struct AttnParams {
   int32_t out_dtype;
 };
 
+// ---------------------------------------------------------------- appending tokens
+struct AppendSeg {
+  void* k;
+  void* v;
+  int64_t first, n, head_stride, tok_stride;   // elements
+};
+
+struct AppendParams {
+  AppendSeg seg[QSA_MAX_SEGMENTS];
+  int32_t n_segs;
+  int32_t n_kv_heads;
+  int64_t n_tokens;          // L after the append
+  int64_t n_new;             // tokens L - n_new .. L - 1 are appended
+  const void* k_new;         // [Hkv, n_new, D]
+  const void* v_new;
+  int64_t row_bytes;         // D x kv element size
+  int64_t row_chunks;        // row_bytes / 16
+  int32_t kv_es;
+  const void* idx_new;       // [n_new, 128]
+  void* idx_keys;            // [>= L, idx_stride]
+  int64_t idx_stride;
+  int32_t idx_dtype;
+  int32_t idx_es;
+  int64_t idx_chunks;        // 128 x idx_es / 16
+  float* pooled;
+  int64_t pooled_stride;
+  int64_t first_block;       // blocks first_block .. first_block + pool_items / 32 - 1 are pooled
+  int64_t kv_items, idx_items, pool_items;
+};
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64_t first_block,
                         int64_t n_blocks, float* pooled, int64_t pstride, cudaStream_t st);

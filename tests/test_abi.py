@@ -148,6 +148,19 @@ def test_attn_validation(L):
     assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c16), FAKE, FAKE, FAKE, 512, FAKE, None, None, 0, None) == 4
 
 
+def test_append_validation(L):
+    c = qsa.AttnConfig(2, 2, 256, qsa.BF16, qsa.BF16, qsa.F32, 0.0, 0)
+    seq = _seq(n_tokens=4099, n_rows=4)
+    ok = lambda s, idx=FAKE, stride=128: L.qsa_append_tokens(s, ctypes.byref(c), FAKE, FAKE, FAKE, idx, stride,
+                                                             qsa.BF16, None)
+    assert ok(seq, idx=None) == 1                                       # null pointer
+    assert ok(seq, stride=64) == 1                                      # index-key stride < 128
+    assert ok(seq, idx=FAKE_MIS) == 3
+    assert ok(_seq(n_tokens=4099, n_rows=4, segs=[(0, 4097)])) == 1     # tokens 4097, 4098 in no segment
+    assert "no KV segment" in L.qsa_last_error().decode()
+    assert ok(_seq(n_tokens=4099, n_rows=5000)) == 1                    # more new tokens than the cache
+
+
 def test_blocked_score_select_validation(L):
     seq = _seq(n_tokens=40_000, n_rows=600)
     need = L.qsa_score_select_blocked_workspace_size(seq, 1, 512, 1024)

@@ -189,6 +189,61 @@ def test_select_ragged_sequences():
     np.testing.assert_array_equal(to_np(sel), rs)
 
 
+# ------------------------------------------------------------------ appending tokens with in-place pooling
+@pytest.mark.parametrize("L,n,kv_dtype,idx_dtype,n_segs", [
+    (4099, 4, torch.bfloat16, torch.bfloat16, 1), (65_536, 1, torch.bfloat16, torch.bfloat16, 1),
+    (2148, 2048, torch.bfloat16, torch.bfloat16, 3), (7, 1, torch.float32, torch.float32, 1),
+    (3, 3, torch.float32, torch.bfloat16, 1), (9001, 5, torch.float32, torch.float32, 4),
+    (2052, 9, torch.bfloat16, torch.float32, 2)])
+def test_append_writes_caches_and_pools(L, n, kv_dtype, idx_dtype, n_segs):
+    x = make_layer(L=L, M=min(n, L), dtype=torch.float32, seed=L + n, device=dev())
+    k_full, v_full = x.k.to(kv_dtype), x.v.to(kv_dtype)
+    idx_full = x.idxk.to(idx_dtype)
+    # Caches hold the first L - n tokens; the rest is garbage (NaN) until the append.
+    k_c, v_c = torch.full_like(k_full, float("nan")), torch.full_like(v_full, float("nan"))
+    idx_c = torch.full_like(idx_full, float("nan"))
+    k_c[:, :L - n], v_c[:, :L - n], idx_c[:L - n] = k_full[:, :L - n], v_full[:, :L - n], idx_full[:L - n]
+    pooled = pooled_buffer(L, dev())
+    b0 = (L - n) // 4
+    if b0:
+        qsa.pool_index_keys(idx_c, pooled, 0, b0)
+    # Segments: views of the caches, one cut inside the new tokens when several.
+    cuts = [0] + sorted({max(1, L - n + (n * j) // n_segs) for j in range(1, n_segs)} - {0, L}) + [L]
+    segs = [qsa.Segment(k_c[:, a:b], v_c[:, a:b], a) for a, b in zip(cuts[:-1], cuts[1:])]
+    seq = qsa.Seq(L, n, pooled, segs, idx_keys=idx_c)
+    qsa.append_tokens(seq, k_full[:, L - n:].contiguous(), v_full[:, L - n:].contiguous(),
+                      idx_full[L - n:].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(k_c, k_full) and torch.equal(v_c, v_full) and torch.equal(idx_c, idx_full)
+    ref = pooled_buffer(L, dev())
+    if L // 4:
+        qsa.pool_index_keys(idx_full, ref, 0, L // 4)
+    torch.cuda.synchronize()
+    # The same numbers as the pooling kernel (itself checked against the oracle above).
+    assert torch.equal(pooled[:L // 4], ref[:L // 4])
+
+
+def test_layer_step_with_append_equals_prewritten_caches():
+    L, M = 9001, 4
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=41, device=dev())
+    pa = pooled_buffer(L, dev())
+    qsa.pool_index_keys(x.idxk, pa, 0, (L - M) // 4)
+    step_a = qsa.LayerStep([qsa.Seq(L, M, pa, [qsa.Segment(x.k, x.v, 0)], idx_keys=x.idxk)], x.q_idx, x.q)
+    out_a, lse_a = step_a.run()
+    k_c, v_c, idx_c = x.k.clone(), x.v.clone(), x.idxk.clone()
+    k_c[:, L - M:] = 0
+    v_c[:, L - M:] = 0
+    idx_c[L - M:] = 0
+    pb = pooled_buffer(L, dev())
+    qsa.pool_index_keys(idx_c, pb, 0, (L - M) // 4)
+    step_b = qsa.LayerStep([qsa.Seq(L, M, pb, [qsa.Segment(k_c, v_c, 0)], idx_keys=idx_c)], x.q_idx, x.q)
+    out_b, lse_b = step_b.run(new_tokens=[(x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(),
+                                           x.idxk[L - M:].contiguous())])
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b) and torch.equal(lse_a, lse_b)
+    assert torch.equal(k_c, x.k) and torch.equal(idx_c, x.idxk)
+
+
 # ------------------------------------------------------------------ steps 2 + 3 over key-axis chunks
 def _blocked_vs_one_pass(seqs, q_idx, block_keys, top_k=512):
     """Selections of the chunked path and of score_blocks + select_topk."""
