@@ -418,10 +418,15 @@ def main():
     # device into the caches, the layer chain runs, outputs come back.
     M = spec["M"]
     L = spec["L"]
-    h2d_items, d2h_items = [], []
+    # The new rows' K, V and index keys arrive as contiguous tensors (what a
+    # model produces) and qsa_append_tokens writes them into the caches and
+    # pools the blocks they complete.
+    h2d_items, d2h_items, new_tokens = [], [], []
     for l in layers:
         x = l.x
-        for t in (x.q, x.q_idx, x.k[:, L - M:], x.v[:, L - M:], x.idxk[L - M:]):
+        staged = [x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(), x.idxk[L - M:].contiguous()]
+        new_tokens.append([tuple(staged)])
+        for t in [x.q, x.q_idx] + staged:
             h2d_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
         for t in (l.step.out, l.step.lse):
             d2h_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
@@ -433,8 +438,8 @@ def main():
     def e2e_step():
         for d, h in h2d_items:
             d.copy_(h, non_blocking=True)
-        for l in layers:
-            l.step.run()
+        for l, nt in zip(layers, new_tokens):
+            l.step.run(new_tokens=nt)
         for d, h in d2h_items:
             h.copy_(d, non_blocking=True)
 
@@ -544,8 +549,10 @@ def main():
         **({"roofline_scoring": roofline_scoring} if roofline_scoring else {}),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "mode": "one CUDA graph per step: pinned host->device input copies, the layer chain through "
-                        "LayerStep (the C ABI), device->host copies of every layer's out and lse"},
+                "mode": "one CUDA graph per step: pinned host->device copies of every layer's q, index queries "
+                        "and new K/V/index-key rows, then per layer qsa_append_tokens (cache write + pooling) and "
+                        "the layer chain through LayerStep (the C ABI), device->host copies of every layer's out "
+                        "and lse"},
         "gpu_launches": launches,
         "us_per_launch_by_step": kernel_us,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
