@@ -116,6 +116,37 @@ typedef struct qsa_attn_config {
   int32_t n_splits;          /* splits of each row's selected rows, <= 256; 0 = library's choice */
 } qsa_attn_config;
 
+/*
+ * Demand-mapped device arena (hipfire, "QSA sparse attention and the VMM KV
+ * backend", section 04 "VMM: reserve big, commit what you touch").  Reserves
+ * a virtual address range for the largest cache and maps physical device
+ * memory into it only as the cache grows; the base pointer never changes, so
+ * segment descriptors and CUDA graphs captured with addresses inside the
+ * arena stay valid across growth.  Host calls; not for concurrent use on one
+ * arena from several threads without the caller's own ordering (ensure() is
+ * internally locked).
+ *   qsa_arena_create   reserve >= reserve_bytes (rounded up to the device's
+ *                      recommended allocation granularity) on `device`;
+ *                      nothing mapped yet
+ *   qsa_arena_ensure   map physical memory so that [base, base + bytes) is
+ *                      backed (granularity multiples; never unmaps); bytes
+ *                      beyond the reservation: QSA_ERR_INVALID_ARG; device
+ *                      memory exhausted: QSA_ERR_CUDA.  Mapping does not
+ *                      disturb work in flight on already-mapped bytes.
+ *   qsa_arena_base / _mapped / _reserved / _granularity   (0 / NULL for NULL)
+ *   qsa_arena_destroy  waits for the device, unmaps and frees the physical
+ *                      memory and the address range; NULL is a no-op
+ * Errors: QSA_ERR_INVALID_ARG, QSA_ERR_CUDA (no device, driver refusal).
+ */
+typedef struct qsa_arena qsa_arena;
+qsa_status qsa_arena_create(int32_t device, uint64_t reserve_bytes, qsa_arena** arena);
+qsa_status qsa_arena_ensure(qsa_arena* arena, uint64_t bytes);
+void* qsa_arena_base(const qsa_arena* arena);
+uint64_t qsa_arena_mapped(const qsa_arena* arena);
+uint64_t qsa_arena_reserved(const qsa_arena* arena);
+uint64_t qsa_arena_granularity(const qsa_arena* arena);
+qsa_status qsa_arena_destroy(qsa_arena* arena);
+
 /* Human-readable name of a status code (static storage). */
 const char* qsa_status_string(qsa_status status);
 

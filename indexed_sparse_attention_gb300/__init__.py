@@ -65,7 +65,8 @@ EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index
            "qsa_select_workspace_size", "qsa_select_topk", "qsa_score_select_workspace_size",
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
            "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
-           "qsa_score_select_topk_blocked", "qsa_append_tokens")
+           "qsa_score_select_topk_blocked", "qsa_append_tokens", "qsa_arena_create", "qsa_arena_ensure",
+           "qsa_arena_base", "qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity", "qsa_arena_destroy")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -101,12 +102,21 @@ def lib() -> ctypes.CDLL:
     L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
     L.qsa_append_tokens.argtypes = [seqp, ctypes.POINTER(AttnConfig), vp, vp, vp, vp, i64, i32, vp]
+    u64 = ctypes.c_uint64
+    L.qsa_arena_create.argtypes = [i32, u64, ctypes.POINTER(vp)]
+    L.qsa_arena_ensure.argtypes = [vp, u64]
+    L.qsa_arena_destroy.argtypes = [vp]
+    L.qsa_arena_base.argtypes = [vp]
+    L.qsa_arena_base.restype = vp
+    for name in ("qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity"):
+        getattr(L, name).argtypes = [vp]
+        getattr(L, name).restype = u64
     L.qsa_score_select_blocked_workspace_size.argtypes = [seqp, i32, i32, i32]
     L.qsa_score_select_blocked_workspace_size.restype = sz
     L.qsa_score_select_topk_blocked.argtypes = [seqp, i32, vp, i32, i32, i32, vp, vp, vp, sz, vp]
     for name in ("qsa_pool_index_keys", "qsa_score_blocks", "qsa_select_topk", "qsa_score_select_topk",
                  "qsa_sparse_attn", "qsa_sparse_attn_noalloc", "qsa_lse_merge", "qsa_score_select_topk_blocked",
-                 "qsa_append_tokens"):
+                 "qsa_append_tokens", "qsa_arena_create", "qsa_arena_ensure", "qsa_arena_destroy"):
         getattr(L, name).restype = i32
     _lib = L
     return L
@@ -269,6 +279,66 @@ def append_tokens(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: t
     _check("qsa_append_tokens", lib().qsa_append_tokens(
         arr, ctypes.byref(cfg), k_new.data_ptr(), v_new.data_ptr(), idx_new.data_ptr(), idxk.data_ptr(),
         idxk.stride(0), _dtype_code(idxk), _stream(stream)))
+
+
+class _DevicePtr:
+    """A device byte range exposed through __cuda_array_interface__ (no ownership)."""
+
+    def __init__(self, ptr: int, n_bytes: int):
+        self.__cuda_array_interface__ = {"shape": (n_bytes,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+
+
+class Arena:
+    """Demand-mapped device memory with one stable base pointer: reserve once,
+    map more physical memory with ensure() as the cache grows.  Views from
+    tensor() do not own the memory; the arena must outlive them."""
+
+    def __init__(self, reserve_bytes: int, device: int | None = None):
+        self.device = torch.cuda.current_device() if device is None else int(device)
+        h = ctypes.c_void_p()
+        _check("qsa_arena_create", lib().qsa_arena_create(self.device, int(reserve_bytes), ctypes.byref(h)))
+        self._h = h.value
+
+    def ensure(self, n_bytes: int):
+        _check("qsa_arena_ensure", lib().qsa_arena_ensure(self._h, int(n_bytes)))
+
+    @property
+    def base(self) -> int:
+        return int(lib().qsa_arena_base(self._h) or 0)
+
+    @property
+    def mapped(self) -> int:
+        return int(lib().qsa_arena_mapped(self._h))
+
+    @property
+    def reserved(self) -> int:
+        return int(lib().qsa_arena_reserved(self._h))
+
+    @property
+    def granularity(self) -> int:
+        return int(lib().qsa_arena_granularity(self._h))
+
+    def tensor(self, offset: int, shape, dtype) -> torch.Tensor:
+        """A view of [offset, offset + bytes) (mapped already) as a tensor."""
+        es = torch.empty(0, dtype=dtype).element_size()
+        n = es
+        for d in shape:
+            n *= int(d)
+        if offset < 0 or offset % 16 or offset + n > self.mapped:
+            raise ValueError("arena view outside the mapped, 16-byte-aligned range")
+        raw = torch.as_tensor(_DevicePtr(self.base + offset, n), device=f"cuda:{self.device}")
+        return raw.view(dtype).view(tuple(shape))
+
+    def destroy(self):
+        if getattr(self, "_h", None):
+            _check("qsa_arena_destroy", lib().qsa_arena_destroy(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
 
 
 def score_select_blocked_workspace_size(seqs, top_k: int = TOP_K, block_keys: int = 4096, seq_array=None) -> int:

@@ -727,6 +727,39 @@ QSA_API qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* 
   return ok();
 }
 
+// ------------------------------------------------------------------ demand-mapped arena
+QSA_API qsa_status qsa_arena_create(int32_t device, uint64_t reserve_bytes, qsa_arena** arena) {
+  const char* fn = "qsa_arena_create";
+  if (!arena) return fail(QSA_ERR_INVALID_ARG, "%s: null output pointer", fn);
+  *arena = nullptr;
+  if (device < 0 || reserve_bytes == 0) return fail(QSA_ERR_INVALID_ARG, "%s: device %d, %llu bytes", fn, device,
+                                                    (unsigned long long)reserve_bytes);
+  const char* why = "";
+  const qsa_status s = arena_create(device, reserve_bytes, arena, &why);
+  return s == QSA_OK ? ok() : fail(s, "%s: %s", fn, why);
+}
+
+QSA_API qsa_status qsa_arena_ensure(qsa_arena* arena, uint64_t bytes) {
+  const char* fn = "qsa_arena_ensure";
+  if (!arena) return fail(QSA_ERR_INVALID_ARG, "%s: null arena", fn);
+  const char* why = "";
+  const qsa_status s = arena_ensure(arena, bytes, &why);
+  return s == QSA_OK ? ok() : fail(s, "%s: %s", fn, why);
+}
+
+QSA_API void* qsa_arena_base(const qsa_arena* arena) { return arena ? arena_base(arena) : nullptr; }
+QSA_API uint64_t qsa_arena_mapped(const qsa_arena* arena) { return arena ? arena_mapped(arena) : 0; }
+QSA_API uint64_t qsa_arena_reserved(const qsa_arena* arena) { return arena ? arena_reserved(arena) : 0; }
+QSA_API uint64_t qsa_arena_granularity(const qsa_arena* arena) { return arena ? arena_granularity(arena) : 0; }
+
+QSA_API qsa_status qsa_arena_destroy(qsa_arena* arena) {
+  const char* fn = "qsa_arena_destroy";
+  if (!arena) return ok();
+  const char* why = "";
+  const qsa_status s = arena_destroy(arena, &why);
+  return s == QSA_OK ? ok() : fail(s, "%s: %s", fn, why);
+}
+
 // ------------------------------------------------------------------ step 5
 QSA_API qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t n_rows,
                          int32_t head_dim, void* out, qsa_dtype out_dtype, float* lse_out, void* stream) {

@@ -145,6 +145,15 @@ struct AppendParams {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 
+// ---------------------------------------------------------------- demand-mapped arena (qsa_arena.cu)
+qsa_status arena_create(int32_t device, uint64_t reserve_bytes, qsa_arena** out, const char** why);
+qsa_status arena_ensure(qsa_arena* a, uint64_t bytes, const char** why);
+qsa_status arena_destroy(qsa_arena* a, const char** why);
+void* arena_base(const qsa_arena* a);
+uint64_t arena_mapped(const qsa_arena* a);
+uint64_t arena_reserved(const qsa_arena* a);
+uint64_t arena_granularity(const qsa_arena* a);
+
 // ---------------------------------------------------------------- launchers
 cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64_t first_block,
                         int64_t n_blocks, float* pooled, int64_t pstride, cudaStream_t st);

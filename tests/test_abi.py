@@ -10,6 +10,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import indexed_sparse_attention_gb300 as qsa
 from indexed_sparse_attention_gb300 import build as qsa_build
@@ -146,6 +147,20 @@ def test_attn_validation(L):
     assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c16), FAKE, FAKE, FAKE, 512, FAKE, None, FAKE, need - 1,
                              None) == 4
     assert L.qsa_sparse_attn(seq, 1, ctypes.byref(c16), FAKE, FAKE, FAKE, 512, FAKE, None, None, 0, None) == 4
+
+
+def test_arena_validation(L):
+    h = ctypes.c_void_p()
+    assert L.qsa_arena_create(0, 1 << 20, None) == 1
+    assert L.qsa_arena_create(-1, 1 << 20, ctypes.byref(h)) == 1
+    assert L.qsa_arena_create(0, 0, ctypes.byref(h)) == 1
+    assert L.qsa_arena_ensure(None, 16) == 1
+    assert L.qsa_arena_destroy(None) == 0
+    assert L.qsa_arena_base(None) is None and L.qsa_arena_mapped(None) == 0
+    if not torch.cuda.is_available():
+        # No GPU here: creation fails with a status and a reason, not a crash.
+        assert L.qsa_arena_create(0, 1 << 20, ctypes.byref(h)) == 5
+        assert L.qsa_last_error().decode().startswith("qsa_arena_create:")
 
 
 def test_append_validation(L):

@@ -244,6 +244,94 @@ def test_layer_step_with_append_equals_prewritten_caches():
     assert torch.equal(k_c, x.k) and torch.equal(idx_c, x.idxk)
 
 
+# ------------------------------------------------------------------ demand-mapped arena
+def test_arena_grows_in_place():
+    a = qsa.Arena(1 << 30)
+    try:
+        base, g = a.base, a.granularity
+        assert base and a.mapped == 0 and a.reserved >= 1 << 30 and g > 0
+        a.ensure(5_000_000)
+        assert a.mapped >= 5_000_000 and a.mapped % g == 0
+        v = a.tensor(0, (5_000_000 // 4,), torch.float32)
+        v.copy_(torch.arange(v.numel(), device=dev(), dtype=torch.float32))
+        a.ensure(300 << 20)
+        assert a.base == base and a.mapped >= 300 << 20
+        assert torch.equal(a.tensor(0, (5_000_000 // 4,), torch.float32),
+                           torch.arange(5_000_000 // 4, device=dev(), dtype=torch.float32))
+        w = a.tensor(a.mapped - 4096, (1024,), torch.float32)
+        w.fill_(3.0)
+        assert float(w.sum()) == 3072.0
+        with pytest.raises(qsa.QSAError):
+            a.ensure(a.reserved + 1)
+    finally:
+        a.destroy()
+
+
+def test_arena_kv_cache_and_graph_survive_growth():
+    # K and V of each token interleaved in one arena ([token][K|V][head][D]),
+    # so the cache grows by mapping more of the same range; a CUDA graph
+    # captured over the arena replays unchanged after growth.
+    Hkv, D, cap = 2, 256, 16_384
+    tok_bytes = 2 * Hkv * D * 2
+    a = qsa.Arena(cap * tok_bytes)
+    try:
+        L1, L2, M = 6000, 12_000, 4
+        x = make_layer(L=L2, M=M, dtype=torch.bfloat16, seed=51, device=dev())
+        a.ensure(L1 * tok_bytes)
+
+        def kv_views(L):
+            t = a.tensor(0, (L, 2, Hkv, D), torch.bfloat16)
+            return t[:, 0].permute(1, 0, 2), t[:, 1].permute(1, 0, 2)   # [Hkv, L, D] views, tok stride 2*Hkv*D
+
+        def fill(t0, t1):
+            t = a.tensor(0, (t1, 2, Hkv, D), torch.bfloat16)
+            t[t0:t1, 0] = x.k[:, t0:t1].permute(1, 0, 2)
+            t[t0:t1, 1] = x.v[:, t0:t1].permute(1, 0, 2)
+
+        fill(0, L1)
+        x1 = make_layer(L=L1, M=M, dtype=torch.bfloat16, seed=51, device=dev())
+        sel, cnt, _ = _oracle_selection(x1)
+        seld, cntd = torch.from_numpy(sel).to(dev()), torch.from_numpy(cnt).to(dev())
+        q1 = x.q[:M].clone()
+        ka, va = kv_views(L1)
+        seqs1 = [qsa.Seq(L1, M, segments=[qsa.Segment(ka, va, 0)])]
+        out_a = torch.empty((M, 24, D), device=dev())
+        lse_a = torch.empty((M, 24), device=dev())
+        ref_o = torch.empty_like(out_a)
+        ref_l = torch.empty_like(lse_a)
+        qsa.sparse_attn([qsa.Seq(L1, M, segments=[qsa.Segment(x.k[:, :L1].contiguous(), x.v[:, :L1].contiguous(),
+                                                                0)])], q1, seld, cntd, ref_o, ref_l)
+        qsa.sparse_attn(seqs1, q1, seld, cntd, out_a, lse_a)   # eager once (kernel attributes)
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, ref_o) and torch.equal(lse_a, ref_l)
+        g = torch.cuda.CUDAGraph()
+        s_ = torch.cuda.Stream()
+        with torch.cuda.graph(g, stream=s_):
+            qsa.sparse_attn(seqs1, q1, seld, cntd, out_a, lse_a)
+        # Grow: map and write tokens L1 .. L2 - 1; the base stays, the graph replays.
+        base = a.base
+        a.ensure(L2 * tok_bytes)
+        fill(L1, L2)
+        assert a.base == base
+        out_a.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_a, ref_o) and torch.equal(lse_a, ref_l)
+        # The grown cache against the oracle.
+        sel2, cnt2, _ = _oracle_selection(x)
+        kb, vb = kv_views(L2)
+        out2, lse2 = torch.empty((M, 24, D), device=dev()), torch.empty((M, 24), device=dev())
+        qsa.sparse_attn([qsa.Seq(L2, M, segments=[qsa.Segment(kb, vb, 0)])], x.q,
+                        torch.from_numpy(sel2).to(dev()), torch.from_numpy(cnt2).to(dev()), out2, lse2)
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel2, cnt2)
+        assert_attn_close(to_np(out2), to_np(lse2), ref_out, ref_lse, True)
+        del ka, va, kb, vb
+    finally:
+        torch.cuda.synchronize()
+        a.destroy()
+
+
 # ------------------------------------------------------------------ steps 2 + 3 over key-axis chunks
 def _blocked_vs_one_pass(seqs, q_idx, block_keys, top_k=512):
     """Selections of the chunked path and of score_blocks + select_topk."""
