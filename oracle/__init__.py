@@ -78,6 +78,18 @@ def _load():
         lib.qsa_oracle_attn.restype = i32
         lib.qsa_oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
         lib.qsa_oracle_lse_merge.restype = i32
+        lib.qsa_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.qsa_oracle_e4m3_decode.restype = dbl
+        lib.qsa_oracle_e4m3_encode.argtypes = [dbl]
+        lib.qsa_oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.qsa_oracle_f16_decode.argtypes = [ctypes.c_uint16]
+        lib.qsa_oracle_f16_decode.restype = dbl
+        lib.qsa_oracle_f16_encode.argtypes = [dbl]
+        lib.qsa_oracle_f16_encode.restype = ctypes.c_uint16
+        lib.qsa_oracle_fp8_quantize.argtypes = [vp, i32, i64, i64, vp, vp]
+        lib.qsa_oracle_fp8_quantize.restype = i32
+        lib.qsa_oracle_fp8_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        lib.qsa_oracle_fp8_dequantize.restype = i32
         _lib = lib
     return _lib
 
@@ -232,3 +244,45 @@ def layer_step(q_idx, idxk, q, k, v, row_pos, top_k: int = TOP_K, scale: float |
     sel, cnt, tau = select(s, row_pos, top_k)
     out, lse = attn(q, k, v, row_pos, sel, cnt, scale=scale, visible=visible)
     return {"pooled": pooled, "scores": s, "sel": sel, "cnt": cnt, "tau": tau, "out": out, "lse": lse}
+
+
+# ---------------------------------------------------------------------- fp8 K/V state
+# hipfire, "QSA sparse attention and the VMM KV backend", section 02, table
+# "State formats": E4M3 K/V with an f16 scale per head and token (reading R9
+# in qsa_oracle.c: how a row is written).
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().qsa_oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().qsa_oracle_e4m3_encode(float(x)))
+
+
+def f16_decode(bits: int) -> float:
+    return float(_load().qsa_oracle_f16_decode(int(bits) & 0xFFFF))
+
+
+def f16_encode(x: float) -> int:
+    return int(_load().qsa_oracle_f16_encode(float(x)))
+
+
+def fp8_quantize(x):
+    """Rows [..., D] (fp32 / bf16 / fp64) -> (codes uint8 [..., D], f16 scale bits uint16 [...])."""
+    a, code = _stored(x)
+    D = a.shape[-1]
+    rows = a.size // D
+    codes = np.empty(a.shape, dtype=np.uint8)
+    scales = np.empty(a.shape[:-1], dtype=np.uint16)
+    _load().qsa_oracle_fp8_quantize(_ptr(a), code, rows, D, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def fp8_dequantize(codes, scales) -> np.ndarray:
+    """(codes uint8 [..., D], f16 scale bits uint16 [...]) -> values fp64 [..., D] (exact)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    s_ = np.ascontiguousarray(np.asarray(scales, dtype=np.uint16))
+    D = c.shape[-1]
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().qsa_oracle_fp8_dequantize(_ptr(c), _ptr(s_), c.size // D, D, _ptr(out))
+    return out

@@ -30,6 +30,14 @@
  *      default on the Python side); lse is a natural logarithm.
  *   R8 with KV segments, attention runs over the selected rows that some
  *      segment covers; a row with no such key has output 0 and lse -inf.
+ *   R9 the fp8 K/V state (hipfire section 02 table "State formats": E4M3
+ *      K/V plus an f16 scale per head and token): a stored element is the
+ *      E4M3 code times its row's scale.  E4M3 is sign, 4 exponent bits
+ *      (bias 7), 3 mantissa bits, subnormals below 2^-6, largest finite 448,
+ *      S.1111.111 NaN, no infinities.  Writing a row (the pages give no
+ *      recipe): scale = f16(f32(amax / 448)), code = the E4M3 value nearest
+ *      to f32(x / scale), ties to even, magnitudes above 448 saturated to
+ *      448; a row whose scale is 0 stores zeros.
  *
  * Arithmetic is IEEE fp64 throughout (built without -ffast-math).  Inputs
  * are read in their stored format (fp32, bf16 bit patterns or fp64) and
@@ -290,6 +298,108 @@ int qsa_oracle_lse_merge(const double* o_parts, const double* lse_parts, int64_t
     }
     for (int64_t d = 0; d < D; ++d) o[d] /= wsum;
     lse[i] = m + log(wsum);
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------- fp8 state (R9) */
+
+/* Value of an E4M3 code (NaN for S.1111.111). */
+double qsa_oracle_e4m3_decode(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);               /* subnormal: m * 2^-9 */
+  else
+    v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to a finite x (ties to even), saturated at +-448. */
+uint8_t qsa_oracle_e4m3_encode(double x) {
+  const uint8_t sign = x < 0 || (x == 0 && signbit(x)) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {                 /* subnormal range: a multiple of 2^-9 */
+    const double q = nearbyint(ldexp(a, 9)); /* 0 .. 8; 8 is the smallest normal */
+    return sign | (uint8_t)q;
+  }
+  int e;
+  frexp(a, &e);                              /* a = f * 2^e, f in [0.5, 1) */
+  e -= 1;                                    /* a = (1 + t) * 2^e, t in [0, 1) */
+  double mant = nearbyint((ldexp(a, -e) - 1.0) * 8.0);
+  if (mant == 8.0) {
+    mant = 0.0;
+    e += 1;
+  }
+  if (e > 8 || (e == 8 && mant > 6.0)) return sign | 0x7E;
+  return sign | (uint8_t)(((e + 7) << 3) | (int)mant);
+}
+
+/* binary16 bits -> double and double -> binary16 bits (nearest, ties to even). */
+double qsa_oracle_f16_decode(uint16_t h) {
+  const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (e == 31) v = m ? NAN : INFINITY;
+  else if (e == 0) v = ldexp((double)m, -24);
+  else v = ldexp(1.0 + m / 1024.0, e - 15);
+  return sign ? -v : v;
+}
+
+uint16_t qsa_oracle_f16_encode(double x) {
+  const uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (isnan(x)) return 0x7E00;
+  if (a < ldexp(1.0, -14)) {                 /* subnormal: multiples of 2^-24 */
+    const double q = nearbyint(ldexp(a, 24));
+    return sign | (uint16_t)q;               /* q = 1024 is the smallest normal */
+  }
+  int e;
+  frexp(a, &e);
+  e -= 1;
+  double mant = nearbyint((ldexp(a, -e) - 1.0) * 1024.0);
+  if (mant == 1024.0) {
+    mant = 0.0;
+    e += 1;
+  }
+  if (e > 15) return sign | 0x7C00;          /* overflow to infinity */
+  return sign | (uint16_t)(((e + 15) << 10) | (int)mant);
+}
+
+/*
+ * Write rows of an fp8 state (R9): x [rows, D] in its stored format ->
+ * codes [rows, D] and f16 scale bits [rows].  The scale and the quotient are
+ * rounded to binary32 before their final rounding, as a GPU computes them.
+ */
+int qsa_oracle_fp8_quantize(const void* x, int dtype, int64_t rows, int64_t D, uint8_t* codes, uint16_t* scales) {
+  for (int64_t r = 0; r < rows; ++r) {
+    double amax = 0.0;
+    for (int64_t d = 0; d < D; ++d) {
+      const double a = fabs(load_elem(x, dtype, r * D + d));
+      if (a > amax) amax = a;
+    }
+    const float s32 = (float)amax / 448.0f;          /* binary32 division (amax is exact in binary32) */
+    const uint16_t sh = qsa_oracle_f16_encode((double)s32);
+    scales[r] = sh;
+    const float sc = (float)qsa_oracle_f16_decode(sh);
+    for (int64_t d = 0; d < D; ++d) {
+      if (sc == 0.0f) {
+        codes[r * D + d] = 0;
+        continue;
+      }
+      const float q = (float)load_elem(x, dtype, r * D + d) / sc;   /* binary32 quotient */
+      codes[r * D + d] = qsa_oracle_e4m3_encode((double)q);
+    }
+  }
+  return 0;
+}
+
+/* Stored fp8 rows back to values: out[r, d] = decode(codes[r, d]) * f16(scales[r]), exact in fp64. */
+int qsa_oracle_fp8_dequantize(const uint8_t* codes, const uint16_t* scales, int64_t rows, int64_t D, double* out) {
+  for (int64_t r = 0; r < rows; ++r) {
+    const double sc = qsa_oracle_f16_decode(scales[r]);
+    for (int64_t d = 0; d < D; ++d) out[r * D + d] = qsa_oracle_e4m3_decode(codes[r * D + d]) * sc;
   }
   return 0;
 }

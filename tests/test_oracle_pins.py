@@ -344,3 +344,100 @@ def test_threads_do_not_change_results():
     oracle.set_threads(old)
     for key in ("scores", "sel", "cnt", "out", "lse"):
         np.testing.assert_array_equal(a[key], b[key])
+
+
+# ------------------------------------------------------------------ fp8 K/V state (E4M3 + f16 scale)
+_FINITE = [c for c in range(256) if c not in (0x7F, 0xFF)]
+
+
+def test_e4m3_decode_known_codes():
+    # Format facts: bias 7, 3 mantissa bits, subnormals m * 2^-9, 448 the
+    # largest finite value, S.1111.111 the only NaN.
+    assert oracle.e4m3_decode(0x00) == 0.0 and math.copysign(1, oracle.e4m3_decode(0x80)) < 0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9 and oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6
+    assert oracle.e4m3_decode(0x38) == 1.0 and oracle.e4m3_decode(0x3F) == 1.875
+    assert oracle.e4m3_decode(0x7E) == 448.0 and oracle.e4m3_decode(0xFE) == -448.0
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+    vals = sorted(oracle.e4m3_decode(c) for c in _FINITE if c < 0x80)
+    assert len(set(vals)) == 127 and vals[-1] == 448.0       # 127 distinct non-negative values
+
+
+def test_e4m3_encode_is_nearest_ties_to_even():
+    table = [(c, oracle.e4m3_decode(c)) for c in _FINITE]
+    for c, v in table:                                        # every finite code round-trips
+        if c != 0x80:
+            assert oracle.e4m3_encode(v) == c
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([rng.standard_normal(1500) * 40, rng.standard_normal(500) * 0.01,
+                         rng.uniform(-470, 470, 500)])
+    for x in xs:
+        c = oracle.e4m3_encode(x)
+        got = oracle.e4m3_decode(c)
+        target = max(-448.0, min(448.0, x))                   # saturation
+        best = min(abs(target - v) for _, v in table)
+        assert abs(target - got) == best, (x, c)
+        ties = [cc for cc, v in table if abs(target - v) == best and (v != 0 or cc == 0)]
+        if len(ties) > 1:                                     # a tie: the even mantissa
+            assert c & 1 == 0
+    # Exact halfway points.
+    assert oracle.e4m3_encode(1.0625) == 0x38 and oracle.e4m3_encode(1.1875) == 0x3A
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00 and oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02
+    assert oracle.e4m3_encode(1e6) == 0x7E and oracle.e4m3_encode(-1e6) == 0xFE
+
+
+def test_f16_codec_matches_numpy():
+    rng = np.random.default_rng(8)
+    xs = np.concatenate([rng.standard_normal(3000), rng.standard_normal(1000) * 1e-5,
+                         rng.standard_normal(500) * 3e4, [0.0, -0.0, 65504.0, 6.0e-8, 2.0 ** -24]])
+    for x in xs:
+        ref = int(np.array([x], dtype=np.float16).view(np.uint16)[0])
+        assert oracle.f16_encode(float(x)) == ref, x
+        assert oracle.f16_decode(ref) == float(np.array([ref], dtype=np.uint16).view(np.float16)[0])
+
+
+def test_fp8_quantize_rows():
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((6, 256)).astype(np.float32)
+    x[1] *= 1e-3
+    x[2] = 0.0                                                # a zero row: scale 0, zero codes
+    x[3, :] = np.arange(256, dtype=np.float32) * 0.5          # exact multiples
+    x[4, 17] = -1000.0                                        # amax from a negative element
+    codes, scales = oracle.fp8_quantize(x)
+    deq = oracle.fp8_dequantize(codes, scales)
+    for r in range(6):
+        amax = float(np.abs(x[r]).max())
+        s32 = np.float32(amax) / np.float32(448.0)
+        assert scales[r] == np.array([s32], dtype=np.float16).view(np.uint16)[0]
+        sc = float(np.array([scales[r]], dtype=np.uint16).view(np.float16)[0])
+        if sc == 0:
+            assert (codes[r] == 0).all() and (deq[r] == 0).all()
+            continue
+        for d in range(256):
+            qv = float(np.float32(x[r, d]) / np.float32(sc))
+            assert codes[r, d] == oracle.e4m3_encode(qv)
+        # Relative error of a stored element: at most half an E4M3 step (2^-4
+        # of the value) plus the f16 rounding of the scale, or a subnormal step.
+        err = np.abs(deq[r] - x[r])
+        assert (err <= np.abs(x[r]) * (2.0 ** -4 + 2.0 ** -10) + 2.0 ** -9 * sc * 1.01).all()
+    # The element of largest magnitude lands at or next to 448.
+    assert abs(oracle.e4m3_decode(codes[4, 17])) >= 416.0
+
+
+def test_fp8_attention_is_attention_on_the_stored_values():
+    # The oracle attends over fp8 state by dequantizing exactly; a row whose
+    # values are exactly representable gives the same result as bf16 state.
+    x = make_layer(L=600, M=2, seed=14, head_dim=64)
+    k = np.round(x.k.numpy() * 4) / 4                         # quarters in [-4, 4]: exact in E4M3 at scale 1/8
+    k = np.clip(k, -4, 4).astype(np.float32)
+    codes = np.vectorize(lambda v: oracle.e4m3_encode(v * 8))(k).astype(np.uint8)
+    scales = np.full(k.shape[:-1], oracle.f16_encode(0.125), dtype=np.uint16)
+    kd = oracle.fp8_dequantize(codes, scales)
+    np.testing.assert_array_equal(kd, k.astype(np.float64))
+    pooled = oracle.pool(x.idxk)
+    s = oracle.score(x.q_idx, pooled, x.row_pos)
+    sel, cnt, _ = oracle.select(s, x.row_pos)
+    v64 = x.v.numpy().astype(np.float64)
+    a = oracle.attn(x.q, kd, v64, x.row_pos, sel, cnt)
+    b = oracle.attn(x.q, k.astype(np.float64), v64, x.row_pos, sel, cnt)
+    np.testing.assert_array_equal(a[0], b[0])
