@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define QSA_VERSION 100            /* 1.0.0 */
+#define QSA_VERSION 110            /* 1.1.0 */
 #define QSA_INDEX_DIM 128          /* width of an index key and an index-query head */
 #define QSA_INDEX_HEADS 4          /* index-query heads per query row */
 #define QSA_BLOCK_TOKENS 4         /* tokens pooled into one block key */
@@ -75,7 +75,8 @@ typedef enum qsa_status {
 
 typedef enum qsa_dtype {
   QSA_F32 = 0,               /* IEEE binary32 */
-  QSA_BF16 = 1               /* bfloat16 */
+  QSA_BF16 = 1,              /* bfloat16 */
+  QSA_FP8_E4M3 = 2           /* K/V state only: E4M3 codes with per-(head, token) f16 scales */
 } qsa_dtype;
 
 /* One contiguous piece of a sequence's K/V cache (MTPLX pull request #610:
@@ -84,7 +85,13 @@ typedef enum qsa_dtype {
  * is at k[h * head_stride + t * tok_stride + d]; V likewise.  The segment
  * holds absolute tokens first_token .. first_token + n_tokens - 1.  Segments
  * of one sequence must not overlap; tokens no segment covers are not
- * attended. */
+ * attended.
+ * fp8 state (kv_dtype QSA_FP8_E4M3; hipfire, section 02, table "State
+ * formats": E4M3 K/V plus an f16 scale per head and token): k and v hold
+ * E4M3 codes (1 byte per element) and the value of an element is its code
+ * times the row's scale.  The two scales of (h, t) are adjacent f16 -- the
+ * K scale, then the V scale -- at kv_scale + 4 * (h * scale_head_stride +
+ * t * scale_tok_stride) bytes (a 4-byte aligned pair).  Unused otherwise. */
 typedef struct qsa_kv_segment {
   const void* k;             /* device, kv_dtype */
   const void* v;             /* device, kv_dtype */
@@ -92,6 +99,9 @@ typedef struct qsa_kv_segment {
   int64_t n_tokens;
   int64_t head_stride;       /* elements between KV heads */
   int64_t tok_stride;        /* elements between tokens, >= head_dim */
+  const void* kv_scale;      /* fp8 state: device f16 (K, V) scale pairs, 4-byte aligned */
+  int64_t scale_head_stride; /* fp8 state: pairs between KV heads */
+  int64_t scale_tok_stride;  /* fp8 state: pairs between tokens */
 } qsa_kv_segment;
 
 /* One sequence of a call (host struct). */
@@ -109,7 +119,7 @@ typedef struct qsa_attn_config {
   int32_t n_q_heads;         /* Hq, e.g. 24 */
   int32_t n_kv_heads;        /* Hkv, e.g. 2; Hq / Hkv must be <= 16 */
   int32_t head_dim;          /* 128 or 256 */
-  qsa_dtype q_dtype;         /* dtype of q; must equal kv_dtype */
+  qsa_dtype q_dtype;         /* dtype of q; kv_dtype, or bf16 with fp8 K/V */
   qsa_dtype kv_dtype;        /* dtype of every segment's K and V */
   qsa_dtype out_dtype;       /* dtype of out */
   float scale;               /* logit scale; 0 means 1/sqrt(head_dim) */
@@ -203,7 +213,11 @@ qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_
  *                  segments, pooled, pooled_stride
  *   cfg            n_kv_heads, head_dim, kv_dtype (other fields checked as
  *                  for qsa_sparse_attn)
- *   k_new, v_new   device [Hkv, n, D] kv_dtype, contiguous
+ *   k_new, v_new   device [Hkv, n, D] kv_dtype, contiguous; bf16 when kv_dtype
+ *                  is QSA_FP8_E4M3, and each (K or V, head, token) row is then
+ *                  written as the fp8 state: scale = f16(f32(amax / 448)),
+ *                  codes = the E4M3 values nearest to f32(x / scale), ties to
+ *                  even, saturated at 448 (0 codes when the scale is 0)
  *   idx_new        device [n, 128] idx_dtype, contiguous
  *   idx_keys       device index-key cache, [>= L, idx_tok_stride] idx_dtype
  * Errors: QSA_ERR_INVALID_ARG (a new token in no segment, null pointers,

@@ -23,7 +23,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqsa.so")
 
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2      # FP8: the E4M3 K/V state (codes + per-(head, token) f16 scales)
 INDEX_DIM = 128
 INDEX_HEADS = 4
 TOP_K = 512
@@ -45,7 +45,9 @@ class QSAError(RuntimeError):
 
 class KVSegment(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("first_token", ctypes.c_int64),
-                ("n_tokens", ctypes.c_int64), ("head_stride", ctypes.c_int64), ("tok_stride", ctypes.c_int64)]
+                ("n_tokens", ctypes.c_int64), ("head_stride", ctypes.c_int64), ("tok_stride", ctypes.c_int64),
+                ("kv_scale", ctypes.c_void_p), ("scale_head_stride", ctypes.c_int64),
+                ("scale_tok_stride", ctypes.c_int64)]
 
 
 class SeqDesc(ctypes.Structure):
@@ -137,6 +139,8 @@ def _dtype_code(t: torch.Tensor) -> int:
         return F32
     if t.dtype == torch.bfloat16:
         return BF16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):   # E4M3 codes
+        return FP8
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -153,10 +157,13 @@ def _ptr(t):
 @dataclasses.dataclass
 class Segment:
     """A contiguous run of one sequence's K/V cache: k, v are [Hkv, n, D]
-    views (channel stride 1) holding absolute tokens first_token .. +n-1."""
+    views (channel stride 1) holding absolute tokens first_token .. +n-1.
+    For the fp8 state, k and v hold E4M3 codes (float8_e4m3fn or uint8) and
+    kv_scale is an [Hkv, n, 2] float16 view of the (K, V) scale pairs."""
     k: torch.Tensor
     v: torch.Tensor
     first_token: int = 0
+    kv_scale: torch.Tensor | None = None
 
 
 @dataclasses.dataclass
@@ -197,6 +204,12 @@ def make_seq_array(seqs: Sequence[Seq]):
             sg.first_token = int(g.first_token)
             sg.n_tokens = int(g.k.shape[1])
             sg.head_stride, sg.tok_stride = int(g.k.stride(0)), int(g.k.stride(1))
+            if g.kv_scale is not None:
+                ks = g.kv_scale
+                if ks.dtype != torch.float16 or ks.shape[-1] != 2 or ks.stride(-1) != 1:
+                    raise TypeError("kv_scale must be a float16 [Hkv, n, 2] view of (K, V) scale pairs")
+                sg.kv_scale = ks.data_ptr()
+                sg.scale_head_stride, sg.scale_tok_stride = int(ks.stride(0)) // 2, int(ks.stride(1)) // 2
     return arr
 
 
@@ -272,9 +285,10 @@ def append_tokens(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: t
     if not (k_new.is_contiguous() and v_new.is_contiguous() and idx_new.is_contiguous()):
         raise ValueError("append_tokens: k_new, v_new and idx_new must be contiguous")
     arr = make_seq_array([seq])
-    if cfg is None:   # only the KV heads, head_dim and dtype matter here
-        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], _dtype_code(k_new), _dtype_code(k_new),
-                         F32, 0.0, 0)
+    if cfg is None:   # only the KV heads, head_dim and the caches' dtype matter here
+        kvd = _kv_dtype([seq])
+        kvd = _dtype_code(k_new) if kvd is None else kvd
+        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], BF16 if kvd == FP8 else kvd, kvd, F32, 0.0, 0)
     idxk = seq.idx_keys
     _check("qsa_append_tokens", lib().qsa_append_tokens(
         arr, ctypes.byref(cfg), k_new.data_ptr(), v_new.data_ptr(), idx_new.data_ptr(), idxk.data_ptr(),
@@ -359,11 +373,21 @@ def score_select_topk_blocked(seqs, q_idx: torch.Tensor, sel: torch.Tensor, cnt:
         cnt.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)))
 
 
-def attn_config(q: torch.Tensor, n_kv_heads: int, out_dtype=None, scale: float = 0.0, n_splits: int = 0):
+def _kv_dtype(seqs):
+    """The K/V dtype code of the first segment (None without segments)."""
+    for sq in seqs or ():
+        for g in sq.segments:
+            return _dtype_code(g.k)
+    return None
+
+
+def attn_config(q: torch.Tensor, n_kv_heads: int, out_dtype=None, scale: float = 0.0, n_splits: int = 0,
+                kv_dtype: int | None = None):
     cfg = AttnConfig()
     cfg.n_q_heads, cfg.head_dim = q.shape[1], q.shape[2]
     cfg.n_kv_heads = n_kv_heads
-    cfg.q_dtype = cfg.kv_dtype = _dtype_code(q)
+    cfg.q_dtype = _dtype_code(q)
+    cfg.kv_dtype = cfg.q_dtype if kv_dtype is None else kv_dtype
     cfg.out_dtype = _dtype_code(torch.empty(0, dtype=out_dtype)) if out_dtype is not None else F32
     cfg.scale = float(scale)
     cfg.n_splits = int(n_splits)
@@ -381,7 +405,7 @@ def sparse_attn(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, out
     """Step 4 (+ the internal step-5 merge of its splits)."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     if cfg is None:
-        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
+        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits, kv_dtype=_kv_dtype(seqs))
     need = lib().qsa_attn_workspace_size(arr, len(arr), ctypes.byref(cfg), sel.stride(0))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -398,7 +422,7 @@ def sparse_attn_noalloc(seqs, q: torch.Tensor, sel: torch.Tensor, cnt: torch.Ten
     own static scratch array is used (see qsa_sparse_attn_noalloc in qsa.h)."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     if cfg is None:
-        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits)
+        cfg = attn_config(q, n_kv_heads, out.dtype, scale, n_splits, kv_dtype=_kv_dtype(seqs))
     _check("qsa_sparse_attn_noalloc", lib().qsa_sparse_attn_noalloc(
         arr, len(arr), ctypes.byref(cfg), q.data_ptr(), sel.data_ptr(), cnt.data_ptr(), sel.stride(0),
         out.data_ptr(), _ptr(lse), _stream(stream)))
@@ -443,7 +467,7 @@ class LayerStep:
         self.ld = max(1, max(s.n_tokens // 4 for s in self.seqs))
         self.ld = (self.ld + 3) // 4 * 4
         self.arr = make_seq_array(self.seqs)
-        self.cfg = attn_config(q, n_kv_heads, out_dtype, scale, n_splits)
+        self.cfg = attn_config(q, n_kv_heads, out_dtype, scale, n_splits, kv_dtype=_kv_dtype(self.seqs))
         self.scores = torch.empty((rows, self.ld), dtype=torch.float32, device=dev)
         gld = max(1, max(n_groups(s.n_tokens) for s in self.seqs))
         self.group_max = torch.empty((rows, (gld + 3) // 4 * 4), dtype=torch.float32, device=dev)

@@ -24,6 +24,8 @@
 
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
 #include "qsa_attn_common.cuh"
 
 namespace qsa {
@@ -108,27 +110,43 @@ constexpr int kPStride = 40;   // bf16 per P row: 80-byte rows keep ldmatrix con
 constexpr int kSStride = kTT + 4;
 constexpr int kAttnThreads = 256;
 
-template <int D, int STAGES>
+// F8: fp8 state -- each stage holds the E4M3 codes (1 byte per element) and
+// one (K, V) scale pair per token; the stage being consumed is converted to
+// bf16 into one tile of the bf16 layout before the MMAs.
+template <int D, int STAGES, bool F8 = false>
 struct MmaSmem {
-  static constexpr int CH = D / 8;                     // 16-byte chunks per K/V/Q row
+  static constexpr int CH = D / 8;                     // 16-byte chunks per bf16 K/V/Q row
   static constexpr size_t q = 16 * D * 2;
-  static constexpr size_t kv_tile = kTT * D * 2;       // one K or V tile
+  static constexpr size_t kv_tile = kTT * D * (F8 ? 1 : 2);   // one K or V tile as gathered
   static constexpr size_t s = 2 * 16 * kSStride * 4;   // logits, one plane per channel half
   static constexpr size_t pm = 16 * kPStride * 2;
   static constexpr size_t off_kv = q;                  // [STAGES][K tile, V tile]
-  static constexpr size_t off_s = off_kv + STAGES * 2 * kv_tile;
+  static constexpr size_t off_bf = off_kv + STAGES * 2 * kv_tile;   // fp8: the converted K, V tile
+  static constexpr size_t off_s = off_bf + (F8 ? 2 * kTT * D * 2 : 0);
   static constexpr size_t off_p = off_s + s;
   static constexpr size_t off_m = off_p + pm;          // m, l, alpha: 3 x 16 floats
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
-  static constexpr size_t off_ids = off_valid + STAGES * kTT * 4;
+  static constexpr size_t off_sc = off_valid + STAGES * kTT * 4;   // fp8: scale pairs per stage
+  static constexpr size_t off_ids = off_sc + (F8 ? STAGES * kTT * 4 : 0);
   static constexpr size_t bytes = off_ids + kIdCache * 4;
   // Three stages keep two CTAs per SM (228 KB per SM, 1 KB reserved per CTA).
   static_assert(STAGES != 3 || 2 * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
-template <int D, int STAGES, int NSEQ>
+// Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly:
+// E4M3 -> f16 -> f32 -> bf16 loses nothing (4 significant bits, exponents
+// 2^-9 .. 2^8).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+template <int D, int STAGES, int NSEQ, bool F8 = false>
 __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_kernel(const AttnParams<NSEQ> p) {
-  using L = MmaSmem<D, STAGES>;
+  using L = MmaSmem<D, STAGES, F8>;
   constexpr int CH = L::CH;
   constexpr int KH = D / 32;   // k-steps (16 channels each) per channel half
   constexpr int NTD = D / 64;  // 8-channel n-tiles per warp in P.V
@@ -142,6 +160,9 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   float* a_s = m_s + 32;
   int* valid_s = reinterpret_cast<int*>(smem + L::off_valid);
   int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L::off_ids);
+  uint8_t* kv8_s = smem + L::off_kv;                                        // fp8 stages
+  __nv_bfloat16* kvb_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_bf);   // fp8: converted tile
+  uint32_t* sc_s = reinterpret_cast<uint32_t*>(smem + L::off_sc);           // fp8: scale pairs
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quarter = warp & 3, half = warp >> 2;
@@ -177,8 +198,30 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
     const int tk = tid >> 3, q8 = tid & 7;
     const int64_t i = i0 + (int64_t)it * kTT + tk;
     int seg = 0;
-    int64_t off = 0;
-    const bool ok = i < i1 && locate(p, c, ic, i, g, seg, off);
+    int64_t off = 0, tseg = 0;
+    const bool ok = i < i1 && locate(p, c, ic, i, g, seg, off, &tseg);
+    if constexpr (F8) {
+      // Codes of the token's K and V rows (D bytes each) into the stage, row
+      // after row; the (K, V) scale pair of (head g, token) beside them.
+      const uint8_t* ks = ok ? static_cast<const uint8_t*>(p.seg[seg].k) + off : static_cast<const uint8_t*>(p.q);
+      const uint8_t* vs = ok ? static_cast<const uint8_t*>(p.seg[seg].v) + off : static_cast<const uint8_t*>(p.q);
+      uint8_t* kd = kv8_s + (size_t)stage * 2 * L::kv_tile + tk * D;
+      uint8_t* vd = kd + L::kv_tile;
+#pragma unroll
+      for (int j = 0; j < D / 128; ++j) {
+        const int ch = 8 * j + q8;
+        cp_async16(kd + ch * 16, ks + (ok ? ch * 16 : 0), ok);
+        cp_async16(vd + ch * 16, vs + (ok ? ch * 16 : 0), ok);
+      }
+      if (q8 == 0) {
+        const uint32_t* sp = ok ? p.seg[seg].kv_scale + (int64_t)g * p.seg[seg].s_head_stride +
+                                      tseg * p.seg[seg].s_tok_stride
+                                : reinterpret_cast<const uint32_t*>(p.q);
+        cp_async4(sc_s + stage * kTT + tk, sp, ok);
+        valid_s[stage * kTT + tk] = ok ? 1 : 0;
+      }
+      return;
+    }
     const __nv_bfloat16* ks = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].k) + off : qg;
     const __nv_bfloat16* vs = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].v) + off : qg;
     __nv_bfloat16* kd = kv_s + (size_t)stage * 2 * kTT * D + tk * D;
@@ -244,6 +287,26 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
       cp_async_commit();
     }
     const __nv_bfloat16* kt = kv_s + (size_t)stage * 2 * kTT * D;
+    if constexpr (F8) {
+      // Codes -> bf16 into the swizzled layout the MMAs read: output chunk ch
+      // (8 elements) of row tk sits at chunk ch ^ (tk & 7).
+      const uint8_t* src = kv8_s + (size_t)stage * 2 * L::kv_tile;
+#pragma unroll
+      for (int k = 0; k < 2 * kTT * CH / kAttnThreads; ++k) {
+        const int job = tid + k * kAttnThreads;
+        const int kv = job / (kTT * CH), rem = job % (kTT * CH);
+        const int tk = rem / CH, ch = rem % CH;
+        const uint2 w = *reinterpret_cast<const uint2*>(src + kv * L::kv_tile + tk * D + ch * 8);
+        uint4 o;
+        o.x = e4m3x2_to_bf16x2(w.x & 0xffffu);
+        o.y = e4m3x2_to_bf16x2(w.x >> 16);
+        o.z = e4m3x2_to_bf16x2(w.y & 0xffffu);
+        o.w = e4m3x2_to_bf16x2(w.y >> 16);
+        *reinterpret_cast<uint4*>(kvb_s + (size_t)kv * kTT * D + (tk * CH + (ch ^ (tk & 7))) * 8) = o;
+      }
+      __syncthreads();
+      kt = kvb_s;
+    }
     const __nv_bfloat16* vt = kt + kTT * D;
     // Partial logits of tokens 8*quarter.. over this warp's channel half, two chains.
     {
@@ -266,6 +329,12 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
     // Online softmax of rows warp and warp+8 (base-2 logits), one lane per token.
     {
       const bool valid = valid_s[stage * kTT + lane] != 0;
+      float kscale = 1.f, vscale = 1.f;
+      if constexpr (F8) {
+        const uint32_t pr = sc_s[stage * kTT + lane];
+        kscale = __half2float(__ushort_as_half((unsigned short)(pr & 0xffffu)));
+        vscale = __half2float(__ushort_as_half((unsigned short)(pr >> 16)));
+      }
       float z[2], mo[2], mx[2];
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -274,7 +343,7 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
         mo[j] = -INFINITY;
         if (rr < G) {
           const float s0 = s_s[rr * kSStride + lane] + s_s[16 * kSStride + rr * kSStride + lane];
-          z[j] = valid ? s0 * zscale : -INFINITY;
+          z[j] = valid ? s0 * kscale * zscale : -INFINITY;
           mo[j] = m_s[rr];
         }
         mx[j] = z[j];
@@ -301,7 +370,7 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
       for (int j = 0; j < 2; ++j) {
         const int rr = warp + 8 * j;
         if (rr < G) {
-          p_s[rr * kPStride + lane] = __float2bfloat16(pz[j]);
+          p_s[rr * kPStride + lane] = __float2bfloat16(F8 ? pz[j] * vscale : pz[j]);
           if (lane == 0) {
             const float alpha = mo[j] == -INFINITY ? 0.f : exp2f(mo[j] - mx[j]);
             a_s[rr] = alpha;
@@ -691,6 +760,20 @@ cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_row
 template <int NSEQ>
 cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
+  if (kv_dtype == QSA_FP8_E4M3) {
+    if (p.head_dim == 256) {
+      if (stages == 2)
+        return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ, true>, p, n_rows, kAttnThreads,
+                                  MmaSmem<256, 2, true>::bytes, st);
+      return launch_attn_kernel(attn_mma_kernel<256, 3, NSEQ, true>, p, n_rows, kAttnThreads,
+                                MmaSmem<256, 3, true>::bytes, st);
+    }
+    if (stages == 2)
+      return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ, true>, p, n_rows, kAttnThreads,
+                                MmaSmem<128, 2, true>::bytes, st);
+    return launch_attn_kernel(attn_mma_kernel<128, 3, NSEQ, true>, p, n_rows, kAttnThreads,
+                              MmaSmem<128, 3, true>::bytes, st);
+  }
   if (kv_dtype == QSA_BF16) {
     if (p.head_dim == 256) {
       if (stages == 2)

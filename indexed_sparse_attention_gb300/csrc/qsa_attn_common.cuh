@@ -77,7 +77,7 @@ struct IdCache {
 // block id or a token no segment covers.
 template <int NSEQ>
 __device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& c, const IdCache& ic, int64_t i,
-                                       int g, int& seg, int64_t& off) {
+                                       int g, int& seg, int64_t& off, int64_t* tok_in_seg = nullptr) {
   int64_t t;
   if (i >= c.n_list) return false;
   if (i < 4 * (int64_t)c.cnt) {
@@ -93,6 +93,7 @@ __device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& 
     if (t >= sg.first && t < sg.first + sg.n) {
       seg = c.seg_begin + s;
       off = (int64_t)g * sg.head_stride + (t - sg.first) * sg.tok_stride;
+      if (tok_in_seg) *tok_in_seg = t - sg.first;
       return true;
     }
   }
@@ -119,6 +120,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(dst)), "l"(src),
                "r"(valid ? 16 : 0));
+}
+// 4-byte copy (zero-filled when !valid); src and dst 4-byte aligned.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 4 : 0));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>

@@ -79,6 +79,9 @@ struct Segment {
   int64_t n;
   int64_t head_stride;
   int64_t tok_stride;
+  const uint32_t* kv_scale;    // fp8 state: (K, V) f16 scale pairs
+  int64_t s_head_stride;       // pairs
+  int64_t s_tok_stride;
 };
 
 struct AttnSeq {
@@ -118,12 +121,16 @@ struct AppendSeg {
   void* k;
   void* v;
   int64_t first, n, head_stride, tok_stride;   // elements
+  void* kv_scale;                              // fp8 state: (K, V) f16 scale pairs
+  int64_t s_head_stride, s_tok_stride;         // pairs
 };
 
 struct AppendParams {
   AppendSeg seg[QSA_MAX_SEGMENTS];
   int32_t n_segs;
   int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t fp8;               // the caches hold the fp8 state; k_new / v_new are bf16
   int64_t n_tokens;          // L after the append
   int64_t n_new;             // tokens L - n_new .. L - 1 are appended
   const void* k_new;         // [Hkv, n_new, D]

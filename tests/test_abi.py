@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.qsa_version() == 100
+    assert L.qsa_version() == 110
     for code, name in qsa.STATUS.items():
         assert L.qsa_status_string(code).decode() == name
     assert L.qsa_status_string(99).decode() == "QSA_ERR_UNKNOWN"

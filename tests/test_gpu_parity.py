@@ -244,6 +244,110 @@ def test_layer_step_with_append_equals_prewritten_caches():
     assert torch.equal(k_c, x.k) and torch.equal(idx_c, x.idxk)
 
 
+# ------------------------------------------------------------------ fp8 K/V state (E4M3 codes + f16 scales)
+def _fp8_state(shape, seed):
+    """Seeded E4M3 codes with exponents 2^-4 .. 2^2 and random signs/mantissas,
+    and f16 (K, V) scale pairs 2^-4 .. 2^-1 per head and token: values of
+    magnitude ~0.5 and at most ~4, like N(0, 1) K/V written as fp8."""
+    g = torch.Generator().manual_seed(seed)
+    Hkv, L, D = shape
+    e = torch.randint(3, 10, (2, Hkv, L, D), generator=g)
+    m = torch.randint(0, 8, (2, Hkv, L, D), generator=g)
+    sgn = torch.randint(0, 2, (2, Hkv, L, D), generator=g)
+    codes = ((sgn << 7) | (e << 3) | m).to(torch.uint8)
+    expo = torch.randint(-4, -1, (Hkv, L, 2), generator=g).double()
+    frac = 1 + torch.randint(0, 1024, (Hkv, L, 2), generator=g).double() / 1024
+    scales = (frac * torch.pow(2.0, expo)).to(torch.float16)
+    return codes[0], codes[1], scales
+
+
+def _fp8_ref(kc, vc, scales):
+    sb = scales.view(torch.int16).numpy().view(np.uint16)
+    return oracle.fp8_dequantize(kc.numpy(), sb[..., 0]), oracle.fp8_dequantize(vc.numpy(), sb[..., 1])
+
+
+@pytest.mark.parametrize("L,M,D,n_splits", [(4099, 4, 256, 0), (9001, 1, 256, 0), (9001, 3, 128, 5),
+                                            (2051, 4, 256, 1), (1200, 600, 256, 0)])
+def test_fp8_attention_matches_oracle(L, M, D, n_splits):
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + D, head_dim=D)
+    kc, vc, scales = _fp8_state((2, L, D), seed=L + M)
+    sel, cnt, _ = _oracle_selection(x)
+    kd, vd = _fp8_ref(kc, vc, scales)
+    ref_out, ref_lse = oracle.attn(x.q, kd, vd, x.row_pos, sel, cnt)
+    seg = [qsa.Segment(kc.to(dev()), vc.to(dev()), 0, kv_scale=scales.to(dev()))]
+    out, lse = _attn_gpu(x, sel, cnt, segments=lambda k, v: seg, n_splits=n_splits)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+def test_fp8_segments_equal_single_buffer():
+    L, M, D = 9001, 4, 256
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=61, head_dim=D)
+    kc, vc, scales = _fp8_state((2, L, D), seed=62)
+    kc, vc, scales = kc.to(dev()), vc.to(dev()), scales.to(dev())
+    sel, cnt, _ = _oracle_selection(x)
+    single, single_lse = _attn_gpu(x, sel, cnt,
+                                   segments=lambda k, v: [qsa.Segment(kc, vc, 0, kv_scale=scales)])
+    cuts = segment_cuts(L, 6, seed=4)
+    segs = [qsa.Segment(kc[:, f:f + n].clone(), vc[:, f:f + n].clone(), f, kv_scale=scales[:, f:f + n].clone())
+            for f, n in cuts]
+    out, lse = _attn_gpu(x, sel, cnt, segments=lambda k, v: segs)
+    np.testing.assert_allclose(out, single, atol=2e-3)
+    kd, vd = _fp8_ref(kc.cpu(), vc.cpu(), scales.cpu())
+    ref_out, ref_lse = oracle.attn(x.q, kd, vd, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+@pytest.mark.parametrize("D", [256, 128])
+def test_fp8_append_quantizes_like_oracle(D):
+    L, n = 5003, 40
+    x = make_layer(L=L, M=n, dtype=torch.bfloat16, seed=63, head_dim=D, device=dev())
+    x.k[0, L - 3] = 0.0                                  # a zero row: scale 0, codes 0
+    x.v[1, L - 2, 5] = 1000.0                            # a large element
+    kc = torch.zeros((2, L, D), dtype=torch.uint8, device=dev())
+    vc = torch.zeros_like(kc)
+    scales = torch.zeros((2, L, 2), dtype=torch.float16, device=dev())
+    idx_c = x.idxk.clone()
+    pooled = pooled_buffer(L, dev())
+    qsa.pool_index_keys(idx_c, pooled, 0, (L - n) // 4)
+    seq = qsa.Seq(L, n, pooled, [qsa.Segment(kc, vc, 0, kv_scale=scales)], idx_keys=idx_c)
+    qsa.append_tokens(seq, x.k[:, L - n:].contiguous(), x.v[:, L - n:].contiguous(), x.idxk[L - n:].contiguous())
+    torch.cuda.synchronize()
+    for which, src, codes in ((0, x.k, kc), (1, x.v, vc)):
+        ref_c, ref_s = oracle.fp8_quantize(src[:, L - n:].cpu())
+        np.testing.assert_array_equal(to_np(codes[:, L - n:]), ref_c)
+        np.testing.assert_array_equal(to_np(scales[:, L - n:, which].view(torch.int16)).view(np.uint16), ref_s)
+        assert (to_np(codes[:, :L - n]) == 0).all()        # earlier tokens untouched
+    assert (to_np(kc[0, L - 3]) == 0).all() and float(scales[0, L - 3, 0]) == 0.0
+
+
+def test_fp8_layer_step_matches_oracle():
+    # A verify step over fp8 K/V written by the append, against the oracle's
+    # quantization of the same rows and attention over its dequantized state.
+    L, M = 9001, 4
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=64, device=dev())
+    rows_k, rows_s = oracle.fp8_quantize(x.k.cpu())
+    rows_v, rows_sv = oracle.fp8_quantize(x.v.cpu())
+    kc = torch.from_numpy(rows_k).to(dev())
+    vc = torch.from_numpy(rows_v).to(dev())
+    sc = torch.from_numpy(np.stack([rows_s, rows_sv], axis=-1).view(np.float16).copy()).to(dev())
+    kc[:, L - M:] = 0
+    vc[:, L - M:] = 0
+    pooled = pooled_buffer(L, dev())
+    qsa.pool_index_keys(x.idxk, pooled, 0, (L - M) // 4)
+    step = qsa.LayerStep([qsa.Seq(L, M, pooled, [qsa.Segment(kc, vc, 0, kv_scale=sc)], idx_keys=x.idxk)],
+                         x.q_idx, x.q)
+    step.run(new_tokens=[(x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(),
+                          x.idxk[L - M:].contiguous())])
+    torch.cuda.synchronize()
+    ref = oracle_layer(x)
+    kd = oracle.fp8_dequantize(rows_k, rows_s)
+    vd = oracle.fp8_dequantize(rows_v, rows_sv)
+    sel, cnt = to_np(step.sel), to_np(step.cnt)
+    assert_selection_close(sel, cnt, ref["sel"], ref["cnt"], ref["tau"], ref["scores"], x.row_pos)
+    ref_out, ref_lse = oracle.attn(x.q.cpu(), kd, vd, x.row_pos, sel, cnt)
+    assert_attn_close(to_np(step.out), to_np(step.lse), ref_out, ref_lse, True)
+
+
 # ------------------------------------------------------------------ demand-mapped arena
 def test_arena_grows_in_place():
     a = qsa.Arena(1 << 30)
