@@ -418,30 +418,54 @@ def main():
     # device into the caches, the layer chain runs, outputs come back.
     M = spec["M"]
     L = spec["L"]
-    # The new rows' K, V and index keys arrive as contiguous tensors (what a
-    # model produces) and qsa_append_tokens writes them into the caches and
-    # pools the blocks they complete.
-    h2d_items, d2h_items, new_tokens = [], [], []
+    # Per step, every layer's inputs -- q, index queries and the new rows'
+    # K, V and index keys (contiguous, as a model produces them) -- arrive in
+    # one pinned host buffer and cross in one copy; qsa_append_tokens writes
+    # the new rows into the caches and pools the blocks they complete; every
+    # layer's out and lse come back in one copy.
+    def packed(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        return offs, n
+
+    per_layer = []
     for l in layers:
         x = l.x
-        staged = [x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(), x.idxk[L - M:].contiguous()]
-        new_tokens.append([tuple(staged)])
-        for t in [x.q, x.q_idx] + staged:
-            h2d_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
-        for t in (l.step.out, l.step.lse):
-            d2h_items.append((t, torch.empty(t.shape, dtype=t.dtype).pin_memory()))
-    for d, h in h2d_items:
-        h.copy_(d.cpu())
-    h2d = sum(h.numel() * h.element_size() for _, h in h2d_items)
-    d2h = sum(h.numel() * h.element_size() for _, h in d2h_items)
+        per_layer.append([x.q, x.q_idx, x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(),
+                          x.idxk[L - M:].contiguous()])
+    flat_in = [t for ts in per_layer for t in ts]
+    in_offs, in_bytes = packed(flat_in)
+    stage_d = torch.empty(in_bytes, dtype=torch.uint8, device=dev)
+    stage_h = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+
+    def view(buf, off, t):
+        n = t.numel() * t.element_size()
+        return buf[off:off + n].view(t.dtype).view(t.shape)
+
+    for off, t in zip(in_offs, flat_in):
+        view(stage_h, off, t).copy_(t.cpu())
+    out_shapes = [(l.step.out, l.step.lse) for l in layers]
+    flat_out = [t for pair in out_shapes for t in pair]
+    out_offs, out_bytes = packed(flat_out)
+    out_d = torch.empty(out_bytes, dtype=torch.uint8, device=dev)
+    out_h = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    e2e_layers = []
+    for i, l in enumerate(layers):
+        q_v, qi_v, k_v, v_v, idx_v = (view(stage_d, in_offs[5 * i + j], per_layer[i][j]) for j in range(5))
+        st = qsa.LayerStep([l.seq], qi_v, q_v, out_dtype=torch.float32)
+        st.out = view(out_d, out_offs[2 * i], l.step.out)
+        st.lse = view(out_d, out_offs[2 * i + 1], l.step.lse)
+        e2e_layers.append((st, [(k_v, v_v, idx_v)]))
+    h2d = sum(t.numel() * t.element_size() for t in flat_in)
+    d2h = sum(t.numel() * t.element_size() for t in flat_out)
 
     def e2e_step():
-        for d, h in h2d_items:
-            d.copy_(h, non_blocking=True)
-        for l, nt in zip(layers, new_tokens):
-            l.step.run(new_tokens=nt)
-        for d, h in d2h_items:
-            h.copy_(d, non_blocking=True)
+        stage_d.copy_(stage_h, non_blocking=True)
+        for st, nt in e2e_layers:
+            st.run(new_tokens=nt)
+        out_h.copy_(out_d, non_blocking=True)
 
     # The step as an application would replay it: one CUDA graph holding the
     # pinned host -> device copies, the layer chain through the public API and
@@ -549,10 +573,10 @@ def main():
         **({"roofline_scoring": roofline_scoring} if roofline_scoring else {}),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "mode": "one CUDA graph per step: pinned host->device copies of every layer's q, index queries "
-                        "and new K/V/index-key rows, then per layer qsa_append_tokens (cache write + pooling) and "
-                        "the layer chain through LayerStep (the C ABI), device->host copies of every layer's out "
-                        "and lse"},
+                "mode": "one CUDA graph per step: one pinned host->device copy of every layer's q, index "
+                        "queries and new K/V/index-key rows, per layer qsa_append_tokens (cache write + pooling) "
+                        "and the layer chain through LayerStep (the C ABI), one device->host copy of every "
+                        "layer's out and lse"},
         "gpu_launches": launches,
         "us_per_launch_by_step": kernel_us,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},
