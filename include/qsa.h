@@ -76,7 +76,8 @@ typedef enum qsa_status {
 typedef enum qsa_dtype {
   QSA_F32 = 0,               /* IEEE binary32 */
   QSA_BF16 = 1,              /* bfloat16 */
-  QSA_FP8_E4M3 = 2           /* K/V state only: E4M3 codes with per-(head, token) f16 scales */
+  QSA_FP8_E4M3 = 2,          /* K/V state only: E4M3 codes with per-(head, token) f16 scales */
+  QSA_Q8_0 = 3               /* K/V state only: int8 codes with an f16 scale per 32 elements */
 } qsa_dtype;
 
 /* One contiguous piece of a sequence's K/V cache (MTPLX pull request #610:
@@ -86,12 +87,17 @@ typedef enum qsa_dtype {
  * holds absolute tokens first_token .. first_token + n_tokens - 1.  Segments
  * of one sequence must not overlap; tokens no segment covers are not
  * attended.
- * fp8 state (kv_dtype QSA_FP8_E4M3; hipfire, section 02, table "State
- * formats": E4M3 K/V plus an f16 scale per head and token): k and v hold
- * E4M3 codes (1 byte per element) and the value of an element is its code
- * times the row's scale.  The two scales of (h, t) are adjacent f16 -- the
- * K scale, then the V scale -- at kv_scale + 4 * (h * scale_head_stride +
- * t * scale_tok_stride) bytes (a 4-byte aligned pair).  Unused otherwise. */
+ * Quantized state (hipfire, section 02, table "State formats"): k and v hold
+ * 1-byte codes with the element layout above, and the scales of (h, t) form
+ * one record at kv_scale + R * (h * scale_head_stride + t * scale_tok_stride)
+ * bytes:
+ *   QSA_FP8_E4M3  E4M3 codes, value = code * scale of the row; the record is
+ *                 the K row's f16 scale then the V row's (R = 4, 4-byte
+ *                 aligned);
+ *   QSA_Q8_0      int8 codes, value = code * scale of its block of 32
+ *                 elements; the record is the K row's D/32 f16 block scales
+ *                 then the V row's (R = D/8 bytes, 16-byte aligned).
+ * Unused for f32 / bf16 state. */
 typedef struct qsa_kv_segment {
   const void* k;             /* device, kv_dtype */
   const void* v;             /* device, kv_dtype */
@@ -99,9 +105,9 @@ typedef struct qsa_kv_segment {
   int64_t n_tokens;
   int64_t head_stride;       /* elements between KV heads */
   int64_t tok_stride;        /* elements between tokens, >= head_dim */
-  const void* kv_scale;      /* fp8 state: device f16 (K, V) scale pairs, 4-byte aligned */
-  int64_t scale_head_stride; /* fp8 state: pairs between KV heads */
-  int64_t scale_tok_stride;  /* fp8 state: pairs between tokens */
+  const void* kv_scale;      /* quantized state: device scale records */
+  int64_t scale_head_stride; /* quantized state: records between KV heads */
+  int64_t scale_tok_stride;  /* quantized state: records between tokens */
 } qsa_kv_segment;
 
 /* One sequence of a call (host struct). */
@@ -119,7 +125,7 @@ typedef struct qsa_attn_config {
   int32_t n_q_heads;         /* Hq, e.g. 24 */
   int32_t n_kv_heads;        /* Hkv, e.g. 2; Hq / Hkv must be <= 16 */
   int32_t head_dim;          /* 128 or 256 */
-  qsa_dtype q_dtype;         /* dtype of q; kv_dtype, or bf16 with fp8 K/V */
+  qsa_dtype q_dtype;         /* dtype of q; kv_dtype, or bf16 with quantized K/V */
   qsa_dtype kv_dtype;        /* dtype of every segment's K and V */
   qsa_dtype out_dtype;       /* dtype of out */
   float scale;               /* logit scale; 0 means 1/sqrt(head_dim) */
@@ -213,11 +219,14 @@ qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_
  *                  segments, pooled, pooled_stride
  *   cfg            n_kv_heads, head_dim, kv_dtype (other fields checked as
  *                  for qsa_sparse_attn)
- *   k_new, v_new   device [Hkv, n, D] kv_dtype, contiguous; bf16 when kv_dtype
- *                  is QSA_FP8_E4M3, and each (K or V, head, token) row is then
- *                  written as the fp8 state: scale = f16(f32(amax / 448)),
- *                  codes = the E4M3 values nearest to f32(x / scale), ties to
- *                  even, saturated at 448 (0 codes when the scale is 0)
+ *   k_new, v_new   device [Hkv, n, D] kv_dtype, contiguous; bf16 when the
+ *                  state is quantized, and each (K or V, head, token) row is
+ *                  then written in it: QSA_FP8_E4M3 -- scale = f16(f32(amax /
+ *                  448)), codes = the E4M3 values nearest to f32(x / scale),
+ *                  ties to even, saturated at 448; QSA_Q8_0 -- per block of
+ *                  32, scale = f16(f32(amax / 127)), codes = the integers
+ *                  nearest to f32(x / scale), halves away from zero, within
+ *                  +-127 (0 codes where a scale is 0)
  *   idx_new        device [n, 128] idx_dtype, contiguous
  *   idx_keys       device index-key cache, [>= L, idx_tok_stride] idx_dtype
  * Errors: QSA_ERR_INVALID_ARG (a new token in no segment, null pointers,

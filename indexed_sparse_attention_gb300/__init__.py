@@ -23,7 +23,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libqsa.so")
 
-F32, BF16, FP8 = 0, 1, 2      # FP8: the E4M3 K/V state (codes + per-(head, token) f16 scales)
+F32, BF16, FP8, Q8 = 0, 1, 2, 3   # FP8 / Q8: quantized K/V state (E4M3 / int8 codes + f16 scales)
 INDEX_DIM = 128
 INDEX_HEADS = 4
 TOP_K = 512
@@ -141,6 +141,8 @@ def _dtype_code(t: torch.Tensor) -> int:
         return BF16
     if t.dtype in (torch.float8_e4m3fn, torch.uint8):   # E4M3 codes
         return FP8
+    if t.dtype == torch.int8:                            # Q8_0 codes
+        return Q8
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -158,8 +160,10 @@ def _ptr(t):
 class Segment:
     """A contiguous run of one sequence's K/V cache: k, v are [Hkv, n, D]
     views (channel stride 1) holding absolute tokens first_token .. +n-1.
-    For the fp8 state, k and v hold E4M3 codes (float8_e4m3fn or uint8) and
-    kv_scale is an [Hkv, n, 2] float16 view of the (K, V) scale pairs."""
+    Quantized state: for fp8, k and v hold E4M3 codes (float8_e4m3fn or
+    uint8) and kv_scale is an [Hkv, n, 2] float16 view of the (K, V) scale
+    pairs; for q8 (Q8_0), k and v hold int8 codes and kv_scale is an
+    [Hkv, n, 2 * D / 32] float16 view of the K then V block scales."""
     k: torch.Tensor
     v: torch.Tensor
     first_token: int = 0
@@ -206,10 +210,12 @@ def make_seq_array(seqs: Sequence[Seq]):
             sg.head_stride, sg.tok_stride = int(g.k.stride(0)), int(g.k.stride(1))
             if g.kv_scale is not None:
                 ks = g.kv_scale
-                if ks.dtype != torch.float16 or ks.shape[-1] != 2 or ks.stride(-1) != 1:
-                    raise TypeError("kv_scale must be a float16 [Hkv, n, 2] view of (K, V) scale pairs")
+                rec = 2 if g.k.dtype != torch.int8 else 2 * g.k.shape[-1] // 32   # f16 per scale record
+                if (ks.dtype != torch.float16 or ks.shape[-1] != rec or ks.stride(-1) != 1
+                        or ks.stride(0) % rec or ks.stride(1) % rec):
+                    raise TypeError(f"kv_scale must be a float16 [Hkv, n, {rec}] view of whole scale records")
                 sg.kv_scale = ks.data_ptr()
-                sg.scale_head_stride, sg.scale_tok_stride = int(ks.stride(0)) // 2, int(ks.stride(1)) // 2
+                sg.scale_head_stride, sg.scale_tok_stride = int(ks.stride(0)) // rec, int(ks.stride(1)) // rec
     return arr
 
 
@@ -288,7 +294,8 @@ def append_tokens(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: t
     if cfg is None:   # only the KV heads, head_dim and the caches' dtype matter here
         kvd = _kv_dtype([seq])
         kvd = _dtype_code(k_new) if kvd is None else kvd
-        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], BF16 if kvd == FP8 else kvd, kvd, F32, 0.0, 0)
+        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], BF16 if kvd in (FP8, Q8) else kvd, kvd, F32,
+                         0.0, 0)
     idxk = seq.idx_keys
     _check("qsa_append_tokens", lib().qsa_append_tokens(
         arr, ctypes.byref(cfg), k_new.data_ptr(), v_new.data_ptr(), idx_new.data_ptr(), idxk.data_ptr(),

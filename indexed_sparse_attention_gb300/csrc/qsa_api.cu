@@ -37,11 +37,12 @@ qsa_status cuda_fail(cudaError_t e, const char* where) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t dtype_size(qsa_dtype d) { return d == QSA_F32 ? 4 : d == QSA_FP8_E4M3 ? 1 : 2; }
+bool quantized(int d) { return d == QSA_FP8_E4M3 || d == QSA_Q8_0; }
+size_t dtype_size(qsa_dtype d) { return d == QSA_F32 ? 4 : quantized(d) ? 1 : 2; }
 
 bool valid_dtype(int d) { return d == QSA_F32 || d == QSA_BF16; }
 // K/V state types: the value types plus the fp8 state.
-bool valid_kv_dtype(int d) { return valid_dtype(d) || d == QSA_FP8_E4M3; }
+bool valid_kv_dtype(int d) { return valid_dtype(d) || quantized(d); }
 
 // Complete blocks the last (furthest) row of a sequence sees: floor(L / 4).
 int64_t max_visible_blocks(const qsa_seq& s) { return s.n_tokens / 4; }
@@ -527,8 +528,8 @@ qsa_status check_attn_config(const qsa_attn_config* cfg, const char* fn) {
     return fail(QSA_ERR_UNSUPPORTED, "%s: head_dim=%d (supported: 128, 256)", fn, cfg->head_dim);
   if (!valid_dtype(cfg->q_dtype) || !valid_kv_dtype(cfg->kv_dtype) || !valid_dtype(cfg->out_dtype))
     return fail(QSA_ERR_UNSUPPORTED, "%s: unknown dtype", fn);
-  if (cfg->kv_dtype == QSA_FP8_E4M3 ? cfg->q_dtype != QSA_BF16 : cfg->q_dtype != cfg->kv_dtype)
-    return fail(QSA_ERR_UNSUPPORTED, "%s: q_dtype must equal kv_dtype (bf16 with fp8 K/V)", fn);
+  if (quantized(cfg->kv_dtype) ? cfg->q_dtype != QSA_BF16 : cfg->q_dtype != cfg->kv_dtype)
+    return fail(QSA_ERR_UNSUPPORTED, "%s: q_dtype must equal kv_dtype (bf16 with quantized K/V)", fn);
   if (!(cfg->scale >= 0.f) || isinf(cfg->scale)) return fail(QSA_ERR_INVALID_ARG, "%s: bad scale", fn);
   return QSA_OK;
 }
@@ -550,10 +551,11 @@ qsa_status check_segments(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_co
         return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has bad strides", fn, i, j);
       if (!aligned16(g.k) || !aligned16(g.v) || (g.tok_stride * es) % 16 != 0 || (g.head_stride * es) % 16 != 0)
         return fail(QSA_ERR_MISALIGNED, "%s: sequence %d segment %d K/V not 16-byte aligned", fn, i, j);
-      if (cfg->kv_dtype == QSA_FP8_E4M3) {
+      if (quantized(cfg->kv_dtype)) {
         if (!g.kv_scale) return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has no scales", fn, i, j);
-        if ((reinterpret_cast<uintptr_t>(g.kv_scale) & 3u) != 0)
-          return fail(QSA_ERR_MISALIGNED, "%s: sequence %d segment %d scales not 4-byte aligned", fn, i, j);
+        const uintptr_t align = cfg->kv_dtype == QSA_FP8_E4M3 ? 3u : 15u;
+        if ((reinterpret_cast<uintptr_t>(g.kv_scale) & align) != 0)
+          return fail(QSA_ERR_MISALIGNED, "%s: sequence %d segment %d scale records misaligned", fn, i, j);
         if (g.scale_head_stride < 0 || g.scale_tok_stride < 1)
           return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d segment %d has bad scale strides", fn, i, j);
       }
@@ -590,7 +592,7 @@ qsa_status attn_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const qsa_a
       d.n = g.n_tokens;
       d.head_stride = g.head_stride;
       d.tok_stride = g.tok_stride;
-      d.kv_scale = static_cast<const uint32_t*>(g.kv_scale);
+      d.kv_scale = static_cast<const uint8_t*>(g.kv_scale);
       d.s_head_stride = g.scale_head_stride;
       d.s_tok_stride = g.scale_tok_stride;
     }
@@ -717,7 +719,7 @@ QSA_API qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* 
   p.n_segs = seq->n_segments;
   p.n_kv_heads = cfg->n_kv_heads;
   p.head_dim = cfg->head_dim;
-  p.fp8 = cfg->kv_dtype == QSA_FP8_E4M3;
+  p.kvq = cfg->kv_dtype == QSA_FP8_E4M3 ? 1 : cfg->kv_dtype == QSA_Q8_0 ? 2 : 0;
   p.n_tokens = L;
   p.n_new = n_new;
   p.k_new = k_new;
@@ -735,7 +737,7 @@ QSA_API qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* 
   p.pooled_stride = seq->pooled_stride;
   p.first_block = b0;
   // fp8 state: one warp (32 items) per K or V row, which it quantizes.
-  p.kv_items = p.fp8 ? 2 * (int64_t)cfg->n_kv_heads * n_new * 32 : 2 * (int64_t)cfg->n_kv_heads * n_new * p.row_chunks;
+  p.kv_items = p.kvq ? 2 * (int64_t)cfg->n_kv_heads * n_new * 32 : 2 * (int64_t)cfg->n_kv_heads * n_new * p.row_chunks;
   p.idx_items = n_new * p.idx_chunks;
   p.pool_items = std::max<int64_t>(0, b1 - b0) * (QSA_INDEX_DIM / 4);
   cudaError_t e = launch_append(p, as_stream(stream));

@@ -8,10 +8,12 @@
 //
 // One launch, three kinds of 16-byte work item (thread = item):
 //   K and V rows of the new tokens -> the KV segment that covers each token
-//   (fp8 state: one warp per row quantizes it -- hipfire, section 02, table
-//   "State formats": E4M3 codes with an f16 scale per head and token; scale
-//   = f16(amax / 448), code = nearest E4M3 to x / scale, ties to even,
-//   saturated at 448, all in binary32);
+//   (quantized state: one warp per row quantizes it -- hipfire, section 02,
+//   table "State formats": fp8 = E4M3 codes with an f16 scale per head and
+//   token, scale = f16(amax / 448), code = nearest E4M3 to x / scale, ties
+//   to even, saturated at 448; q8 = Q8_0, int8 codes with an f16 scale per
+//   block of 32, scale = f16(amax / 127), code = nearest integer to
+//   x / scale, halves away from zero, within +-127; all in binary32);
 //   index keys of the new tokens  -> the index-key cache;
 //   pooled keys of every block a new token completes -> pooled, averaging
 //   the block's four index keys in the order ((k0 + k1) + k2) + k3, x 0.25
@@ -78,14 +80,25 @@ __device__ __forceinline__ void quantize_row(const AppendParams& p, int64_t row,
   float amax = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
-#pragma unroll
-  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const __half sh = __float2half_rn(__fdiv_rn(amax, 448.0f));
+  // fp8: the whole row (all 32 lanes); q8: the lane's block of 32 elements
+  // (32 / per lanes, aligned).
+  const int span = p.kvq == 1 ? 32 : 32 / per;
+  for (int o = 1; o < span; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const __half sh = __float2half_rn(__fdiv_rn(amax, p.kvq == 1 ? 448.0f : 127.0f));
   const float sc = __half2float(sh);
   uint32_t c[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    c[k] = sc == 0.f ? 0u : f32x2_to_e4m3x2(__fdiv_rn(x[2 * k], sc), __fdiv_rn(x[2 * k + 1], sc));
+  for (int k = 0; k < 4; ++k) {
+    if (sc == 0.f) {
+      c[k] = 0u;
+    } else if (p.kvq == 1) {
+      c[k] = f32x2_to_e4m3x2(__fdiv_rn(x[2 * k], sc), __fdiv_rn(x[2 * k + 1], sc));
+    } else {
+      const float a = fminf(127.f, fmaxf(-127.f, roundf(__fdiv_rn(x[2 * k], sc))));
+      const float b = fminf(127.f, fmaxf(-127.f, roundf(__fdiv_rn(x[2 * k + 1], sc))));
+      c[k] = ((uint32_t)(int)a & 0xffu) | (((uint32_t)(int)b & 0xffu) << 8);
+    }
+  }
   const AppendSeg* sg = seg_of(p, t);
   if (!sg) return;
   uint8_t* dst = static_cast<uint8_t*>(which ? sg->v : sg->k) + (int64_t)h * sg->head_stride +
@@ -94,10 +107,14 @@ __device__ __forceinline__ void quantize_row(const AppendParams& p, int64_t row,
     *reinterpret_cast<uint2*>(dst) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
   else
     *reinterpret_cast<uint32_t*>(dst) = c[0] | (c[1] << 16);
-  if (lane == 0) {
-    __half* pair = reinterpret_cast<__half*>(static_cast<uint32_t*>(sg->kv_scale) + (int64_t)h * sg->s_head_stride +
-                                             (t - sg->first) * sg->s_tok_stride);
-    pair[which] = sh;
+  const int rec_bytes = p.kvq == 1 ? 4 : p.head_dim / 8;
+  __half* rec = reinterpret_cast<__half*>(static_cast<uint8_t*>(sg->kv_scale) +
+                                          ((int64_t)h * sg->s_head_stride + (t - sg->first) * sg->s_tok_stride) *
+                                              rec_bytes);
+  if (p.kvq == 1) {
+    if (lane == 0) rec[which] = sh;
+  } else if (lane % span == 0) {
+    rec[which * (p.head_dim / 32) + lane / span] = sh;
   }
 }
 
@@ -107,7 +124,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   grid_dependency_release();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t first_new = p.n_tokens - p.n_new;
-  if (p.fp8 && i < p.kv_items) {   // a whole warp per row (kv_items is a multiple of 32)
+  if (p.kvq && i < p.kv_items) {   // a whole warp per row (kv_items is a multiple of 32)
     quantize_row(p, i / 32, (int)(i % 32));
     return;
   }

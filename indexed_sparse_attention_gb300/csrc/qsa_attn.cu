@@ -110,11 +110,15 @@ constexpr int kPStride = 40;   // bf16 per P row: 80-byte rows keep ldmatrix con
 constexpr int kSStride = kTT + 4;
 constexpr int kAttnThreads = 256;
 
-// F8: fp8 state -- each stage holds the E4M3 codes (1 byte per element) and
-// one (K, V) scale pair per token; the stage being consumed is converted to
-// bf16 into one tile of the bf16 layout before the MMAs.
-template <int D, int STAGES, bool F8 = false>
+// KVQ (quantized state): 1 = fp8 (E4M3 codes, one (K, V) scale pair per
+// token), 2 = q8 (int8 codes, an f16 scale per 32 elements of each row).
+// Each stage holds the codes (1 byte per element) and the tokens' scale
+// records; the stage being consumed is converted to bf16 into one tile of the
+// bf16 layout before the MMAs.
+template <int D, int STAGES, int KVQ = 0>
 struct MmaSmem {
+  static constexpr bool F8 = KVQ != 0;
+  static constexpr int kRec = KVQ == 1 ? 4 : KVQ == 2 ? D / 8 : 0;   // scale record bytes per token
   static constexpr int CH = D / 8;                     // 16-byte chunks per bf16 K/V/Q row
   static constexpr size_t q = 16 * D * 2;
   static constexpr size_t kv_tile = kTT * D * (F8 ? 1 : 2);   // one K or V tile as gathered
@@ -126,8 +130,8 @@ struct MmaSmem {
   static constexpr size_t off_p = off_s + s;
   static constexpr size_t off_m = off_p + pm;          // m, l, alpha: 3 x 16 floats
   static constexpr size_t off_valid = off_m + 3 * 16 * 4;
-  static constexpr size_t off_sc = off_valid + STAGES * kTT * 4;   // fp8: scale pairs per stage
-  static constexpr size_t off_ids = off_sc + (F8 ? STAGES * kTT * 4 : 0);
+  static constexpr size_t off_sc = off_valid + STAGES * kTT * 4;   // scale records per stage
+  static constexpr size_t off_ids = off_sc + (size_t)STAGES * kTT * kRec;
   static constexpr size_t bytes = off_ids + kIdCache * 4;
   // Three stages keep two CTAs per SM (228 KB per SM, 1 KB reserved per CTA).
   static_assert(STAGES != 3 || 2 * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
@@ -136,6 +140,14 @@ struct MmaSmem {
 // Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly:
 // E4M3 -> f16 -> f32 -> bf16 loses nothing (4 significant bits, exponents
 // 2^-9 .. 2^8).
+// Two int8 codes (low byte first) times a block scale -> two bf16.
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t two_codes, float d) {
+  const float a = (float)(int8_t)(two_codes & 0xffu) * d;
+  const float b = (float)(int8_t)((two_codes >> 8) & 0xffu) * d;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
@@ -144,9 +156,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int D, int STAGES, int NSEQ, bool F8 = false>
+template <int D, int STAGES, int NSEQ, int KVQ = 0>
 __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_kernel(const AttnParams<NSEQ> p) {
-  using L = MmaSmem<D, STAGES, F8>;
+  using L = MmaSmem<D, STAGES, KVQ>;
+  constexpr bool F8 = KVQ != 0;
   constexpr int CH = L::CH;
   constexpr int KH = D / 32;   // k-steps (16 channels each) per channel half
   constexpr int NTD = D / 64;  // 8-channel n-tiles per warp in P.V
@@ -162,7 +175,7 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
   int32_t* ids_s = reinterpret_cast<int32_t*>(smem + L::off_ids);
   uint8_t* kv8_s = smem + L::off_kv;                                        // fp8 stages
   __nv_bfloat16* kvb_s = reinterpret_cast<__nv_bfloat16*>(smem + L::off_bf);   // fp8: converted tile
-  uint32_t* sc_s = reinterpret_cast<uint32_t*>(smem + L::off_sc);           // fp8: scale pairs
+  uint8_t* sc_s = smem + L::off_sc;                                         // scale records
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int quarter = warp & 3, half = warp >> 2;
@@ -213,13 +226,16 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
         cp_async16(kd + ch * 16, ks + (ok ? ch * 16 : 0), ok);
         cp_async16(vd + ch * 16, vs + (ok ? ch * 16 : 0), ok);
       }
-      if (q8 == 0) {
-        const uint32_t* sp = ok ? p.seg[seg].kv_scale + (int64_t)g * p.seg[seg].s_head_stride +
-                                      tseg * p.seg[seg].s_tok_stride
-                                : reinterpret_cast<const uint32_t*>(p.q);
-        cp_async4(sc_s + stage * kTT + tk, sp, ok);
-        valid_s[stage * kTT + tk] = ok ? 1 : 0;
+      const uint8_t* sp = ok ? p.seg[seg].kv_scale +
+                                   ((int64_t)g * p.seg[seg].s_head_stride + tseg * p.seg[seg].s_tok_stride) * L::kRec
+                             : static_cast<const uint8_t*>(p.q);
+      uint8_t* sd = sc_s + (size_t)(stage * kTT + tk) * L::kRec;
+      if constexpr (KVQ == 1) {
+        if (q8 == 0) cp_async4(sd, sp, ok);
+      } else {
+        if (q8 < L::kRec / 16) cp_async16(sd + q8 * 16, sp + (ok ? q8 * 16 : 0), ok);
       }
+      if (q8 == 0) valid_s[stage * kTT + tk] = ok ? 1 : 0;
       return;
     }
     const __nv_bfloat16* ks = ok ? static_cast<const __nv_bfloat16*>(p.seg[seg].k) + off : qg;
@@ -298,10 +314,21 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
         const int tk = rem / CH, ch = rem % CH;
         const uint2 w = *reinterpret_cast<const uint2*>(src + kv * L::kv_tile + tk * D + ch * 8);
         uint4 o;
-        o.x = e4m3x2_to_bf16x2(w.x & 0xffffu);
-        o.y = e4m3x2_to_bf16x2(w.x >> 16);
-        o.z = e4m3x2_to_bf16x2(w.y & 0xffffu);
-        o.w = e4m3x2_to_bf16x2(w.y >> 16);
+        if constexpr (KVQ == 1) {
+          o.x = e4m3x2_to_bf16x2(w.x & 0xffffu);
+          o.y = e4m3x2_to_bf16x2(w.x >> 16);
+          o.z = e4m3x2_to_bf16x2(w.y & 0xffffu);
+          o.w = e4m3x2_to_bf16x2(w.y >> 16);
+        } else {
+          // q8: code x the scale of its 32-element block (chunk ch lies in block ch / 4),
+          // rounded once to bf16.
+          const __half* rec = reinterpret_cast<const __half*>(sc_s + (size_t)(stage * kTT + tk) * L::kRec);
+          const float d = __half2float(rec[kv * (D / 32) + ch / 4]);
+          o.x = i8x2_to_bf16x2(w.x & 0xffffu, d);
+          o.y = i8x2_to_bf16x2(w.x >> 16, d);
+          o.z = i8x2_to_bf16x2(w.y & 0xffffu, d);
+          o.w = i8x2_to_bf16x2(w.y >> 16, d);
+        }
         *reinterpret_cast<uint4*>(kvb_s + (size_t)kv * kTT * D + (tk * CH + (ch ^ (tk & 7))) * 8) = o;
       }
       __syncthreads();
@@ -330,8 +357,8 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
     {
       const bool valid = valid_s[stage * kTT + lane] != 0;
       float kscale = 1.f, vscale = 1.f;
-      if constexpr (F8) {
-        const uint32_t pr = sc_s[stage * kTT + lane];
+      if constexpr (KVQ == 1) {
+        const uint32_t pr = *reinterpret_cast<const uint32_t*>(sc_s + (stage * kTT + lane) * 4);
         kscale = __half2float(__ushort_as_half((unsigned short)(pr & 0xffffu)));
         vscale = __half2float(__ushort_as_half((unsigned short)(pr >> 16)));
       }
@@ -370,7 +397,7 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
       for (int j = 0; j < 2; ++j) {
         const int rr = warp + 8 * j;
         if (rr < G) {
-          p_s[rr * kPStride + lane] = __float2bfloat16(F8 ? pz[j] * vscale : pz[j]);
+          p_s[rr * kPStride + lane] = __float2bfloat16(KVQ == 1 ? pz[j] * vscale : pz[j]);
           if (lane == 0) {
             const float alpha = mo[j] == -INFINITY ? 0.f : exp2f(mo[j] - mx[j]);
             a_s[rr] = alpha;
@@ -757,23 +784,27 @@ cudaError_t launch_attn_kernel(Kern kernel, const AttnParams<NSEQ>& p, int n_row
 
 }  // namespace
 
+template <int KVQ, int NSEQ>
+cudaError_t launch_quantized(const AttnParams<NSEQ>& p, int n_rows, int stages, cudaStream_t st) {
+  if (p.head_dim == 256) {
+    if (stages == 2)
+      return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ, KVQ>, p, n_rows, kAttnThreads,
+                                MmaSmem<256, 2, KVQ>::bytes, st);
+    return launch_attn_kernel(attn_mma_kernel<256, 3, NSEQ, KVQ>, p, n_rows, kAttnThreads,
+                              MmaSmem<256, 3, KVQ>::bytes, st);
+  }
+  if (stages == 2)
+    return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ, KVQ>, p, n_rows, kAttnThreads,
+                              MmaSmem<128, 2, KVQ>::bytes, st);
+  return launch_attn_kernel(attn_mma_kernel<128, 3, NSEQ, KVQ>, p, n_rows, kAttnThreads,
+                            MmaSmem<128, 3, KVQ>::bytes, st);
+}
+
 template <int NSEQ>
 cudaError_t launch_attn(const AttnParams<NSEQ>& p, int n_rows, qsa_dtype kv_dtype, int stages, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
-  if (kv_dtype == QSA_FP8_E4M3) {
-    if (p.head_dim == 256) {
-      if (stages == 2)
-        return launch_attn_kernel(attn_mma_kernel<256, 2, NSEQ, true>, p, n_rows, kAttnThreads,
-                                  MmaSmem<256, 2, true>::bytes, st);
-      return launch_attn_kernel(attn_mma_kernel<256, 3, NSEQ, true>, p, n_rows, kAttnThreads,
-                                MmaSmem<256, 3, true>::bytes, st);
-    }
-    if (stages == 2)
-      return launch_attn_kernel(attn_mma_kernel<128, 2, NSEQ, true>, p, n_rows, kAttnThreads,
-                                MmaSmem<128, 2, true>::bytes, st);
-    return launch_attn_kernel(attn_mma_kernel<128, 3, NSEQ, true>, p, n_rows, kAttnThreads,
-                              MmaSmem<128, 3, true>::bytes, st);
-  }
+  if (kv_dtype == QSA_FP8_E4M3) return launch_quantized<1, NSEQ>(p, n_rows, stages, st);
+  if (kv_dtype == QSA_Q8_0) return launch_quantized<2, NSEQ>(p, n_rows, stages, st);
   if (kv_dtype == QSA_BF16) {
     if (p.head_dim == 256) {
       if (stages == 2)

@@ -79,8 +79,8 @@ struct Segment {
   int64_t n;
   int64_t head_stride;
   int64_t tok_stride;
-  const uint32_t* kv_scale;    // fp8 state: (K, V) f16 scale pairs
-  int64_t s_head_stride;       // pairs
+  const uint8_t* kv_scale;     // quantized state: scale records (4 bytes fp8, D/8 bytes q8)
+  int64_t s_head_stride;       // records
   int64_t s_tok_stride;
 };
 
@@ -121,8 +121,8 @@ struct AppendSeg {
   void* k;
   void* v;
   int64_t first, n, head_stride, tok_stride;   // elements
-  void* kv_scale;                              // fp8 state: (K, V) f16 scale pairs
-  int64_t s_head_stride, s_tok_stride;         // pairs
+  void* kv_scale;                              // quantized state: scale records
+  int64_t s_head_stride, s_tok_stride;         // records
 };
 
 struct AppendParams {
@@ -130,7 +130,7 @@ struct AppendParams {
   int32_t n_segs;
   int32_t n_kv_heads;
   int32_t head_dim;
-  int32_t fp8;               // the caches hold the fp8 state; k_new / v_new are bf16
+  int32_t kvq;               // 1: fp8 state, 2: q8 state (k_new / v_new are bf16 and get quantized)
   int64_t n_tokens;          // L after the append
   int64_t n_new;             // tokens L - n_new .. L - 1 are appended
   const void* k_new;         // [Hkv, n_new, D]

@@ -90,6 +90,10 @@ def _load():
         lib.qsa_oracle_fp8_quantize.restype = i32
         lib.qsa_oracle_fp8_dequantize.argtypes = [vp, vp, i64, i64, vp]
         lib.qsa_oracle_fp8_dequantize.restype = i32
+        lib.qsa_oracle_q8_quantize.argtypes = [vp, i32, i64, i64, vp, vp]
+        lib.qsa_oracle_q8_quantize.restype = i32
+        lib.qsa_oracle_q8_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        lib.qsa_oracle_q8_dequantize.restype = i32
         _lib = lib
     return _lib
 
@@ -285,4 +289,30 @@ def fp8_dequantize(codes, scales) -> np.ndarray:
     D = c.shape[-1]
     out = np.empty(c.shape, dtype=np.float64)
     _load().qsa_oracle_fp8_dequantize(_ptr(c), _ptr(s_), c.size // D, D, _ptr(out))
+    return out
+
+
+# ---------------------------------------------------------------------- q8 K/V state
+# The same table: Q8_0 K/V -- blocks of 32 elements, an f16 scale and 32 int8
+# codes each (reading R10 in qsa_oracle.c: how a block is written).
+
+def q8_quantize(x):
+    """Rows [..., D] -> (codes int8 [..., D], f16 scale bits uint16 [..., D // 32])."""
+    a, code = _stored(x)
+    D = a.shape[-1]
+    rows = a.size // D
+    codes = np.empty(a.shape, dtype=np.int8)
+    scales = np.empty(a.shape[:-1] + (D // 32,), dtype=np.uint16)
+    if _load().qsa_oracle_q8_quantize(_ptr(a), code, rows, D, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("q8_quantize: D must be a multiple of 32")
+    return codes, scales
+
+
+def q8_dequantize(codes, scales) -> np.ndarray:
+    """(codes int8 [..., D], f16 scale bits [..., D // 32]) -> values fp64 [..., D] (exact)."""
+    c = np.ascontiguousarray(np.asarray(codes, dtype=np.int8))
+    s_ = np.ascontiguousarray(np.asarray(scales, dtype=np.uint16))
+    D = c.shape[-1]
+    out = np.empty(c.shape, dtype=np.float64)
+    _load().qsa_oracle_q8_dequantize(_ptr(c), _ptr(s_), c.size // D, D, _ptr(out))
     return out

@@ -38,6 +38,11 @@
  *      recipe): scale = f16(f32(amax / 448)), code = the E4M3 value nearest
  *      to f32(x / scale), ties to even, magnitudes above 448 saturated to
  *      448; a row whose scale is 0 stores zeros.
+ *   R10 the q8 K/V state (the same table: "Q8_0 K/V"): a row is stored in
+ *      blocks of 32 consecutive elements, each block as an f16 scale d and
+ *      32 int8 codes, value = code * d.  Writing a block: d = f16(f32(amax
+ *      / 127)), code = the integer nearest to f32(x / d), halves away from
+ *      zero, limited to +-127; a block whose scale is 0 stores zeros.
  *
  * Arithmetic is IEEE fp64 throughout (built without -ffast-math).  Inputs
  * are read in their stored format (fp32, bf16 bit patterns or fp64) and
@@ -401,5 +406,43 @@ int qsa_oracle_fp8_dequantize(const uint8_t* codes, const uint16_t* scales, int6
     const double sc = qsa_oracle_f16_decode(scales[r]);
     for (int64_t d = 0; d < D; ++d) out[r * D + d] = qsa_oracle_e4m3_decode(codes[r * D + d]) * sc;
   }
+  return 0;
+}
+
+/* ---------------------------------------------------------------- q8 state (R10) */
+
+int qsa_oracle_q8_quantize(const void* x, int dtype, int64_t rows, int64_t D, int8_t* codes, uint16_t* scales) {
+  if (D % 32) return -1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < D / 32; ++b) {
+      double amax = 0.0;
+      for (int64_t d = 0; d < 32; ++d) {
+        const double a = fabs(load_elem(x, dtype, r * D + 32 * b + d));
+        if (a > amax) amax = a;
+      }
+      const float s32 = (float)amax / 127.0f;
+      const uint16_t sh = qsa_oracle_f16_encode((double)s32);
+      scales[r * (D / 32) + b] = sh;
+      const float sc = (float)qsa_oracle_f16_decode(sh);
+      for (int64_t d = 0; d < 32; ++d) {
+        int8_t c = 0;
+        if (sc != 0.0f) {
+          const float q = (float)load_elem(x, dtype, r * D + 32 * b + d) / sc;
+          double n = round((double)q);                     /* halves away from zero */
+          if (n > 127.0) n = 127.0;
+          if (n < -127.0) n = -127.0;
+          c = (int8_t)n;
+        }
+        codes[r * D + 32 * b + d] = c;
+      }
+    }
+  return 0;
+}
+
+int qsa_oracle_q8_dequantize(const int8_t* codes, const uint16_t* scales, int64_t rows, int64_t D, double* out) {
+  if (D % 32) return -1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t d = 0; d < D; ++d)
+      out[r * D + d] = (double)codes[r * D + d] * qsa_oracle_f16_decode(scales[r * (D / 32) + d / 32]);
   return 0;
 }

@@ -348,6 +348,62 @@ def test_fp8_layer_step_matches_oracle():
     assert_attn_close(to_np(step.out), to_np(step.lse), ref_out, ref_lse, True)
 
 
+# ------------------------------------------------------------------ q8 K/V state (Q8_0: int8 + f16 per 32)
+def _q8_state(shape, seed):
+    """Seeded int8 codes in [-127, 127] and f16 block scales 2^-7 .. 2^-6
+    (values within about +-2), the K scales then the V scales of each row."""
+    g = torch.Generator().manual_seed(seed)
+    Hkv, L, D = shape
+    codes = torch.randint(-127, 128, (2, Hkv, L, D), generator=g).to(torch.int8)
+    expo = torch.randint(-7, -5, (Hkv, L, 2 * D // 32), generator=g).double()
+    frac = 1 + torch.randint(0, 1024, (Hkv, L, 2 * D // 32), generator=g).double() / 1024
+    return codes[0], codes[1], (frac * torch.pow(2.0, expo)).to(torch.float16)
+
+
+def _q8_ref(kc, vc, scales):
+    D = kc.shape[-1]
+    sb = scales.view(torch.int16).numpy().view(np.uint16)
+    return (oracle.q8_dequantize(kc.numpy(), sb[..., :D // 32]),
+            oracle.q8_dequantize(vc.numpy(), sb[..., D // 32:]))
+
+
+@pytest.mark.parametrize("L,M,D,n_splits", [(4099, 4, 256, 0), (9001, 1, 128, 0), (9001, 3, 256, 7),
+                                            (1200, 600, 256, 0)])
+def test_q8_attention_matches_oracle(L, M, D, n_splits):
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + D + 1, head_dim=D)
+    kc, vc, scales = _q8_state((2, L, D), seed=L + M + 1)
+    sel, cnt, _ = _oracle_selection(x)
+    kd, vd = _q8_ref(kc, vc, scales)
+    ref_out, ref_lse = oracle.attn(x.q, kd, vd, x.row_pos, sel, cnt)
+    seg = [qsa.Segment(kc.to(dev()), vc.to(dev()), 0, kv_scale=scales.to(dev()))]
+    out, lse = _attn_gpu(x, sel, cnt, segments=lambda k, v: seg, n_splits=n_splits)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+@pytest.mark.parametrize("D", [256, 128])
+def test_q8_append_quantizes_like_oracle(D):
+    L, n = 5003, 40
+    x = make_layer(L=L, M=n, dtype=torch.bfloat16, seed=65, head_dim=D, device=dev())
+    x.k[0, L - 3, :32] = 0.0                             # a zero block: scale 0, codes 0
+    x.v[1, L - 2, 5] = 1000.0                            # a large element
+    kc = torch.zeros((2, L, D), dtype=torch.int8, device=dev())
+    vc = torch.zeros_like(kc)
+    scales = torch.zeros((2, L, 2 * D // 32), dtype=torch.float16, device=dev())
+    idx_c = x.idxk.clone()
+    pooled = pooled_buffer(L, dev())
+    qsa.pool_index_keys(idx_c, pooled, 0, (L - n) // 4)
+    seq = qsa.Seq(L, n, pooled, [qsa.Segment(kc, vc, 0, kv_scale=scales)], idx_keys=idx_c)
+    qsa.append_tokens(seq, x.k[:, L - n:].contiguous(), x.v[:, L - n:].contiguous(), x.idxk[L - n:].contiguous())
+    torch.cuda.synchronize()
+    nb = D // 32
+    for which, src, codes in ((0, x.k, kc), (1, x.v, vc)):
+        ref_c, ref_s = oracle.q8_quantize(src[:, L - n:].cpu())
+        np.testing.assert_array_equal(to_np(codes[:, L - n:]), ref_c)
+        got_s = to_np(scales[:, L - n:, which * nb:(which + 1) * nb].contiguous().view(torch.int16)).view(np.uint16)
+        np.testing.assert_array_equal(got_s, ref_s)
+        assert (to_np(codes[:, :L - n]) == 0).all()
+
+
 # ------------------------------------------------------------------ demand-mapped arena
 def test_arena_grows_in_place():
     a = qsa.Arena(1 << 30)

@@ -441,3 +441,31 @@ def test_fp8_attention_is_attention_on_the_stored_values():
     a = oracle.attn(x.q, kd, v64, x.row_pos, sel, cnt)
     b = oracle.attn(x.q, k.astype(np.float64), v64, x.row_pos, sel, cnt)
     np.testing.assert_array_equal(a[0], b[0])
+
+
+# ------------------------------------------------------------------ q8 K/V state (Q8_0 blocks of 32)
+def test_q8_quantize_blocks():
+    rng = np.random.default_rng(15)
+    x = rng.standard_normal((5, 256)).astype(np.float32)
+    x[1, :32] = 0.0                                           # a zero block
+    x[2, 40] = 254.0                                          # amax 254: scale exactly 2
+    x[3, 64:96] = np.arange(-16, 16, dtype=np.float32) * 0.5  # halves: ties away from zero
+    codes, scales = oracle.q8_quantize(x)
+    deq = oracle.q8_dequantize(codes, scales)
+    f16 = lambda b: float(np.array([b], dtype=np.uint16).view(np.float16)[0])
+    for r in range(5):
+        for b in range(8):
+            blk = x[r, 32 * b:32 * b + 32]
+            s32 = np.float32(np.abs(blk).max()) / np.float32(127.0)
+            assert scales[r, b] == np.array([s32], dtype=np.float16).view(np.uint16)[0]
+            sc = f16(scales[r, b])
+            want = np.zeros(32, dtype=np.int8) if sc == 0 else np.clip(
+                np.sign(blk / np.float32(sc)) * np.floor(np.abs(blk / np.float32(sc)) + 0.5), -127, 127)
+            np.testing.assert_array_equal(codes[r, 32 * b:32 * b + 32], want.astype(np.int8))
+            np.testing.assert_array_equal(deq[r, 32 * b:32 * b + 32], codes[r, 32 * b:32 * b + 32] * sc)
+    assert (codes[1, :32] == 0).all() and scales[1, 0] == 0
+    assert codes[2, 40] == 127 and f16(scales[2, 1]) == 2.0
+    assert np.abs(codes).max() <= 127
+    # Error of a stored element: at most half a code step plus the scale's f16 rounding.
+    steps = np.repeat(np.vectorize(f16)(scales), 32, axis=1)
+    assert (np.abs(deq - x) <= 0.5 * steps * 1.001 + np.abs(x) * 2.0 ** -10).all()
