@@ -221,26 +221,37 @@ def host_layer(x, rows=None):
             "row_pos": pos, "b0": b0, "nb": x.L // 4, "pooled_old": oracle.pool(idxk, 0, b0)}
 
 
-def cpu_baseline(layers, budget_s=20.0, max_layers=3, max_rows=64):
-    """The oracle on a bounded sample of the workload: whole layer-steps when
-    a layer has few rows; else max_rows sampled rows of one layer-step
-    (first and last included), timed and scaled linearly to all rows."""
+def cpu_baseline(layers, min_s=10.0, max_s=30.0, max_layers=3, max_rows=64):
+    """The oracle on a bounded sample of the workload (about min_s .. max_s
+    seconds of host work): whole layer-steps, cycling over up to max_layers
+    layers, when a layer has few rows; else a sample of rows of one
+    layer-step (first and last included), grown until it takes about min_s,
+    timed and scaled linearly to all rows (rows are independent)."""
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0))
     M = layers[0].x.M
     if M <= max_rows:
         hosts = [host_layer(l.x) for l in layers[:max_layers]]
-        n, secs = oracle_layer_steps(hosts, cores, budget_s)
+        n, secs = 0, 0.0
+        while secs < min_s:
+            dn, ds = oracle_layer_steps(hosts, cores, max_s - secs)
+            n, secs = n + dn, secs + ds
         return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
-                "sample": f"{n} of the workload's layer-steps (pool new blocks, score all blocks, select, "
-                          f"attention over all rows and heads) in fp64 C with OpenMP, {secs:.2f} s"}
-    rows = sorted(set([0, M - 1] + [int(i * (M - 1) / (max_rows - 1)) for i in range(max_rows)]))
-    n, secs = oracle_layer_steps([host_layer(layers[0].x, rows)], cores, budget_s)
+                "sample": f"{n} layer-steps of the workload (pool new blocks, score all blocks, select, attention "
+                          f"over all rows and heads), cycling over {len(hosts)} layers, in fp64 C with OpenMP, "
+                          f"{secs:.1f} s"}
+    n_rows = max_rows
+    while True:
+        rows = sorted(set([0, M - 1] + [int(i * (M - 1) / (n_rows - 1)) for i in range(n_rows)]))
+        _, secs = oracle_layer_steps([host_layer(layers[0].x, rows)], cores, max_s)
+        if secs >= min_s or len(rows) >= M:
+            break
+        n_rows = min(M, int(len(rows) * min_s / max(secs, 1e-3) * 1.1) + 1)
     full = secs * M / len(rows)
     return {"value": 1.0 / full, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows)} of the {M} rows of one layer-step in fp64 C with OpenMP ({secs:.2f} s), "
-                      f"extrapolated linearly in rows to {full:.1f} s per layer-step"}
+            "sample": f"{len(rows)} of the {M} rows of one layer-step in fp64 C with OpenMP ({secs:.1f} s), "
+                      f"scaled linearly in rows to {full:.1f} s per layer-step"}
 
 
 # ---------------------------------------------------------------------- main
