@@ -137,25 +137,6 @@ struct MmaSmem {
   static_assert(STAGES != 3 || 2 * (bytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
-// Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly:
-// E4M3 -> f16 -> f32 -> bf16 loses nothing (4 significant bits, exponents
-// 2^-9 .. 2^8).
-// Two int8 codes (low byte first) times a block scale -> two bf16.
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t two_codes, float d) {
-  const float a = (float)(int8_t)(two_codes & 0xffu) * d;
-  const float b = (float)(int8_t)((two_codes >> 8) & 0xffu) * d;
-  const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-  return *reinterpret_cast<const uint32_t*>(&b);
-}
-
 template <int D, int STAGES, int NSEQ, int KVQ = 0>
 __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_kernel(const AttnParams<NSEQ> p) {
   using L = MmaSmem<D, STAGES, KVQ>;

@@ -5,6 +5,8 @@
 // segment table (MTPLX pull request #610).
 #pragma once
 
+#include <cuda_fp16.h>
+
 #include "qsa_internal.cuh"
 
 namespace qsa {
@@ -129,6 +131,26 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- quantized K/V codes
+// Two E4M3 codes (low byte first) -> two bf16 (low half first), exactly:
+// E4M3 -> f16 -> f32 -> bf16 loses nothing (4 significant bits, exponents
+// 2^-9 .. 2^8).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)two_codes));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+// Two int8 codes (low byte first) times a block scale -> two bf16 (the
+// binary32 product is exact, rounded once).
+__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t two_codes, float d) {
+  const float a = (float)(int8_t)(two_codes & 0xffu) * d;
+  const float b = (float)(int8_t)((two_codes >> 8) & 0xffu) * d;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 }  // namespace attn

@@ -266,8 +266,11 @@ def _fp8_ref(kc, vc, scales):
     return oracle.fp8_dequantize(kc.numpy(), sb[..., 0]), oracle.fp8_dequantize(vc.numpy(), sb[..., 1])
 
 
+# Many-row calls (one split per row) at both head sizes; 9,001-token rows
+# have full 2,051-entry lists with ragged tails.
 @pytest.mark.parametrize("L,M,D,n_splits", [(4099, 4, 256, 0), (9001, 1, 256, 0), (9001, 3, 128, 5),
-                                            (2051, 4, 256, 1), (1200, 600, 256, 0)])
+                                            (2051, 4, 256, 1), (1200, 600, 256, 0), (1200, 600, 128, 0),
+                                            (9001, 512, 128, 0)])
 def test_fp8_attention_matches_oracle(L, M, D, n_splits):
     x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + D, head_dim=D)
     kc, vc, scales = _fp8_state((2, L, D), seed=L + M)
@@ -279,8 +282,9 @@ def test_fp8_attention_matches_oracle(L, M, D, n_splits):
     assert_attn_close(out, lse, ref_out, ref_lse, True)
 
 
-def test_fp8_segments_equal_single_buffer():
-    L, M, D = 9001, 4, 256
+@pytest.mark.parametrize("L,M", [(9001, 4), (1500, 520)])
+def test_fp8_segments_equal_single_buffer(L, M):
+    D = 256
     x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=61, head_dim=D)
     kc, vc, scales = _fp8_state((2, L, D), seed=62)
     kc, vc, scales = kc.to(dev()), vc.to(dev()), scales.to(dev())
@@ -368,7 +372,7 @@ def _q8_ref(kc, vc, scales):
 
 
 @pytest.mark.parametrize("L,M,D,n_splits", [(4099, 4, 256, 0), (9001, 1, 128, 0), (9001, 3, 256, 7),
-                                            (1200, 600, 256, 0)])
+                                            (1200, 600, 256, 0), (1200, 600, 128, 0), (9001, 512, 128, 0)])
 def test_q8_attention_matches_oracle(L, M, D, n_splits):
     x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + D + 1, head_dim=D)
     kc, vc, scales = _q8_state((2, L, D), seed=L + M + 1)
