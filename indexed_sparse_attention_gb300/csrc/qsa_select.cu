@@ -262,8 +262,10 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
   }
 }
 
-template <int NSEQ>
-__global__ void __launch_bounds__(kThreads) select_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
+// MINB: CTAs per SM the register budget allows (2 for calls of many rows,
+// whose CTAs then share SMs; 1 keeps the fewest-row latency lowest).
+template <int NSEQ, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
   extern __shared__ __align__(16) uint32_t sm[];
   __shared__ uint32_t wt[2][kWarps];
   __shared__ uint32_t s_res[2];
@@ -597,9 +599,12 @@ template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
   const size_t smem = select_smem_bytes(max_nb);
-  cudaError_t e = allow_dynamic_smem((const void*)select_kernel<NSEQ>, smem);
+  // More rows than SMs: two CTAs per SM where shared memory allows it.
+  const bool two = n_rows > device_sm_count() && 2 * (smem + 2048) <= 228 * 1024;
+  auto* kernel = two ? select_kernel<NSEQ, 2> : select_kernel<NSEQ, 1>;
+  cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(select_kernel<NSEQ>, dim3((unsigned)n_rows), dim3(kThreads), smem, st, 0u, p, max_nb);
+  return launch_kernel(kernel, dim3((unsigned)n_rows), dim3(kThreads), smem, st, 0u, p, max_nb);
 }
 
 template cudaError_t launch_select<1>(const SelectParams<1>&, int, int64_t, cudaStream_t);
