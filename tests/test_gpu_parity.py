@@ -590,7 +590,8 @@ def _attn_gpu(x, sel, cnt, *, segments=None, out_dtype=torch.float32, n_splits=0
     lse = torch.full((x.M, x.q.shape[1]), float("nan"), device=device)
     seld = torch.from_numpy(np.ascontiguousarray(sel)).to(device)
     cntd = torch.from_numpy(np.ascontiguousarray(cnt)).to(device)
-    qsa.sparse_attn([qsa.Seq(x.L, x.M, segments=segs)], q, seld, cntd, out, lse, n_splits=n_splits)
+    qsa.sparse_attn([qsa.Seq(x.L, x.M, segments=segs)], q, seld, cntd, out, lse, n_splits=n_splits,
+                    n_kv_heads=x.k.shape[0])
     torch.cuda.synchronize()
     return to_np(out.float()), to_np(lse)
 
@@ -604,6 +605,33 @@ def test_attention_matches_oracle(dtype, D, n_splits):
     out, lse = _attn_gpu(x, sel, cnt, n_splits=n_splits)
     ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
     assert_attn_close(out, lse, ref_out, ref_lse, dtype == torch.bfloat16)
+
+
+# Other grouped-query shapes (up to 16 query heads per KV head), on the
+# few-row path and on the tensor-core path (>= 512 rows).
+@pytest.mark.parametrize("Hq,Hkv,M,D", [(32, 2, 4, 256), (8, 1, 4, 128), (4, 4, 3, 128), (32, 2, 520, 128),
+                                        (8, 1, 600, 256), (16, 4, 512, 128)])
+def test_attention_other_head_groupings(Hq, Hkv, M, D):
+    L = 9001 if M <= 8 else 1500
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=7 * Hq + Hkv + M, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=D)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
+# Budgets other than 512 blocks: lists of 4 top_k + tail entries (900 blocks
+# at 520 rows fill 29 of the tensor-core path's 30 logit tiles; 1,024 blocks
+# exceed them and run split-free on the warp-level path).
+@pytest.mark.parametrize("top_k,M", [(64, 4), (1024, 4), (900, 520), (1024, 520)])
+def test_attention_other_budgets(top_k, M):
+    L = 20_011 if M <= 8 else 5000
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=top_k + M, head_dim=128)
+    s = oracle.score(x.q_idx, oracle.pool(x.idxk), x.row_pos)
+    sel, cnt, _ = oracle.select(s, x.row_pos, top_k)
+    out, lse = _attn_gpu(x, sel, cnt)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
 
 
 def test_attention_many_splits_reuse_workspace():
