@@ -53,7 +53,7 @@
 extern "C" {
 #endif
 
-#define QSA_VERSION 110            /* 1.1.0 */
+#define QSA_VERSION 111            /* 1.1.1 */
 #define QSA_INDEX_DIM 128          /* width of an index key and an index-query head */
 #define QSA_INDEX_HEADS 4          /* index-query heads per query row */
 #define QSA_BLOCK_TOKENS 4         /* tokens pooled into one block key */
@@ -70,7 +70,9 @@ typedef enum qsa_status {
   QSA_ERR_UNSUPPORTED = 2,   /* dtype / head_dim / head count / size the library does not build */
   QSA_ERR_MISALIGNED = 3,    /* pointer or stride not 16-byte aligned */
   QSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than the *_workspace_size result */
-  QSA_ERR_CUDA = 5           /* a CUDA runtime call or launch failed */
+  QSA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+  QSA_ERR_DEVICE_CHECK = 6,  /* qsa_check_device_status: kernels met inputs outside the contract */
+  QSA_ERR_TIMEOUT = 7        /* qsa_check_device_status: a device-side wait gave up */
 } qsa_status;
 
 typedef enum qsa_dtype {
@@ -181,6 +183,34 @@ int32_t qsa_version(void);
  * not be read.  Reads device memory: waits for the device to be idle.
  */
 int32_t qsa_wait_timeouts(void);
+
+/*
+ * The device-side checks since the previous call (or since the library was
+ * loaded), after synchronizing `stream`:
+ *   QSA_ERR_TIMEOUT       a wait of a pipelined kernel (or of
+ *                         qsa_selftest_wait_timeout) gave up -- that
+ *                         launch's result is invalid;
+ *   QSA_ERR_DEVICE_CHECK  the attention met selected block ids outside
+ *                         [0, nb) among a row's first cnt entries (skipped),
+ *                         or the selection met NaN scores among its
+ *                         candidates (NaN ranks above every number);
+ *   QSA_OK                neither.
+ * qsa_last_error() gives the counts.  The counters are global to the
+ * library (all streams and threads); a call reads and clears them.  Launches
+ * still running on other streams may be counted by the next call.
+ * Errors: QSA_ERR_CUDA (the stream or the counters could not be read).
+ */
+qsa_status qsa_check_device_status(void* stream);
+
+/*
+ * Test hook for the timeout path: one thread waits on a shared-memory
+ * barrier that nothing completes, gives up after limit_us microseconds
+ * (1 .. 2,000,000) and records the expired wait, which the next
+ * qsa_check_device_status reports as QSA_ERR_TIMEOUT (qsa_wait_timeouts does
+ * not count it).  The kernel ends by itself; the context stays usable.
+ * Errors: QSA_ERR_INVALID_ARG (limit), QSA_ERR_CUDA (launch).
+ */
+qsa_status qsa_selftest_wait_timeout(int32_t limit_us, void* stream);
 
 /*
  * Step 1 -- pooling (hipfire, section 02: every 4 consecutive index keys are

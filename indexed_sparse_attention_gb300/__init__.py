@@ -32,7 +32,8 @@ MAX_SEGMENTS = 12
 SCORE_GROUP = 16
 
 STATUS = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_MISALIGNED",
-          4: "QSA_ERR_WORKSPACE", 5: "QSA_ERR_CUDA"}
+          4: "QSA_ERR_WORKSPACE", 5: "QSA_ERR_CUDA", 6: "QSA_ERR_DEVICE_CHECK", 7: "QSA_ERR_TIMEOUT"}
+ERR_DEVICE_CHECK, ERR_TIMEOUT = 6, 7
 
 
 class QSAError(RuntimeError):
@@ -68,7 +69,8 @@ EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index
            "qsa_score_select_topk", "qsa_attn_workspace_size", "qsa_sparse_attn", "qsa_sparse_attn_noalloc",
            "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
            "qsa_score_select_topk_blocked", "qsa_append_tokens", "qsa_arena_create", "qsa_arena_ensure",
-           "qsa_arena_base", "qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity", "qsa_arena_destroy")
+           "qsa_arena_base", "qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity", "qsa_arena_destroy",
+           "qsa_check_device_status", "qsa_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -88,6 +90,8 @@ def lib() -> ctypes.CDLL:
     L.qsa_last_error.restype = ctypes.c_char_p
     L.qsa_version.restype = i32
     L.qsa_wait_timeouts.restype = i32
+    L.qsa_check_device_status.argtypes = [vp]
+    L.qsa_selftest_wait_timeout.argtypes = [i32, vp]
     L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
     L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp, sz, vp]
     L.qsa_score_workspace_size.argtypes = [seqp, i32, i32]
@@ -127,6 +131,19 @@ def lib() -> ctypes.CDLL:
 def wait_timeouts() -> int:
     """Device-side barrier waits that gave up (0 in normal operation)."""
     return int(lib().qsa_wait_timeouts())
+
+
+def check_device_status(stream=None) -> tuple[int, str]:
+    """qsa_check_device_status: (status, reason) for the device-side checks
+    since the previous call -- 0, ERR_TIMEOUT or ERR_DEVICE_CHECK."""
+    st = int(lib().qsa_check_device_status(_stream(stream)))
+    return st, (lib().qsa_last_error().decode() if st else "")
+
+
+def selftest_wait_timeout(limit_us: int, stream=None):
+    """Launch one bounded wait that nothing completes (a test of the
+    timeout reporting)."""
+    _check("qsa_selftest_wait_timeout", lib().qsa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def _check(fn: str, status: int):

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libqsa.so")
-SOURCES = ["qsa_api.cu", "qsa_score.cu", "qsa_score_tc.cu", "qsa_select.cu", "qsa_attn.cu", "qsa_attn_tc.cu", "qsa_append.cu", "qsa_arena.cu"]
+SOURCES = ["qsa_api.cu", "qsa_score.cu", "qsa_score_tc.cu", "qsa_select.cu", "qsa_attn.cu", "qsa_attn_tc.cu", "qsa_append.cu", "qsa_arena.cu", "qsa_check.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -118,6 +118,8 @@ QSA_API const char* qsa_status_string(qsa_status s) {
     case QSA_ERR_MISALIGNED: return "QSA_ERR_MISALIGNED";
     case QSA_ERR_WORKSPACE: return "QSA_ERR_WORKSPACE";
     case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+    case QSA_ERR_DEVICE_CHECK: return "QSA_ERR_DEVICE_CHECK";
+    case QSA_ERR_TIMEOUT: return "QSA_ERR_TIMEOUT";
   }
   return "QSA_ERR_UNKNOWN";
 }
@@ -130,6 +132,37 @@ QSA_API int32_t qsa_wait_timeouts(void) {
   const int a = score_wait_timeouts(), b = score_tc_wait_timeouts(), c = attn_tc_wait_timeouts();
   if (a < 0 || b < 0 || c < 0) return -1;
   return a + b + c;
+}
+
+QSA_API qsa_status qsa_check_device_status(void* stream) {
+  const char* fn = "qsa_check_device_status";
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  static std::mutex mu;
+  static int seen_waits = 0;   // qsa_wait_timeouts() at the previous call
+  std::lock_guard<std::mutex> lock(mu);
+  const int w = qsa_wait_timeouts(), st = selftest_timeouts_take();
+  const int bad_a = attn_bad_ids_take(), bad_t = attn_tc_bad_ids_take(), nan = select_nan_keys_take();
+  if (w < 0 || st < 0 || bad_a < 0 || bad_t < 0 || nan < 0)
+    return fail(QSA_ERR_CUDA, "%s: the device counters could not be read", fn);
+  const int waits = (w - seen_waits) + st, bad = bad_a + bad_t;
+  seen_waits = w;
+  if (waits > 0)
+    return fail(QSA_ERR_TIMEOUT, "%s: %d device wait(s) gave up; %d out-of-range selected ids, %d NaN scores", fn,
+                waits, bad, nan);
+  if (bad > 0 || nan > 0)
+    return fail(QSA_ERR_DEVICE_CHECK, "%s: %d out-of-range selected ids (skipped), %d NaN scores among the selection's candidates",
+                fn, bad, nan);
+  return ok();
+}
+
+QSA_API qsa_status qsa_selftest_wait_timeout(int32_t limit_us, void* stream) {
+  const char* fn = "qsa_selftest_wait_timeout";
+  if (limit_us < 1 || limit_us > 2000000)
+    return fail(QSA_ERR_INVALID_ARG, "%s: limit_us=%d outside 1..2,000,000", fn, limit_us);
+  cudaError_t e = launch_selftest_wait(limit_us, as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
 }
 
 // ------------------------------------------------------------------ step 1

@@ -821,4 +821,6 @@ cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int n_par
                        out, out_dtype, lse_out);
 }
 
+int attn_bad_ids_take() { return take_counter(attn::g_bad_ids); }
+
 }  // namespace qsa

@@ -12,6 +12,12 @@
 namespace qsa {
 namespace attn {
 
+namespace {
+// Selected block ids outside [0, nb) met by this translation unit's kernels
+// (skipped; read and cleared by qsa_check_device_status).
+__device__ int g_bad_ids;
+}  // namespace
+
 // Per-row context: position, visible blocks, selected list length.  The
 // list's longest possible length (cnt = min(sel_ld, nb)) is known without
 // reading cnt, so the splits' ranges and id loads need not wait for it.
@@ -85,7 +91,10 @@ __device__ __forceinline__ bool locate(const AttnParams<NSEQ>& p, const RowCtx& 
   if (i < 4 * (int64_t)c.cnt) {
     const int64_t k = (i >> 2) - ic.blk0;
     const int32_t b = (k >= 0 && k < ic.n) ? ic.ids[k] : __ldg(c.sel_row + (i >> 2));
-    if (b < 0 || (int64_t)b >= c.nb) return false;
+    if (b < 0 || (int64_t)b >= c.nb) {
+      atomicAdd(&g_bad_ids, 1);
+      return false;
+    }
     t = 4 * (int64_t)b + (i & 3);
   } else {
     t = 4 * c.nb + (i - 4 * (int64_t)c.cnt);

@@ -147,7 +147,10 @@ __device__ __forceinline__ bool locate_tok(const RowCtx& c, const int32_t* ids, 
   int64_t t;
   if (i < 4 * (int64_t)c.cnt) {
     const int32_t b = ids[i >> 2];
-    if (b < 0 || (int64_t)b >= c.nb) return false;
+    if (b < 0 || (int64_t)b >= c.nb) {
+      atomicAdd(&g_bad_ids, 1);
+      return false;
+    }
     t = 4 * (int64_t)b + (i & 3);
   } else {
     t = 4 * c.nb + (i - 4 * (int64_t)c.cnt);
@@ -481,6 +484,8 @@ cudaError_t launch_attn_tc(const AttnParams<NSEQ>& p, int n_rows, cudaStream_t s
 
 template cudaError_t launch_attn_tc<1>(const AttnParams<1>&, int, cudaStream_t);
 template cudaError_t launch_attn_tc<kLaunchSeqs>(const AttnParams<kLaunchSeqs>&, int, cudaStream_t);
+
+int attn_tc_bad_ids_take() { return take_counter(g_bad_ids); }
 
 int attn_tc_wait_timeouts() {
   int v = 0;

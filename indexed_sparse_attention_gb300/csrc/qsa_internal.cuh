@@ -238,6 +238,23 @@ int score_wait_timeouts();
 int score_tc_wait_timeouts();
 int attn_tc_wait_timeouts();
 
+// Reads a device-side event counter of the calling translation unit and
+// clears it (-1 if it cannot be read).
+template <typename T>
+inline int take_counter(T& symbol) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, symbol, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(symbol, &zero, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+// Counters behind qsa_check_device_status, each read and cleared.
+int attn_bad_ids_take();        // selected ids outside [0, nb) (qsa_attn.cu)
+int attn_tc_bad_ids_take();     // the same in the tensor-core attention
+int select_nan_keys_take();     // NaN scores among selection candidates
+int selftest_timeouts_take();   // expired waits of qsa_selftest_wait_timeout
+cudaError_t launch_selftest_wait(int32_t limit_us, cudaStream_t st);
+
 int device_sm_count();
 
 // Raise a kernel's dynamic shared-memory limit (once per device and size).

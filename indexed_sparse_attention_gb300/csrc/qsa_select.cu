@@ -32,6 +32,10 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
+
+// NaN scores met among the candidates (read and cleared by
+// qsa_check_device_status): order keys above +inf's or below -inf's.
+__device__ int g_nan_keys;
 constexpr int kGroup = QSA_SCORE_GROUP;
 constexpr int kBins = 4096;                        // radix levels 1 and 2: 12 key bits each
 constexpr int kBins3 = 256;                        // radix level 3: the last 8 key bits
@@ -216,6 +220,7 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
   // to K when all of them fit, else the `need` lowest ids among them.
   const bool all_eq = n_eq == need;
   for_each([&](uint32_t key, int32_t id) {
+    if (key > 0xff800000u || key < 0x007fffffu) atomicAdd(&g_nan_keys, 1);
     const uint32_t m = key & mask;
     if (m > K || (all_eq && m == K)) atomicOr(&selw[id >> 5], 1u << (id & 31));
     else if (m == K) atomicOr(&eqw[id >> 5], 1u << (id & 31));
@@ -584,6 +589,8 @@ __global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelec
 size_t select_smem_bytes(int64_t max_nb) { return sizeof(uint32_t) * (size_t)SelLayout(max_nb).total; }
 
 int merge_select_max_union() { return kListCap; }
+
+int select_nan_keys_take() { return take_counter(g_nan_keys); }
 
 cudaError_t launch_merge_select(const MergeSelectParams& p, cudaStream_t st) {
   if (p.n_rows == 0) return cudaSuccess;

@@ -46,10 +46,16 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.qsa_version() == 110
+    assert L.qsa_version() == 111
     for code, name in qsa.STATUS.items():
         assert L.qsa_status_string(code).decode() == name
     assert L.qsa_status_string(99).decode() == "QSA_ERR_UNKNOWN"
+
+
+def test_selftest_wait_limits_checked_before_launch(L):
+    for bad in (0, -3, 2_000_001):
+        assert L.qsa_selftest_wait_timeout(bad, None) == 1
+        assert "limit_us" in L.qsa_last_error().decode()
 
 
 def _seq(n_tokens=4099, n_rows=4, pooled=FAKE, n_segments=1, segs=None):

@@ -868,3 +868,60 @@ def test_layer_step_ragged_batch_small():
         ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
         assert_attn_close(to_np(step.out)[rows], to_np(step.lse)[rows], ref_out, ref_lse, True)
         row += x.M
+
+
+# ------------------------------------------------------------------ device-side checks
+def test_device_status_clean_after_normal_work():
+    qsa.check_device_status()   # clears what earlier tests left
+    L, M = 9001, 4
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=71, device=dev())
+    pooled = pooled_buffer(L, dev())
+    qsa.pool_index_keys(x.idxk, pooled, 0, L // 4)
+    step = qsa.LayerStep([qsa.Seq(L, M, pooled, [qsa.Segment(x.k, x.v, 0)], idx_keys=x.idxk)], x.q_idx, x.q)
+    step.run()
+    assert qsa.check_device_status() == (0, "")
+
+
+@pytest.mark.parametrize("L,M", [(3001, 2), (1200, 600)])
+def test_device_status_reports_out_of_range_ids(L, M):
+    # Few rows (warp-level path) and >= 512 rows (tensor cores): the bad ids
+    # are skipped and counted.
+    qsa.check_device_status()
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=L + M)
+    sel, cnt, _ = _oracle_selection(x)
+    bad = sel.copy()
+    bad[0, 3] = 10_000_000
+    bad[M - 1, 5] = -5
+    _attn_gpu(x, bad, cnt)
+    st, why = qsa.check_device_status()
+    assert st == qsa.ERR_DEVICE_CHECK and "out-of-range" in why
+    assert qsa.check_device_status() == (0, "")     # read and cleared
+
+
+def test_device_status_reports_nan_scores():
+    qsa.check_device_status()
+    L, M = 20_011, 2
+    rng = np.random.default_rng(3)
+    s = np.abs(rng.standard_normal((M, (L // 4 + 3) // 4 * 4))).astype(np.float32)
+    s[0, 64:80] = 100.0        # the group of block 77 is surely a candidate
+    s[0, 77] = np.nan
+    _select_gpu(s, [L - M + j for j in range(M)], L)
+    st, why = qsa.check_device_status()
+    assert st == qsa.ERR_DEVICE_CHECK and "NaN" in why
+
+
+def test_device_status_reports_expired_wait():
+    # One wait on a barrier nothing completes, limited to 2 ms: reported as a
+    # timeout, and the context stays usable.
+    qsa.check_device_status()
+    before = qsa.wait_timeouts()
+    qsa.selftest_wait_timeout(2000)
+    st, why = qsa.check_device_status()
+    assert st == qsa.ERR_TIMEOUT and "gave up" in why
+    assert qsa.wait_timeouts() == before          # the library's own kernels are not blamed
+    x = make_layer(L=2052, M=1, dtype=torch.bfloat16, seed=9)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+    assert qsa.check_device_status() == (0, "")
