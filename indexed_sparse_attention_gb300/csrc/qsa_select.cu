@@ -42,8 +42,9 @@ constexpr int kBins3 = 256;                        // radix level 3: the last 8 
 constexpr int kGroupCap = 1024;                    // candidate groups read back (16,384 blocks)
 constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
 constexpr int kMaxGroups = QSA_MAX_BLOCKS / kGroup;
-constexpr int kGroupsPerThread = kMaxGroups / kThreads;
-constexpr int kChunksPerThread = kGroupCap * (kGroup / 4) / kThreads;   // float4 chunks of candidate groups
+constexpr int kLoadBatch = 16;                                  // group maxima a thread loads per pass
+constexpr int kChunkBatch = 4;                                  // float4 chunks a thread loads per pass
+
 
 // Shared-memory layout (32-bit words); R1 holds the group-maximum keys, then
 // the list keys.
@@ -71,13 +72,14 @@ __device__ __forceinline__ uint32_t lanes_below() {
 }
 
 // Exclusive prefix sum of v over the warps of the CTA (v uniform within each
-// warp, warp order); *total = the sum over warps.  wt (kWarps words) must not
+// warp, warp order); *total = the sum over warps.  wt (NT / 32 words) must not
 // be touched again before the next __syncthreads() after this call.
+template <int NT>
 __device__ __forceinline__ uint32_t warp_prefix(uint32_t v, uint32_t* wt, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) wt[warp] = v;
   __syncthreads();
-  const uint32_t w = wt[lane];   // kWarps == 32
+  const uint32_t w = lane < NT / 32 ? wt[lane] : 0u;
   uint32_t before = lane < warp ? w : 0u;
   uint32_t all = w;
 #pragma unroll
@@ -90,6 +92,7 @@ __device__ __forceinline__ uint32_t warp_prefix(uint32_t v, uint32_t* wt, uint32
 }
 
 // Exclusive prefix sum of v over the CTA in thread order (same contract on wt).
+template <int NT>
 __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
   const int lane = threadIdx.x & 31;
   uint32_t x = v;
@@ -98,35 +101,47 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* wt, uint32_
     const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  return warp_prefix(__shfl_sync(0xffffffffu, x, 31), wt, total) + x - v;
+  return warp_prefix<NT>(__shfl_sync(0xffffffffu, x, 31), wt, total) + x - v;
 }
 
 // Bin (of nbins = kBins or kBins3) holding the need-th largest key counted in
 // hist: s_res[0] = the bin, s_res[1] = keys in higher bins.  The histogram
 // holds at least need >= 1 keys.  Ends with a barrier.
+template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nbins, uint32_t need, uint32_t* wt,
                                          uint32_t* s_res) {
   const int tid = threadIdx.x;
-  uint32_t c[4];   // c[j] = count of bin top - 1 - j
+  constexpr int P = kBins / NT;
+  static_assert(kBins % (4 * NT) == 0 && NT >= kBins3 && NT <= 1024, "thread count");
+  uint32_t c[P];   // c[j] = count of bin top - 1 - j
   int per, top;
   if (nbins == kBins) {
-    per = 4;
-    top = kBins - 4 * tid;
-    const uint4 u = *reinterpret_cast<const uint4*>(hist + top - 4);
-    c[0] = u.w; c[1] = u.z; c[2] = u.y; c[3] = u.x;
+    per = P;
+    top = kBins - P * tid;
+#pragma unroll
+    for (int q = 0; q < P / 4; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(hist + top - 4 * (q + 1));
+      c[4 * q] = u.w;
+      c[4 * q + 1] = u.z;
+      c[4 * q + 2] = u.y;
+      c[4 * q + 3] = u.x;
+    }
   } else {
     per = tid < nbins ? 1 : 0;
     top = nbins - tid;
     c[0] = per ? hist[top - 1] : 0u;
-    c[1] = c[2] = c[3] = 0u;
+#pragma unroll
+    for (int j = 1; j < P; ++j) c[j] = 0u;
   }
-  const uint32_t local = (c[0] + c[1]) + (c[2] + c[3]);
+  uint32_t local = 0u;
+#pragma unroll
+  for (int j = 0; j < P; ++j) local += c[j];
   uint32_t total;
-  const uint32_t above = block_scan(local, wt, &total);
+  const uint32_t above = block_scan<NT>(local, wt, &total);
   if (above < need && above + local >= need) {
     uint32_t acc = above;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < P; ++j) {
       if (j < per) {
         if (acc + c[j] >= need) {
           s_res[0] = (uint32_t)(top - 1 - j);
@@ -171,10 +186,10 @@ __device__ __forceinline__ float group_max_of(const float* srow, int64_t g, int6
 // for_each_warp(f) does the same with all 32 lanes of every warp calling f
 // the same number of times (f(key, id, active)).  level1_done: the caller
 // already filled the level-1 histogram.
-template <typename ForEach, typename ForEachWarp>
+template <int NT, typename ForEach, typename ForEachWarp>
 __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_each, ForEachWarp for_each_warp,
                                                 uint32_t* sm, const SelLayout& L, bool level1_done,
-                                                uint32_t (*wt)[kWarps], uint32_t* s_res, int32_t* out) {
+                                                uint32_t (*wt)[NT / 32], uint32_t* s_res, int32_t* out) {
   const int tid = threadIdx.x;
   uint32_t* h1 = sm + L.h1;
   uint32_t* h2 = sm + L.h2;
@@ -186,7 +201,7 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
     __syncthreads();
   }
   uint32_t need = k;
-  find_bin(h2, kBins, need, wt[0], s_res);
+  find_bin<NT>(h2, kBins, need, wt[0], s_res);
   const uint32_t b1 = s_res[0];
   need -= s_res[1];
   uint32_t K = b1 << 20, mask = 0xfff00000u;
@@ -197,7 +212,7 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
       if ((key & 0xfff00000u) == K) atomicAdd(&h1[(key >> 8) & (kBins - 1)], 1u);
     });
     __syncthreads();
-    find_bin(h1, kBins, need, wt[1], s_res);
+    find_bin<NT>(h1, kBins, need, wt[1], s_res);
     const uint32_t b2 = s_res[0];
     need -= s_res[1];
     K |= b2 << 8;
@@ -209,7 +224,7 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
         if ((key & 0xffffff00u) == K) atomicAdd(&h3[key & (kBins3 - 1)], 1u);
       });
       __syncthreads();
-      find_bin(h3, kBins3, need, wt[0], s_res);
+      find_bin<NT>(h3, kBins3, need, wt[0], s_res);
       K |= s_res[0];
       mask = 0xffffffffu;
       need -= s_res[1];
@@ -226,13 +241,13 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
     else if (m == K) atomicOr(&eqw[id >> 5], 1u << (id & 31));
   });
   __syncthreads();
-  const int wpt = (nw + kThreads - 1) / kThreads;
+  const int wpt = (nw + NT - 1) / NT;
   const int a0 = min(nw, tid * wpt), a1 = min(nw, a0 + wpt);
   uint32_t total;
   if (!all_eq) {
     uint32_t c = 0u;
     for (int i = a0; i < a1; ++i) c += __popc(eqw[i]);
-    uint32_t before = block_scan(c, wt[1], &total);
+    uint32_t before = block_scan<NT>(c, wt[1], &total);
     for (int i = a0; i < a1; ++i) {
       uint32_t e = eqw[i];
       const uint32_t pc = __popc(e);
@@ -253,7 +268,7 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
   }
   uint32_t c = 0u;
   for (int i = a0; i < a1; ++i) c += __popc(selw[i]);
-  uint32_t at = block_scan(c, wt[0], &total);
+  uint32_t at = block_scan<NT>(c, wt[0], &total);
   for (int i = a0; i < a1; ++i) {
     uint32_t e = selw[i];
     while (e) {
@@ -269,16 +284,16 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
 
 // MINB: CTAs per SM the register budget allows (2 for calls of many rows,
 // whose CTAs then share SMs; 1 keeps the fewest-row latency lowest).
-template <int NSEQ, int MINB>
-__global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
+template <int NSEQ, int MINB, int NT>
+__global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
   extern __shared__ __align__(16) uint32_t sm[];
-  __shared__ uint32_t wt[2][kWarps];
+  __shared__ uint32_t wt[2][(NT / 32)];
   __shared__ uint32_t s_res[2];
   __shared__ uint32_t s_cnt;
   const SelLayout L(max_nb);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < L.cg; i += kThreads) sm[i] = 0u;          // the three histograms
-  for (int i = L.selw + tid; i < L.total; i += kThreads) sm[i] = 0u;   // the two bitmaps
+  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;          // the three histograms
+  for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;   // the two bitmaps
   if (tid == 0) {
     s_res[0] = 0u;
     s_res[1] = 0u;
@@ -295,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
   const int k = p.top_k;
   int32_t* out = p.sel + (int64_t)r * k;
   if (nb <= k) {
-    for (int i = tid; i < k; i += kThreads) out[i] = i < nb ? i : -1;
+    for (int i = tid; i < k; i += NT) out[i] = i < nb ? i : -1;
     if (tid == 0) p.cnt[r] = (int32_t)nb;
     return;
   }
@@ -313,24 +328,26 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
   // top-12-bit histogram.
   if (p.gmax) {
     const float* grow = p.gmax + (int64_t)r * p.gld;
-    float v[kGroupsPerThread];
+    for (int g0 = 0; g0 < G; g0 += kLoadBatch * NT) {
+      float v[kLoadBatch];
 #pragma unroll
-    for (int j = 0; j < kGroupsPerThread; ++j) {
-      const int g = tid + j * kThreads;
-      v[j] = g < G ? __ldg(grow + g) : 0.f;
-    }
+      for (int j = 0; j < kLoadBatch; ++j) {
+        const int g = g0 + tid + j * NT;
+        v[j] = g < G ? __ldg(grow + g) : 0.f;
+      }
 #pragma unroll
-    for (int j = 0; j < kGroupsPerThread; ++j) {
-      const int g = tid + j * kThreads;
-      if (g < G) {
-        const uint32_t key = order_key(v[j]);
-        r1[g] = key;
-        atomicAdd(&h1[key >> 20], 1u);
+      for (int j = 0; j < kLoadBatch; ++j) {
+        const int g = g0 + tid + j * NT;
+        if (g < G) {
+          const uint32_t key = order_key(v[j]);
+          r1[g] = key;
+          atomicAdd(&h1[key >> 20], 1u);
+        }
       }
     }
   } else {
 #pragma unroll 1
-    for (int g = tid; g < G; g += kThreads) {
+    for (int g = tid; g < G; g += NT) {
       const uint32_t key = order_key(group_max_of(srow, g, nb));
       r1[g] = key;
       atomicAdd(&h1[key >> 20], 1u);
@@ -340,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
   const bool prune = G >= k;
   uint32_t B = 0u;
   if (prune) {
-    find_bin(h1, kBins, (uint32_t)k, wt[0], s_res);
+    find_bin<NT>(h1, kBins, (uint32_t)k, wt[0], s_res);
     B = s_res[0];
   }
 
   // 2a. Candidate groups: warp w owns a contiguous run of groups, 32 per round.
-  const int gpw = (G + kWarps * 32 - 1) / (kWarps * 32) * 32;
+  const int gpw = (G + (NT / 32) * 32 - 1) / ((NT / 32) * 32) * 32;
   const int ga = min(G, warp * gpw), gb = min(G, ga + gpw);
   uint32_t c = 0u;
   for (int g0 = ga; g0 < gb; g0 += 32) {
@@ -353,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
     c += __popc(__ballot_sync(0xffffffffu, g < gb && (r1[g] >> 20) >= B));
   }
   uint32_t n_cg;
-  uint32_t q = warp_prefix(c, wt[1], &n_cg);
+  uint32_t q = warp_prefix<NT>(c, wt[1], &n_cg);
   bool overflow = n_cg > (uint32_t)kGroupCap;
   if (!overflow) {
     const uint32_t below = lanes_below();
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
       q += __popc(bal);
     }
   }
-  for (int i = tid; i < kBins; i += kThreads) h1[i] = 0u;   // reused by radix level 2
+  for (int i = tid; i < kBins; i += NT) h1[i] = 0u;   // reused by radix level 2
   __syncthreads();
 
   uint32_t n_list = 0u;
@@ -374,10 +391,11 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
     // flight at once; keys in a bin >= B join the list and its level-1
     // histogram.
     const int n_ch = (int)n_cg * (kGroup / 4);
-    float4 v[kChunksPerThread];
+    for (int c0 = 0; c0 < n_ch; c0 += kChunkBatch * NT) {
+    float4 v[kChunkBatch];
 #pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int ch = tid + j * kThreads;
+    for (int j = 0; j < kChunkBatch; ++j) {
+      const int ch = c0 + tid + j * NT;
       v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (ch < n_ch) {
         const int64_t b0 = (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3);
@@ -391,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
       }
     }
 #pragma unroll
-    for (int j = 0; j < kChunksPerThread; ++j) {
-      const int ch = tid + j * kThreads;
+    for (int j = 0; j < kChunkBatch; ++j) {
+      const int ch = c0 + tid + j * NT;
       if (ch < n_ch) {
         const int64_t b0 = (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3);
         const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
@@ -420,55 +438,56 @@ __global__ void __launch_bounds__(kThreads, MINB) select_kernel(const SelectPara
         }
       }
     }
+    }
     __syncthreads();
     n_list = s_cnt;
     overflow = n_list > (uint32_t)kListCap;
   }
   if (!overflow) {
     const int n = (int)n_list;
-    radix_and_write(
+    radix_and_write<NT>(
         (uint32_t)k, nw,
         [&](auto f) {
-          for (int i = tid; i < n; i += kThreads) f(r1[i], (int32_t)r2[i]);
+          for (int i = tid; i < n; i += NT) f(r1[i], (int32_t)r2[i]);
         },
         [&](auto f) {
           const int n_pad = (n + 31) / 32 * 32;
-          for (int i = tid; i < n_pad; i += kThreads) f(i < n ? r1[i] : 0u, i < n ? (int32_t)r2[i] : 0, i < n);
+          for (int i = tid; i < n_pad; i += NT) f(i < n ? r1[i] : 0u, i < n ? (int32_t)r2[i] : 0, i < n);
         },
         sm, L, true, wt, s_res, out);
   } else {
     // The whole row from global memory (the level-1 histogram is rebuilt).
     if (n_list) {
-      for (int i = tid; i < kBins; i += kThreads) h2[i] = 0u;
+      for (int i = tid; i < kBins; i += NT) h2[i] = 0u;
       __syncthreads();
     }
     const int nbi = (int)nb;
-    radix_and_write(
+    radix_and_write<NT>(
         (uint32_t)k, nw,
         [&](auto f) {
-          for (int b0 = tid; b0 < nbi; b0 += 8 * kThreads) {   // 8 loads in flight
+          for (int b0 = tid; b0 < nbi; b0 += 8 * NT) {   // 8 loads in flight
             uint32_t kk[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int b = b0 + j * kThreads;
+              const int b = b0 + j * NT;
               kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              if (b0 + j * kThreads < nbi) f(kk[j], (int32_t)(b0 + j * kThreads));
+              if (b0 + j * NT < nbi) f(kk[j], (int32_t)(b0 + j * NT));
           }
         },
         [&](auto f) {
           const int n_pad = (nbi + 31) / 32 * 32;   // warp-uniform trip counts
-          for (int b0 = tid; b0 < n_pad; b0 += 8 * kThreads) {
+          for (int b0 = tid; b0 < n_pad; b0 += 8 * NT) {
             uint32_t kk[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const int b = b0 + j * kThreads;
+              const int b = b0 + j * NT;
               kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
             }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f(kk[j], (int32_t)(b0 + j * kThreads), b0 + j * kThreads < nbi);
+            for (int j = 0; j < 8; ++j) f(kk[j], (int32_t)(b0 + j * NT), b0 + j * NT < nbi);
           }
         },
         sm, L, false, wt, s_res, out);
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelec
   for (int o = 16; o; o >>= 1) run_min = min(run_min, __shfl_xor_sync(0xffffffffu, run_min, o));
   if ((tid & 31) == 0) wt[0][tid >> 5] = run_min;
   __syncthreads();
-  run_min = wt[0][tid & 31];
+  run_min = (tid & 31) < kWarps ? wt[0][tid & 31] : 0xffffffffu;
 #pragma unroll
   for (int o = 16; o; o >>= 1) run_min = min(run_min, __shfl_xor_sync(0xffffffffu, run_min, o));
   const uint32_t floor_key = n_run == k ? run_min : 0u;   // chunk keys must exceed this
@@ -535,7 +554,7 @@ __global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelec
   uint32_t c = 0u;
   for (int j = j0; j < j1; ++j) c += order_key(__ldg(crow + j)) > floor_key;
   uint32_t total;
-  uint32_t at = (uint32_t)n_run + block_scan(c, wt[1], &total);
+  uint32_t at = (uint32_t)n_run + block_scan<kThreads>(c, wt[1], &total);
   for (int j = j0; j < j1; ++j) {
     const uint32_t key = order_key(__ldg(crow + j));
     if (key > floor_key) {
@@ -552,7 +571,7 @@ __global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelec
     for (int i = tid; i < n_union; i += kThreads) out_s[i] = i;
   } else {
     n_sel = k;
-    radix_and_write(
+    radix_and_write<kThreads>(
         (uint32_t)k, (n_union + 31) / 32,
         [&](auto f) {
           for (int i = tid; i < n_union; i += kThreads) f(keys[i], (int32_t)i);
@@ -606,12 +625,14 @@ template <int NSEQ>
 cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_nb, cudaStream_t st) {
   if (n_rows == 0) return cudaSuccess;
   const size_t smem = select_smem_bytes(max_nb);
-  // More rows than SMs: two CTAs per SM where shared memory allows it.
-  const bool two = n_rows > device_sm_count() && 2 * (smem + 2048) <= 228 * 1024;
-  auto* kernel = two ? select_kernel<NSEQ, 2> : select_kernel<NSEQ, 1>;
+  // More rows than SMs: CTAs of 512 threads, two per SM where shared memory
+  // allows it (more rows in flight); few rows: 1,024 threads, whose per-row
+  // latency is lowest.
+  const bool many = n_rows > device_sm_count() && 2 * (smem + 2048) <= 228 * 1024;
+  auto* kernel = many ? select_kernel<NSEQ, 2, 512> : select_kernel<NSEQ, 1, 1024>;
   cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);
   if (e != cudaSuccess) return e;
-  return launch_kernel(kernel, dim3((unsigned)n_rows), dim3(kThreads), smem, st, 0u, p, max_nb);
+  return launch_kernel(kernel, dim3((unsigned)n_rows), dim3(many ? 512 : 1024), smem, st, 0u, p, max_nb);
 }
 
 template cudaError_t launch_select<1>(const SelectParams<1>&, int, int64_t, cudaStream_t);
