@@ -551,7 +551,8 @@ def main():
         achieved = flops / (score_us * 1e-6) / 1e12
         roofline_scoring = dict(roofline)
         roofline_scoring.update({"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                                 "frac": achieved / peak_tf, "traffic": None, "peak_source": tf_src,
+                                 "frac": achieved / peak_tf, "traffic": traffic_of("score_tc_kernel"),
+                                 "peak_source": tf_src,
                                  "algorithmic_flops_per_launch": flops, "executed_flops_per_launch": 3 * flops})
         roofline_scoring.pop("algorithmic_bytes_per_launch")
         # The dominant kernel is the gathered attention (tcgen05): every row
@@ -602,7 +603,8 @@ def main():
 
 # Revision tags of the kernels as built now; DRAM counters in
 # profiles/kernel_traffic.json count only for the revision they were taken on.
-KERNEL_REVS = {"score_tma_kernel": "score_tma_ring8_v4", "attn_tc_kernel": "attn_tc_ring3_v1"}
+KERNEL_REVS = {"score_tma_kernel": "score_tma_ring8_v4", "attn_tc_kernel": "attn_tc_ring3_v1",
+               "score_tc_kernel": "score_tc_planes3_v1"}
 
 if __name__ == "__main__":
     main()
