@@ -296,6 +296,28 @@ qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_i
                             int64_t group_ld, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Steps 1 and 2 in one call (hipfire, section 02): pools the blocks that each
+ * sequence's rows complete -- blocks floor((L - n_rows) / 4) .. floor(L / 4)
+ * - 1, from idx_keys[i] as qsa_pool_index_keys does, written into the
+ * sequence's pooled array -- and scores every visible block as
+ * qsa_score_blocks does.  On the few-row path (bf16 index queries, at most 4
+ * rows per sequence) the scoring kernel pools those blocks itself, so the two
+ * steps are one launch; elsewhere a pooling launch precedes the scoring.
+ *   idx_keys        HOST array of n_seqs device pointers: sequence i's index
+ *                   keys [>= L tokens] x idx_tok_stride of idx_dtype (f32 or
+ *                   bf16), 16-byte aligned; may be NULL for a sequence whose
+ *                   rows complete no block
+ *   idx_tok_stride  elements between tokens, >= 128, a multiple of 16 bytes
+ *   the rest        as qsa_score_blocks; seqs[i].pooled is written for the
+ *                   completed blocks
+ * Errors: as qsa_score_blocks and qsa_pool_index_keys.
+ */
+qsa_status qsa_pool_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* const* idx_keys,
+                                 int64_t idx_tok_stride, qsa_dtype idx_dtype, const void* q_idx, qsa_dtype q_idx_dtype,
+                                 float* scores, int64_t ld, float* group_max, int64_t group_ld, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * Scratch bytes qsa_score_blocks can use: with bf16 index queries, sequences
  * of more than 4 rows (prefill chunks) are scored as one tensor-core product
  * (tcgen05) against the pooled keys split into three bf16 planes, kept in the

@@ -70,7 +70,7 @@ EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index
            "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
            "qsa_score_select_topk_blocked", "qsa_append_tokens", "qsa_arena_create", "qsa_arena_ensure",
            "qsa_arena_base", "qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity", "qsa_arena_destroy",
-           "qsa_check_device_status", "qsa_selftest_wait_timeout")
+           "qsa_check_device_status", "qsa_selftest_wait_timeout", "qsa_pool_score_blocks")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -94,6 +94,7 @@ def lib() -> ctypes.CDLL:
     L.qsa_selftest_wait_timeout.argtypes = [i32, vp]
     L.qsa_pool_index_keys.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp]
     L.qsa_score_blocks.argtypes = [seqp, i32, vp, i32, vp, i64, vp, i64, vp, sz, vp]
+    L.qsa_pool_score_blocks.argtypes = [seqp, i32, ctypes.POINTER(vp), i64, i32, vp, i32, vp, i64, vp, i64, vp, sz, vp]
     L.qsa_score_workspace_size.argtypes = [seqp, i32, i32]
     L.qsa_score_workspace_size.restype = sz
     L.qsa_select_workspace_size.argtypes = [seqp, i32, i32]
@@ -269,6 +270,35 @@ def score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, s
     _check("qsa_score_blocks", lib().qsa_score_blocks(
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0),
         _ptr(group_max), 0 if group_max is None else group_max.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
+def _idx_key_array(seqs):
+    """(host pointer array, token stride, dtype code) of the sequences' index
+    keys for qsa_pool_score_blocks, or None when they are missing or differ
+    in dtype or stride."""
+    keys = [sq.idx_keys for sq in seqs]
+    if not keys or any(k is None for k in keys) or len({(k.dtype, k.stride(0)) for k in keys}) != 1:
+        return None
+    return (ctypes.c_void_p * len(keys))(*[k.data_ptr() for k in keys]), keys[0].stride(0), _dtype_code(keys[0])
+
+
+def pool_score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=None, seq_array=None,
+                      group_max: torch.Tensor | None = None, workspace: torch.Tensor | None = None, idx_array=None):
+    """Steps 1 and 2 in one call: pools the blocks each sequence's rows
+    complete (from its idx_keys into its pooled keys) and scores every visible
+    block, in one launch on the few-row path."""
+    arr = seq_array if seq_array is not None else make_seq_array(seqs)
+    ia = idx_array if idx_array is not None else _idx_key_array(seqs)
+    if ia is None:
+        raise ValueError("pool_score_blocks: every sequence needs index keys of one dtype and stride")
+    if workspace is None:
+        need = score_workspace_size(None, q_idx, seq_array=arr)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
+    _check("qsa_pool_score_blocks", lib().qsa_pool_score_blocks(
+        arr, len(arr), ia[0], ia[1], ia[2], q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(),
+        scores.stride(0), _ptr(group_max), 0 if group_max is None else group_max.stride(0), _ptr(workspace),
         0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
@@ -514,6 +544,8 @@ class LayerStep:
             b1 = s.n_tokens // 4
             if b1 > b0:
                 self.pool_jobs.append((s.idx_keys, s.pooled, b0, b1 - b0))
+        # Steps 1 and 2 in one call when every sequence has index keys and pooled keys.
+        self.idx_array = _idx_key_array(self.seqs) if all(s.pooled is not None for s in self.seqs) else None
 
     def pool(self, stream=None):
         for idxk, pooled, b0, n in self.pool_jobs:
@@ -522,6 +554,15 @@ class LayerStep:
     def score(self, stream=None):
         score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr, group_max=self.group_max,
                      workspace=self.score_ws)
+
+    def pool_score(self, stream=None):
+        """pool() then score(), as one call (one launch on the few-row path)."""
+        if self.idx_array is None:
+            self.pool(stream)
+            self.score(stream)
+            return
+        pool_score_blocks(None, self.q_idx, self.scores, stream, seq_array=self.arr, group_max=self.group_max,
+                          workspace=self.score_ws, idx_array=self.idx_array)
 
     def select(self, stream=None):
         select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr,
@@ -546,10 +587,10 @@ class LayerStep:
         """One layer step: pool (or append new_tokens and pool), score,
         select, attend."""
         if new_tokens is None:
-            self.pool(stream)
+            self.pool_score(stream)
         else:
             self.append(new_tokens, stream)
-        self.score(stream)
+            self.score(stream)
         self.select(stream)
         self.attend(stream)
         return self.out, self.lse

@@ -185,9 +185,19 @@ QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype
 }
 
 // ------------------------------------------------------------------ step 2
+namespace {
+// Index-key caches of the sequences of a pooling + scoring call.
+struct IdxKeys {
+  const void* const* keys;   // host array: one device pointer per sequence
+  int64_t tok_stride;
+  qsa_dtype dtype;
+};
+}  // namespace
+
 template <int NSEQ>
 static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const void* q_idx, qsa_dtype qd,
-                              float* scores, int64_t ld, float* gmax, int64_t gld, cudaStream_t st) {
+                              float* scores, int64_t ld, float* gmax, int64_t gld, const IdxKeys* ik,
+                              cudaStream_t st) {
   ScoreParams<NSEQ> p{};
   p.gmax = gmax;
   p.gld = gld;
@@ -204,6 +214,13 @@ static qsa_status score_chunk(const qsa_seq* seqs, int n, int32_t row_begin, con
     q.n_tiles = (int32_t)((max_visible_blocks(seqs[i]) + tile - 1) / tile);
     q.n_groups = (q.n_rows + kRowGroup - 1) / kRowGroup;
     q.work_begin = work;
+    if (ik) {   // step 1 for the blocks the rows complete, inside the launch where the kernel allows it
+      q.idx_keys = ik->keys[i];
+      q.idx_stride = ik->tok_stride;
+      q.idx_dtype = ik->dtype;
+      q.pool_b0 = (seqs[i].n_tokens - seqs[i].n_rows) / 4;
+      q.pool_b1 = seqs[i].n_tokens / 4;
+    }
     work += (int64_t)q.n_tiles * q.n_groups;
     max_rows = std::max(max_rows, std::min(kRowGroup, q.n_rows));
     row_begin += seqs[i].n_rows;
@@ -232,13 +249,20 @@ QSA_API size_t qsa_score_workspace_size(const qsa_seq* seqs, int32_t n_seqs, qsa
   return need;
 }
 
-QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
-                            float* scores, int64_t ld, float* group_max, int64_t group_ld, void* workspace,
-                            size_t workspace_bytes, void* stream) {
-  const char* fn = "qsa_score_blocks";
+static qsa_status score_blocks_impl(const char* fn, const qsa_seq* seqs, int32_t n_seqs, const IdxKeys* ik,
+                                   const void* q_idx, qsa_dtype q_idx_dtype, float* scores, int64_t ld,
+                                   float* group_max, int64_t group_ld, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
   if (s != QSA_OK) return s;
+  if (ik) {
+    if (!ik->keys) return fail(QSA_ERR_INVALID_ARG, "%s: null idx_keys array", fn);
+    if (!valid_dtype(ik->dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: idx_dtype %d", fn, (int)ik->dtype);
+    if (ik->tok_stride < QSA_INDEX_DIM) return fail(QSA_ERR_INVALID_ARG, "%s: idx_tok_stride < %d", fn, QSA_INDEX_DIM);
+    if ((ik->tok_stride * (int64_t)dtype_size(ik->dtype)) % 16 != 0)
+      return fail(QSA_ERR_MISALIGNED, "%s: idx_tok_stride not a multiple of 16 bytes", fn);
+  }
   if (!valid_dtype(q_idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: q_idx_dtype %d", fn, (int)q_idx_dtype);
   if (!q_idx || !scores) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (!aligned16(q_idx) || !aligned16(scores)) return fail(QSA_ERR_MISALIGNED, "%s: q_idx/scores not aligned", fn);
@@ -258,6 +282,11 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
       if (!aligned16(q.pooled) || q.pooled_stride % 4 != 0)
         return fail(QSA_ERR_MISALIGNED, "%s: pooled keys of sequence %d not 16-byte aligned", fn, i);
     }
+    if (ik && q.n_tokens / 4 > (q.n_tokens - q.n_rows) / 4) {
+      if (!ik->keys[i]) return fail(QSA_ERR_INVALID_ARG, "%s: sequence %d has no index keys", fn, i);
+      if (!aligned16(ik->keys[i]))
+        return fail(QSA_ERR_MISALIGNED, "%s: index keys of sequence %d not 16-byte aligned", fn, i);
+    }
   }
   cudaStream_t st = as_stream(stream);
   const size_t tc_need = qsa_score_workspace_size(seqs, n_seqs, q_idx_dtype);
@@ -269,28 +298,54 @@ QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const v
     for (int i = 0; i < n_seqs && s == QSA_OK; ++i) {
       const qsa_seq& q = seqs[i];
       if (wide_seq(q, q_idx_dtype)) {
+        const int64_t pb0 = (q.n_tokens - q.n_rows) / 4, pb1 = q.n_tokens / 4;
+        if (ik && pb1 > pb0) {   // step 1 first: the tensor-core kernel reads pooled keys only
+          cudaError_t e = launch_pool(ik->keys[i], ik->dtype, ik->tok_stride, pb0, pb1 - pb0,
+                                      const_cast<float*>(q.pooled), q.pooled_stride, st);
+          if (e != cudaSuccess) return cuda_fail(e, fn);
+        }
         cudaError_t e = launch_score_tc(q_idx, row_begin, q.n_rows, q.n_tokens, q.pooled, q.pooled_stride, 0,
                                         q.n_tokens / 4, scores, ld, group_max, group_ld, workspace, st);
         if (e == cudaErrorNotSupported)
-          s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+          s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, nullptr, st);
         else if (e != cudaSuccess)
           s = cuda_fail(e, fn);
       } else {
-        s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+        IdxKeys one{ik ? ik->keys + i : nullptr, ik ? ik->tok_stride : 0, ik ? ik->dtype : QSA_F32};
+        s = score_chunk<1>(seqs + i, 1, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld,
+                           ik ? &one : nullptr, st);
       }
       row_begin += q.n_rows;
     }
   } else if (n_seqs == 1) {
-    s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+    s = score_chunk<1>(seqs, 1, 0, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, ik, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = score_chunk<kLaunchSeqs>(seqs + c, n, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld, st);
+      IdxKeys part{ik ? ik->keys + c : nullptr, ik ? ik->tok_stride : 0, ik ? ik->dtype : QSA_F32};
+      s = score_chunk<kLaunchSeqs>(seqs + c, n, row_begin, q_idx, q_idx_dtype, scores, ld, group_max, group_ld,
+                                   ik ? &part : nullptr, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
   return s == QSA_OK ? ok() : s;
+}
+
+QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
+                                    float* scores, int64_t ld, float* group_max, int64_t group_ld, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return score_blocks_impl("qsa_score_blocks", seqs, n_seqs, nullptr, q_idx, q_idx_dtype, scores, ld, group_max,
+                           group_ld, workspace, workspace_bytes, stream);
+}
+
+QSA_API qsa_status qsa_pool_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* const* idx_keys,
+                                         int64_t idx_tok_stride, qsa_dtype idx_dtype, const void* q_idx,
+                                         qsa_dtype q_idx_dtype, float* scores, int64_t ld, float* group_max,
+                                         int64_t group_ld, void* workspace, size_t workspace_bytes, void* stream) {
+  const IdxKeys ik{idx_keys, idx_tok_stride, idx_dtype};
+  return score_blocks_impl("qsa_pool_score_blocks", seqs, n_seqs, &ik, q_idx, q_idx_dtype, scores, ld, group_max,
+                           group_ld, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ step 3

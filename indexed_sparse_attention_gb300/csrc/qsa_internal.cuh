@@ -28,6 +28,13 @@ struct ScoreSeq {
   int32_t n_rows;
   int32_t n_tiles;       // ceil(floor(L/4) / kScoreTile)
   int32_t n_groups;      // ceil(n_rows / kRowGroup)
+  // Optional step 1 inside the scoring launch: blocks [pool_b0, pool_b1) are
+  // pooled from their four index keys (idx_keys, idx_stride elements between
+  // tokens, idx_dtype) and written to pooled before they are scored.
+  const void* idx_keys;
+  int64_t idx_stride;
+  int32_t idx_dtype;
+  int64_t pool_b0, pool_b1;
 };
 
 template <int NSEQ>

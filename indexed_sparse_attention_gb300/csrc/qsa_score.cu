@@ -386,7 +386,9 @@ constexpr int kBoxBytes = kBoxRows * 128;                     // 32 rows x 32 fp
 constexpr int kItemBytes = 4 * kBoxBytes;                     // 16 KB
 static_assert((kTmaItems * kItemTiles) % kTmaConsumers == 0, "tile slots split evenly over consumers");
 static_assert(kTmaItems <= 32, "one producer lane per ring slot");
+constexpr int kPoolScratch = 4 * QSA_INDEX_DIM * 4;               // one block's four f32 index keys
 constexpr size_t kTmaSmem = (size_t)kTmaItems * kItemBytes + 1024;   // + alignment slack
+constexpr size_t kTmaPoolSmem = kTmaSmem + (size_t)kTmaConsumers * kPoolScratch;   // + a scratch per consumer
 
 __device__ int g_score_wait_timeouts;   // waits that gave up (never expected)
 
@@ -433,6 +435,32 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Lane l's channels 4l .. 4l + 3 of the four index keys of block b.
+__device__ __forceinline__ void load_index_keys(const ScoreSeq& sq, int64_t b, int lane, float4 (&k)[4]) {
+  if (sq.idx_dtype == QSA_F32) {
+    const float* src = static_cast<const float*>(sq.idx_keys) + 4 * b * sq.idx_stride + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) k[j] = *reinterpret_cast<const float4*>(src + j * sq.idx_stride);
+  } else {
+    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(sq.idx_keys) + 4 * b * sq.idx_stride + 4 * lane;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint2 w = *reinterpret_cast<const uint2*>(src + j * sq.idx_stride);
+      k[j] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+  }
+}
+
+// The pooling kernel's arithmetic: ((k0 + k1) + k2) + k3, times 0.25.
+__device__ __forceinline__ float4 pool4(const float4 (&k)[4]) {
+  float4 m;
+  m.x = (((k[0].x + k[1].x) + k[2].x) + k[3].x) * 0.25f;
+  m.y = (((k[0].y + k[1].y) + k[2].y) + k[3].y) * 0.25f;
+  m.z = (((k[0].z + k[1].z) + k[2].z) + k[3].z) * 0.25f;
+  m.w = (((k[0].w + k[1].w) + k[2].w) + k[3].w) * 0.25f;
+  return m;
+}
+
 template <int NSEQ>
 struct ScoreTmaParams {
   CUtensorMap tmap[NSEQ];      // pooled keys of sequence i: [n_tokens / 4 rows, 128] fp32
@@ -450,7 +478,8 @@ __device__ __forceinline__ int find_seq_by_item(const ScoreTmaParams<NSEQ>& P, i
   return s;
 }
 
-template <int NT, int NSEQ>
+// POOL: the launch also pools the step's completed blocks (qsa_pool_score_blocks).
+template <int NT, int NSEQ, bool POOL>
 __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     score_tma_kernel(const __grid_constant__ ScoreTmaParams<NSEQ> P) {
   static_assert(NT <= 2, "the TMA path serves groups of <= 4 rows");
@@ -507,6 +536,35 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
   // Consumers.
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
+  // The first block this warp pools (a completed block of the step in one of
+  // its tiles): its four index keys are copied now into the warp's scratch,
+  // so the copy overlaps the stream; any further ones are read when reached.
+  unsigned char* keys_s = items + (size_t)kTmaItems * kItemBytes + (size_t)cw * kPoolScratch;
+  int64_t pf_b = -1;
+  int pf_si = -1;
+#pragma unroll
+  for (int s = 0; s < NSEQ; ++s) {
+    if (!POOL || s >= p.n_seqs) break;
+    const ScoreSeq& sq = p.seq[s];
+    for (int64_t b = sq.pool_b0; b < sq.pool_b1 && pf_b < 0; ++b) {
+      const int64_t item = P.item_begin[s] + b / kItemBlocks;
+      if (item < i0 || item >= i1) continue;
+      const int q = (int)((item - i0) % kTmaItems);
+      const int j = (int)((b % kItemBlocks) / kScoreTile);
+      if ((kItemTiles * q + j) % kTmaConsumers != cw) continue;
+      const int es = sq.idx_dtype == QSA_F32 ? 4 : 2;
+      const int chunks = QSA_INDEX_DIM * es / 16;   // per key row
+      for (int c = lane; c < 4 * chunks; c += 32) {
+        const char* src = static_cast<const char*>(sq.idx_keys) + ((4 * b + c / chunks) * sq.idx_stride) * es +
+                          (c % chunks) * 16;
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(keys_s + c * 16);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+      }
+      asm volatile("cp.async.commit_group;\n" ::: "memory");
+      pf_b = b;
+      pf_si = s;
+    }
+  }
   uint32_t bq[NT][8][2];   // packed bf16 pairs (channels +0, +1) and (+2, +3)
   int bq_si = -1;
   for (int n = 0; n < n_items; ++n) {
@@ -540,6 +598,34 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     float acc[NT][4];
     if (valid) {
       const unsigned char* tl = items + (size_t)q * kItemBytes + j * (kScoreTile * 128);
+      // Step 1 for the tile's completed blocks: replace the rows the tensor
+      // copy brought with the mean of their index keys, and store it.
+      const int64_t plo = POOL ? max(sq.pool_b0, b0) : 0, phi = POOL ? min(sq.pool_b1, b0 + kScoreTile) : 0;
+      for (int64_t b = plo; b < phi; ++b) {
+        float4 k4[4];
+        if (b == pf_b && si == pf_si) {
+          asm volatile("cp.async.wait_all;\n" ::: "memory");
+          __syncwarp();
+          if (sq.idx_dtype == QSA_F32) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) k4[e] = *reinterpret_cast<const float4*>(keys_s + e * 512 + 16 * lane);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const uint2 w = *reinterpret_cast<const uint2*>(keys_s + e * 256 + 8 * lane);
+              k4[e] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+            }
+          }
+        } else {
+          load_index_keys(sq, b, lane, k4);
+        }
+        const float4 m = pool4(k4);
+        const int rr = (int)(b - b0);   // row of the tile
+        *reinterpret_cast<float4*>(items + (size_t)q * kItemBytes + j * (kScoreTile * 128) + (lane >> 3) * kBoxBytes +
+                                   rr * 128 + (((lane & 7) ^ (rr & 7)) << 4)) = m;
+        *reinterpret_cast<float4*>(const_cast<float*>(sq.pooled) + b * sq.pooled_stride + 4 * lane) = m;
+      }
+      if (phi > plo) __syncwarp();
       float ah[2][NT][4], al[2][NT][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u)
@@ -612,6 +698,8 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
       }
     }
   }
+  // A key copy whose tile was never reached (a wait that gave up) lands before exit.
+  if constexpr (POOL) asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
@@ -740,30 +828,51 @@ cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorNotSupported;
   }
-  const void* k = max_rows_per_group <= 2 ? (const void*)score_tma_kernel<1, NSEQ> : (const void*)score_tma_kernel<2, NSEQ>;
-  cudaError_t e = allow_dynamic_smem(k, kTmaSmem);
+  bool pool = false;
+  for (int i = 0; i < p.n_seqs; ++i) pool |= p.seq[i].pool_b1 > p.seq[i].pool_b0;
+  const size_t smem = pool ? kTmaPoolSmem : kTmaSmem;
+  const void* k = max_rows_per_group <= 2 ? (pool ? (const void*)score_tma_kernel<1, NSEQ, true>
+                                                  : (const void*)score_tma_kernel<1, NSEQ, false>)
+                                          : (pool ? (const void*)score_tma_kernel<2, NSEQ, true>
+                                                  : (const void*)score_tma_kernel<2, NSEQ, false>);
+  cudaError_t e = allow_dynamic_smem(k, smem);
   if (e != cudaSuccess) return e;
   P.n_items = n_items;
   if (n_items == 0) return cudaSuccess;
   const int64_t ctas = (int64_t)sms * kTmaCtasPerSm;
   const unsigned grid = (unsigned)(n_items < ctas ? n_items : ctas);
   const dim3 block(32 * (1 + kTmaConsumers));
-  if (max_rows_per_group <= 2) return launch_kernel(score_tma_kernel<1, NSEQ>, dim3(grid), block, kTmaSmem, st, 0u, P);
-  return launch_kernel(score_tma_kernel<2, NSEQ>, dim3(grid), block, kTmaSmem, st, 0u, P);
+  if (max_rows_per_group <= 2) {
+    if (pool) return launch_kernel(score_tma_kernel<1, NSEQ, true>, dim3(grid), block, smem, st, 0u, P);
+    return launch_kernel(score_tma_kernel<1, NSEQ, false>, dim3(grid), block, smem, st, 0u, P);
+  }
+  if (pool) return launch_kernel(score_tma_kernel<2, NSEQ, true>, dim3(grid), block, smem, st, 0u, P);
+  return launch_kernel(score_tma_kernel<2, NSEQ, false>, dim3(grid), block, smem, st, 0u, P);
 }
 
 }  // namespace
 
 template <int NSEQ>
-cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
-  if (p.n_work == 0) return cudaSuccess;
+cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
+  if (p_in.n_work == 0) return cudaSuccess;
+  const int sms = device_sm_count();
+  if (q_dtype != QSA_F32 && max_rows_per_group <= 4) {
+    cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
+  // The other kernels do not pool: the pooling launches first.
+  ScoreParams<NSEQ> p = p_in;
+  for (int i = 0; i < p.n_seqs; ++i) {
+    ScoreSeq& sq = p.seq[i];
+    if (sq.pool_b1 > sq.pool_b0) {
+      cudaError_t e = launch_pool(sq.idx_keys, (qsa_dtype)sq.idx_dtype, sq.idx_stride, sq.pool_b0,
+                                  sq.pool_b1 - sq.pool_b0, const_cast<float*>(sq.pooled), sq.pooled_stride, st);
+      if (e != cudaSuccess) return e;
+    }
+    sq.pool_b0 = sq.pool_b1 = 0;
+  }
   if (q_dtype == QSA_F32) {
     return launch_kernel(score_simt_kernel<NSEQ>, dim3((unsigned)p.n_work), dim3(256), 0, st, 0u, p);
-  }
-  const int sms = device_sm_count();
-  if (max_rows_per_group <= 4) {
-    cudaError_t e = launch_score_tma(p, max_rows_per_group, sms, st);
-    if (e != cudaErrorNotSupported) return e;
   }
   constexpr int Ws = 12;
   const size_t smem = sizeof(float) * Ws * kScoreStages * kStageFloats;

@@ -98,6 +98,57 @@ def test_scores_zero_query_and_nonnegative():
     assert (got[0, :399] >= 0).all() and (got[1] >= 0).all()
 
 
+# ------------------------------------------------------------------ steps 1 + 2 in one call
+# (idx dtype, q_idx dtype): bf16/bf16 takes the few-row kernel that pools in
+# place; f32 index queries, 600-row sequences (tensor cores) and ragged
+# batches check the paths that pool in a launch of their own.
+@pytest.mark.parametrize("Ls,Ms,idx_dtype,q_dtype", [
+    ([261_120], [4], torch.bfloat16, torch.bfloat16), ([65_536], [1], torch.bfloat16, torch.bfloat16),
+    ([9001], [3], torch.float32, torch.bfloat16), ([9001], [4], torch.bfloat16, torch.float32),
+    ([4099], [600], torch.bfloat16, torch.bfloat16), ([4097], [1], torch.bfloat16, torch.bfloat16),
+    ([4099, 700, 30_000, 9, 2052, 65_540], [4, 1, 2, 3, 1, 4], torch.bfloat16, torch.bfloat16)])
+def test_pool_score_equals_pool_then_score(Ls, Ms, idx_dtype, q_dtype):
+    runs = []
+    for fused in (True, False):
+        seqs, rows = [], 0
+        q_parts = []
+        for i, (L, M) in enumerate(zip(Ls, Ms)):
+            x = make_layer(L=L, M=M, dtype=torch.float32, seed=100 + i, device=dev())
+            idxk = x.idxk.to(idx_dtype)
+            pooled = pooled_buffer(L, dev())              # NaN: new blocks must be written
+            b0 = (L - M) // 4
+            if b0:
+                qsa.pool_index_keys(idxk, pooled, 0, b0)
+            seqs.append(qsa.Seq(L, M, pooled, idx_keys=idxk))
+            q_parts.append(x.q_idx.to(q_dtype))
+            rows += M
+        q_idx = torch.cat(q_parts)
+        ld = (max(L // 4 for L in Ls) + 3) // 4 * 4
+        scores = torch.full((rows, ld), float("nan"), device=dev())
+        gmax = torch.full((rows, (qsa.n_groups(max(Ls)) + 3) // 4 * 4), float("nan"), device=dev())
+        if fused:
+            qsa.pool_score_blocks(seqs, q_idx, scores, group_max=gmax)
+        else:
+            for sq in seqs:
+                b0, b1 = (sq.n_tokens - sq.n_rows) // 4, sq.n_tokens // 4
+                if b1 > b0:
+                    qsa.pool_index_keys(sq.idx_keys, sq.pooled, b0, b1 - b0)
+            qsa.score_blocks(seqs, q_idx, scores, group_max=gmax)
+        torch.cuda.synchronize()
+        runs.append((seqs, scores, gmax))
+    (sa, sc_a, gm_a), (sb, sc_b, gm_b) = runs
+    r = 0
+    for qa, qb in zip(sa, sb):
+        L, M = qa.n_tokens, qa.n_rows
+        assert torch.equal(qa.pooled[:L // 4], qb.pooled[:L // 4])
+        for j in range(M):
+            nb = (L - M + j + 1) // 4
+            assert torch.equal(sc_a[r, :nb], sc_b[r, :nb])
+            ng = (nb + 15) // 16
+            assert torch.equal(gm_a[r, :ng], gm_b[r, :ng])
+            r += 1
+
+
 # ------------------------------------------------------------------ step 3
 def group_maxima(scores_f32: np.ndarray, row_pos) -> np.ndarray:
     """Per row, the maximum score of every group of 16 visible blocks (the
