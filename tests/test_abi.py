@@ -93,6 +93,23 @@ def test_pool_validation(L):
     assert L.qsa_last_error().decode() == ""
 
 
+def test_pool_score_validation(L):
+    # Checks that run before any launch (a null key array, dtypes, strides,
+    # a sequence that completes a block without keys).
+    seq = _seq()
+    keys = (ctypes.c_void_p * 1)(FAKE)
+    none = (ctypes.c_void_p * 1)(None)
+    mis = (ctypes.c_void_p * 1)(FAKE_MIS)
+    args = (FAKE, qsa.BF16, FAKE, 1024, None, 0, None, 0, None)
+    assert L.qsa_pool_score_blocks(seq, 1, None, 128, qsa.BF16, *args) == 1
+    assert L.qsa_pool_score_blocks(seq, 1, keys, 128, 9, *args) == 2
+    assert L.qsa_pool_score_blocks(seq, 1, keys, 64, qsa.BF16, *args) == 1
+    assert L.qsa_pool_score_blocks(seq, 1, keys, 132, qsa.BF16, *args) == 3       # 264 bytes per token
+    assert L.qsa_pool_score_blocks(seq, 1, none, 128, qsa.BF16, *args) == 1       # rows complete block 1,024
+    assert L.qsa_pool_score_blocks(seq, 1, mis, 128, qsa.BF16, *args) == 3
+    assert "qsa_pool_score_blocks" in L.qsa_last_error().decode()
+
+
 def test_score_validation(L):
     seq = _seq()
     assert L.qsa_score_blocks(seq, 0, FAKE, qsa.BF16, FAKE, 1024, None, 0, None, 0, None) == 1
