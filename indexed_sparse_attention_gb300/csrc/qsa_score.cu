@@ -16,6 +16,13 @@
 // bf16 queries are exact in both formats.  Every tile of 16 blocks is one
 // group of the group maxima the selection starts from.  fp32 index queries
 // take a CUDA-core kernel.
+//
+// Steps 1 and 2 in one call (qsa_pool_score_blocks): on the few-row path the
+// scoring launch pools the blocks the step's rows complete -- the consumer
+// warp whose tile holds such a block averages the block's four index keys
+// (the pooling kernel's order of operations), overwrites that row of the
+// landed tile and stores it to the pooled keys -- so the step has no pooling
+// launch; the other kernels get a pooling launch before them.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
