@@ -108,6 +108,23 @@ def test_scores_zero_query_and_nonnegative():
     ([4099], [600], torch.bfloat16, torch.bfloat16), ([4097], [1], torch.bfloat16, torch.bfloat16),
     ([4099, 700, 30_000, 9, 2052, 65_540], [4, 1, 2, 3, 1, 4], torch.bfloat16, torch.bfloat16)])
 def test_pool_score_equals_pool_then_score(Ls, Ms, idx_dtype, q_dtype):
+    _pool_score_vs_separate(Ls, Ms, idx_dtype, q_dtype)
+
+
+# Batches of 8 sequences, long and short mixed.  On a 152-SM GB300 each of
+# these puts the completed blocks of two sequences in one consumer warp of
+# the few-row kernel (the last items of a long and of a short sequence, 4
+# items apart in one CTA), so one warp pools a second block from keys read
+# when its tile is reached rather than from its prefetched copy.
+@pytest.mark.parametrize("Ls,Ms", [
+    ([386, 122_275, 255, 38, 79, 161_101, 214, 232], [1, 1, 3, 2, 3, 4, 2, 2]),
+    ([176_377, 124, 109, 237, 188, 392, 351, 390], [3, 2, 1, 3, 3, 4, 4, 4]),
+    ([102_237, 120, 145_450, 195_651, 24, 263, 196_566, 465], [4, 1, 1, 1, 2, 2, 4, 4])])
+def test_pool_score_many_sequences(Ls, Ms):
+    _pool_score_vs_separate(Ls, Ms, torch.bfloat16, torch.bfloat16)
+
+
+def _pool_score_vs_separate(Ls, Ms, idx_dtype, q_dtype):
     runs = []
     for fused in (True, False):
         seqs, rows = [], 0
