@@ -4,11 +4,16 @@ Default workload: the fixed four-row verify at a 261,120-token context,
 bf16 K/V and index keys (pooled keys fp32), 24 query heads over 2 KV heads,
 head_dim 256, 12 independent QSA layers, top 512 blocks plus the tail.
 One bench "step" is one pass of the whole hot path -- pool the block the new
-rows completed, score every visible block, select the top 512, sparse
+rows completed and score every visible block (one launch), select the top 512, sparse
 attention with its split merge -- over all 12 layers, layer after layer on
 one stream, captured once in a CUDA graph.  The metric is QSA layer-steps/s.
 
-Prints ONE JSON line (rank 0).  See the design doc for the accounting.
+Prints ONE JSON line (rank 0): layer-steps/s, the roofline of the step's
+scoring launch (algorithmic bytes / isolated launch time against the
+measured HBM copy bandwidth), the end-to-end rate through the public API
+with host buffers, the oracle's rate on the host cores, and the SM clocks.
+Other workloads: the 65,536-token decode, a 2,048-row prefill chunk, and the
+decode and verify steps over fp8 or q8 K/V state.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--layers N] [--impl ours|reference] [--no-cpu-baseline]
@@ -43,21 +48,37 @@ L2_BYTES = 129 * 2 ** 20
 class Layer:
     """Device-resident state of one QSA layer for one sequence."""
 
-    def __init__(self, L, M, dtype, seed, layer, n_planted, head_dim, device):
+    def __init__(self, L, M, dtype, seed, layer, n_planted, head_dim, device, kv_state=None):
         import indexed_sparse_attention_gb300 as qsa
         x = make_layer(L=L, M=M, dtype=dtype, seed=seed, layer=layer, n_planted=n_planted, head_dim=head_dim,
                        device=device)
         self.x = x
+        self.kv_state = kv_state
         self.pooled = torch.empty((qsa.n_pooled_slots(L), 128), dtype=torch.float32, device=device)
         first_new = (L - M) // 4
         if first_new:
             qsa.pool_index_keys(x.idxk, self.pooled, 0, first_new)    # state from earlier steps (untimed)
-        self.seq = qsa.Seq(L, M, self.pooled, [qsa.Segment(x.k, x.v, 0)], idx_keys=x.idxk)
+        if kv_state is None:
+            seg = qsa.Segment(x.k, x.v, 0)
+        else:
+            # Quantized caches written from the bf16 draw by the library's
+            # append of every token (untimed): codes and scale records.
+            codes = torch.uint8 if kv_state == "fp8" else torch.int8
+            rec = 2 if kv_state == "fp8" else 2 * head_dim // 32
+            kc = torch.zeros(x.k.shape, dtype=codes, device=device)
+            vc = torch.zeros_like(kc)
+            sc = torch.zeros((x.k.shape[0], L, rec), dtype=torch.float16, device=device)
+            seg = qsa.Segment(kc, vc, 0, kv_scale=sc)
+            fill = qsa.Seq(L, L, self.pooled, [seg], idx_keys=x.idxk)
+            qsa.append_tokens(fill, x.k.contiguous(), x.v.contiguous(), x.idxk.clone())
+            torch.cuda.synchronize(device)
+        self.seq = qsa.Seq(L, M, self.pooled, [seg], idx_keys=x.idxk)
         self.step = qsa.LayerStep([self.seq], x.q_idx, x.q, out_dtype=torch.float32)
 
 
 def build_layers(spec, n_layers, device, seed=0):
-    return [Layer(spec["L"], spec["M"], spec["dtype"], seed, l, spec["n_planted"], spec["head_dim"], device)
+    return [Layer(spec["L"], spec["M"], spec["dtype"], seed, l, spec["n_planted"], spec["head_dim"], device,
+                  spec.get("kv_state"))
             for l in range(n_layers)]
 
 
@@ -75,10 +96,21 @@ def launches_per_layer(layer) -> int:
 
 
 def algorithmic_bytes(layer) -> dict:
-    """Bytes one layer-step must move (measurement)."""
+    """Bytes one layer-step must move: the pooled keys once, the scores, the
+    index queries, the selected K/V rows of both KV heads (each row once per
+    query row), the queries and the outputs; not the dense K/V left unread."""
     x = layer.x
     L, M = x.L, x.M
+    # K/V bytes per (KV head, token): both rows, plus their scale record for
+    # quantized state.
     kv_es = x.k.element_size()
+    D_ = x.q.shape[2]
+    if layer.kv_state == "fp8":
+        kv_tok = 2 * D_ + 4
+    elif layer.kv_state == "q8":
+        kv_tok = 2 * D_ + D_ // 8
+    else:
+        kv_tok = 2 * D_ * kv_es
     D, Hq, Hkv = x.q.shape[2], x.q.shape[1], x.k.shape[0]
     idx_es = x.idxk.element_size()
     nb_max = L // 4
@@ -90,7 +122,7 @@ def algorithmic_bytes(layer) -> dict:
     for p in x.row_pos:
         nb = (p + 1) // 4
         rows.append(4 * min(512, nb) + (p + 1) % 4)
-    attn_b = sum(rows) * Hkv * D * 2 * kv_es + x.q.numel() * x.q.element_size() + M * Hq * (D * 4 + 4)
+    attn_b = sum(rows) * Hkv * kv_tok + x.q.numel() * x.q.element_size() + M * Hq * (D * 4 + 4)
     return {"pool": pool_b, "score": score_b, "attn": attn_b, "total": pool_b + score_b + attn_b,
             "score_pooled_only": nb_max * 128 * 4}
 
@@ -297,7 +329,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="verify_m4_261k_bf16",
                     choices=["verify_m4_261k_bf16", "decode_m1_65k_bf16", "prefill_t2048_100k_bf16",
-                             "tiny_verify_f32"])
+                             "tiny_verify_f32", "verify_m4_261k_fp8", "decode_m1_65k_fp8", "verify_m4_261k_q8",
+                             "decode_m1_65k_q8"])
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's 12)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -583,6 +616,7 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "context": L, "rows": M, "layers_per_step": n_layers,
                    "q_heads": 24, "kv_heads": 2, "head_dim": spec["head_dim"], "top_k_blocks": 512,
+                   "kv_state": spec.get("kv_state") or "bf16",
                    "index_heads": 4, "index_dim": 128, "graph": "one CUDA graph per step (all layers)",
                    "l2": f"inputs larger than L2: {n_layers} distinct layers, "
                          f"{ab['total'] * n_layers / 2**20:.0f} MiB algorithmic bytes per step",

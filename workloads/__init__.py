@@ -131,4 +131,16 @@ WORKLOADS = {
     "prefill_t2048_100k_bf16": dict(L=100_352 + 2048, M=2048, dtype=torch.bfloat16, layers=1, n_planted=256,
                                     head_dim=256),
     "ragged_segmented_bf16": dict(n_seqs=16, dtype=torch.bfloat16, n_planted=256, head_dims=(256, 128)),
+    # The same decode and verify steps over quantized K/V state (fp8: E4M3 codes
+    # with an f16 scale pair per head and token; q8: Q8_0, int8 codes with an
+    # f16 scale per 32 elements), the caches written from the bf16 draw by the
+    # library's own append, as a model's cache would be.
+    "decode_m1_65k_fp8": dict(L=65_536, M=1, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256,
+                              kv_state="fp8"),
+    "verify_m4_261k_fp8": dict(L=261_120, M=4, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256,
+                               kv_state="fp8"),
+    "decode_m1_65k_q8": dict(L=65_536, M=1, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256,
+                             kv_state="q8"),
+    "verify_m4_261k_q8": dict(L=261_120, M=4, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256,
+                              kv_state="q8"),
 }
