@@ -305,10 +305,8 @@ __global__ void __launch_bounds__(kAttnThreads, STAGES <= 3 ? 2 : 1) attn_mma_ke
           // rounded once to bf16.
           const __half* rec = reinterpret_cast<const __half*>(sc_s + (size_t)(stage * kTT + tk) * L::kRec);
           const float d = __half2float(rec[kv * (D / 32) + ch / 4]);
-          o.x = i8x2_to_bf16x2(w.x & 0xffffu, d);
-          o.y = i8x2_to_bf16x2(w.x >> 16, d);
-          o.z = i8x2_to_bf16x2(w.y & 0xffffu, d);
-          o.w = i8x2_to_bf16x2(w.y >> 16, d);
+          i8x4_to_bf16x4(w.x, d, o.x, o.y);
+          i8x4_to_bf16x4(w.y, d, o.z, o.w);
         }
         *reinterpret_cast<uint4*>(kvb_s + (size_t)kv * kTT * D + (tk * CH + (ch ^ (tk & 7))) * 8) = o;
       }

@@ -153,13 +153,21 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
   const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
   return *reinterpret_cast<const uint32_t*>(&b);
 }
-// Two int8 codes (low byte first) times a block scale -> two bf16 (the
-// binary32 product is exact, rounded once).
-__device__ __forceinline__ uint32_t i8x2_to_bf16x2(uint32_t two_codes, float d) {
-  const float a = (float)(int8_t)(two_codes & 0xffu) * d;
-  const float b = (float)(int8_t)((two_codes >> 8) & 0xffu) * d;
-  const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&r);
+// Four int8 codes (low byte first) times a block scale d -> four bf16 (two
+// words, low half first), each rounded once.  Code c becomes the binary32
+// 2^23 + 128 + c exactly -- its biased byte c ^ 0x80 placed in the mantissa
+// of 2^23 -- less 2^23 + 128; the product with d is exact in binary32 (8 x 11
+// significant bits).
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t four_codes, float d, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = four_codes ^ 0x80808080u;
+  const float c0 = __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7440)) - 8388736.0f;
+  const float c1 = __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7441)) - 8388736.0f;
+  const float c2 = __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7442)) - 8388736.0f;
+  const float c3 = __uint_as_float(__byte_perm(u, 0x4b000000u, 0x7443)) - 8388736.0f;
+  const __nv_bfloat162 a = __floats2bfloat162_rn(c0 * d, c1 * d);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(c2 * d, c3 * d);
+  lo = *reinterpret_cast<const uint32_t*>(&a);
+  hi = *reinterpret_cast<const uint32_t*>(&b);
 }
 
 }  // namespace attn
