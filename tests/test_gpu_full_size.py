@@ -1,7 +1,8 @@
 """GPU parity at the workloads' full sizes: the 65,536-token decode (M = 1),
-the 261,120-token verify (M = 4), the 2,048-row prefill at a 100,352-token
-prefix (sampled rows), and the ragged 16-sequence segmented batch.  One layer
-each (layers are independent).  Tolerances as in qsa_cases."""
+the 261,120-token verify (M = 4) -- over bf16, fp8 and q8 K/V state -- the
+2,048-row prefill at a 100,352-token prefix (sampled rows), and the ragged
+16-sequence segmented batch.  One layer each (layers are independent).
+Tolerances as in qsa_cases."""
 import os
 
 import numpy as np
@@ -71,6 +72,46 @@ def test_decode_and_verify_full_size(L, M):
     assert_attn_close(to_np(out), to_np(lse), out_ref2, lse_ref2, True)
     # Every row attends 2,048 selected rows plus its tail.
     assert (cnt == 512).all()
+
+
+@pytest.mark.parametrize("state", ["fp8", "q8"])
+@pytest.mark.parametrize("L,M", [(65_536, 1), (261_120, 4)])
+def test_decode_and_verify_full_size_quantized(L, M, state):
+    # The quantized-state steps as the bench runs them: caches written by the
+    # library's append of every token of the bf16 draw -- which must equal
+    # the oracle's quantizer on the same draw -- then the whole step, against
+    # the oracle's attention on the oracle's dequantized K/V.
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=0, n_planted=256, device=dev())
+    D = x.k.shape[2]
+    rec = 2 if state == "fp8" else 2 * D // 32
+    kc = torch.zeros(x.k.shape, dtype=torch.uint8 if state == "fp8" else torch.int8, device=dev())
+    vc = torch.zeros_like(kc)
+    sc = torch.zeros((x.k.shape[0], L, rec), dtype=torch.float16, device=dev())
+    seg = qsa.Segment(kc, vc, 0, kv_scale=sc)
+    pooled = pooled_buffer(L, dev())
+    qsa.append_tokens(qsa.Seq(L, L, pooled, [seg], idx_keys=x.idxk), x.k.contiguous(), x.v.contiguous(),
+                      x.idxk.clone())
+    step = qsa.LayerStep([qsa.Seq(L, M, pooled, [seg], idx_keys=x.idxk)], x.q_idx, x.q)
+    step.run()
+    torch.cuda.synchronize()
+    h = _host(x)
+    quant, dequant = ((oracle.fp8_quantize, oracle.fp8_dequantize) if state == "fp8"
+                      else (oracle.q8_quantize, oracle.q8_dequantize))
+    kq, ks = quant(h["k"])
+    vq, vs = quant(h["v"])
+    np.testing.assert_array_equal(to_np(kc), kq)
+    np.testing.assert_array_equal(to_np(vc), vq)
+    sb = to_np(sc.view(torch.int16)).view(np.uint16)
+    np.testing.assert_array_equal(sb[..., :rec // 2] if state == "q8" else sb[..., 0], ks)
+    np.testing.assert_array_equal(sb[..., rec // 2:] if state == "q8" else sb[..., 1], vs)
+    pooled_ref = oracle.pool(h["idxk"])
+    s_ref = oracle.score(h["q_idx"], pooled_ref, x.row_pos)
+    sel_ref, cnt_ref, tau = oracle.select(s_ref, x.row_pos)
+    sel, cnt = to_np(step.sel), to_np(step.cnt)
+    assert_selection_close(sel, cnt, sel_ref, cnt_ref, tau, s_ref, x.row_pos)
+    kd, vd = dequant(kq, ks), dequant(vq, vs)
+    out_ref, lse_ref = oracle.attn(h["q"], kd, vd, x.row_pos, sel, cnt)
+    assert_attn_close(to_np(step.out), to_np(step.lse), out_ref, lse_ref, True)
 
 
 def test_prefill_chunk_sampled_rows():
