@@ -41,6 +41,9 @@ from workloads import WORKLOADS, make_layer  # noqa: E402
 METRIC = "QSA layer-steps/s at 261,120-ctx verify M=4; HBM GB/s as % of GB300 roofline"
 UNIT = "layer-steps/s"
 L2_BYTES = 129 * 2 ** 20
+FEW_ROWS = 8                  # rows per sequence the streaming few-row scoring serves
+NOMINAL_HBM_GBS = 8000.0      # the 8 TB/s HBM roofline the target fraction is stated against
+DTYPE_NAMES = {torch.bfloat16: "bf16", torch.float32: "f32"}
 
 
 # ---------------------------------------------------------------------- workload setup
@@ -87,18 +90,19 @@ def launches_per_layer(layer) -> int:
     x = layer.x
     # Pooling runs inside the few-row scoring launch (bf16 index queries, <= 4
     # rows) when the step pools and scores in one call; else its own launch.
-    fused = st.idx_array is not None and x.M <= 4 and x.q_idx.dtype == torch.bfloat16
+    fused = st.idx_array is not None and x.M <= FEW_ROWS and x.q_idx.dtype == torch.bfloat16
     n = (0 if fused else len(st.pool_jobs)) + 1 + 1 + 1   # pool, score, select, attention
-    if x.M > 4 and x.q_idx.dtype == torch.bfloat16:
+    if x.M > FEW_ROWS and x.q_idx.dtype == torch.bfloat16:
         n += 1                                   # scoring on the tensor cores: + the key-plane split
     ws_needed = st.ws.numel() > 16
     return n + (1 if ws_needed else 0)           # + split merge (several splits per row)
 
 
 def algorithmic_bytes(layer) -> dict:
-    """Bytes one layer-step must move: the pooled keys once, the scores, the
-    index queries, the selected K/V rows of both KV heads (each row once per
-    query row), the queries and the outputs; not the dense K/V left unread."""
+    """Bytes one layer-step must move: the pooled keys once, the index
+    queries, the selected K/V rows of both KV heads (each row once per query
+    row), the queries and the outputs; not the dense K/V left unread and not
+    the scores intermediate."""
     x = layer.x
     L, M = x.L, x.M
     # K/V bytes per (KV head, token): both rows, plus their scale record for
@@ -116,8 +120,9 @@ def algorithmic_bytes(layer) -> dict:
     nb_max = L // 4
     new_blocks = sum(n for *_, n in layer.step.pool_jobs)
     pool_b = new_blocks * (4 * 128 * idx_es + 128 * 4)
-    score_b = nb_max * 128 * 4 + x.q_idx.numel() * x.q_idx.element_size() + sum(
-        ((p + 1) // 4) * 4 for p in x.row_pos)
+    # The pooled keys once and the index queries; the scores the launch
+    # writes for the selection are an intermediate and are not counted.
+    score_b = nb_max * 128 * 4 + x.q_idx.numel() * x.q_idx.element_size()
     rows = []
     for p in x.row_pos:
         nb = (p + 1) // 4
@@ -329,6 +334,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default="verify_m4_261k_bf16",
                     choices=["verify_m4_261k_bf16", "decode_m1_65k_bf16", "prefill_t2048_100k_bf16",
+                             "verify_m8_261k_bf16",
                              "tiny_verify_f32", "verify_m4_261k_fp8", "decode_m1_65k_fp8", "verify_m4_261k_q8",
                              "decode_m1_65k_q8"])
     ap.add_argument("--layers", type=int, default=0, help="layers per step (default: the workload's 12)")
@@ -460,9 +466,9 @@ def main():
 
     # Few rows with bf16 index queries: the step pools inside its scoring
     # launch (qsa_pool_score_blocks), so that launch is the one timed.
-    fused = layers[0].step.idx_array is not None and spec["M"] <= 4 and spec["dtype"] == torch.bfloat16
+    fused = layers[0].step.idx_array is not None and spec["M"] <= FEW_ROWS and spec["dtype"] == torch.bfloat16
     score_us = time_isolated(lambda st: st.pool_score() if fused else st.score())
-    attn_us = time_isolated(lambda st: st.attend()) if spec["M"] > 4 else None
+    attn_us = time_isolated(lambda st: st.attend()) if spec["M"] > FEW_ROWS else None
 
     # End to end through the public API with host buffers: per step, the new
     # rows' q, index queries, K/V and index keys of every layer go host ->
@@ -574,14 +580,14 @@ def main():
 
     roofline = {"kernel": "pool_score_blocks (steps 1 + 2, one launch)" if fused else "score_blocks",
                 "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
-                "unit": "GB/s", "frac": score_gbs / peak_gbs,
-                "traffic": traffic_of("score_tma_pool_kernel" if fused else "score_tma_kernel"),
+                "unit": "GB/s", "frac": score_gbs / peak_gbs, "frac_of_8tbs": score_gbs / NOMINAL_HBM_GBS,
+                "traffic": traffic_of("score_direct_kernel"),
                 "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
                 "timing": "graph of 12 launches each followed by a one-element non-PDL kernel, minus a graph "
                           "of those kernels alone (no overlap with neighbours)",
                 "algorithmic_bytes_per_launch": score_bytes}
     roofline_scoring = None
-    if M > 4:
+    if M > FEW_ROWS:
         # Many rows (prefill).  Scoring is a dense contraction on the tensor
         # cores: algorithmic flops 2 x rows x 4 heads x blocks x 128; the
         # kernel executes three times as many (three bf16 planes of the fp32
@@ -605,6 +611,7 @@ def main():
         attn_gbs = ab["attn"] / (attn_us * 1e-6) / 1e9
         roofline = {"kernel": "sparse_attn (tcgen05 path)", "bound": "hbm", "achieved": attn_gbs,
                     "peak": peak_gbs, "unit": "GB/s", "frac": attn_gbs / peak_gbs,
+                    "frac_of_8tbs": attn_gbs / NOMINAL_HBM_GBS,
                     "traffic": traffic_of("attn_tc_kernel"), "peak_source": f"{peak_src} (hbm_gbs, burst)",
                     "us_per_launch": attn_us, "timing": roofline["timing"],
                     "algorithmic_bytes_per_launch": ab["attn"]}
@@ -613,9 +620,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": DTYPE_NAMES[spec["dtype"]], "data": "synthetic",
         "config": {"workload": args.workload, "context": L, "rows": M, "layers_per_step": n_layers,
-                   "q_heads": 24, "kv_heads": 2, "head_dim": spec["head_dim"], "top_k_blocks": 512,
+                   "q_heads": layers[0].x.q.shape[1], "kv_heads": layers[0].x.k.shape[0],
+                   "head_dim": layers[0].x.q.shape[2], "top_k_blocks": 512,
                    "kv_state": spec.get("kv_state") or "bf16",
                    "index_heads": 4, "index_dim": 128, "graph": "one CUDA graph per step (all layers)",
                    "l2": f"inputs larger than L2: {n_layers} distinct layers, "
@@ -625,6 +633,7 @@ def main():
         "algorithmic_bytes_per_layer_step": ab["total"],
         "step_hbm_gbs": step_gbs,
         "step_frac_of_peak": step_gbs / peak_gbs,
+        "step_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
         "roofline": roofline,
         **({"roofline_scoring": roofline_scoring} if roofline_scoring else {}),
         "cpu_baseline": cpu,
@@ -647,7 +656,7 @@ def main():
 
 # Revision tags of the kernels as built now; DRAM counters in
 # profiles/kernel_traffic.json count only for the revision they were taken on.
-KERNEL_REVS = {"score_tma_kernel": "score_tma_ring8_v4", "score_tma_pool_kernel": "score_tma_pool_v1",
+KERNEL_REVS = {"score_direct_kernel": "score_direct_v1",
                "attn_tc_kernel": "attn_tc_ring3_v1", "score_tc_kernel": "score_tc_planes3_v1"}
 
 if __name__ == "__main__":

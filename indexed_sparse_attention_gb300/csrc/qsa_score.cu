@@ -709,6 +709,301 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
   if constexpr (POOL) asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
+// ------------------------------------------------------------------ few-row scoring, direct loads
+// Decode and verify (<= 8 rows per sequence, bf16 index queries): every
+// pooled block is read once with plain 128-bit loads straight into registers,
+// and the dot products run as tf32 MMAs (m16n8k8) on the two-plane split of
+// the key (split_tf32), so no product loses precision beyond one fp32 ulp of
+// the key.  MMA rows are (row, head) pairs rh = 4 row + head (NMT tiles of
+// 16: <= 4 rows per tile), MMA columns are 8 blocks, and the 128 channels
+// are 16 k-steps of 8.  The k-slots of a step are mapped to channels so
+// that the four lanes of a quad read 64 contiguous bytes per load: lane
+// (g, t) (g = lane / 4, t = lane % 4) holds block g's channels 16q + 4t ..
+// 16q + 4t + 3 (q < 8) and supplies channel 16q + 4t + 2p (slot t) and
+// 16q + 4t + 2p + 1 (slot t + 4) at k-step j = 2q + p; the queries use the
+// same mapping, which leaves every dot product unchanged.
+//
+// Persistent warps: warp w of the grid takes tiles (16 blocks = 8 KB) w,
+// w + W, w + 2W, ... of the call, so consecutive warps read consecutive
+// memory.  A tile is two 8-block halves; the next tile's halves are loaded
+// while the current one is multiplied, so every warp keeps 8 KB in flight.
+// The epilogue adds the four heads' ReLUs across lanes, writes each row's
+// visible scores and the tile's maximum per row (the group maximum).
+// Step 1 rides along (qsa_pool_score_blocks): a half holding a block the
+// step's rows complete replaces that block's loaded values with the mean of
+// its four index keys (the pooling kernel's order of operations) and stores
+// it to the pooled keys.
+// Warps per CTA and CTAs per SM by row-head tiles (registers: ~220 per
+// thread for one tile, the most for two).
+template <int NMT>
+struct DirShape {
+  static constexpr int warps = 4;
+  static constexpr int ctas_per_sm = NMT == 1 ? 3 : 2;
+  // Per warp: query fragments, then a pooling scratch of two blocks.
+  static constexpr size_t q_bytes = (size_t)NMT * 16 * 32 * sizeof(uint2);
+  static constexpr size_t warp_bytes = q_bytes + 2 * 4 * QSA_INDEX_DIM * 4;
+  static constexpr size_t smem = (size_t)warps * warp_bytes;
+};
+
+// split_tf32 issued where it is used (volatile), so the compiler does not
+// hoist the splits of a whole half ahead of its MMAs and hold them all live.
+__device__ __forceinline__ void split_tf32_at_use(float x, uint32_t& hi, uint32_t& lo) {
+  asm volatile(
+      "{\n\t.reg .b32 r, f;\n\t"
+      "add.u32 r, %2, 0x1000;\n\t"
+      "and.b32 %0, r, 0xffffe000;\n\t"
+      "sub.f32 f, %3, %0;\n\t"
+      "mov.b32 %1, f;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "r"(__float_as_uint(x)), "f"(x));
+}
+
+struct HalfTile {
+  float4 v[8];   // channels 16q + 4t .. 16q + 4t + 3 of block g of the half, q < 8
+};
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Block b's channels 16q + 4t .. 16q + 4t + 3, q < 8 (zeros past the sequence's blocks).
+__device__ __forceinline__ void load_half(HalfTile& h, const ScoreSeq& sq, int64_t b, int64_t nb, int t) {
+  if (b < nb) {
+    const float4* src = reinterpret_cast<const float4*>(sq.pooled + b * sq.pooled_stride + 4 * t);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h.v[q] = ld_stream(src + 4 * q);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) h.v[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+__device__ __forceinline__ float elem(const HalfTile& h, int e) {
+  const float4 v = h.v[e >> 2];
+  return (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
+}
+
+// Step 1 inside the scoring launch.  The index keys of the blocks a tile
+// completes (at most 2: <= 8 rows complete <= 2 blocks) are copied into the
+// warp's scratch with cp.async when the tile's pooled keys are requested,
+// so they arrive with them.  Scratch slot i holds block
+// max(pool_b0, b0) + i: its 4 tokens' 128 index-key channels as stored.
+constexpr int kPoolSlotBytes = 4 * QSA_INDEX_DIM * 4;   // 4 tokens of f32 keys (bf16 use half)
+
+__device__ __forceinline__ void pool_prefetch(unsigned char* scratch, const ScoreSeq& sq, int64_t b0, int lane) {
+  const int64_t lo = max(sq.pool_b0, b0), hi = min(sq.pool_b1, b0 + (int64_t)kScoreTile);
+  const int es = sq.idx_dtype == QSA_F32 ? 4 : 2;
+  const int chunks = QSA_INDEX_DIM * es / 16;   // 16-byte chunks per token row
+  for (int64_t b = lo; b < hi && b < lo + 2; ++b) {
+    for (int c = lane; c < 4 * chunks; c += 32) {
+      const char* src = static_cast<const char*>(sq.idx_keys) + ((4 * b + c / chunks) * sq.idx_stride) * es +
+                        (c % chunks) * 16;
+      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(scratch + (b - lo) * kPoolSlotBytes + c * 16);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// Block b = b0 + 8h + g of a tile with completed blocks: the mean of its
+// four index keys (((k0 + k1) + k2) + k3, times 0.25) over the lane's
+// channels 16q + 4t .. 16q + 4t + 3 replaces the loaded values and is stored
+// to the pooled keys.  The warp's scratch must have landed.
+__device__ __forceinline__ void pool_from_scratch(HalfTile& h, const unsigned char* scratch, const ScoreSeq& sq,
+                                                  int64_t b0, int64_t b, int t) {
+  const unsigned char* slot = scratch + (b - max(sq.pool_b0, b0)) * kPoolSlotBytes;
+  float4* dst = reinterpret_cast<float4*>(const_cast<float*>(sq.pooled) + b * sq.pooled_stride + 4 * t);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    float4 k[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = 16 * q + 4 * t;
+      if (sq.idx_dtype == QSA_F32) {
+        k[j] = *reinterpret_cast<const float4*>(slot + (j * QSA_INDEX_DIM + c) * 4);
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(slot + (j * QSA_INDEX_DIM + c) * 2);
+        k[j] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+      }
+    }
+    h.v[q] = pool4(k);
+    dst[4 * q] = h.v[q];
+  }
+}
+
+__device__ __forceinline__ bool tile_pools(const ScoreSeq& sq, int64_t b0) {
+  return sq.pool_b1 > sq.pool_b0 && b0 < sq.pool_b1 && b0 + kScoreTile > sq.pool_b0;
+}
+
+// The MMAs of one half: s[mt] = the 16 x 8 (row-head x block) products.
+// qs: this warp's query fragments, [mt][j][lane] = (rows g, g + 8) x the two
+// channels of k-step j, as bf16 pairs.
+template <int NMT>
+__device__ __forceinline__ void mma_half(const HalfTile& h, const uint2* qs, int lane, float (&s)[NMT][4]) {
+  float ah[NMT][2][4], al[NMT][2][4];
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ah[mt][c][e] = al[mt][c][e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    uint32_t h0, l0, h1, l1;
+    split_tf32_at_use(elem(h, 2 * j), h0, l0);       // k-slot t:     channel 16(j / 2) + 4t + 2(j % 2)
+    split_tf32_at_use(elem(h, 2 * j + 1), h1, l1);   // k-slot t + 4: the next channel
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      const uint2 w = qs[(mt * 16 + j) * 32 + lane];   // rows g, g + 8: the step's two channels
+      const uint32_t a0 = w.x << 16, a1 = w.y << 16, a2 = w.x & 0xffff0000u, a3 = w.y & 0xffff0000u;
+      mma_tf32(al[mt][j & 1], a0, a1, a2, a3, l0, l1);
+      mma_tf32(ah[mt][j & 1], a0, a1, a2, a3, h0, h1);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[mt][e] = (ah[mt][0][e] + ah[mt][1][e]) + (al[mt][0][e] + al[mt][1][e]);
+}
+
+template <int NMT, int NSEQ>
+__global__ void __launch_bounds__(32 * DirShape<NMT>::warps, DirShape<NMT>::ctas_per_sm)
+    score_direct_kernel(const __grid_constant__ ScoreParams<NSEQ> p) {
+  constexpr int kWarps = DirShape<NMT>::warps;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t W = (int64_t)gridDim.x * kWarps;
+  int64_t u = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  extern __shared__ __align__(16) unsigned char dir_smem[];
+  uint2* qs = reinterpret_cast<uint2*>(dir_smem + (size_t)(threadIdx.x >> 5) * DirShape<NMT>::warp_bytes);
+  unsigned char* scratch = dir_smem + (size_t)(threadIdx.x >> 5) * DirShape<NMT>::warp_bytes + DirShape<NMT>::q_bytes;
+  HalfTile ha, hb;
+  // The first tile's pooled keys: blocks older than those the step's rows
+  // complete are state that no launch of this step writes, so they may be
+  // requested before the dependency wait.
+  bool waited = false;
+  if (u < p.n_work) {
+    const ScoreSeq& sq = p.seq[find_seq_by_work(p, u)];
+    const int64_t b0 = (u - sq.work_begin) * kScoreTile;
+    const int64_t nbs = sq.n_tokens / 4;
+    if (b0 + kScoreTile > (sq.n_tokens - sq.n_rows) / 4) {
+      grid_dependency_wait();
+      waited = true;
+    }
+    load_half(ha, sq, b0 + g, nbs, t);
+    load_half(hb, sq, b0 + 8 + g, nbs, t);
+    if (tile_pools(sq, b0)) pool_prefetch(scratch, sq, b0, lane);
+  }
+  if (!waited) grid_dependency_wait();
+  grid_dependency_release();
+  int q_si = -1;
+  for (; u < p.n_work; u += W) {
+    const int si = find_seq_by_work(p, u);
+    const ScoreSeq& sq = p.seq[si];
+    const int64_t b0 = (u - sq.work_begin) * kScoreTile;
+    const int rows = sq.n_rows;
+    if (si != q_si) {
+      // Index queries of rows rh / 4 (heads rh % 4), rh = 16 mt + g + 8 hs:
+      // channels 16q + 4t .. 16q + 4t + 3 as two bf16 pairs per q, laid out
+      // as the fragments of k-steps j = 2q and 2q + 1.
+      const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q_idx);
+      __syncwarp();
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        uint2 w[2][8];
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          const int rh = 16 * mt + g + 8 * hs, r = rh >> 2;
+          const uint2* src = reinterpret_cast<const uint2*>(
+              qb + ((int64_t)(sq.row_begin + r) * QSA_INDEX_HEADS + (rh & 3)) * QSA_INDEX_DIM + 4 * t);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) w[hs][q] = r < rows ? src[4 * q] : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          qs[(mt * 16 + 2 * q) * 32 + lane] = make_uint2(w[0][q].x, w[1][q].x);
+          qs[(mt * 16 + 2 * q + 1) * 32 + lane] = make_uint2(w[0][q].y, w[1][q].y);
+        }
+      }
+      __syncwarp();
+      q_si = si;
+    }
+    // Step 1 for the tile's completed blocks, from the scratch requested with the tile.
+    if (tile_pools(sq, b0)) {
+      asm volatile("cp.async.wait_all;\n" ::: "memory");
+      __syncwarp();
+      const int64_t ba = b0 + g, bb = b0 + 8 + g;
+      if (ba >= sq.pool_b0 && ba < sq.pool_b1) pool_from_scratch(ha, scratch, sq, b0, ba, t);
+      if (bb >= sq.pool_b0 && bb < sq.pool_b1) pool_from_scratch(hb, scratch, sq, b0, bb, t);
+      __syncwarp();   // the scratch is free for the next tile's copies
+    }
+    float sa[NMT][4], sb[NMT][4];
+    mma_half<NMT>(ha, qs, lane, sa);
+    const int64_t un = u + W;
+    int sin = si;
+    int64_t bn = 0, nbn = 0;
+    if (un < p.n_work) {
+      sin = find_seq_by_work(p, un);
+      bn = (un - p.seq[sin].work_begin) * kScoreTile;
+      nbn = p.seq[sin].n_tokens / 4;
+      load_half(ha, p.seq[sin], bn + g, nbn, t);
+      if (tile_pools(p.seq[sin], bn)) pool_prefetch(scratch, p.seq[sin], bn, lane);
+    }
+    mma_half<NMT>(hb, qs, lane, sb);
+    if (un < p.n_work) load_half(hb, p.seq[sin], bn + 8 + g, nbn, t);
+    // Epilogue: ReLU per head, the four heads added across lanes g % 4.
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) {
+      float v[2][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[0][e] = fmaxf(sa[mt][e], 0.f);
+        v[1][e] = fmaxf(sb[mt][e], 0.f);
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[hf][e] += __shfl_xor_sync(0xffffffffu, v[hf][e], 4);
+          v[hf][e] += __shfl_xor_sync(0xffffffffu, v[hf][e], 8);
+          v[hf][e] *= kScoreScale;
+        }
+      // Lanes g = 0 and g = 4 hold rows 4 mt + g / 4 (elements 0, 1) and
+      // 4 mt + 2 + g / 4 (elements 2, 3), blocks b0 + 8 hf + 2t (+ 1).
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = 4 * mt + 2 * rr + (g >> 2);
+        const int64_t nb = r < rows ? visible_blocks(row_position(sq.n_tokens, sq.n_rows, r)) : 0;
+        float m = -INFINITY;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int64_t b = b0 + 8 * hf + 2 * t + c;
+            if (b < nb) m = fmaxf(m, v[hf][2 * rr + c]);
+          }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if ((g & 3) == 0 && r < rows) {
+          float* dst = p.scores + (int64_t)(sq.row_begin + r) * p.ld;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int64_t b = b0 + 8 * hf + 2 * t + c;
+              if (b < nb) dst[b] = v[hf][2 * rr + c];
+            }
+          if (p.gmax && t == 0 && b0 < nb) p.gmax[(int64_t)(sq.row_begin + r) * p.gld + b0 / kScoreTile] = m;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ scoring, CUDA cores (fp32 queries)
 // One CTA per (32-block tile, group of <= 8 rows); lane = (row, head) pair,
 // warp w = blocks 4w..4w+3 of the tile.
@@ -863,6 +1158,27 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
   if (p_in.n_work == 0) return cudaSuccess;
   const int sms = device_sm_count();
+  if (q_dtype == QSA_BF16 && max_rows_per_group <= kRowGroup) {
+    bool one_group = true;
+    for (int i = 0; i < p_in.n_seqs; ++i) one_group &= p_in.seq[i].n_groups == 1;
+    if (one_group) {
+      // Persistent: as many CTAs as fit on the SMs, no more than the tiles need.
+      auto grid_of = [&](int warps, int per_sm) {
+        const int64_t need = (p_in.n_work + warps - 1) / warps;
+        const int64_t ctas = (int64_t)sms * per_sm;
+        return (unsigned)(need < ctas ? need : ctas);
+      };
+      cudaError_t e = allow_dynamic_smem((const void*)(max_rows_per_group <= 4 ? score_direct_kernel<1, NSEQ>
+                                                                                 : score_direct_kernel<2, NSEQ>),
+                                         max_rows_per_group <= 4 ? DirShape<1>::smem : DirShape<2>::smem);
+      if (e != cudaSuccess) return e;
+      if (max_rows_per_group <= 4)
+        return launch_kernel(score_direct_kernel<1, NSEQ>, dim3(grid_of(DirShape<1>::warps, DirShape<1>::ctas_per_sm)),
+                             dim3(32 * DirShape<1>::warps), DirShape<1>::smem, st, 0u, p_in);
+      return launch_kernel(score_direct_kernel<2, NSEQ>, dim3(grid_of(DirShape<2>::warps, DirShape<2>::ctas_per_sm)),
+                           dim3(32 * DirShape<2>::warps), DirShape<2>::smem, st, 0u, p_in);
+    }
+  }
   if (q_dtype != QSA_F32 && max_rows_per_group <= 4) {
     cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st);
     if (e != cudaErrorNotSupported) return e;

@@ -42,8 +42,10 @@ constexpr int kBins3 = 256;                        // radix level 3: the last 8 
 constexpr int kGroupCap = 1024;                    // candidate groups read back (16,384 blocks)
 constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
 constexpr int kMaxGroups = QSA_MAX_BLOCKS / kGroup;
+static_assert(kMaxGroups <= 16 * kThreads, "select_split_kernel loads every group maximum in one pass");
 constexpr int kLoadBatch = 16;                                  // group maxima a thread loads per pass
 constexpr int kChunkBatch = 4;                                  // float4 chunks a thread loads per pass
+constexpr int kMaxSplit = kSelectMaxSplit;                      // CTAs per row of select_split_kernel
 
 
 // Shared-memory layout (32-bit words); R1 holds the group-maximum keys, then
@@ -181,21 +183,26 @@ __device__ __forceinline__ float group_max_of(const float* srow, int64_t g, int6
   return m;
 }
 
-// Steps 3 and 4 over the candidates: for_each(f) calls f(key, id) for every
+// The k-th key of a candidate set by radix levels of 12, 12 and 8 key bits
+// (stopping early when a bin is taken whole): entries whose masked key
+// (key & mask) exceeds K are kept; of those equal to K, all when all_eq,
+// else the `need` lowest ids.  for_each(f) calls f(key, id) for every
 // candidate (key != 0), each exactly once over the CTA's threads, and
 // for_each_warp(f) does the same with all 32 lanes of every warp calling f
 // the same number of times (f(key, id, active)).  level1_done: the caller
-// already filled the level-1 histogram.
+// already filled the level-1 histogram (h2).  Ends with a barrier.
+struct Threshold {
+  uint32_t K, mask, need;
+  bool all_eq;
+};
+
 template <int NT, typename ForEach, typename ForEachWarp>
-__device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_each, ForEachWarp for_each_warp,
-                                                uint32_t* sm, const SelLayout& L, bool level1_done,
-                                                uint32_t (*wt)[NT / 32], uint32_t* s_res, int32_t* out) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ Threshold radix_threshold(uint32_t k, ForEach for_each, ForEachWarp for_each_warp,
+                                                     uint32_t* sm, const SelLayout& L, bool level1_done,
+                                                     uint32_t (*wt)[NT / 32], uint32_t* s_res) {
   uint32_t* h1 = sm + L.h1;
   uint32_t* h2 = sm + L.h2;
   uint32_t* h3 = sm + L.h3;
-  uint32_t* selw = sm + L.selw;
-  uint32_t* eqw = sm + L.eqw;
   if (!level1_done) {
     for_each_warp([&](uint32_t key, int32_t, bool act) { hist_add(h2, act, key >> 20); });
     __syncthreads();
@@ -231,9 +238,24 @@ __device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_
       n_eq = h3[s_res[0]];
     }
   }
+  return Threshold{K, mask, need, n_eq == need};
+}
+
+// Steps 3 and 4 over the candidates (for_each, for_each_warp and
+// level1_done as for radix_threshold): the kept ids are marked in a bitmap
+// over the row's blocks and written ascending to out.
+template <int NT, typename ForEach, typename ForEachWarp>
+__device__ __forceinline__ void radix_and_write(uint32_t k, int nw, ForEach for_each, ForEachWarp for_each_warp,
+                                                uint32_t* sm, const SelLayout& L, bool level1_done,
+                                                uint32_t (*wt)[NT / 32], uint32_t* s_res, int32_t* out) {
+  const int tid = threadIdx.x;
+  uint32_t* selw = sm + L.selw;
+  uint32_t* eqw = sm + L.eqw;
+  const Threshold th = radix_threshold<NT>(k, for_each, for_each_warp, sm, L, level1_done, wt, s_res);
+  const uint32_t K = th.K, mask = th.mask, need = th.need;
   // Step 4: mark the kept ids.  Entries above K are kept; so are those equal
   // to K when all of them fit, else the `need` lowest ids among them.
-  const bool all_eq = n_eq == need;
+  const bool all_eq = th.all_eq;
   for_each([&](uint32_t key, int32_t id) {
     if (key > 0xff800000u || key < 0x007fffffu) atomicAdd(&g_nan_keys, 1);
     const uint32_t m = key & mask;
@@ -495,6 +517,255 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
   if (tid == 0) p.cnt[r] = k;
 }
 
+// ------------------------------------------------------------------ one row over several CTAs
+// Rows of few-row calls (decode, verify) are split over n_split CTAs each, so
+// the selection's loads and list building run on many SMs instead of one:
+//  1. every CTA of the row reads all the row's group maxima and finds the bin
+//     B of the k-th largest (the bound of step 1 above; the same B in every
+//     CTA);
+//  2. CTA c takes groups [c G / n, (c + 1) G / n): it reads the blocks of its
+//     candidate groups and writes the (key, id) pairs whose key is in a bin
+//     >= B to its own slot of the workspace, in ascending id order, with
+//     their count;
+//  3. each CTA then takes a ticket (an atomic count per row); the CTA that
+//     draws the last one knows every slot is written.  It concatenates the
+//     slots in part order -- ascending ids -- into shared memory, runs the
+//     radix levels of step 3 over the list, and writes the kept ids in list
+//     order: an entry is kept when its key exceeds the k-th key K, or equals
+//     it and fewer than `need` entries equal to K precede it, and its
+//     position is the number of kept entries before it (one prefix scan
+//     over the list).  It resets the row's ticket to zero.
+// No CTA waits for another.  A list longer than the shared-memory capacity
+// is selected from the whole score row in global memory, as in select_kernel.
+template <int NSEQ>
+__global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
+  constexpr int NT = kThreads;
+  extern __shared__ __align__(16) uint32_t sm[];
+  __shared__ uint32_t wt[2][kWarps];
+  __shared__ uint32_t s_res[2];
+  __shared__ uint32_t s_last;
+  __shared__ uint32_t s_off[kMaxSplit], s_cnt[kMaxSplit];
+  const SelLayout L(max_nb);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = p.split.n_split, part = (int)blockIdx.x;
+  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;               // the three histograms
+  for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;   // the two bitmaps (long lists)
+  if (tid == 0) {
+    s_res[0] = 0u;
+    s_res[1] = 0u;
+  }
+  grid_dependency_sync();
+  const int r = p.row_base + (int)blockIdx.y;
+  int si = 0;
+#pragma unroll
+  for (int i = 1; i < NSEQ; ++i)
+    if (i < p.n_seqs && r >= p.seq[i].row_begin) si = i;
+  const RowSeq sq = p.seq[si];
+  const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin));
+  const int k = p.top_k;
+  int32_t* out = p.sel + (int64_t)r * k;
+  if (nb <= k) {   // every visible block; no ticket is drawn
+    if (part == 0) {
+      for (int i = tid; i < k; i += NT) out[i] = i < nb ? i : -1;
+      if (tid == 0) p.cnt[r] = (int32_t)nb;
+    }
+    return;
+  }
+  const float* srow = p.scores + (int64_t)r * p.ld;
+  const int G = (int)((nb + kGroup - 1) / kGroup);   // <= kMaxGroups = 4 * 4 * NT
+  uint32_t* r1 = sm + L.r1;
+  uint32_t* r2 = sm + L.r2;
+  uint32_t* h1 = sm + L.h1;
+  __syncthreads();   // histograms and bitmaps cleared
+
+  // 1. All group maxima of the row (four float4 loads per thread in flight),
+  // their keys kept in r1, their top-12-bit histogram in h1.
+  {
+    const float* grow = p.gmax + (int64_t)r * p.gld;
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g0 = 4 * (tid + j * NT);
+      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g0 + 4 <= G) {
+        v[j] = __ldg(reinterpret_cast<const float4*>(grow + g0));
+      } else if (g0 < G) {
+        v[j].x = __ldg(grow + g0);
+        if (g0 + 1 < G) v[j].y = __ldg(grow + g0 + 1);
+        if (g0 + 2 < G) v[j].z = __ldg(grow + g0 + 2);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int g0 = 4 * (tid + j * NT);
+      const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (g0 + e < G) {
+          const uint32_t key = order_key(x[e]);
+          r1[g0 + e] = key;
+          atomicAdd(&h1[key >> 20], 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t B = 0u;
+  if (G >= k) {
+    find_bin<NT>(h1, kBins, (uint32_t)k, wt[0], s_res);
+    B = s_res[0];
+  }
+  for (int i = tid; i < kBins; i += NT) h1[i] = 0u;   // reused by radix level 2
+
+  // 2. This CTA's candidate groups: thread t of a round takes group gs + t
+  // and keeps its blocks whose key is in a bin >= B; a prefix scan over the
+  // CTA places them in ascending id order in the slot.
+  const int ga = (int)((int64_t)G * part / C), gb = (int)((int64_t)G * (part + 1) / C);
+  uint2* slot = p.split.slots + ((int64_t)r * C + part) * p.split.cap;
+  uint32_t n_out = 0u;
+  int wb = 1;
+  int nan_keys = 0;
+  for (int gs = ga; gs < gb; gs += NT) {
+    const int g = gs + tid;
+    const int64_t b0 = (int64_t)g * kGroup;
+    float x[kGroup];
+    uint32_t keep = 0u;   // bit e: block b0 + e is kept
+    if (g < gb && (r1[g] >> 20) >= B) {
+      if (b0 + kGroup <= nb) {
+#pragma unroll
+        for (int q = 0; q < kGroup / 4; ++q) {
+          const float4 w = __ldg(reinterpret_cast<const float4*>(srow + b0) + q);
+          x[4 * q] = w.x;
+          x[4 * q + 1] = w.y;
+          x[4 * q + 2] = w.z;
+          x[4 * q + 3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) x[e] = b0 + e < nb ? __ldg(srow + b0 + e) : 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < kGroup; ++e) {
+        const uint32_t key = order_key(x[e]);
+        if (b0 + e < nb && (key >> 20) >= B) {
+          keep |= 1u << e;
+          nan_keys += key > 0xff800000u || key < 0x007fffffu;
+        }
+      }
+    }
+    uint32_t tot;
+    uint32_t at = n_out + block_scan<NT>((uint32_t)__popc(keep), wt[wb], &tot);
+    wb ^= 1;
+#pragma unroll
+    for (int e = 0; e < kGroup; ++e)
+      if (keep & (1u << e)) slot[at++] = make_uint2(order_key(x[e]), (uint32_t)(b0 + e));
+    n_out += tot;
+  }
+  if (nan_keys) atomicAdd(&g_nan_keys, nan_keys);
+  if (tid == 0) p.split.counts[(int64_t)r * C + part] = n_out;
+  // Publish the slot, then draw a ticket.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(p.split.tickets + r, 1u) == (uint32_t)(C - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // 3. The last CTA: slot counts -> offsets, the list in ascending id order.
+  const uint32_t c_t = tid < C ? __ldcg(p.split.counts + (int64_t)r * C + tid) : 0u;
+  uint32_t n_list;
+  const uint32_t off = block_scan<NT>(c_t, wt[wb], &n_list);
+  if (tid < C) {
+    s_off[tid] = off;
+    s_cnt[tid] = c_t;
+  }
+  if (tid == 0) p.split.tickets[r] = 0u;   // ready for the next call (stream order)
+  __syncthreads();
+  const int nw = (int)((nb + 31) / 32);
+  if (n_list <= (uint32_t)kListCap) {
+    const int n = (int)n_list;
+    for (int c = warp; c < C; c += kWarps) {
+      const uint32_t o = s_off[c], cn = s_cnt[c];
+      const uint2* src = p.split.slots + ((int64_t)r * C + c) * p.split.cap;
+      for (uint32_t j = lane; j < cn; j += 32) {
+        const uint2 e = __ldcg(src + j);
+        r1[o + j] = e.x;
+        r2[o + j] = e.y;
+      }
+    }
+    __syncthreads();
+    const Threshold th = radix_threshold<NT>(
+        (uint32_t)k,
+        [&](auto f) {
+          for (int i = tid; i < n; i += NT) f(r1[i], (int32_t)r2[i]);
+        },
+        [&](auto f) {
+          const int n_pad = (n + 31) / 32 * 32;
+          for (int i = tid; i < n_pad; i += NT) f(i < n ? r1[i] : 0u, i < n ? (int32_t)r2[i] : 0, i < n);
+        },
+        sm, L, false, wt, s_res);
+    // 4. Kept entries in list order = ascending ids: position = kept entries
+    // before (above-K count + equal-to-K count capped at need, one scan of
+    // the packed pair).
+    const uint32_t need_eff = th.all_eq ? 0xffffffffu : th.need;
+    const int per = (n + NT - 1) / NT;
+    const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
+    uint32_t gt = 0u, eq = 0u;
+    for (int i = a0; i < a1; ++i) {
+      const uint32_t m = r1[i] & th.mask;
+      gt += m > th.K;
+      eq += m == th.K;
+    }
+    uint32_t tot;
+    const uint32_t before = block_scan<NT>((gt << 16) | eq, wt[0], &tot);
+    uint32_t gtb = before >> 16, eqb = before & 0xffffu;
+    for (int i = a0; i < a1; ++i) {
+      const uint32_t m = r1[i] & th.mask;
+      if (m > th.K) {
+        const uint32_t pos = gtb + min(eqb, need_eff);
+        if (pos < (uint32_t)k) out[pos] = (int32_t)r2[i];
+        ++gtb;
+      } else if (m == th.K) {
+        if (eqb < need_eff && gtb + eqb < (uint32_t)k) out[gtb + eqb] = (int32_t)r2[i];
+        ++eqb;
+      }
+    }
+  } else {
+    // The whole row from global memory (the list would not fit).
+    const int nbi = (int)nb;
+    radix_and_write<NT>(
+        (uint32_t)k, nw,
+        [&](auto f) {
+          for (int b0 = tid; b0 < nbi; b0 += 8 * NT) {
+            uint32_t kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int b = b0 + j * NT;
+              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (b0 + j * NT < nbi) f(kk[j], (int32_t)(b0 + j * NT));
+          }
+        },
+        [&](auto f) {
+          const int n_pad = (nbi + 31) / 32 * 32;
+          for (int b0 = tid; b0 < n_pad; b0 += 8 * NT) {
+            uint32_t kk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int b = b0 + j * NT;
+              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f(kk[j], (int32_t)(b0 + j * NT), b0 + j * NT < nbi);
+          }
+        },
+        sm, L, false, wt, s_res, out);
+  }
+  if (tid == 0) p.cnt[r] = k;
+}
+
 // ------------------------------------------------------------------ selection over key-axis chunks
 // One CTA per row merges the row's running top-k (keys and ids, ascending
 // ids) with the scores of one chunk of blocks [block_lo, block_lo + n_blocks):
@@ -628,6 +899,13 @@ cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_n
   // More rows than SMs: CTAs of 512 threads, two per SM where shared memory
   // allows it (more rows in flight); few rows: 1,024 threads, whose per-row
   // latency is lowest.
+  if (p.split.n_split > 0) {
+    if (p.split.n_split > kMaxSplit || !p.gmax) return cudaErrorInvalidValue;
+    cudaError_t e = allow_dynamic_smem((const void*)select_split_kernel<NSEQ>, smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(select_split_kernel<NSEQ>, dim3((unsigned)p.split.n_split, (unsigned)n_rows), dim3(kThreads),
+                         smem, st, 0u, p, max_nb);
+  }
   const bool many = n_rows > device_sm_count() && 2 * (smem + 2048) <= 228 * 1024;
   auto* kernel = many ? select_kernel<NSEQ, 2, 512> : select_kernel<NSEQ, 1, 1024>;
   cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);

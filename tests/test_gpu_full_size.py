@@ -46,7 +46,7 @@ def _host(x):
     return {k: getattr(x, k).cpu() for k in ("idxk", "q_idx", "q", "k", "v")}
 
 
-@pytest.mark.parametrize("L,M", [(65_536, 1), (261_120, 4)])
+@pytest.mark.parametrize("L,M", [(65_536, 1), (261_120, 4), (261_120, 8)])
 def test_decode_and_verify_full_size(L, M):
     x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=0, n_planted=256, device=dev())
     step, _ = _gpu_step(x)

@@ -128,6 +128,9 @@ WORKLOADS = {
     "tiny_verify_f32": dict(L=4099, M=4, dtype=torch.float32, layers=1, n_planted=64, head_dim=256),
     "decode_m1_65k_bf16": dict(L=65_536, M=1, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256),
     "verify_m4_261k_bf16": dict(L=261_120, M=4, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256),
+    # A wider verify window (MTPLX #482 verifies 3-8 rows): eight rows on the
+    # same 261,120-token cache.
+    "verify_m8_261k_bf16": dict(L=261_120, M=8, dtype=torch.bfloat16, layers=12, n_planted=256, head_dim=256),
     "prefill_t2048_100k_bf16": dict(L=100_352 + 2048, M=2048, dtype=torch.bfloat16, layers=1, n_planted=256,
                                     head_dim=256),
     "ragged_segmented_bf16": dict(n_seqs=16, dtype=torch.bfloat16, n_planted=256, head_dims=(256, 128)),
