@@ -195,9 +195,10 @@ int32_t qsa_wait_timeouts(void);
  *                         or the selection met NaN scores among its
  *                         candidates (NaN ranks above every number);
  *   QSA_OK                neither.
- * qsa_last_error() gives the counts.  The counters are global to the
- * library (all streams and threads); a call reads and clears them.  Launches
- * still running on other streams may be counted by the next call.
+ * qsa_last_error() gives the counts.  The counters belong to the current
+ * device (each GPU keeps its own) and cover all its streams and threads; a
+ * call reads and clears those of the current device.  Launches still running
+ * on other streams may be counted by the next call.
  * Errors: QSA_ERR_CUDA (the stream or the counters could not be read).
  */
 qsa_status qsa_check_device_status(void* stream);
@@ -461,9 +462,12 @@ qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_c
  * scratch the split merge needs taken from one array of static device memory
  * inside libqsa.so: QSA_NOALLOC_SCRATCH_BYTES (4 MiB), which every GPU that
  * loads the library holds until the process exits.
- *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture.
+ *  - A call made outside a stream capture looks up the array's device
+ *    address on the current device (a cheap driver query, repeated so that a
+ *    device reset never leaves a stale address); a call inside a capture uses
+ *    the address an earlier call on that device found, so make one call on
+ *    the device before capturing (else QSA_ERR_INVALID_ARG).  A call whose
+ *    plan needs no scratch (one split) looks up nothing.
  *  - It allocates and frees nothing.
  *  - Every call on a device shares the array: calls whose work overlaps on
  *    the GPU (other streams, other threads) race and must not be issued.

@@ -600,12 +600,16 @@ class LayerStep:
 
     def run(self, stream=None, new_tokens=None):
         """One layer step: pool (or append new_tokens and pool), score,
-        select, attend."""
-        if new_tokens is None:
-            self.pool_score(stream)
-        else:
-            self.append(new_tokens, stream)
-            self.score(stream)
-        self.select(stream)
-        self.attend(stream)
+        select, attend (an NVTX range "qsa.layer_step" around the calls)."""
+        torch.cuda.nvtx.range_push("qsa.layer_step")
+        try:
+            if new_tokens is None:
+                self.pool_score(stream)
+            else:
+                self.append(new_tokens, stream)
+                self.score(stream)
+            self.select(stream)
+            self.attend(stream)
+        finally:
+            torch.cuda.nvtx.range_pop()
         return self.out, self.lse

@@ -68,7 +68,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             if log.strip():
                 print(f"--- {src}\n{log}", file=sys.stderr)
     tmp = LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *[o for o, _ in results]]
+    # --no-undefined: a declaration without a definition fails the build, not the load.
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-Xlinker", "--no-undefined", "-o", tmp,
+           *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -10,11 +10,23 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "qsa_internal.cuh"
 
 namespace {
 
 thread_local std::string g_last_error;
+
+// An NVTX range around each call that enqueues work (named after the entry
+// point): a profiler attributes the call's launches to the QSA step they
+// serve.  Without a profiler attached the push and pop are no-ops.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 qsa_status fail(qsa_status s, const char* fmt, ...) {
   char buf[512];
@@ -139,14 +151,17 @@ QSA_API qsa_status qsa_check_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn);
   static std::mutex mu;
-  static int seen_waits = 0;   // qsa_wait_timeouts() at the previous call
+  static int seen_waits[64];   // per device: qsa_wait_timeouts() at the previous call
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, fn);
+  if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "%s: device %d", fn, dev);
   std::lock_guard<std::mutex> lock(mu);
   const int w = qsa_wait_timeouts(), st = selftest_timeouts_take();
   const int bad_a = attn_bad_ids_take(), bad_t = attn_tc_bad_ids_take(), nan = select_nan_keys_take();
   if (w < 0 || st < 0 || bad_a < 0 || bad_t < 0 || nan < 0)
     return fail(QSA_ERR_CUDA, "%s: the device counters could not be read", fn);
-  const int waits = (w - seen_waits) + st, bad = bad_a + bad_t;
-  seen_waits = w;
+  const int waits = (w - seen_waits[dev]) + st, bad = bad_a + bad_t;
+  seen_waits[dev] = w;
   if (waits > 0)
     return fail(QSA_ERR_TIMEOUT, "%s: %d device wait(s) gave up; %d out-of-range selected ids, %d NaN scores", fn,
                 waits, bad, nan);
@@ -168,6 +183,7 @@ QSA_API qsa_status qsa_selftest_wait_timeout(int32_t limit_us, void* stream) {
 // ------------------------------------------------------------------ step 1
 QSA_API qsa_status qsa_pool_index_keys(const void* idx_keys, qsa_dtype idx_dtype, int64_t tok_stride, int64_t first_block,
                                int64_t n_blocks, float* pooled, int64_t pooled_stride, void* stream) {
+  const NvtxRange nvtx_range("qsa_pool_index_keys");
   const char* fn = "qsa_pool_index_keys";
   if (!valid_dtype(idx_dtype)) return fail(QSA_ERR_UNSUPPORTED, "%s: idx_dtype %d", fn, (int)idx_dtype);
   if (first_block < 0 || n_blocks < 0) return fail(QSA_ERR_INVALID_ARG, "%s: negative block range", fn);
@@ -335,6 +351,7 @@ static qsa_status score_blocks_impl(const char* fn, const qsa_seq* seqs, int32_t
 QSA_API qsa_status qsa_score_blocks(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx, qsa_dtype q_idx_dtype,
                                     float* scores, int64_t ld, float* group_max, int64_t group_ld, void* workspace,
                                     size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("qsa_score_blocks");
   return score_blocks_impl("qsa_score_blocks", seqs, n_seqs, nullptr, q_idx, q_idx_dtype, scores, ld, group_max,
                            group_ld, workspace, workspace_bytes, stream);
 }
@@ -343,6 +360,7 @@ QSA_API qsa_status qsa_pool_score_blocks(const qsa_seq* seqs, int32_t n_seqs, co
                                          int64_t idx_tok_stride, qsa_dtype idx_dtype, const void* q_idx,
                                          qsa_dtype q_idx_dtype, float* scores, int64_t ld, float* group_max,
                                          int64_t group_ld, void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("qsa_pool_score_blocks");
   const IdxKeys ik{idx_keys, idx_tok_stride, idx_dtype};
   return score_blocks_impl("qsa_pool_score_blocks", seqs, n_seqs, &ik, q_idx, q_idx_dtype, scores, ld, group_max,
                            group_ld, workspace, workspace_bytes, stream);
@@ -420,6 +438,7 @@ static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, co
 QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const float* scores, int64_t ld,
                                    const float* group_max, int64_t group_ld, int32_t top_k, int32_t* sel, int32_t* cnt,
                                    void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("qsa_select_topk");
   const char* fn = "qsa_select_topk";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -496,6 +515,7 @@ QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, co
                                          qsa_dtype q_idx_dtype, float* scores, int64_t ld, int32_t top_k,
                                          int32_t* sel, int32_t* cnt, void* workspace, size_t workspace_bytes,
                                          void* stream) {
+  const NvtxRange nvtx_range("qsa_score_select_topk");
   const char* fn = "qsa_score_select_topk";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -561,6 +581,7 @@ QSA_API qsa_status qsa_score_select_topk_blocked(const qsa_seq* seqs, int32_t n_
                                                  qsa_dtype q_idx_dtype, int32_t top_k, int32_t block_keys,
                                                  int32_t* sel, int32_t* cnt, void* workspace,
                                                  size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("qsa_score_select_topk_blocked");
   const char* fn = "qsa_score_select_topk_blocked";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -768,6 +789,7 @@ QSA_API size_t qsa_attn_workspace_size(const qsa_seq* seqs, int32_t n_seqs, cons
 QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg, const void* q,
                            const int32_t* sel, const int32_t* cnt, int32_t sel_ld, void* out, float* lse,
                            void* workspace, size_t workspace_bytes, void* stream) {
+  const NvtxRange nvtx_range("qsa_sparse_attn");
   const char* fn = "qsa_sparse_attn";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
@@ -816,6 +838,7 @@ QSA_API qsa_status qsa_sparse_attn(const qsa_seq* seqs, int32_t n_seqs, const qs
 QSA_API qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* cfg, const void* k_new,
                                      const void* v_new, const void* idx_new, void* idx_keys, int64_t idx_tok_stride,
                                      qsa_dtype idx_dtype, void* stream) {
+  const NvtxRange nvtx_range("qsa_append_tokens");
   const char* fn = "qsa_append_tokens";
   int64_t rows = 0;
   qsa_status s = check_rows(seq, 1, fn, &rows);
@@ -918,6 +941,7 @@ QSA_API qsa_status qsa_arena_destroy(qsa_arena* arena) {
 // ------------------------------------------------------------------ step 5
 QSA_API qsa_status qsa_lse_merge(const float* o_parts, const float* lse_parts, int32_t n_parts, int64_t n_rows,
                          int32_t head_dim, void* out, qsa_dtype out_dtype, float* lse_out, void* stream) {
+  const NvtxRange nvtx_range("qsa_lse_merge");
   const char* fn = "qsa_lse_merge";
   if (n_parts < 1 || n_rows < 0) return fail(QSA_ERR_INVALID_ARG, "%s: n_parts >= 1 and n_rows >= 0 required", fn);
   if (head_dim < 4 || head_dim % 4 != 0) return fail(QSA_ERR_UNSUPPORTED, "%s: head_dim must be a multiple of 4", fn);
@@ -947,19 +971,27 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code must not pass the array's name to a kernel).
-qsa_status noalloc_scratch(void** out) {
+// Device address of the scratch array on the current device (host code must
+// not pass the array's name to a kernel).  Looked up on every call made
+// outside a stream capture, so a device reset (which reloads the module)
+// never leaves a stale address behind; a call inside a capture reuses the
+// address an earlier call on that device found.
+qsa_status noalloc_scratch(const char* fn, cudaStream_t st, void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn_noalloc");
-  if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_attn_noalloc: device %d", dev);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  if (dev < 0 || dev >= 64) return fail(QSA_ERR_UNSUPPORTED, "%s: device %d", fn, dev);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "qsa_sparse_attn_noalloc: cudaGetSymbolAddress");
     g_noalloc_ptr[dev] = p;
+  } else if (!g_noalloc_ptr[dev]) {
+    return fail(QSA_ERR_INVALID_ARG, "%s: the first call on a device must come before any stream capture", fn);
   }
   *out = g_noalloc_ptr[dev];
   return QSA_OK;
@@ -970,17 +1002,22 @@ qsa_status noalloc_scratch(void** out) {
 QSA_API qsa_status qsa_sparse_attn_noalloc(const qsa_seq* seqs, int32_t n_seqs, const qsa_attn_config* cfg,
                                            const void* q, const int32_t* sel, const int32_t* cnt, int32_t sel_ld,
                                            void* out, float* lse, void* stream) {
+  const NvtxRange nvtx_range("qsa_sparse_attn_noalloc");
   const char* fn = "qsa_sparse_attn_noalloc";
   int64_t rows = 0;
   qsa_status s = check_rows(seqs, n_seqs, fn, &rows);
   if (s != QSA_OK) return s;
   if ((s = check_attn_config(cfg, fn)) != QSA_OK) return s;
   if (sel_ld < 1) return fail(QSA_ERR_INVALID_ARG, "%s: sel_ld < 1", fn);
+  if (!q || !sel || !cnt || !out) return fail(QSA_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q) || !aligned16(out)) return fail(QSA_ERR_MISALIGNED, "%s: q/out not 16-byte aligned", fn);
+  if ((s = check_segments(seqs, n_seqs, cfg, fn)) != QSA_OK) return s;
   const size_t need = qsa_attn_workspace_size(seqs, n_seqs, cfg, sel_ld);
   if (need > kNoAllocScratchBytes)
     return fail(QSA_ERR_UNSUPPORTED, "%s: this call needs %zu bytes of scratch; the built-in array holds %zu", fn,
                 need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  if ((s = noalloc_scratch(&scratch)) != QSA_OK) return s;
-  return qsa_sparse_attn(seqs, n_seqs, cfg, q, sel, cnt, sel_ld, out, lse, scratch, kNoAllocScratchBytes, stream);
+  if (need > 0 && (s = noalloc_scratch(fn, as_stream(stream), &scratch)) != QSA_OK) return s;
+  return qsa_sparse_attn(seqs, n_seqs, cfg, q, sel, cnt, sel_ld, out, lse, scratch, need > 0 ? kNoAllocScratchBytes : 0,
+                         stream);
 }

@@ -57,6 +57,19 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// ---------------------------------------------------------------- KV segments
+struct Segment {
+  const void* k;
+  const void* v;
+  int64_t first;
+  int64_t n;
+  int64_t head_stride;
+  int64_t tok_stride;
+  const uint8_t* kv_scale;     // quantized state: scale records (4 bytes fp8, D/8 bytes q8)
+  int64_t s_head_stride;       // records
+  int64_t s_tok_stride;
+};
+
 // ---------------------------------------------------------------- selection
 struct RowSeq {
   int64_t n_tokens;
@@ -66,7 +79,7 @@ struct RowSeq {
 
 // Few-row selection split over several CTAs per row (select_split_kernel):
 // per-row scratch in the caller's workspace.  n_split = 0: one CTA per row.
-constexpr int kSelectMaxSplit = 256;
+constexpr int kSelectMaxSplit = 160;
 struct SelectSplit {
   int32_t n_split;       // CTAs per row
   int64_t cap;           // entries per slot
@@ -91,18 +104,6 @@ struct SelectParams {
 };
 
 // ---------------------------------------------------------------- attention
-struct Segment {
-  const void* k;
-  const void* v;
-  int64_t first;
-  int64_t n;
-  int64_t head_stride;
-  int64_t tok_stride;
-  const uint8_t* kv_scale;     // quantized state: scale records (4 bytes fp8, D/8 bytes q8)
-  int64_t s_head_stride;       // records
-  int64_t s_tok_stride;
-};
-
 struct AttnSeq {
   int64_t n_tokens;
   int32_t row_begin;

@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "qsa_internal.cuh"
+#include "qsa_tc.cuh"
 
 namespace qsa {
 
@@ -399,49 +400,6 @@ constexpr size_t kTmaPoolSmem = kTmaSmem + (size_t)kTmaConsumers * kPoolScratch;
 
 __device__ int g_score_wait_timeouts;   // waits that gave up (never expected)
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for the phase of the given parity to complete; gives up after about
-// two seconds (counted in g_score_wait_timeouts) instead of hanging.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > 2000000000ull) {
-      atomicAdd(&g_score_wait_timeouts, 1);
-      return false;
-    }
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
-          "r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
 // Lane l's channels 4l .. 4l + 3 of the four index keys of block b.
 __device__ __forceinline__ void load_index_keys(const ScoreSeq& sq, int64_t b, int lane, float4 (&k)[4]) {
   if (sq.idx_dtype == QSA_F32) {
@@ -498,8 +456,8 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTmaItems; ++i) {
-      mbar_init((uint32_t)__cvta_generic_to_shared(&full_bar[i]), 1);
-      mbar_init((uint32_t)__cvta_generic_to_shared(&empty_bar[i]), kItemTiles);
+      tc::bar_init(&full_bar[i], 1);
+      tc::bar_init(&empty_bar[i], kItemTiles);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -515,9 +473,9 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     // before the dependency wait when it holds only such blocks.
     bool waited = false;
     if (lane < kTmaItems) {
-      const uint32_t fb = (uint32_t)__cvta_generic_to_shared(&full_bar[lane]);
-      const uint32_t eb = (uint32_t)__cvta_generic_to_shared(&empty_bar[lane]);
-      const uint32_t dst = (uint32_t)__cvta_generic_to_shared(items + (size_t)lane * kItemBytes);
+      uint64_t* fb = &full_bar[lane];
+      uint64_t* eb = &empty_bar[lane];
+      unsigned char* dst = items + (size_t)lane * kItemBytes;
       for (int n = lane; n < n_items; n += kTmaItems) {
         const int si = find_seq_by_item(P, i0 + n);
         const int64_t y = (i0 + n - P.item_begin[si]) * kItemBlocks;
@@ -527,10 +485,11 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
           grid_dependency_wait();
           waited = true;
         }
-        if (n >= kTmaItems && !mbar_wait(eb, (uint32_t)((n / kTmaItems - 1) & 1))) break;
-        mbar_expect_tx(fb, kItemBytes);
+        if (n >= kTmaItems && !tc::bar_wait_spin(eb, (uint32_t)((n / kTmaItems - 1) & 1), &g_score_wait_timeouts))
+          break;
+        tc::bar_expect_tx(fb, kItemBytes);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kBoxBytes, &P.tmap[si], 32 * c, (int)y, fb);
+        for (int c = 0; c < 4; ++c) tc::tma_2d(dst + c * kBoxBytes, &P.tmap[si], 32 * c, (int)y, fb);
       }
     }
     if (!waited) grid_dependency_wait();
@@ -601,7 +560,7 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
       }
       bq_si = si;
     }
-    if (!mbar_wait((uint32_t)__cvta_generic_to_shared(&full_bar[q]), (uint32_t)((n / kTmaItems) & 1))) break;
+    if (!tc::bar_wait_spin(&full_bar[q], (uint32_t)((n / kTmaItems) & 1), &g_score_wait_timeouts)) break;
     float acc[NT][4];
     if (valid) {
       const unsigned char* tl = items + (size_t)q * kItemBytes + j * (kScoreTile * 128);
@@ -676,7 +635,7 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     }
     // The tile is free once every lane has read it.
     __syncwarp();
-    if (lane == 0) mbar_arrive((uint32_t)__cvta_generic_to_shared(&empty_bar[q]));
+    if (lane == 0) tc::bar_arrive(&empty_bar[q]);
     if (!valid) continue;
     // Epilogue as in score_mma_kernel: scores and the tile's group maximum.
 #pragma unroll
@@ -1158,6 +1117,11 @@ template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
   if (p_in.n_work == 0) return cudaSuccess;
   const int sms = device_sm_count();
+  // Up to 4 rows: the TMA ring (score_tma_kernel); 5 to 8 rows: direct loads.
+  if (q_dtype == QSA_BF16 && max_rows_per_group <= 4) {
+    cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (q_dtype == QSA_BF16 && max_rows_per_group <= kRowGroup) {
     bool one_group = true;
     for (int i = 0; i < p_in.n_seqs; ++i) one_group &= p_in.seq[i].n_groups == 1;
@@ -1172,16 +1136,12 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int m
                                                                                  : score_direct_kernel<2, NSEQ>),
                                          max_rows_per_group <= 4 ? DirShape<1>::smem : DirShape<2>::smem);
       if (e != cudaSuccess) return e;
-      if (max_rows_per_group <= 4)
+      if (max_rows_per_group <= 4)   // (the TMA ring declined the call)
         return launch_kernel(score_direct_kernel<1, NSEQ>, dim3(grid_of(DirShape<1>::warps, DirShape<1>::ctas_per_sm)),
                              dim3(32 * DirShape<1>::warps), DirShape<1>::smem, st, 0u, p_in);
       return launch_kernel(score_direct_kernel<2, NSEQ>, dim3(grid_of(DirShape<2>::warps, DirShape<2>::ctas_per_sm)),
                            dim3(32 * DirShape<2>::warps), DirShape<2>::smem, st, 0u, p_in);
     }
-  }
-  if (q_dtype != QSA_F32 && max_rows_per_group <= 4) {
-    cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st);
-    if (e != cudaErrorNotSupported) return e;
   }
   // The other kernels do not pool: the pooling launches first.
   ScoreParams<NSEQ> p = p_in;

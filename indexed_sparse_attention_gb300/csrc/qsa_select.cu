@@ -60,7 +60,7 @@ struct SelLayout {
     h3 = h2 + kBins;                               // radix level 3
     cg = h3 + kBins3;                              // candidate group ids
     r1 = cg + kGroupCap;
-    r2 = r1 + (groups > kListCap ? groups : kListCap);   // list ids
+    r2 = r1 + (groups > kListCap ? (groups + 3) / 4 * 4 : kListCap);   // list ids (16-byte aligned)
     selw = r2 + kListCap;                          // kept ids, one bit per block
     eqw = selw + (nw + 3) / 4 * 4;                 // entries equal to the k-th key
     total = eqw + (nw + 3) / 4 * 4;
@@ -522,21 +522,25 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
 // the selection's loads and list building run on many SMs instead of one:
 //  1. every CTA of the row reads all the row's group maxima and finds the bin
 //     B of the k-th largest (the bound of step 1 above; the same B in every
-//     CTA);
-//  2. CTA c takes groups [c G / n, (c + 1) G / n): it reads the blocks of its
-//     candidate groups and writes the (key, id) pairs whose key is in a bin
-//     >= B to its own slot of the workspace, in ascending id order, with
-//     their count;
-//  3. each CTA then takes a ticket (an atomic count per row); the CTA that
-//     draws the last one knows every slot is written.  It concatenates the
-//     slots in part order -- ascending ids -- into shared memory, runs the
-//     radix levels of step 3 over the list, and writes the kept ids in list
-//     order: an entry is kept when its key exceeds the k-th key K, or equals
-//     it and fewer than `need` entries equal to K precede it, and its
-//     position is the number of kept entries before it (one prefix scan
-//     over the list).  It resets the row's ticket to zero.
+//     CTA); in the same round trip it reads the scores of its own part of the
+//     row, groups [c G / n, (c + 1) G / n);
+//  2. CTA c keeps the blocks of its part whose group maximum and own key are
+//     in a bin >= B and writes their (key, id) pairs to its own slot of the
+//     workspace, in ascending id order, with their count;
+//  3. each CTA then takes a ticket (an atomic count per row, released after
+//     the slot is written); the CTA that draws the last one knows every slot
+//     is written.  It reads the counts and the slots' first entries in one
+//     round trip, concatenates the slots in part order -- ascending ids --
+//     in shared memory, runs the radix levels of step 3 over the list, and
+//     writes the kept ids in list order: an entry is kept when its key
+//     exceeds the k-th key K, or equals it and fewer than `need` entries
+//     equal to K precede it, and its position is the number of kept entries
+//     before it (one prefix scan over the list).  It resets the row's ticket
+//     to zero.
 // No CTA waits for another.  A list longer than the shared-memory capacity
 // is selected from the whole score row in global memory, as in select_kernel.
+constexpr int kSlotPeek = 64;   // entries of each slot the last CTA reads with the counts
+
 template <int NSEQ>
 __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
   constexpr int NT = kThreads;
@@ -548,8 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
   const SelLayout L(max_nb);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = p.split.n_split, part = (int)blockIdx.x;
-  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;               // the three histograms
-  for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;   // the two bitmaps (long lists)
+  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;   // the three histograms
   if (tid == 0) {
     s_res[0] = 0u;
     s_res[1] = 0u;
@@ -576,13 +579,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
   uint32_t* r1 = sm + L.r1;
   uint32_t* r2 = sm + L.r2;
   uint32_t* h1 = sm + L.h1;
-  __syncthreads();   // histograms and bitmaps cleared
+  float* slice = reinterpret_cast<float*>(r2);       // this part's scores (phase 2)
+  const int ga = (int)((int64_t)G * part / C), gb = (int)((int64_t)G * (part + 1) / C);
+  const int64_t sb0 = (int64_t)ga * kGroup, sb1 = min(nb, (int64_t)gb * kGroup);
+  const int n_slice = (int)max((int64_t)0, sb1 - sb0);
+  const bool in_smem = n_slice <= kListCap;
+  __syncthreads();   // histograms cleared
 
-  // 1. All group maxima of the row (four float4 loads per thread in flight),
-  // their keys kept in r1, their top-12-bit histogram in h1.
+  // 1. All group maxima of the row (four float4 loads per thread) and this
+  // part's scores (up to two float4 per thread) in one round trip; the
+  // maxima's keys in r1 and their top-12-bit histogram in h1.
   {
     const float* grow = p.gmax + (int64_t)r * p.gld;
-    float4 v[4];
+    float4 v[4], w[2];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int g0 = 4 * (tid + j * NT);
@@ -593,6 +602,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
         v[j].x = __ldg(grow + g0);
         if (g0 + 1 < G) v[j].y = __ldg(grow + g0 + 1);
         if (g0 + 2 < G) v[j].z = __ldg(grow + g0 + 2);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int b = 4 * (tid + j * NT);
+      w[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in_smem && b < n_slice) {
+        if (b + 4 <= n_slice) {
+          w[j] = __ldg(reinterpret_cast<const float4*>(srow + sb0 + b));
+        } else {
+          w[j].x = __ldg(srow + sb0 + b);
+          if (b + 1 < n_slice) w[j].y = __ldg(srow + sb0 + b + 1);
+          if (b + 2 < n_slice) w[j].z = __ldg(srow + sb0 + b + 2);
+        }
       }
     }
 #pragma unroll
@@ -608,6 +631,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
         }
       }
     }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int b = 4 * (tid + j * NT);
+      if (in_smem && b < n_slice) *reinterpret_cast<float4*>(slice + b) = w[j];   // (4-aligned: the slice holds >= b + 4)
+    }
   }
   __syncthreads();
   uint32_t B = 0u;
@@ -617,10 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
   }
   for (int i = tid; i < kBins; i += NT) h1[i] = 0u;   // reused by radix level 2
 
-  // 2. This CTA's candidate groups: thread t of a round takes group gs + t
+  // 2. This part's candidate groups: thread t of a round takes group ga + t
   // and keeps its blocks whose key is in a bin >= B; a prefix scan over the
   // CTA places them in ascending id order in the slot.
-  const int ga = (int)((int64_t)G * part / C), gb = (int)((int64_t)G * (part + 1) / C);
   uint2* slot = p.split.slots + ((int64_t)r * C + part) * p.split.cap;
   uint32_t n_out = 0u;
   int wb = 1;
@@ -631,7 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
     float x[kGroup];
     uint32_t keep = 0u;   // bit e: block b0 + e is kept
     if (g < gb && (r1[g] >> 20) >= B) {
-      if (b0 + kGroup <= nb) {
+      if (in_smem) {
+#pragma unroll
+        for (int e = 0; e < kGroup; ++e) x[e] = b0 + e < nb ? slice[b0 + e - sb0] : 0.f;
+      } else if (b0 + kGroup <= nb) {
 #pragma unroll
         for (int q = 0; q < kGroup / 4; ++q) {
           const float4 w = __ldg(reinterpret_cast<const float4*>(srow + b0) + q);
@@ -663,16 +693,34 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
   }
   if (nan_keys) atomicAdd(&g_nan_keys, nan_keys);
   if (tid == 0) p.split.counts[(int64_t)r * C + part] = n_out;
-  // Publish the slot, then draw a ticket.
-  __threadfence();
+  // Publish the slot: the CTA barrier orders every thread's writes before
+  // thread 0's release; the ticket's acquire orders the last CTA's reads after
+  // every CTA's writes.
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(p.split.tickets + r, 1u) == (uint32_t)(C - 1);
+  if (tid == 0) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(p.split.tickets + r) : "memory");
+    s_last = old == (uint32_t)(C - 1);
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
-  // 3. The last CTA: slot counts -> offsets, the list in ascending id order.
+  // 3. The last CTA: the counts and each slot's first kSlotPeek entries in
+  // one round trip (warp w holds slots w, w + 32, ...), the offsets by a
+  // prefix scan, then the list in shared memory in ascending id order.
   const uint32_t c_t = tid < C ? __ldcg(p.split.counts + (int64_t)r * C + tid) : 0u;
+  constexpr int kPeekPerLane = kSlotPeek / 32;
+  constexpr int kSlotsPerWarp = (kMaxSplit + kWarps - 1) / kWarps;
+  uint2 peek[kSlotsPerWarp][kPeekPerLane];
+#pragma unroll
+  for (int u = 0; u < kSlotsPerWarp; ++u) {
+    const int c = warp + u * kWarps;
+#pragma unroll
+    for (int j = 0; j < kPeekPerLane; ++j)
+      peek[u][j] = c < C && lane + 32 * j < p.split.cap
+                       ? __ldcg(p.split.slots + ((int64_t)r * C + c) * p.split.cap + lane + 32 * j)
+                       : make_uint2(0u, 0u);
+  }
   uint32_t n_list;
   const uint32_t off = block_scan<NT>(c_t, wt[wb], &n_list);
   if (tid < C) {
@@ -684,13 +732,24 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
   const int nw = (int)((nb + 31) / 32);
   if (n_list <= (uint32_t)kListCap) {
     const int n = (int)n_list;
-    for (int c = warp; c < C; c += kWarps) {
+#pragma unroll
+    for (int u = 0; u < kSlotsPerWarp; ++u) {
+      const int c = warp + u * kWarps;
+      if (c >= C) break;
       const uint32_t o = s_off[c], cn = s_cnt[c];
+#pragma unroll
+      for (int j = 0; j < kPeekPerLane; ++j) {
+        const uint32_t e = lane + 32 * j;
+        if (e < cn) {
+          r1[o + e] = peek[u][j].x;
+          r2[o + e] = peek[u][j].y;
+        }
+      }
       const uint2* src = p.split.slots + ((int64_t)r * C + c) * p.split.cap;
-      for (uint32_t j = lane; j < cn; j += 32) {
-        const uint2 e = __ldcg(src + j);
-        r1[o + j] = e.x;
-        r2[o + j] = e.y;
+      for (uint32_t e = kSlotPeek + lane; e < cn; e += 32) {   // longer slots
+        const uint2 v = __ldcg(src + e);
+        r1[o + e] = v.x;
+        r2[o + e] = v.y;
       }
     }
     __syncthreads();
@@ -731,7 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectP
       }
     }
   } else {
-    // The whole row from global memory (the list would not fit).
+    // The whole row from global memory (the list would not fit): the bitmaps
+    // of radix_and_write start at zero.
+    for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;
+    __syncthreads();
     const int nbi = (int)nb;
     radix_and_write<NT>(
         (uint32_t)k, nw,

@@ -70,6 +70,19 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, int* time
   return true;
 }
 
+// As bar_wait, without the suspend hint (the waiting thread keeps polling):
+// for waits on a stream's next slot, where the data is usually about to land.
+__device__ __forceinline__ bool bar_wait_spin(uint64_t* b, uint32_t parity, int* timeouts) {
+  if (bar_try(b, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (!bar_try(b, parity))
+    if (now_ns() - t0 > 2000000000ull) {
+      atomicAdd(timeouts, 1);
+      return false;
+    }
+  return true;
+}
+
 // ---------------------------------------------------------------- copies
 __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(

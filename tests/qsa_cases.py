@@ -43,6 +43,24 @@ def pool_all(idxk_dev: torch.Tensor, pooled: torch.Tensor, L: int):
     qsa.pool_index_keys(idxk_dev, pooled, 0, L // 4)
 
 
+def assert_pooled_close(got: np.ndarray, idxk, blocks):
+    """Pooled keys of the listed blocks against the oracle's fp64 mean of the
+    four stored index keys: three fp32 additions and an exact scaling, so
+    |err| <= 3 u mean_j |k_j| + u |mean| (u = 2^-24)."""
+    blocks = np.asarray(list(blocks), dtype=np.int64)
+    if blocks.size == 0:
+        return
+    if isinstance(idxk, torch.Tensor):
+        idxk = idxk.cpu()
+    keys = idxk.double().numpy() if isinstance(idxk, torch.Tensor) else np.asarray(idxk, dtype=np.float64)
+    want = oracle.pool(idxk)[blocks]
+    rows = keys[: 4 * (int(blocks.max()) + 1)].reshape(-1, 4, keys.shape[1])[blocks]
+    u = 2.0 ** -24
+    bound = 3 * u * np.abs(rows).mean(axis=1) + u * np.abs(want)
+    err = np.abs(got[blocks].astype(np.float64) - want)
+    assert (err <= bound).all(), f"pooled keys off by up to {err.max():.3e}"
+
+
 def score_bound(q_idx, pooled_f64: np.ndarray, row_pos) -> np.ndarray:
     """Per-entry absolute error bound of an fp32 score (see module docstring)."""
     q = q_idx.double().cpu().numpy() if isinstance(q_idx, torch.Tensor) else np.asarray(q_idx, dtype=np.float64)

@@ -156,6 +156,15 @@ def test_prefill_chunk_blocked_selection_equals_one_pass():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(to_np(cnt), to_np(step.cnt))
     np.testing.assert_array_equal(to_np(sel), to_np(step.sel))
+    # ... and the blocked selection against the oracle on a sample of rows
+    # (rows are independent), chunk edges included.
+    rows = [0, 1, 1023, 1024, 2047]
+    h = _host(x)
+    pos = [x.row_pos[r] for r in rows]
+    pooled_ref = oracle.pool(h["idxk"])
+    s_ref = oracle.score(h["q_idx"][rows], pooled_ref, pos)
+    sel_ref, cnt_ref, tau = oracle.select(s_ref, pos)
+    assert_selection_close(to_np(sel)[rows], to_np(cnt)[rows], sel_ref, cnt_ref, tau, s_ref, pos)
 
 
 @pytest.mark.parametrize("D", [256, 128])

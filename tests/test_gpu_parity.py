@@ -9,8 +9,8 @@ import torch
 
 import indexed_sparse_attention_gb300 as qsa
 import oracle
-from qsa_cases import (assert_attn_close, assert_scores_close, assert_selection_close, dev, oracle_layer,
-                       pool_all, pooled_buffer, score_bound, to_np, DeviceLayer)
+from qsa_cases import (assert_attn_close, assert_pooled_close, assert_scores_close, assert_selection_close, dev,
+                       oracle_layer, pool_all, pooled_buffer, score_bound, to_np, DeviceLayer)
 from workloads import make_layer, segment_cuts
 
 pytestmark = pytest.mark.gpu
@@ -155,8 +155,20 @@ def _pool_score_vs_separate(Ls, Ms, idx_dtype, q_dtype):
                     qsa.pool_index_keys(sq.idx_keys, sq.pooled, b0, b1 - b0)
             qsa.score_blocks(seqs, q_idx, scores, group_max=gmax)
         torch.cuda.synchronize()
-        runs.append((seqs, scores, gmax))
-    (sa, sc_a, gm_a), (sb, sc_b, gm_b) = runs
+        runs.append((seqs, scores, gmax, q_idx))
+    (sa, sc_a, gm_a, q_a), (sb, sc_b, gm_b, _) = runs
+    # The fused call against the oracle: the blocks it pooled, and every
+    # visible score of a sample of rows (scores of the stored pooled keys).
+    r = 0
+    for qa in sa:
+        L, M = qa.n_tokens, qa.n_rows
+        assert_pooled_close(to_np(qa.pooled), qa.idx_keys.float(), range((L - M) // 4, L // 4))
+        pos = qa.row_pos
+        pooled_ref = to_np(qa.pooled)[:L // 4].astype(np.float64)
+        s_ref = oracle.score(q_a[r:r + M].float().cpu(), pooled_ref, pos)
+        nb = s_ref.shape[1]
+        assert_scores_close(to_np(sc_a)[r:r + M, :nb], s_ref, score_bound(q_a[r:r + M].float(), pooled_ref, pos), pos)
+        r += M
     r = 0
     for qa, qb in zip(sa, sb):
         L, M = qa.n_tokens, qa.n_rows
@@ -324,7 +336,9 @@ def test_append_writes_caches_and_pools(L, n, kv_dtype, idx_dtype, n_segs):
     if L // 4:
         qsa.pool_index_keys(idx_full, ref, 0, L // 4)
     torch.cuda.synchronize()
-    # The same numbers as the pooling kernel (itself checked against the oracle above).
+    # The blocks the append pooled, against the oracle's mean of the stored
+    # index keys, and the same numbers as the pooling kernel.
+    assert_pooled_close(to_np(pooled), idx_full.float(), range(b0, L // 4))
     assert torch.equal(pooled[:L // 4], ref[:L // 4])
 
 

@@ -83,6 +83,34 @@ def test_noalloc_matches_workspace_entry_point(L, M, n_splits):
         _close((to_np(out), to_np(lse)), *want)
 
 
+def test_noalloc_shapes_in_turn_leave_nothing_behind():
+    """The shared array keeps the previous call's partials; a call with another
+    shape or split count must not read them.  A 40-split call, a one-row
+    65,536-token call with the library's own plan, then the 40-split call
+    again, each against the workspace entry point."""
+    L_ = qsa.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    for (L, M, n_splits) in ((9001, 4, 40), (65_536, 1, 0), (9001, 4, 40)):
+        x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=37 + M, n_planted=64)
+        sel, cnt = _selection(x)[:2]
+        q, k, v = x.q.to(dev()), x.k.to(dev()), x.v.to(dev())
+        seqs = qsa.make_seq_array([qsa.Seq(x.L, x.M, segments=[qsa.Segment(k, v, 0)])])
+        seld, cntd = torch.from_numpy(sel).to(dev()), torch.from_numpy(cnt).to(dev())
+        cfg = qsa.attn_config(q, 2, torch.float32, 0.0, n_splits)
+        need = L_.qsa_attn_workspace_size(seqs, 1, ctypes.byref(cfg), sel.shape[1])
+        ws = torch.zeros(max(need, 16), dtype=torch.uint8, device=dev())
+        ref = [torch.empty((M, 24, 256), device=dev()), torch.empty((M, 24), device=dev())]
+        got = [torch.full((M, 24, 256), float("nan"), device=dev()), torch.full((M, 24), float("nan"), device=dev())]
+        assert L_.qsa_sparse_attn(seqs, 1, ctypes.byref(cfg), q.data_ptr(), seld.data_ptr(), cntd.data_ptr(),
+                                  sel.shape[1], ref[0].data_ptr(), ref[1].data_ptr(), ws.data_ptr(), ws.numel(),
+                                  stream) == 0, L_.qsa_last_error()
+        assert L_.qsa_sparse_attn_noalloc(seqs, 1, ctypes.byref(cfg), q.data_ptr(), seld.data_ptr(), cntd.data_ptr(),
+                                          sel.shape[1], got[0].data_ptr(), got[1].data_ptr(), stream) == 0, \
+            L_.qsa_last_error()
+        torch.cuda.synchronize()
+        _close((to_np(got[0]), to_np(got[1])), to_np(ref[0]), to_np(ref[1]))
+
+
 def test_noalloc_rejects_plans_beyond_its_scratch():
     # 2,048 prefill rows forced to 40 splits need far more than the built-in
     # 4 MiB; the call is refused on the host before any launch.
