@@ -302,25 +302,15 @@ def pool_score_blocks(seqs, q_idx: torch.Tensor, scores: torch.Tensor, stream=No
         0 if workspace is None else workspace.numel(), _stream(stream)))
 
 
-def select_workspace_size(seqs, top_k: int = TOP_K, seq_array=None) -> int:
-    arr = seq_array if seq_array is not None else make_seq_array(seqs)
-    return int(lib().qsa_select_workspace_size(arr, len(arr), top_k))
-
-
 def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor, top_k: int = TOP_K,
                 workspace: torch.Tensor | None = None, stream=None, seq_array=None,
-                group_max: torch.Tensor | None = None, one_cta: bool = False):
+                group_max: torch.Tensor | None = None):
     """Step 3: the top_k best blocks per row, ascending ids, -1 padded.
-    group_max: the group maxima score_blocks wrote for these scores, or None.
-    workspace: zero-filled before its first use (the library leaves it so);
-    allocated here when None.  one_cta: pass no workspace, so every row runs
-    in one CTA."""
+    group_max: the group maxima score_blocks wrote for these scores, or None."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     need = lib().qsa_select_workspace_size(arr, len(arr), top_k)
-    if one_cta:
-        workspace = None
-    elif need and workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=scores.device)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
     _check("qsa_select_topk", lib().qsa_select_topk(
         arr, len(arr), scores.data_ptr(), scores.stride(0), _ptr(group_max),
         0 if group_max is None else group_max.stride(0), int(top_k), sel.data_ptr(), cnt.data_ptr(),
@@ -329,12 +319,11 @@ def select_topk(seqs, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor
 
 def score_select_topk(seqs, q_idx: torch.Tensor, scores: torch.Tensor, sel: torch.Tensor, cnt: torch.Tensor,
                       top_k: int = TOP_K, workspace: torch.Tensor | None = None, stream=None, seq_array=None):
-    """Steps 2 and 3 in one call; the workspace holds the group maxima and
-    the selection's scratch (zero-filled before its first use)."""
+    """Steps 2 and 3 in one call; the workspace holds the group maxima."""
     arr = seq_array if seq_array is not None else make_seq_array(seqs)
     need = lib().qsa_score_select_workspace_size(arr, len(arr), top_k)
     if need and workspace is None:
-        workspace = torch.zeros(need, dtype=torch.uint8, device=scores.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
     _check("qsa_score_select_topk", lib().qsa_score_select_topk(
         arr, len(arr), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0), int(top_k),
         sel.data_ptr(), cnt.data_ptr(), _ptr(workspace), 0 if workspace is None else workspace.numel(),
@@ -545,10 +534,7 @@ class LayerStep:
         sel_ws = int(lib().qsa_score_select_workspace_size(self.arr, len(self.arr), self.top_k))
         attn_ws = attn_workspace_size(None, self.cfg, self.top_k, seq_array=self.arr)
         # Selection scratch: zero-filled once; every call leaves it zeroed.
-        self.sel_ws = torch.zeros(max(sel_ws, 16), dtype=torch.uint8, device=dev)
-        split_ws = select_workspace_size(None, self.top_k, seq_array=self.arr)
-        self.split_select = False
-        self.split_ws = torch.zeros(split_ws, dtype=torch.uint8, device=dev) if split_ws else None
+        self.sel_ws = torch.empty(max(sel_ws, 16), dtype=torch.uint8, device=dev)
         self.ws = torch.empty(max(attn_ws, 16), dtype=torch.uint8, device=dev)
         # Blocks completed by each sequence's new rows: [first, last] of nb(p) over its rows.
         self.pool_jobs = []
@@ -580,8 +566,8 @@ class LayerStep:
                           workspace=self.score_ws, idx_array=self.idx_array)
 
     def select(self, stream=None):
-        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, self.split_ws, stream, seq_array=self.arr,
-                    group_max=self.group_max, one_cta=self.split_ws is None or not self.split_select)
+        select_topk(None, self.scores, self.sel, self.cnt, self.top_k, None, stream, seq_array=self.arr,
+                    group_max=self.group_max)
 
     def score_select(self, stream=None):
         score_select_topk(None, self.q_idx, self.scores, self.sel, self.cnt, self.top_k, self.sel_ws, stream,

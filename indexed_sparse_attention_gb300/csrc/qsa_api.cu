@@ -367,53 +367,20 @@ QSA_API qsa_status qsa_pool_score_blocks(const qsa_seq* seqs, int32_t n_seqs, co
 }
 
 // ------------------------------------------------------------------ step 3
-namespace {
-// Calls with few rows split each row's selection over several CTAs
-// (select_split_kernel); the workspace holds a ticket per row, then a count
-// per (row, CTA), then each CTA's candidate slot.  Byte offsets.
-struct SelectSplitPlan {
-  int32_t n_split = 0;   // 0: one CTA per row (no workspace used)
-  int64_t cap = 0;       // entries per slot
-  size_t counts = 0, slots = 0, total = 0;
-};
-
-size_t round256(size_t b) { return (b + 255) / 256 * 256; }
-
-SelectSplitPlan select_split_plan(const qsa_seq* seqs, int32_t n_seqs) {
-  SelectSplitPlan pl;
-  if (!seqs || n_seqs < 1) return pl;
-  int64_t rows = 0, groups = 0;
-  for (int i = 0; i < n_seqs; ++i) {
-    rows += std::max(0, seqs[i].n_rows);
-    groups = std::max(groups, n_groups(std::max<int64_t>(0, max_visible_blocks(seqs[i]))));
-  }
-  const int64_t sms = device_sm_count();
-  if (rows < 1 || 2 * rows > sms) return pl;   // many rows: one CTA per row already fills the GPU
-  // About one CTA per SM over the call, each with at least 32 groups.
-  const int64_t C = std::min<int64_t>({(int64_t)kSelectMaxSplit, sms / rows, (groups + 31) / 32});
-  if (C < 2) return pl;
-  pl.n_split = (int32_t)C;
-  pl.cap = (groups + C - 1) / C * QSA_SCORE_GROUP;
-  pl.counts = round256(sizeof(uint32_t) * (size_t)rows);
-  pl.slots = pl.counts + round256(sizeof(uint32_t) * (size_t)(rows * C));
-  pl.total = pl.slots + sizeof(uint2) * (size_t)(rows * C * pl.cap);
-  return pl;
-}
-}  // namespace
-
 QSA_API size_t qsa_select_workspace_size(const qsa_seq* seqs, int32_t n_seqs, int32_t top_k) {
+  (void)seqs;
+  (void)n_seqs;
   (void)top_k;
-  return select_split_plan(seqs, n_seqs).total;
+  return 0;
 }
 
 template <int NSEQ>
 static qsa_status select_chunk(const qsa_seq* seqs, int n, int32_t row_begin, const float* scores, int64_t ld,
                                const float* gmax, int64_t gld, int32_t top_k, int32_t* sel, int32_t* cnt,
-                               const SelectSplit& split, cudaStream_t st) {
+                               cudaStream_t st) {
   SelectParams<NSEQ> p{};
   p.gmax = gmax;
   p.gld = gld;
-  p.split = split;
   int rows = 0;
   int64_t max_nb = 0;
   p.row_base = row_begin;
@@ -455,29 +422,16 @@ QSA_API qsa_status qsa_select_topk(const qsa_seq* seqs, int32_t n_seqs, const fl
     if (group_max && n_groups(max_visible_blocks(seqs[i])) > group_ld)
       return fail(QSA_ERR_INVALID_ARG, "%s: group_ld smaller than the groups of sequence %d", fn, i);
   }
-  // Few rows with group maxima and a workspace: each row over several CTAs.
-  SelectSplit split{};
-  const SelectSplitPlan pl = select_split_plan(seqs, n_seqs);
-  if (pl.n_split > 0 && group_max && workspace) {
-    if (workspace_bytes < pl.total)
-      return fail(QSA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, pl.total, workspace_bytes);
-    if (!aligned16(workspace)) return fail(QSA_ERR_MISALIGNED, "%s: workspace not aligned", fn);
-    char* w = static_cast<char*>(workspace);
-    split.n_split = pl.n_split;
-    split.cap = pl.cap;
-    split.tickets = reinterpret_cast<uint32_t*>(w);
-    split.counts = reinterpret_cast<uint32_t*>(w + pl.counts);
-    split.slots = reinterpret_cast<uint2*>(w + pl.slots);
-  }
+  (void)workspace;
+  (void)workspace_bytes;
   cudaStream_t st = as_stream(stream);
   if (n_seqs == 1) {
-    s = select_chunk<1>(seqs, 1, 0, scores, ld, group_max, group_ld, top_k, sel, cnt, split, st);
+    s = select_chunk<1>(seqs, 1, 0, scores, ld, group_max, group_ld, top_k, sel, cnt, st);
   } else {
     int32_t row_begin = 0;
     for (int c = 0; c < n_seqs && s == QSA_OK; c += kLaunchSeqs) {
       const int n = std::min(kLaunchSeqs, n_seqs - c);
-      s = select_chunk<kLaunchSeqs>(seqs + c, n, row_begin, scores, ld, group_max, group_ld, top_k, sel, cnt, split,
-                                    st);
+      s = select_chunk<kLaunchSeqs>(seqs + c, n, row_begin, scores, ld, group_max, group_ld, top_k, sel, cnt, st);
       for (int i = 0; i < n; ++i) row_begin += seqs[c + i].n_rows;
     }
   }
@@ -507,8 +461,7 @@ QSA_API size_t qsa_score_select_workspace_size(const qsa_seq* seqs, int32_t n_se
   if (!seqs || n_seqs < 1) return 0;
   // Group maxima, the selection's scratch, then the scoring's (bf16 queries
   // assumed: the tensor-core planes are counted whenever a sequence is wide).
-  return fused_gmax_bytes(seqs, n_seqs) + round256(select_split_plan(seqs, n_seqs).total) +
-         qsa_score_workspace_size(seqs, n_seqs, QSA_BF16);
+  return fused_gmax_bytes(seqs, n_seqs) + qsa_score_workspace_size(seqs, n_seqs, QSA_BF16);
 }
 
 QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, const void* q_idx,
@@ -532,14 +485,12 @@ QSA_API qsa_status qsa_score_select_topk(const qsa_seq* seqs, int32_t n_seqs, co
   float* gmax = static_cast<float*>(workspace);
   const int64_t gld = fused_group_ld(seqs, n_seqs);
   const size_t gb = fused_gmax_bytes(seqs, n_seqs);
-  const size_t sb = round256(select_split_plan(seqs, n_seqs).total);
-  char* sel_ws = static_cast<char*>(workspace) + gb;
-  void* planes = sel_ws + sb;
-  const size_t planes_bytes = workspace_bytes - gb - sb;
+  void* planes = static_cast<char*>(workspace) + gb;
+  const size_t planes_bytes = workspace_bytes - gb;
   if ((s = qsa_score_blocks(seqs, n_seqs, q_idx, q_idx_dtype, scores, ld, gmax, gld, planes, planes_bytes, stream)) !=
       QSA_OK)
     return s;
-  return qsa_select_topk(seqs, n_seqs, scores, ld, gmax, gld, top_k, sel, cnt, sb ? sel_ws : nullptr, sb, stream);
+  return qsa_select_topk(seqs, n_seqs, scores, ld, gmax, gld, top_k, sel, cnt, nullptr, 0, stream);
 }
 
 // ------------------------------------------------------------------ steps 2 + 3 over key-axis chunks

@@ -77,17 +77,6 @@ struct RowSeq {
   int32_t n_rows;
 };
 
-// Few-row selection split over several CTAs per row (select_split_kernel):
-// per-row scratch in the caller's workspace.  n_split = 0: one CTA per row.
-constexpr int kSelectMaxSplit = 160;
-struct SelectSplit {
-  int32_t n_split;       // CTAs per row
-  int64_t cap;           // entries per slot
-  uint2* slots;          // [rows][n_split][cap] (order key, block id) of each CTA's candidates
-  uint32_t* counts;      // [rows][n_split] entries written to each slot
-  uint32_t* tickets;     // [rows] CTAs of the row done; zero between calls
-};
-
 template <int NSEQ>
 struct SelectParams {
   RowSeq seq[NSEQ];
@@ -100,7 +89,6 @@ struct SelectParams {
   int32_t top_k;
   int32_t* sel;
   int32_t* cnt;
-  SelectSplit split;
 };
 
 // ---------------------------------------------------------------- attention

@@ -41,11 +41,8 @@ constexpr int kBins = 4096;                        // radix levels 1 and 2: 12 k
 constexpr int kBins3 = 256;                        // radix level 3: the last 8 key bits
 constexpr int kGroupCap = 1024;                    // candidate groups read back (16,384 blocks)
 constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
-constexpr int kMaxGroups = QSA_MAX_BLOCKS / kGroup;
-static_assert(kMaxGroups <= 16 * kThreads, "select_split_kernel loads every group maximum in one pass");
 constexpr int kLoadBatch = 16;                                  // group maxima a thread loads per pass
 constexpr int kChunkBatch = 4;                                  // float4 chunks a thread loads per pass
-constexpr int kMaxSplit = kSelectMaxSplit;                      // CTAs per row of select_split_kernel
 
 
 // Shared-memory layout (32-bit words); R1 holds the group-maximum keys, then
@@ -517,317 +514,6 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
   if (tid == 0) p.cnt[r] = k;
 }
 
-// ------------------------------------------------------------------ one row over several CTAs
-// Rows of few-row calls (decode, verify) are split over n_split CTAs each, so
-// the selection's loads and list building run on many SMs instead of one:
-//  1. every CTA of the row reads all the row's group maxima and finds the bin
-//     B of the k-th largest (the bound of step 1 above; the same B in every
-//     CTA); in the same round trip it reads the scores of its own part of the
-//     row, groups [c G / n, (c + 1) G / n);
-//  2. CTA c keeps the blocks of its part whose group maximum and own key are
-//     in a bin >= B and writes their (key, id) pairs to its own slot of the
-//     workspace, in ascending id order, with their count;
-//  3. each CTA then takes a ticket (an atomic count per row, released after
-//     the slot is written); the CTA that draws the last one knows every slot
-//     is written.  It reads the counts and the slots' first entries in one
-//     round trip, concatenates the slots in part order -- ascending ids --
-//     in shared memory, runs the radix levels of step 3 over the list, and
-//     writes the kept ids in list order: an entry is kept when its key
-//     exceeds the k-th key K, or equals it and fewer than `need` entries
-//     equal to K precede it, and its position is the number of kept entries
-//     before it (one prefix scan over the list).  It resets the row's ticket
-//     to zero.
-// No CTA waits for another.  A list longer than the shared-memory capacity
-// is selected from the whole score row in global memory, as in select_kernel.
-constexpr int kSlotPeek = 64;   // entries of each slot the last CTA reads with the counts
-
-template <int NSEQ>
-__global__ void __launch_bounds__(kThreads, 1) select_split_kernel(const SelectParams<NSEQ> p, int64_t max_nb) {
-  constexpr int NT = kThreads;
-  extern __shared__ __align__(16) uint32_t sm[];
-  __shared__ uint32_t wt[2][kWarps];
-  __shared__ uint32_t s_res[2];
-  __shared__ uint32_t s_last;
-  __shared__ uint32_t s_off[kMaxSplit], s_cnt[kMaxSplit];
-  const SelLayout L(max_nb);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int C = p.split.n_split, part = (int)blockIdx.x;
-  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;   // the three histograms
-  if (tid == 0) {
-    s_res[0] = 0u;
-    s_res[1] = 0u;
-  }
-  grid_dependency_sync();
-  const int r = p.row_base + (int)blockIdx.y;
-  int si = 0;
-#pragma unroll
-  for (int i = 1; i < NSEQ; ++i)
-    if (i < p.n_seqs && r >= p.seq[i].row_begin) si = i;
-  const RowSeq sq = p.seq[si];
-  const int64_t nb = visible_blocks(row_position(sq.n_tokens, sq.n_rows, r - sq.row_begin));
-  const int k = p.top_k;
-  int32_t* out = p.sel + (int64_t)r * k;
-  if (nb <= k) {   // every visible block; no ticket is drawn
-    if (part == 0) {
-      for (int i = tid; i < k; i += NT) out[i] = i < nb ? i : -1;
-      if (tid == 0) p.cnt[r] = (int32_t)nb;
-    }
-    return;
-  }
-  const float* srow = p.scores + (int64_t)r * p.ld;
-  const int G = (int)((nb + kGroup - 1) / kGroup);   // <= kMaxGroups = 4 * 4 * NT
-  uint32_t* r1 = sm + L.r1;
-  uint32_t* r2 = sm + L.r2;
-  uint32_t* h1 = sm + L.h1;
-  float* slice = reinterpret_cast<float*>(r2);       // this part's scores (phase 2)
-  const int ga = (int)((int64_t)G * part / C), gb = (int)((int64_t)G * (part + 1) / C);
-  const int64_t sb0 = (int64_t)ga * kGroup, sb1 = min(nb, (int64_t)gb * kGroup);
-  const int n_slice = (int)max((int64_t)0, sb1 - sb0);
-  const bool in_smem = n_slice <= kListCap;
-  __syncthreads();   // histograms cleared
-
-  // 1. All group maxima of the row (four float4 loads per thread) and this
-  // part's scores (up to two float4 per thread) in one round trip; the
-  // maxima's keys in r1 and their top-12-bit histogram in h1.
-  {
-    const float* grow = p.gmax + (int64_t)r * p.gld;
-    float4 v[4], w[2];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int g0 = 4 * (tid + j * NT);
-      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g0 + 4 <= G) {
-        v[j] = __ldg(reinterpret_cast<const float4*>(grow + g0));
-      } else if (g0 < G) {
-        v[j].x = __ldg(grow + g0);
-        if (g0 + 1 < G) v[j].y = __ldg(grow + g0 + 1);
-        if (g0 + 2 < G) v[j].z = __ldg(grow + g0 + 2);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int b = 4 * (tid + j * NT);
-      w[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (in_smem && b < n_slice) {
-        if (b + 4 <= n_slice) {
-          w[j] = __ldg(reinterpret_cast<const float4*>(srow + sb0 + b));
-        } else {
-          w[j].x = __ldg(srow + sb0 + b);
-          if (b + 1 < n_slice) w[j].y = __ldg(srow + sb0 + b + 1);
-          if (b + 2 < n_slice) w[j].z = __ldg(srow + sb0 + b + 2);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int g0 = 4 * (tid + j * NT);
-      const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (g0 + e < G) {
-          const uint32_t key = order_key(x[e]);
-          r1[g0 + e] = key;
-          atomicAdd(&h1[key >> 20], 1u);
-        }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int b = 4 * (tid + j * NT);
-      if (in_smem && b < n_slice) *reinterpret_cast<float4*>(slice + b) = w[j];   // (4-aligned: the slice holds >= b + 4)
-    }
-  }
-  __syncthreads();
-  uint32_t B = 0u;
-  if (G >= k) {
-    find_bin<NT>(h1, kBins, (uint32_t)k, wt[0], s_res);
-    B = s_res[0];
-  }
-  for (int i = tid; i < kBins; i += NT) h1[i] = 0u;   // reused by radix level 2
-
-  // 2. This part's candidate groups: thread t of a round takes group ga + t
-  // and keeps its blocks whose key is in a bin >= B; a prefix scan over the
-  // CTA places them in ascending id order in the slot.
-  uint2* slot = p.split.slots + ((int64_t)r * C + part) * p.split.cap;
-  uint32_t n_out = 0u;
-  int wb = 1;
-  int nan_keys = 0;
-  for (int gs = ga; gs < gb; gs += NT) {
-    const int g = gs + tid;
-    const int64_t b0 = (int64_t)g * kGroup;
-    float x[kGroup];
-    uint32_t keep = 0u;   // bit e: block b0 + e is kept
-    if (g < gb && (r1[g] >> 20) >= B) {
-      if (in_smem) {
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e) x[e] = b0 + e < nb ? slice[b0 + e - sb0] : 0.f;
-      } else if (b0 + kGroup <= nb) {
-#pragma unroll
-        for (int q = 0; q < kGroup / 4; ++q) {
-          const float4 w = __ldg(reinterpret_cast<const float4*>(srow + b0) + q);
-          x[4 * q] = w.x;
-          x[4 * q + 1] = w.y;
-          x[4 * q + 2] = w.z;
-          x[4 * q + 3] = w.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kGroup; ++e) x[e] = b0 + e < nb ? __ldg(srow + b0 + e) : 0.f;
-      }
-#pragma unroll
-      for (int e = 0; e < kGroup; ++e) {
-        const uint32_t key = order_key(x[e]);
-        if (b0 + e < nb && (key >> 20) >= B) {
-          keep |= 1u << e;
-          nan_keys += key > 0xff800000u || key < 0x007fffffu;
-        }
-      }
-    }
-    uint32_t tot;
-    uint32_t at = n_out + block_scan<NT>((uint32_t)__popc(keep), wt[wb], &tot);
-    wb ^= 1;
-#pragma unroll
-    for (int e = 0; e < kGroup; ++e)
-      if (keep & (1u << e)) slot[at++] = make_uint2(order_key(x[e]), (uint32_t)(b0 + e));
-    n_out += tot;
-  }
-  if (nan_keys) atomicAdd(&g_nan_keys, nan_keys);
-  if (tid == 0) p.split.counts[(int64_t)r * C + part] = n_out;
-  // Publish the slot: the CTA barrier orders every thread's writes before
-  // thread 0's release; the ticket's acquire orders the last CTA's reads after
-  // every CTA's writes.
-  __syncthreads();
-  if (tid == 0) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(p.split.tickets + r) : "memory");
-    s_last = old == (uint32_t)(C - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-
-  // 3. The last CTA: the counts and each slot's first kSlotPeek entries in
-  // one round trip (warp w holds slots w, w + 32, ...), the offsets by a
-  // prefix scan, then the list in shared memory in ascending id order.
-  const uint32_t c_t = tid < C ? __ldcg(p.split.counts + (int64_t)r * C + tid) : 0u;
-  constexpr int kPeekPerLane = kSlotPeek / 32;
-  constexpr int kSlotsPerWarp = (kMaxSplit + kWarps - 1) / kWarps;
-  uint2 peek[kSlotsPerWarp][kPeekPerLane];
-#pragma unroll
-  for (int u = 0; u < kSlotsPerWarp; ++u) {
-    const int c = warp + u * kWarps;
-#pragma unroll
-    for (int j = 0; j < kPeekPerLane; ++j)
-      peek[u][j] = c < C && lane + 32 * j < p.split.cap
-                       ? __ldcg(p.split.slots + ((int64_t)r * C + c) * p.split.cap + lane + 32 * j)
-                       : make_uint2(0u, 0u);
-  }
-  uint32_t n_list;
-  const uint32_t off = block_scan<NT>(c_t, wt[wb], &n_list);
-  if (tid < C) {
-    s_off[tid] = off;
-    s_cnt[tid] = c_t;
-  }
-  if (tid == 0) p.split.tickets[r] = 0u;   // ready for the next call (stream order)
-  __syncthreads();
-  const int nw = (int)((nb + 31) / 32);
-  if (n_list <= (uint32_t)kListCap) {
-    const int n = (int)n_list;
-#pragma unroll
-    for (int u = 0; u < kSlotsPerWarp; ++u) {
-      const int c = warp + u * kWarps;
-      if (c >= C) break;
-      const uint32_t o = s_off[c], cn = s_cnt[c];
-#pragma unroll
-      for (int j = 0; j < kPeekPerLane; ++j) {
-        const uint32_t e = lane + 32 * j;
-        if (e < cn) {
-          r1[o + e] = peek[u][j].x;
-          r2[o + e] = peek[u][j].y;
-        }
-      }
-      const uint2* src = p.split.slots + ((int64_t)r * C + c) * p.split.cap;
-      for (uint32_t e = kSlotPeek + lane; e < cn; e += 32) {   // longer slots
-        const uint2 v = __ldcg(src + e);
-        r1[o + e] = v.x;
-        r2[o + e] = v.y;
-      }
-    }
-    __syncthreads();
-    const Threshold th = radix_threshold<NT>(
-        (uint32_t)k,
-        [&](auto f) {
-          for (int i = tid; i < n; i += NT) f(r1[i], (int32_t)r2[i]);
-        },
-        [&](auto f) {
-          const int n_pad = (n + 31) / 32 * 32;
-          for (int i = tid; i < n_pad; i += NT) f(i < n ? r1[i] : 0u, i < n ? (int32_t)r2[i] : 0, i < n);
-        },
-        sm, L, false, wt, s_res);
-    // 4. Kept entries in list order = ascending ids: position = kept entries
-    // before (above-K count + equal-to-K count capped at need, one scan of
-    // the packed pair).
-    const uint32_t need_eff = th.all_eq ? 0xffffffffu : th.need;
-    const int per = (n + NT - 1) / NT;
-    const int a0 = min(n, tid * per), a1 = min(n, a0 + per);
-    uint32_t gt = 0u, eq = 0u;
-    for (int i = a0; i < a1; ++i) {
-      const uint32_t m = r1[i] & th.mask;
-      gt += m > th.K;
-      eq += m == th.K;
-    }
-    uint32_t tot;
-    const uint32_t before = block_scan<NT>((gt << 16) | eq, wt[0], &tot);
-    uint32_t gtb = before >> 16, eqb = before & 0xffffu;
-    for (int i = a0; i < a1; ++i) {
-      const uint32_t m = r1[i] & th.mask;
-      if (m > th.K) {
-        const uint32_t pos = gtb + min(eqb, need_eff);
-        if (pos < (uint32_t)k) out[pos] = (int32_t)r2[i];
-        ++gtb;
-      } else if (m == th.K) {
-        if (eqb < need_eff && gtb + eqb < (uint32_t)k) out[gtb + eqb] = (int32_t)r2[i];
-        ++eqb;
-      }
-    }
-  } else {
-    // The whole row from global memory (the list would not fit): the bitmaps
-    // of radix_and_write start at zero.
-    for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;
-    __syncthreads();
-    const int nbi = (int)nb;
-    radix_and_write<NT>(
-        (uint32_t)k, nw,
-        [&](auto f) {
-          for (int b0 = tid; b0 < nbi; b0 += 8 * NT) {
-            uint32_t kk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int b = b0 + j * NT;
-              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (b0 + j * NT < nbi) f(kk[j], (int32_t)(b0 + j * NT));
-          }
-        },
-        [&](auto f) {
-          const int n_pad = (nbi + 31) / 32 * 32;
-          for (int b0 = tid; b0 < n_pad; b0 += 8 * NT) {
-            uint32_t kk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int b = b0 + j * NT;
-              kk[j] = b < nbi ? order_key(__ldg(srow + b)) : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) f(kk[j], (int32_t)(b0 + j * NT), b0 + j * NT < nbi);
-          }
-        },
-        sm, L, false, wt, s_res, out);
-  }
-  if (tid == 0) p.cnt[r] = k;
-}
-
 // ------------------------------------------------------------------ selection over key-axis chunks
 // One CTA per row merges the row's running top-k (keys and ids, ascending
 // ids) with the scores of one chunk of blocks [block_lo, block_lo + n_blocks):
@@ -961,13 +647,6 @@ cudaError_t launch_select(const SelectParams<NSEQ>& p, int n_rows, int64_t max_n
   // More rows than SMs: CTAs of 512 threads, two per SM where shared memory
   // allows it (more rows in flight); few rows: 1,024 threads, whose per-row
   // latency is lowest.
-  if (p.split.n_split > 0) {
-    if (p.split.n_split > kMaxSplit || !p.gmax) return cudaErrorInvalidValue;
-    cudaError_t e = allow_dynamic_smem((const void*)select_split_kernel<NSEQ>, smem);
-    if (e != cudaSuccess) return e;
-    return launch_kernel(select_split_kernel<NSEQ>, dim3((unsigned)p.split.n_split, (unsigned)n_rows), dim3(kThreads),
-                         smem, st, 0u, p, max_nb);
-  }
   const bool many = n_rows > device_sm_count() && 2 * (smem + 2048) <= 228 * 1024;
   auto* kernel = many ? select_kernel<NSEQ, 2, 512> : select_kernel<NSEQ, 1, 1024>;
   cudaError_t e = allow_dynamic_smem((const void*)kernel, smem);

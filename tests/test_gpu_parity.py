@@ -194,24 +194,23 @@ def group_maxima(scores_f32: np.ndarray, row_pos) -> np.ndarray:
     return out
 
 
-def _select_gpu(scores_f32: np.ndarray, row_pos, L, top_k=512, with_group_max=False, one_cta=False):
+def _select_gpu(scores_f32: np.ndarray, row_pos, L, top_k=512, with_group_max=False):
     M, ld = scores_f32.shape
     n_rows = len(row_pos)
     s = torch.from_numpy(np.ascontiguousarray(scores_f32)).to(dev())
     sel = torch.full((M, top_k), -7, dtype=torch.int32, device=dev())
     cnt = torch.full((M,), -7, dtype=torch.int32, device=dev())
     gm = torch.from_numpy(group_maxima(scores_f32, row_pos)).to(dev()) if with_group_max else None
-    qsa.select_topk([qsa.Seq(L, n_rows)], s, sel, cnt, top_k, group_max=gm, one_cta=one_cta)
+    qsa.select_topk([qsa.Seq(L, n_rows)], s, sel, cnt, top_k, group_max=gm)
     return to_np(sel), to_np(cnt)
 
 
 def _select_case(scores_f32, L, M, top_k=512):
     row_pos = [L - M + j for j in range(M)]
     rs, rc, _ = oracle.select(scores_f32.astype(np.float64), row_pos, top_k)
-    # One CTA per row without group maxima (the kernel derives them) and with
-    # them; with group maxima and a workspace, each row over several CTAs.
-    for with_gm, one_cta in ((False, True), (True, True), (True, False)):
-        sel, cnt = _select_gpu(scores_f32, row_pos, L, top_k, with_gm, one_cta)
+    # Without group maxima (the kernel derives them) and with them.
+    for with_gm in (False, True):
+        sel, cnt = _select_gpu(scores_f32, row_pos, L, top_k, with_gm)
         np.testing.assert_array_equal(cnt, rc)
         np.testing.assert_array_equal(sel, rs)
 
@@ -271,39 +270,13 @@ def test_select_ragged_sequences():
     rs, rc, _ = oracle.select(s.astype(np.float64), pos)
     np.testing.assert_array_equal(to_np(cnt), rc)
     np.testing.assert_array_equal(to_np(sel), rs)
-    # With group maxima: 28 rows, each split over several CTAs.
-    assert qsa.select_workspace_size(seqs) > 0
+    # With the group maxima score_blocks would write.
     gm = torch.from_numpy(group_maxima(s, pos)).to(dev())
     sel.fill_(-7)
     cnt.fill_(-7)
     qsa.select_topk(seqs, sd, sel, cnt, group_max=gm)
     np.testing.assert_array_equal(to_np(cnt), rc)
     np.testing.assert_array_equal(to_np(sel), rs)
-
-
-def test_select_split_workspace_reused_across_calls():
-    """The split selection's workspace (tickets, slots) carries nothing from
-    one call to the next: calls alternating between two score sets of
-    different shapes on one workspace each equal the oracle."""
-    rng = np.random.default_rng(11)
-    cases = []
-    for L, M in ((261_120, 4), (65_536, 1), (9001, 3)):
-        nb = L // 4
-        s = np.zeros((M, (nb + 3) // 4 * 4), dtype=np.float32)
-        s[:, :nb] = np.abs(rng.standard_normal((M, nb))).astype(np.float32) * 3
-        pos = [L - M + j for j in range(M)]
-        rs, rc, _ = oracle.select(s.astype(np.float64), pos)
-        cases.append((qsa.Seq(L, M), s, pos, rs, rc))
-    ws = torch.zeros(max(qsa.select_workspace_size([c[0]]) for c in cases), dtype=torch.uint8, device=dev())
-    for i in (0, 1, 2, 0, 2, 1, 1, 0):
-        sq, s, pos, rs, rc = cases[i]
-        sd = torch.from_numpy(s).to(dev())
-        gm = torch.from_numpy(group_maxima(s, pos)).to(dev())
-        sel = torch.full((sq.n_rows, 512), -7, dtype=torch.int32, device=dev())
-        cnt = torch.full((sq.n_rows,), -7, dtype=torch.int32, device=dev())
-        qsa.select_topk([sq], sd, sel, cnt, workspace=ws, group_max=gm)
-        np.testing.assert_array_equal(to_np(cnt), rc)
-        np.testing.assert_array_equal(to_np(sel), rs)
 
 
 # ------------------------------------------------------------------ appending tokens with in-place pooling
