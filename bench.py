@@ -574,6 +574,15 @@ def main():
             pass
         return None
 
+    # The scoring kernel this call runs (the library's choice by rows per
+    # sequence): the TMA ring up to 4 rows, direct loads for 5 to 8.
+    if M <= 4:
+        score_kernel = "score_tma_pool_kernel" if fused else "score_tma_kernel"
+    elif M <= FEW_ROWS:
+        score_kernel = "score_direct_kernel"
+    else:
+        score_kernel = "score_tc_kernel"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(layers)
@@ -581,7 +590,7 @@ def main():
     roofline = {"kernel": "pool_score_blocks (steps 1 + 2, one launch)" if fused else "score_blocks",
                 "bound": "hbm", "achieved": score_gbs, "peak": peak_gbs,
                 "unit": "GB/s", "frac": score_gbs / peak_gbs, "frac_of_8tbs": score_gbs / NOMINAL_HBM_GBS,
-                "traffic": traffic_of("score_direct_kernel"),
+                "traffic": traffic_of(score_kernel), "traffic_kernel": score_kernel,
                 "peak_source": f"{peak_src} (hbm_gbs, burst)", "us_per_launch": score_us,
                 "timing": "graph of 12 launches each followed by a one-element non-PDL kernel, minus a graph "
                           "of those kernels alone (no overlap with neighbours)",
@@ -656,7 +665,8 @@ def main():
 
 # Revision tags of the kernels as built now; DRAM counters in
 # profiles/kernel_traffic.json count only for the revision they were taken on.
-KERNEL_REVS = {"score_direct_kernel": "score_direct_v1",
+KERNEL_REVS = {"score_tma_kernel": "score_tma_ring8_v6", "score_tma_pool_kernel": "score_tma_pool_v3",
+               "score_direct_kernel": "score_direct_v1",
                "attn_tc_kernel": "attn_tc_ring3_v1", "score_tc_kernel": "score_tc_planes3_v1"}
 
 if __name__ == "__main__":

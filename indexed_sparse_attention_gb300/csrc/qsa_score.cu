@@ -138,15 +138,6 @@ constexpr int kScoreStages = 2;
 constexpr int kRowPitch = 144;   // floats per staged row: 576 bytes keep the float4 reads conflict-free
 constexpr int kStageFloats = kScoreTile * kRowPitch;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src), "r"(valid ? 16 : 0));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
 
 struct ScoreItem {
   int64_t b0;        // first block of the tile
@@ -599,13 +590,23 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
         for (int jj = 0; jj < NT; ++jj)
 #pragma unroll
           for (int e = 0; e < 4; ++e) ah[u][jj][e] = al[u][jj][e] = 0.f;
+      // The tile's fragments into registers first: the slot is released
+      // before the MMAs run, so its refill is requested one tile earlier.
+      float4 fa[8], fb[8];
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         // Rows g and g + 8 of the tile (same swizzle: g & 7), chunk 2t + (s & 1) of box s / 2.
         const unsigned char* box = tl + (s >> 1) * kBoxBytes;
         const int chunk = (2 * t + (s & 1)) ^ g;
-        const float4 ra = *reinterpret_cast<const float4*>(box + g * 128 + 16 * chunk);
-        const float4 rb = *reinterpret_cast<const float4*>(box + (g + 8) * 128 + 16 * chunk);
+        fa[s] = *reinterpret_cast<const float4*>(box + g * 128 + 16 * chunk);
+        fb[s] = *reinterpret_cast<const float4*>(box + (g + 8) * 128 + 16 * chunk);
+      }
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&empty_bar[q]);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const float4 ra = fa[s];
+        const float4 rb = fb[s];
         uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
         split_tf32(ra.x, h0, l0);  // row g,   k = t     (first channel of the chunk)
         split_tf32(rb.x, h1, l1);  // row g+8, k = t
@@ -633,10 +634,11 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[jj][e] = (ah[0][jj][e] + ah[1][jj][e]) + (al[0][jj][e] + al[1][jj][e]);
     }
-    // The tile is free once every lane has read it.
-    __syncwarp();
-    if (lane == 0) tc::bar_arrive(&empty_bar[q]);
-    if (!valid) continue;
+    if (!valid) {   // (a valid tile released its slot above)
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(&empty_bar[q]);
+      continue;
+    }
     // Epilogue as in score_mma_kernel: scores and the tile's group maximum.
 #pragma unroll
     for (int jj = 0; jj < NT; ++jj) {

@@ -726,6 +726,19 @@ def test_attention_other_budgets(top_k, M):
     assert_attn_close(out, lse, ref_out, ref_lse, True)
 
 
+# The split count the plan picks follows the number of rows (about two CTAs
+# per SM over the call): 64 splits for one row down to 2 for 100 rows.
+@pytest.mark.parametrize("M,D,out_dtype", [(1, 256, torch.float32), (16, 256, torch.float32),
+                                           (32, 128, torch.bfloat16), (100, 256, torch.float32),
+                                           (4, 128, torch.bfloat16)])
+def test_attention_auto_split_counts(M, D, out_dtype):
+    x = make_layer(L=9001, M=M, dtype=torch.bfloat16, seed=M + D, head_dim=D)
+    sel, cnt, _ = _oracle_selection(x)
+    out, lse = _attn_gpu(x, sel, cnt, out_dtype=out_dtype)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, x.row_pos, sel, cnt)
+    assert_attn_close(out, lse, ref_out, ref_lse, True)
+
+
 def test_attention_many_splits_reuse_workspace():
     # 40 splits per (row, KV group) merge through the workspace; a second call
     # on the same (now dirty) workspace gives the same result.
