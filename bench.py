@@ -477,9 +477,9 @@ def main():
     L = spec["L"]
     # Per step, every layer's inputs -- q, index queries and the new rows'
     # K, V and index keys (contiguous, as a model produces them) -- arrive in
-    # one pinned host buffer and cross in one copy; qsa_append_tokens writes
-    # the new rows into the caches and pools the blocks they complete; every
-    # layer's out and lse come back in one copy.
+    # one pinned host buffer and cross in one copy; qsa_append_score_blocks
+    # writes the new rows into the caches, pools the blocks they complete and
+    # scores; every layer's out and lse come back in one copy.
     def packed(tensors):
         offs, n = [], 0
         for t in tensors:
@@ -575,8 +575,8 @@ def main():
         return None
 
     # The scoring kernel this call runs (the library's choice by rows per
-    # sequence): the TMA ring up to 4 rows, direct loads for 5 to 8.
-    if M <= 4:
+    # sequence): the TMA ring for 2 to 4 rows, direct loads for 1 and 5 to 8.
+    if 2 <= M <= 4:
         score_kernel = "score_tma_pool_kernel" if fused else "score_tma_kernel"
     elif M <= FEW_ROWS:
         score_kernel = "score_direct_kernel"
@@ -648,9 +648,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "mode": "one CUDA graph per step: one pinned host->device copy of every layer's q, index "
-                        "queries and new K/V/index-key rows, per layer qsa_append_tokens (cache write + pooling) "
-                        "and the layer chain through LayerStep (the C ABI), one device->host copy of every "
-                        "layer's out and lse"},
+                        "queries and new K/V/index-key rows, per layer qsa_append_score_blocks (cache write, "
+                        "pooling and scoring, one launch on the few-row path), selection and attention through "
+                        "LayerStep (the C ABI), one device->host copy of every layer's out and lse"},
         "gpu_launches": launches,
         "us_per_launch_by_step": kernel_us,
         "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")},

@@ -268,6 +268,29 @@ qsa_status qsa_append_tokens(const qsa_seq* seq, const qsa_attn_config* cfg, con
                              void* stream);
 
 /*
+ * qsa_append_tokens, then qsa_pool_score_blocks's step 2 (every visible
+ * block of seq scored as qsa_score_blocks does), in one call for one
+ * sequence: the same caches, pooled keys, scores and group maxima as the
+ * two calls.  With bf16 index queries, at most 4 rows and K/V state that is
+ * not quantized (bf16 or f32), the scoring launch does the whole append
+ * itself -- the new tokens' K/V rows and index keys are copied by threads
+ * that issue no loads of pooled keys, and the blocks they complete are
+ * pooled from idx_new (new tokens) and idx_keys (earlier ones) before they
+ * are scored -- so the step keeps one launch; otherwise an append launch
+ * precedes the scoring.
+ *   seq, cfg, k_new, v_new, idx_new, idx_keys, idx_tok_stride, idx_dtype
+ *                  as qsa_append_tokens
+ *   q_idx ... workspace_bytes, stream   as qsa_score_blocks (one sequence)
+ * Errors: those of the two calls; nothing is launched when either's
+ * arguments fail their checks.
+ */
+qsa_status qsa_append_score_blocks(const qsa_seq* seq, const qsa_attn_config* cfg, const void* k_new,
+                                   const void* v_new, const void* idx_new, void* idx_keys, int64_t idx_tok_stride,
+                                   qsa_dtype idx_dtype, const void* q_idx, qsa_dtype q_idx_dtype, float* scores,
+                                   int64_t ld, float* group_max, int64_t group_ld, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/*
  * Step 2 -- block scoring (hipfire, section 02: four index-query heads score
  * every pooled block; section 03: a few-row variant for decode and verify
  * and a wide variant for prefill).

@@ -70,7 +70,8 @@ EXPORTS = ("qsa_status_string", "qsa_last_error", "qsa_version", "qsa_pool_index
            "qsa_lse_merge", "qsa_wait_timeouts", "qsa_score_select_blocked_workspace_size",
            "qsa_score_select_topk_blocked", "qsa_append_tokens", "qsa_arena_create", "qsa_arena_ensure",
            "qsa_arena_base", "qsa_arena_mapped", "qsa_arena_reserved", "qsa_arena_granularity", "qsa_arena_destroy",
-           "qsa_check_device_status", "qsa_selftest_wait_timeout", "qsa_pool_score_blocks")
+           "qsa_check_device_status", "qsa_selftest_wait_timeout", "qsa_pool_score_blocks",
+           "qsa_append_score_blocks")
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -109,6 +110,8 @@ def lib() -> ctypes.CDLL:
     L.qsa_sparse_attn_noalloc.argtypes = [seqp, i32, ctypes.POINTER(AttnConfig), vp, vp, vp, i32, vp, vp, vp]
     L.qsa_lse_merge.argtypes = [vp, vp, i32, i64, i32, vp, i32, vp, vp]
     L.qsa_append_tokens.argtypes = [seqp, ctypes.POINTER(AttnConfig), vp, vp, vp, vp, i64, i32, vp]
+    L.qsa_append_score_blocks.argtypes = [seqp, ctypes.POINTER(AttnConfig), vp, vp, vp, vp, i64, i32, vp, i32, vp, i64,
+                                          vp, i64, vp, sz, vp]
     u64 = ctypes.c_uint64
     L.qsa_arena_create.argtypes = [i32, u64, ctypes.POINTER(vp)]
     L.qsa_arena_ensure.argtypes = [vp, u64]
@@ -349,6 +352,31 @@ def append_tokens(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: t
         idxk.stride(0), _dtype_code(idxk), _stream(stream)))
 
 
+def append_score_blocks(seq: Seq, k_new: torch.Tensor, v_new: torch.Tensor, idx_new: torch.Tensor,
+                        q_idx: torch.Tensor, scores: torch.Tensor, stream=None, cfg=None,
+                        group_max: torch.Tensor | None = None, workspace: torch.Tensor | None = None, seq_array=None):
+    """append_tokens and the scoring of every visible block (score_blocks)
+    in one call for one sequence: one launch on the few-row path."""
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and idx_new.is_contiguous()):
+        raise ValueError("append_score_blocks: k_new, v_new and idx_new must be contiguous")
+    arr = seq_array if seq_array is not None else make_seq_array([seq])
+    if cfg is None:
+        kvd = _kv_dtype([seq])
+        kvd = _dtype_code(k_new) if kvd is None else kvd
+        cfg = AttnConfig(k_new.shape[0], k_new.shape[0], k_new.shape[2], BF16 if kvd in (FP8, Q8) else kvd, kvd, F32,
+                         0.0, 0)
+    if workspace is None:
+        need = score_workspace_size(None, q_idx, seq_array=arr)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=scores.device)
+    idxk = seq.idx_keys
+    _check("qsa_append_score_blocks", lib().qsa_append_score_blocks(
+        arr, ctypes.byref(cfg), k_new.data_ptr(), v_new.data_ptr(), idx_new.data_ptr(), idxk.data_ptr(),
+        idxk.stride(0), _dtype_code(idxk), q_idx.data_ptr(), _dtype_code(q_idx), scores.data_ptr(), scores.stride(0),
+        _ptr(group_max), 0 if group_max is None else group_max.stride(0), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _stream(stream)))
+
+
 class _DevicePtr:
     """A device byte range exposed through __cuda_array_interface__ (no ownership)."""
 
@@ -584,6 +612,17 @@ class LayerStep:
         for sq, (k_new, v_new, idx_new) in zip(self.seqs, new_tokens):
             append_tokens(sq, k_new, v_new, idx_new, stream, cfg=self.cfg)
 
+    def append_score(self, new_tokens, stream=None):
+        """append() then score() as one call (one launch on the few-row
+        path); one sequence."""
+        if len(self.seqs) != 1:
+            self.append(new_tokens, stream)
+            self.score(stream)
+            return
+        k_new, v_new, idx_new = new_tokens[0]
+        append_score_blocks(self.seqs[0], k_new, v_new, idx_new, self.q_idx, self.scores, stream, cfg=self.cfg,
+                            group_max=self.group_max, workspace=self.score_ws, seq_array=self.arr)
+
     def run(self, stream=None, new_tokens=None):
         """One layer step: pool (or append new_tokens and pool), score,
         select, attend (an NVTX range "qsa.layer_step" around the calls)."""
@@ -592,8 +631,7 @@ class LayerStep:
             if new_tokens is None:
                 self.pool_score(stream)
             else:
-                self.append(new_tokens, stream)
-                self.score(stream)
+                self.append_score(new_tokens, stream)
             self.select(stream)
             self.attend(stream)
         finally:

@@ -128,36 +128,11 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     quantize_row(p, i / 32, (int)(i % 32));
     return;
   }
-  if (i < p.kv_items) {
-    // (K or V, KV head, new token, 16-byte chunk of the row)
-    const int64_t per_row = p.row_chunks;
-    const int64_t row = i / per_row, c = i % per_row;
-    const int which = (int)(row / ((int64_t)p.n_kv_heads * p.n_new));   // 0: K, 1: V
-    const int64_t hr = row % ((int64_t)p.n_kv_heads * p.n_new);
-    const int h = (int)(hr / p.n_new);
-    const int64_t j = hr % p.n_new;
-    const int64_t t = first_new + j;
-    const char* src = static_cast<const char*>(which ? p.v_new : p.k_new) +
-                      ((int64_t)h * p.n_new + j) * p.row_bytes + c * 16;
-    for (int s = 0; s < p.n_segs; ++s) {
-      const AppendSeg& sg = p.seg[s];
-      if (t >= sg.first && t < sg.first + sg.n) {
-        char* dst = static_cast<char*>(which ? sg.v : sg.k) +
-                    ((int64_t)h * sg.head_stride + (t - sg.first) * sg.tok_stride) * p.kv_es + c * 16;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-        break;
-      }
-    }
+  if (i < p.kv_items + p.idx_items) {
+    append_copy(p, i);
     return;
   }
   const int64_t i2 = i - p.kv_items;
-  if (i2 < p.idx_items) {
-    const int64_t j = i2 / p.idx_chunks, c = i2 % p.idx_chunks;
-    const char* src = static_cast<const char*>(p.idx_new) + j * QSA_INDEX_DIM * p.idx_es + c * 16;
-    char* dst = static_cast<char*>(p.idx_keys) + (first_new + j) * p.idx_stride * p.idx_es + c * 16;
-    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-    return;
-  }
   const int64_t i3 = i2 - p.idx_items;
   if (i3 < p.pool_items) {
     const int64_t b = p.first_block + i3 / (QSA_INDEX_DIM / 4);

@@ -35,6 +35,11 @@ struct ScoreSeq {
   int64_t idx_stride;
   int32_t idx_dtype;
   int64_t pool_b0, pool_b1;
+  // With an append in the same launch: the index keys of tokens >= first_new
+  // are read from idx_new ([n_new, 128] of idx_dtype) -- the launch itself
+  // writes them into idx_keys, and no thread reads what another writes.
+  const void* idx_new;
+  int64_t first_new;
 };
 
 template <int NSEQ>
@@ -160,6 +165,50 @@ struct AppendParams {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t st);
 
+// Copy item i of an append with K/V state that is not quantized: items
+// [0, kv_items) are 16-byte pieces of the new tokens' K and V rows
+// (K or V, KV head, new token, piece), written into the segment that covers
+// the token; items [kv_items, kv_items + idx_items) are 16-byte pieces of
+// their index keys, written into the index-key cache.  Sets the piece's
+// source and destination (dst null: no segment covers the token, or no item).
+__device__ __forceinline__ void append_item(const AppendParams& p, int64_t i, const uint4*& src, uint4*& dst) {
+  const int64_t first_new = p.n_tokens - p.n_new;
+  dst = nullptr;
+  if (i < p.kv_items) {
+    const int64_t row = i / p.row_chunks, c = i % p.row_chunks;
+    const int which = (int)(row / ((int64_t)p.n_kv_heads * p.n_new));   // 0: K, 1: V
+    const int64_t hr = row % ((int64_t)p.n_kv_heads * p.n_new);
+    const int h = (int)(hr / p.n_new);
+    const int64_t j = hr % p.n_new;
+    const int64_t t = first_new + j;
+    src = reinterpret_cast<const uint4*>(static_cast<const char*>(which ? p.v_new : p.k_new) +
+                                         ((int64_t)h * p.n_new + j) * p.row_bytes + c * 16);
+    for (int s = 0; s < p.n_segs; ++s) {
+      const AppendSeg& sg = p.seg[s];
+      if (t >= sg.first && t < sg.first + sg.n) {
+        dst = reinterpret_cast<uint4*>(static_cast<char*>(which ? sg.v : sg.k) +
+                                       ((int64_t)h * sg.head_stride + (t - sg.first) * sg.tok_stride) * p.kv_es +
+                                       c * 16);
+        break;
+      }
+    }
+    return;
+  }
+  const int64_t i2 = i - p.kv_items;
+  if (i2 < p.idx_items) {
+    const int64_t j = i2 / p.idx_chunks, c = i2 % p.idx_chunks;
+    src = reinterpret_cast<const uint4*>(static_cast<const char*>(p.idx_new) + j * QSA_INDEX_DIM * p.idx_es + c * 16);
+    dst = reinterpret_cast<uint4*>(static_cast<char*>(p.idx_keys) + (first_new + j) * p.idx_stride * p.idx_es +
+                                   c * 16);
+  }
+}
+__device__ __forceinline__ void append_copy(const AppendParams& p, int64_t i) {
+  const uint4* src;
+  uint4* dst;
+  append_item(p, i, src, dst);
+  if (dst) *dst = *src;
+}
+
 // ---------------------------------------------------------------- demand-mapped arena (qsa_arena.cu)
 qsa_status arena_create(int32_t device, uint64_t reserve_bytes, qsa_arena** out, const char** why);
 qsa_status arena_ensure(qsa_arena* a, uint64_t bytes, const char** why);
@@ -173,9 +222,12 @@ uint64_t arena_granularity(const qsa_arena* a);
 cudaError_t launch_pool(const void* idx, qsa_dtype dt, int64_t tok_stride, int64_t first_block,
                         int64_t n_blocks, float* pooled, int64_t pstride, cudaStream_t st);
 
+// ap (optional): an append (K/V state not quantized, pool_items 0) done by
+// the scoring launch itself where the kernel takes it (the few-row kernels),
+// else by an append launch first.
 template <int NSEQ>
 cudaError_t launch_score(const ScoreParams<NSEQ>& p, qsa_dtype q_dtype, int max_rows_per_group,
-                         cudaStream_t st);
+                         cudaStream_t st, const AppendParams* ap = nullptr);
 
 // Wide scoring on the tensor cores (one sequence; see qsa_score_tc.cu).
 size_t score_tc_workspace_bytes(int64_t n_blocks);

@@ -391,17 +391,25 @@ constexpr size_t kTmaPoolSmem = kTmaSmem + (size_t)kTmaConsumers * kPoolScratch;
 
 __device__ int g_score_wait_timeouts;   // waits that gave up (never expected)
 
+// The index keys of token t (es bytes per element): from the appended
+// tokens' input when the launch also appends t, else from the cache.
+__device__ __forceinline__ const char* idx_row(const ScoreSeq& sq, int64_t t, int es) {
+  if (sq.idx_new && t >= sq.first_new)
+    return static_cast<const char*>(sq.idx_new) + (t - sq.first_new) * QSA_INDEX_DIM * es;
+  return static_cast<const char*>(sq.idx_keys) + t * sq.idx_stride * es;
+}
+
 // Lane l's channels 4l .. 4l + 3 of the four index keys of block b.
 __device__ __forceinline__ void load_index_keys(const ScoreSeq& sq, int64_t b, int lane, float4 (&k)[4]) {
   if (sq.idx_dtype == QSA_F32) {
-    const float* src = static_cast<const float*>(sq.idx_keys) + 4 * b * sq.idx_stride + 4 * lane;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) k[j] = *reinterpret_cast<const float4*>(src + j * sq.idx_stride);
+    for (int j = 0; j < 4; ++j)
+      k[j] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(idx_row(sq, 4 * b + j, 4)) + 4 * lane);
   } else {
-    const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(sq.idx_keys) + 4 * b * sq.idx_stride + 4 * lane;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint2 w = *reinterpret_cast<const uint2*>(src + j * sq.idx_stride);
+      const uint2 w =
+          *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(idx_row(sq, 4 * b + j, 2)) + 4 * lane);
       k[j] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
     }
   }
@@ -423,6 +431,7 @@ struct ScoreTmaParams {
   int64_t item_begin[NSEQ];    // first item of sequence i
   int64_t n_items;
   ScoreParams<NSEQ> p;
+  AppendParams ap;             // an append done by the launch (no items: none)
 };
 
 template <int NSEQ>
@@ -485,6 +494,14 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
     }
     if (!waited) grid_dependency_wait();
     grid_dependency_release();
+    // The append's copies, on the lanes that issue no tensor copies.
+    if (lane >= kTmaItems) {
+      constexpr int kCopyLanes = 32 - kTmaItems;
+      const int64_t n_copy = P.ap.kv_items + P.ap.idx_items;
+      for (int64_t i = (int64_t)blockIdx.x * kCopyLanes + (lane - kTmaItems); i < n_copy;
+           i += (int64_t)gridDim.x * kCopyLanes)
+        append_copy(P.ap, i);
+    }
     return;
   }
   grid_dependency_wait();
@@ -512,8 +529,7 @@ __global__ void __launch_bounds__(32 * (1 + kTmaConsumers), kTmaCtasPerSm)
       const int es = sq.idx_dtype == QSA_F32 ? 4 : 2;
       const int chunks = QSA_INDEX_DIM * es / 16;   // per key row
       for (int c = lane; c < 4 * chunks; c += 32) {
-        const char* src = static_cast<const char*>(sq.idx_keys) + ((4 * b + c / chunks) * sq.idx_stride) * es +
-                          (c % chunks) * 16;
+        const char* src = idx_row(sq, 4 * b + c / chunks, es) + (c % chunks) * 16;
         const uint32_t dst = (uint32_t)__cvta_generic_to_shared(keys_s + c * 16);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
       }
@@ -761,8 +777,7 @@ __device__ __forceinline__ void pool_prefetch(unsigned char* scratch, const Scor
   const int chunks = QSA_INDEX_DIM * es / 16;   // 16-byte chunks per token row
   for (int64_t b = lo; b < hi && b < lo + 2; ++b) {
     for (int c = lane; c < 4 * chunks; c += 32) {
-      const char* src = static_cast<const char*>(sq.idx_keys) + ((4 * b + c / chunks) * sq.idx_stride) * es +
-                        (c % chunks) * 16;
+      const char* src = idx_row(sq, 4 * b + c / chunks, es) + (c % chunks) * 16;
       const uint32_t dst = (uint32_t)__cvta_generic_to_shared(scratch + (b - lo) * kPoolSlotBytes + c * 16);
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
     }
@@ -831,9 +846,17 @@ __device__ __forceinline__ void mma_half(const HalfTile& h, const uint2* qs, int
     for (int e = 0; e < 4; ++e) s[mt][e] = (ah[mt][0][e] + ah[mt][1][e]) + (al[mt][0][e] + al[mt][1][e]);
 }
 
-template <int NMT, int NSEQ>
+// The append a direct-load launch also does (APPEND), else nothing.
+template <bool APPEND>
+struct DirAppend {
+  AppendParams ap;
+};
+template <>
+struct DirAppend<false> {};
+
+template <int NMT, int NSEQ, bool APPEND>
 __global__ void __launch_bounds__(32 * DirShape<NMT>::warps, DirShape<NMT>::ctas_per_sm)
-    score_direct_kernel(const __grid_constant__ ScoreParams<NSEQ> p) {
+    score_direct_kernel(const __grid_constant__ ScoreParams<NSEQ> p, const __grid_constant__ DirAppend<APPEND> da) {
   constexpr int kWarps = DirShape<NMT>::warps;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -861,6 +884,12 @@ __global__ void __launch_bounds__(32 * DirShape<NMT>::warps, DirShape<NMT>::ctas
   }
   if (!waited) grid_dependency_wait();
   grid_dependency_release();
+  // The append's copies, spread over the launch's threads.
+  if constexpr (APPEND) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < da.ap.kv_items + da.ap.idx_items;
+         i += (int64_t)gridDim.x * blockDim.x)
+      append_copy(da.ap, i);
+  }
   int q_si = -1;
   for (; u < p.n_work; u += W) {
     const int si = find_seq_by_work(p, u);
@@ -1068,12 +1097,14 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // cudaErrorNotSupported: the TMA path does not apply (no encoder, a tensor
 // map the driver refuses); the caller then launches the cp.async kernel.
 template <int NSEQ>
-cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group, int sms, cudaStream_t st) {
+cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group, int sms, cudaStream_t st,
+                             const AppendParams* ap) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   ScoreTmaParams<NSEQ> P;
   memset(&P, 0, sizeof(P));
   P.p = p;
+  if (ap) P.ap = *ap;
   int64_t n_items = 0;
   for (int i = 0; i < p.n_seqs; ++i) {
     const ScoreSeq& q = p.seq[i];
@@ -1113,15 +1144,33 @@ cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group,
   return launch_kernel(score_tma_kernel<2, NSEQ, false>, dim3(grid), block, smem, st, 0u, P);
 }
 
+template <int NMT, int NSEQ>
+cudaError_t launch_direct(const ScoreParams<NSEQ>& p, const AppendParams* ap, unsigned grid, cudaStream_t st) {
+  constexpr size_t smem = DirShape<NMT>::smem;
+  const dim3 block(32 * DirShape<NMT>::warps);
+  if (ap) {
+    cudaError_t e = allow_dynamic_smem((const void*)score_direct_kernel<NMT, NSEQ, true>, smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(score_direct_kernel<NMT, NSEQ, true>, dim3(grid), block, smem, st, 0u, p, DirAppend<true>{*ap});
+  }
+  cudaError_t e = allow_dynamic_smem((const void*)score_direct_kernel<NMT, NSEQ, false>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(score_direct_kernel<NMT, NSEQ, false>, dim3(grid), block, smem, st, 0u, p, DirAppend<false>{});
+}
+
 }  // namespace
 
 template <int NSEQ>
-cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st) {
-  if (p_in.n_work == 0) return cudaSuccess;
+cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int max_rows_per_group, cudaStream_t st,
+                         const AppendParams* ap) {
+  if (p_in.n_work == 0) return ap ? launch_append(*ap, st) : cudaSuccess;
   const int sms = device_sm_count();
-  // Up to 4 rows: the TMA ring (score_tma_kernel); 5 to 8 rows: direct loads.
-  if (q_dtype == QSA_BF16 && max_rows_per_group <= 4) {
-    cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st);
+  // 2 to 4 rows: the TMA ring (score_tma_kernel); 1 row and 5 to 8 rows:
+  // direct loads.  (One row, measured at 65,536 tokens: the decode layer
+  // chain takes 18.4 us with the direct kernel against 19.0 with the ring,
+  // though the launch alone takes 3.6 against 3.3 us.)
+  if (q_dtype == QSA_BF16 && max_rows_per_group >= 2 && max_rows_per_group <= 4) {
+    cudaError_t e = launch_score_tma(p_in, max_rows_per_group, sms, st, ap);
     if (e != cudaErrorNotSupported) return e;
   }
   if (q_dtype == QSA_BF16 && max_rows_per_group <= kRowGroup) {
@@ -1134,18 +1183,17 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int m
         const int64_t ctas = (int64_t)sms * per_sm;
         return (unsigned)(need < ctas ? need : ctas);
       };
-      cudaError_t e = allow_dynamic_smem((const void*)(max_rows_per_group <= 4 ? score_direct_kernel<1, NSEQ>
-                                                                                 : score_direct_kernel<2, NSEQ>),
-                                         max_rows_per_group <= 4 ? DirShape<1>::smem : DirShape<2>::smem);
-      if (e != cudaSuccess) return e;
-      if (max_rows_per_group <= 4)   // (the TMA ring declined the call)
-        return launch_kernel(score_direct_kernel<1, NSEQ>, dim3(grid_of(DirShape<1>::warps, DirShape<1>::ctas_per_sm)),
-                             dim3(32 * DirShape<1>::warps), DirShape<1>::smem, st, 0u, p_in);
-      return launch_kernel(score_direct_kernel<2, NSEQ>, dim3(grid_of(DirShape<2>::warps, DirShape<2>::ctas_per_sm)),
-                           dim3(32 * DirShape<2>::warps), DirShape<2>::smem, st, 0u, p_in);
+      if (max_rows_per_group <= 4)   // one row, or the TMA ring declined the call
+        return launch_direct<1, NSEQ>(p_in, ap, grid_of(DirShape<1>::warps, DirShape<1>::ctas_per_sm), st);
+      return launch_direct<2, NSEQ>(p_in, ap, grid_of(DirShape<2>::warps, DirShape<2>::ctas_per_sm), st);
     }
   }
-  // The other kernels do not pool: the pooling launches first.
+  // The other kernels neither append nor pool: those launches come first
+  // (the pooling then reads the appended keys from the cache).
+  if (ap) {
+    cudaError_t e = launch_append(*ap, st);
+    if (e != cudaSuccess) return e;
+  }
   ScoreParams<NSEQ> p = p_in;
   for (int i = 0; i < p.n_seqs; ++i) {
     ScoreSeq& sq = p.seq[i];
@@ -1174,8 +1222,9 @@ cudaError_t launch_score(const ScoreParams<NSEQ>& p_in, qsa_dtype q_dtype, int m
   return launch_kernel(score_mma_kernel<4, NSEQ, Ws>, dim3(grid), block, smem, st, 0u, p);
 }
 
-template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t);
-template cudaError_t launch_score<kLaunchSeqs>(const ScoreParams<kLaunchSeqs>&, qsa_dtype, int, cudaStream_t);
+template cudaError_t launch_score<1>(const ScoreParams<1>&, qsa_dtype, int, cudaStream_t, const AppendParams*);
+template cudaError_t launch_score<kLaunchSeqs>(const ScoreParams<kLaunchSeqs>&, qsa_dtype, int, cudaStream_t,
+                                               const AppendParams*);
 
 int score_wait_timeouts() {
   int v = 0;

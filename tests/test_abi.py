@@ -199,6 +199,23 @@ def test_append_validation(L):
     assert ok(_seq(n_tokens=4099, n_rows=5000)) == 1                    # more new tokens than the cache
 
 
+def test_append_score_validation(L):
+    # The append's checks and the scoring's both run before anything is launched.
+    c = qsa.AttnConfig(2, 2, 256, qsa.BF16, qsa.BF16, qsa.F32, 0.0, 0)
+    seq = _seq(n_tokens=4099, n_rows=4)
+
+    def call(s=seq, idx=FAKE, q=FAKE, scores=FAKE, ld=1028):
+        return L.qsa_append_score_blocks(s, ctypes.byref(c), FAKE, FAKE, FAKE, idx, 128, qsa.BF16, q, qsa.BF16,
+                                         scores, ld, None, 0, None, 0, None)
+    assert call(idx=None) == 1                                              # append: null index keys
+    assert call(_seq(n_tokens=4099, n_rows=4, segs=[(0, 4097)])) == 1        # append: token in no segment
+    assert "no KV segment" in L.qsa_last_error().decode()
+    assert call(q=None) == 1                                                # scoring: null index queries
+    assert call(scores=FAKE_MIS) == 3                                       # scoring: misaligned scores
+    assert call(ld=100) == 1                                                # scoring: ld below the blocks
+    assert "qsa_append_score_blocks" in L.qsa_last_error().decode()
+
+
 def test_blocked_score_select_validation(L):
     seq = _seq(n_tokens=40_000, n_rows=600)
     need = L.qsa_score_select_blocked_workspace_size(seq, 1, 512, 1024)

@@ -109,6 +109,7 @@ def test_scores_zero_query_and_nonnegative():
     ([9003], [7], torch.float32, torch.bfloat16),
     ([9001], [3], torch.float32, torch.bfloat16), ([9001], [4], torch.bfloat16, torch.float32),
     ([4099], [600], torch.bfloat16, torch.bfloat16), ([4097], [1], torch.bfloat16, torch.bfloat16),
+    ([9002], [1], torch.float32, torch.bfloat16), ([9002], [2], torch.bfloat16, torch.bfloat16),
     ([4099, 700, 30_000, 9, 2052, 65_540], [4, 1, 2, 3, 1, 4], torch.bfloat16, torch.bfloat16)])
 def test_pool_score_equals_pool_then_score(Ls, Ms, idx_dtype, q_dtype):
     _pool_score_vs_separate(Ls, Ms, idx_dtype, q_dtype)
@@ -313,6 +314,67 @@ def test_append_writes_caches_and_pools(L, n, kv_dtype, idx_dtype, n_segs):
     # index keys, and the same numbers as the pooling kernel.
     assert_pooled_close(to_np(pooled), idx_full.float(), range(b0, L // 4))
     assert torch.equal(pooled[:L // 4], ref[:L // 4])
+
+
+# The append and the scoring in one call (qsa_append_score_blocks): one
+# launch on the few-row path (bf16 index queries, <= 4 rows, K/V state not
+# quantized), else an append launch then the scoring.  The caches, pooled
+# keys, scores and group maxima equal those of the two separate calls, and
+# the pooled keys and scores match the oracle.
+@pytest.mark.parametrize("L,n,kv_dtype,idx_dtype,n_segs,q_dtype", [
+    (65_536, 1, torch.bfloat16, torch.bfloat16, 1, torch.bfloat16),
+    (261_120, 4, torch.bfloat16, torch.bfloat16, 1, torch.bfloat16),
+    (9001, 8, torch.bfloat16, torch.float32, 3, torch.bfloat16),
+    (9002, 2, torch.float32, torch.bfloat16, 2, torch.bfloat16),
+    (4099, 3, torch.bfloat16, torch.bfloat16, 1, torch.float32),
+    (2148, 20, torch.bfloat16, torch.bfloat16, 1, torch.bfloat16),
+    (9003, 1, torch.bfloat16, torch.float32, 2, torch.bfloat16),
+    (5, 3, torch.bfloat16, torch.bfloat16, 1, torch.bfloat16),
+    (5, 5, torch.bfloat16, torch.bfloat16, 1, torch.bfloat16)])
+def test_append_score_equals_append_then_score(L, n, kv_dtype, idx_dtype, n_segs, q_dtype):
+    x = make_layer(L=L, M=n, dtype=torch.float32, seed=L + 3 * n, device=dev())
+    k_full, v_full, idx_full = x.k.to(kv_dtype), x.v.to(kv_dtype), x.idxk.to(idx_dtype)
+    q_idx = x.q_idx.to(q_dtype)
+    ld = (L // 4 + 3) // 4 * 4
+    runs = []
+    for fused in (True, False):
+        k_c, v_c = torch.full_like(k_full, float("nan")), torch.full_like(v_full, float("nan"))
+        idx_c = torch.full_like(idx_full, float("nan"))
+        k_c[:, :L - n], v_c[:, :L - n], idx_c[:L - n] = k_full[:, :L - n], v_full[:, :L - n], idx_full[:L - n]
+        pooled = pooled_buffer(L, dev())
+        b0 = (L - n) // 4
+        if b0:
+            qsa.pool_index_keys(idx_c, pooled, 0, b0)
+        cuts = [0] + sorted({max(1, L - n + (n * j) // n_segs) for j in range(1, n_segs)} - {0, L}) + [L]
+        segs = [qsa.Segment(k_c[:, a:b], v_c[:, a:b], a) for a, b in zip(cuts[:-1], cuts[1:])]
+        seq = qsa.Seq(L, n, pooled, segs, idx_keys=idx_c)
+        scores = torch.full((n, ld), float("nan"), device=dev())
+        gmax = torch.full((n, (qsa.n_groups(L) + 3) // 4 * 4), float("nan"), device=dev())
+        new = (k_full[:, L - n:].contiguous(), v_full[:, L - n:].contiguous(), idx_full[L - n:].contiguous())
+        if fused:
+            qsa.append_score_blocks(seq, *new, q_idx, scores, group_max=gmax)
+        else:
+            qsa.append_tokens(seq, *new)
+            qsa.score_blocks([seq], q_idx, scores, group_max=gmax)
+        torch.cuda.synchronize()
+        runs.append((k_c, v_c, idx_c, pooled, scores, gmax, seq))
+    (ka, va, ia, pa, sa, ga, seq), (kb, vb, ib, pb, sb, gb, _) = runs
+    assert torch.equal(ka, k_full) and torch.equal(va, v_full) and torch.equal(ia, idx_full)
+    nb = L // 4
+    assert torch.equal(pa[:nb], pb[:nb])
+    pos = seq.row_pos
+    for r, p_ in enumerate(pos):
+        vis = (p_ + 1) // 4
+        assert torch.equal(sa[r, :vis], sb[r, :vis])
+        ng = (vis + 15) // 16
+        assert torch.equal(ga[r, :ng], gb[r, :ng])
+    # Against the oracle: the blocks the call pooled, and the scores of the
+    # stored pooled keys.
+    if nb:
+        assert_pooled_close(to_np(pa), idx_full.float(), range((L - n) // 4, nb))
+        pooled_ref = to_np(pa)[:nb].astype(np.float64)
+        s_ref = oracle.score(q_idx.float().cpu(), pooled_ref, pos)
+        assert_scores_close(to_np(sa)[:, :s_ref.shape[1]], s_ref, score_bound(q_idx.float(), pooled_ref, pos), pos)
 
 
 def test_layer_step_with_append_equals_prewritten_caches():
