@@ -41,7 +41,7 @@ constexpr int kBins = 4096;                        // radix levels 1 and 2: 12 k
 constexpr int kBins3 = 256;                        // radix level 3: the last 8 key bits
 constexpr int kGroupCap = 1024;                    // candidate groups read back (16,384 blocks)
 constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
-constexpr int kLoadBatch = 16;                                  // group maxima a thread loads per pass
+constexpr int kLoadBatch = 4;                                  // group maxima a thread loads per pass
 constexpr int kChunkBatch = 4;                                  // float4 chunks a thread loads per pass
 
 
