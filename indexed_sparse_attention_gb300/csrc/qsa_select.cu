@@ -416,16 +416,10 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
     for (int j = 0; j < kChunkBatch; ++j) {
       const int ch = c0 + tid + j * NT;
       v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ch < n_ch) {
-        const int64_t b0 = (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3);
-        if (b0 + 4 <= nb) {
-          v[j] = __ldg(reinterpret_cast<const float4*>(srow + b0));
-        } else {
-          v[j].x = b0 < nb ? __ldg(srow + b0) : 0.f;
-          v[j].y = b0 + 1 < nb ? __ldg(srow + b0 + 1) : 0.f;
-          v[j].z = b0 + 2 < nb ? __ldg(srow + b0 + 2) : 0.f;
-        }
-      }
+      // A chunk that starts below nb ends within the row stride (both
+      // multiples of 4); its blocks >= nb are dropped below.
+      const int64_t b0 = ch < n_ch ? (int64_t)cg[ch >> 2] * kGroup + 4 * (ch & 3) : nb;
+      if (b0 < nb) v[j] = __ldg(reinterpret_cast<const float4*>(srow + b0));
     }
 #pragma unroll
     for (int j = 0; j < kChunkBatch; ++j) {
