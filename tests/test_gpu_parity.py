@@ -377,6 +377,40 @@ def test_append_score_equals_append_then_score(L, n, kv_dtype, idx_dtype, n_segs
         assert_scores_close(to_np(sa)[:, :s_ref.shape[1]], s_ref, score_bound(q_idx.float(), pooled_ref, pos), pos)
 
 
+@pytest.mark.parametrize("M", [4, 1])
+def test_layer_step_with_append_replays_in_a_graph(M):
+    # The step with new tokens (append, pooling and scoring in one launch)
+    # captured in a CUDA graph and replayed gives what the eager step gives,
+    # caches included.
+    L = 9001
+    x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=43 + M, device=dev())
+    new = [(x.k[:, L - M:].contiguous(), x.v[:, L - M:].contiguous(), x.idxk[L - M:].contiguous())]
+    runs = []
+    for graphed in (False, True):
+        k_c, v_c, idx_c = x.k.clone(), x.v.clone(), x.idxk.clone()
+        k_c[:, L - M:] = 0
+        v_c[:, L - M:] = 0
+        idx_c[L - M:] = 0
+        pooled = pooled_buffer(L, dev())
+        qsa.pool_index_keys(idx_c, pooled, 0, (L - M) // 4)
+        step = qsa.LayerStep([qsa.Seq(L, M, pooled, [qsa.Segment(k_c, v_c, 0)], idx_keys=idx_c)], x.q_idx, x.q)
+        if graphed:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                step.run(new_tokens=new)
+            g.replay()
+        else:
+            step.run(new_tokens=new)
+        torch.cuda.synchronize()
+        runs.append((step.out.clone(), step.lse.clone(), k_c, v_c, idx_c, pooled))
+    (oa, la, ka, va, ia, pa), (ob, lb, kb, vb, ib, pb) = runs
+    assert torch.equal(oa, ob) and torch.equal(la, lb)
+    assert torch.equal(ka, x.k) and torch.equal(kb, x.k) and torch.equal(vb, x.v) and torch.equal(ib, x.idxk)
+    assert torch.equal(pa[:L // 4], pb[:L // 4])
+
+
 def test_layer_step_with_append_equals_prewritten_caches():
     L, M = 9001, 4
     x = make_layer(L=L, M=M, dtype=torch.bfloat16, seed=41, device=dev())
