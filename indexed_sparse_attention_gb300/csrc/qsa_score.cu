@@ -357,14 +357,17 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
 
 // ------------------------------------------------------------------ scoring, tensor pipe, TMA-fed
 // The few-row path (<= 4 rows per sequence, bf16 queries): persistent CTAs,
-// each owning a contiguous range of items; an item is 2 tiles (32 blocks) of
+// each owning a contiguous range of items; an item is 4 tiles (64 blocks) of
 // one sequence.  Warp 0 is the producer: lane L < kTmaItems loads the items
-// of ring slot L, each with four 2-D tensor copies of 32 blocks x 32 channels
-// (4 KB, 128-byte swizzle) completing on the slot's barrier, so a CTA keeps
-// kTmaItems x 16 KB of pooled keys in flight and refills each slot as soon
+// of ring slot L, each with four 2-D tensor copies of 64 blocks x 32 channels
+// (8 KB, 128-byte swizzle) completing on the slot's barrier, so a CTA keeps
+// kTmaItems x 32 KB of pooled keys in flight and refills each slot as soon
 // as it is consumed (the tensor-copy engine spends a fixed time per copy and
-// per barrier transaction, so copies are issued from several lanes, and a
-// steady ring keeps HBM busier than requesting a CTA's whole range at once).
+// per barrier transaction, so copies are issued from several lanes and are
+// as large as the ring allows: 8 KB boxes in 4 slots took the 261,120-token
+// verify's launch from 9.8 to 9.2 us against 4 KB boxes in 8 slots, with the
+// same 128 KB in flight; a steady ring keeps HBM busier than requesting a
+// CTA's whole range at once, and 192 KB rings were slower).
 // kTmaConsumers consumer warps run the tf32 MMAs of the kernel above, one
 // tile at a time: tile j of the item in slot q belongs to consumer
 // (kItemTiles q + j) % kTmaConsumers, so each consumer waits on a slot's
@@ -375,14 +378,14 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
 // -- so the 8 lanes of one shared-memory phase (rows g, g ^ 1, t = 0..3)
 // cover all 8 chunks of a bank row.  The queries take the same channel
 // mapping.
-constexpr int kItemTiles = 2;
-constexpr int kItemBlocks = kItemTiles * kScoreTile;          // 32
-constexpr int kTmaItems = 8;                                  // ring slots: 128 KB in flight
+constexpr int kItemTiles = 4;
+constexpr int kItemBlocks = kItemTiles * kScoreTile;          // 64
+constexpr int kTmaItems = 4;                                  // ring slots: 128 KB in flight
 constexpr int kTmaConsumers = 8;
 constexpr int kTmaCtasPerSm = 1;
 constexpr int kBoxRows = kItemBlocks;
-constexpr int kBoxBytes = kBoxRows * 128;                     // 32 rows x 32 fp32 = 4 KB
-constexpr int kItemBytes = 4 * kBoxBytes;                     // 16 KB
+constexpr int kBoxBytes = kBoxRows * 128;                     // 64 rows x 32 fp32 = 8 KB
+constexpr int kItemBytes = 4 * kBoxBytes;                     // 32 KB
 static_assert((kTmaItems * kItemTiles) % kTmaConsumers == 0, "tile slots split evenly over consumers");
 static_assert(kTmaItems <= 32, "one producer lane per ring slot");
 constexpr int kPoolScratch = 4 * QSA_INDEX_DIM * 4;               // one block's four f32 index keys
