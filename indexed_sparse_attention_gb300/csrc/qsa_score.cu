@@ -7,7 +7,8 @@
 // block is read once per row-group of <= 8 query rows.  For bf16 index
 // queries the dot products run on the tensor pipe with fp32 accumulation,
 // and the fp32 pooled key is split so that no product loses precision:
-//  - rows groups of <= 4 rows (decode, verify): tf32 MMAs (m16n8k8) on two
+//  - decode and verify (<= 8 rows on the TMA-ring and direct-load kernels,
+//    <= 4 rows on the warp-level kernel): tf32 MMAs (m16n8k8) on two
 //    planes, hi = the key rounded to tf32 and lo = key - hi (exact; the MMA
 //    keeps at least its top 11 bits, so hi + lo is the key to within one
 //    fp32 ulp); 3 integer/fp32 ops per key element;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
 }
 
 // ------------------------------------------------------------------ scoring, tensor pipe, TMA-fed
-// The few-row path (<= 4 rows per sequence, bf16 queries): persistent CTAs,
+// The few-row path (2 to 4 rows per sequence, bf16 queries): persistent CTAs,
 // each owning a contiguous range of items; an item is 4 tiles (64 blocks) of
 // one sequence.  Warp 0 is the producer: lane L < kTmaItems loads the items
 // of ring slot L, each with four 2-D tensor copies of 64 blocks x 32 channels
@@ -367,7 +368,10 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
 // as large as the ring allows: 8 KB boxes in 4 slots took the 261,120-token
 // verify's launch from 9.8 to 9.2 us against 4 KB boxes in 8 slots, with the
 // same 128 KB in flight; a steady ring keeps HBM busier than requesting a
-// CTA's whole range at once, and 192 KB rings were slower).
+// CTA's whole range at once, and 192 KB rings were slower).  Two CTAs share
+// an SM, each with two slots and four consumers: the same 128 KB in flight
+// per SM, but two producers and half as many consumers per barrier, which
+// took the same launch from 9.2 to 8.6 us.
 // kTmaConsumers consumer warps run the tf32 MMAs of the kernel above, one
 // tile at a time: tile j of the item in slot q belongs to consumer
 // (kItemTiles q + j) % kTmaConsumers, so each consumer waits on a slot's
@@ -380,9 +384,9 @@ __global__ void __launch_bounds__(WARPS * 32, 1) score_mma_kernel(const ScorePar
 // mapping.
 constexpr int kItemTiles = 4;
 constexpr int kItemBlocks = kItemTiles * kScoreTile;          // 64
-constexpr int kTmaItems = 4;                                  // ring slots: 128 KB in flight
-constexpr int kTmaConsumers = 8;
-constexpr int kTmaCtasPerSm = 1;
+constexpr int kTmaItems = 2;                                  // ring slots: 64 KB in flight per CTA
+constexpr int kTmaConsumers = 4;
+constexpr int kTmaCtasPerSm = 2;
 constexpr int kBoxRows = kItemBlocks;
 constexpr int kBoxBytes = kBoxRows * 128;                     // 64 rows x 32 fp32 = 8 KB
 constexpr int kItemBytes = 4 * kBoxBytes;                     // 32 KB
