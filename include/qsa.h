@@ -36,7 +36,12 @@
  *  - Rows: a call covers the query rows of n_seqs sequences, concatenated in
  *    sequence order (row index r = rows of earlier sequences + j).  Row j of
  *    a sequence with n_tokens = L and n_rows = M sits at absolute position
- *    p = L - M + j and sees tokens 0..p (causal).
+ *    p = L - M + j and sees tokens 0..p (causal).  Nothing past L is read,
+ *    so the cache may hold more tokens than L: a run of consecutive rows
+ *    anywhere in a cache is one descriptor with L = its last position + 1,
+ *    and rows at scattered positions (or one sequence's rows split over
+ *    several calls) are several descriptors over the same pooled keys and
+ *    K/V segments.
  *  - Blocks: block b holds tokens 4b..4b+3.  A row at p sees
  *    nb(p) = floor((p+1)/4) complete blocks and a tail of (p+1) mod 4 tokens
  *    4*nb(p)..p.
@@ -306,12 +311,12 @@ qsa_status qsa_append_score_blocks(const qsa_seq* seq, const qsa_attn_config* cf
  *   group_max      device [rows, group_ld] f32, group_ld >= max_r ceil(nb(p_r) / 16)
  *                  and a multiple of 4; may be NULL (not written)
  *   workspace      device scratch of >= qsa_score_workspace_size bytes, or NULL
- *                  (then sequences of more than 4 rows use a slower
+ *                  (then sequences of more than 8 rows use a slower
  *                  warp-level tensor-pipe kernel); its contents need no
  *                  initialisation; calls sharing it must not run concurrently
  * Arithmetic: fp32 accumulation of products that lose nothing of the fp32
  * pooled key beyond one fp32 ulp (bf16 index queries on the tensor pipe:
- * for <= 4 rows per sequence the key is split into two tf32 parts; for more
+ * for <= 8 rows per sequence the key is split into two tf32 parts; for more
  * rows into three bf16 parts that sum to it exactly; fp32 index queries on
  * the CUDA cores).
  */

@@ -194,7 +194,10 @@ class Segment:
 @dataclasses.dataclass
 class Seq:
     """One sequence of a call.  Its n_rows query rows are its last tokens:
-    row j sits at absolute position n_tokens - n_rows + j."""
+    row j sits at absolute position n_tokens - n_rows + j.  Nothing past
+    n_tokens is read, so rows elsewhere in a longer cache take n_tokens =
+    their last position + 1, and scattered rows take one Seq per run of
+    consecutive positions over the same tensors."""
     n_tokens: int
     n_rows: int
     pooled: torch.Tensor | None = None       # [>= n_tokens // 4, >= 128] f32

@@ -1071,6 +1071,33 @@ def test_layer_step_ragged_batch_small():
         row += x.M
 
 
+def test_layer_step_rows_at_any_position():
+    # A row at position p sees tokens 0..p only, so a descriptor whose
+    # n_tokens is its last row's position + 1 places a run of consecutive
+    # rows anywhere in a longer cache (the last run below ends two tokens
+    # before the cache's end), and rows at scattered positions are several
+    # descriptors over one cache: the same pooled keys and K/V segments.
+    L = 9001
+    runs = [(1203, 1), (5000, 2), (7003, 1), (8997, 2)]   # (first position, rows)
+    row_pos = [p + j for p, n in runs for j in range(n)]
+    x = make_layer(L=L, M=len(row_pos), dtype=torch.bfloat16, seed=41, head_dim=256)
+    k, v, idxk = x.k.to(dev()), x.v.to(dev()), x.idxk.to(dev())
+    pooled = pooled_buffer(L, dev())
+    pool_all(idxk, pooled, L)
+    segs = [qsa.Segment(k, v, 0)]
+    seqs = [qsa.Seq(p + n, n, pooled, segs, idx_keys=idxk) for p, n in runs]
+    step = qsa.LayerStep(seqs, x.q_idx.to(dev()), x.q.to(dev()))
+    step.run()
+    torch.cuda.synchronize()
+    ref = oracle.layer_step(x.q_idx, x.idxk, x.q, x.k, x.v, row_pos)
+    sel, cnt = to_np(step.sel), to_np(step.cnt)
+    assert_selection_close(sel, cnt, ref["sel"], ref["cnt"], ref["tau"], ref["scores"], row_pos)
+    ref_out, ref_lse = oracle.attn(x.q, x.k, x.v, row_pos, sel, cnt)
+    assert_attn_close(to_np(step.out), to_np(step.lse), ref_out, ref_lse, True)
+    # The pooled keys the step rewrote (each run's completed block) are the oracle's.
+    assert_pooled_close(to_np(pooled), x.idxk, [(p + n) // 4 - 1 for p, n in runs])
+
+
 # ------------------------------------------------------------------ device-side checks
 def test_device_status_clean_after_normal_work():
     qsa.check_device_status()   # clears what earlier tests left
