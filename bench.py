@@ -665,7 +665,7 @@ def main():
 
 # Revision tags of the kernels as built now; DRAM counters in
 # profiles/kernel_traffic.json count only for the revision they were taken on.
-KERNEL_REVS = {"score_tma_kernel": "score_tma_2cta_v1", "score_tma_pool_kernel": "score_tma_pool_2cta_v1",
+KERNEL_REVS = {"score_tma_kernel": "score_tma_2cta_bal_v1", "score_tma_pool_kernel": "score_tma_pool_2cta_bal_v1",
                "score_direct_kernel": "score_direct_v1",
                "attn_tc_kernel": "attn_tc_ring3_v1", "score_tc_kernel": "score_tc_planes3_v1"}
 
