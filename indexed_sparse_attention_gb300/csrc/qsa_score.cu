@@ -1141,11 +1141,11 @@ cudaError_t launch_score_tma(const ScoreParams<NSEQ>& p, int max_rows_per_group,
   P.n_items = n_items;
   if (n_items == 0) return cudaSuccess;
   // As many items per CTA as the resident CTAs need, and then as few CTAs
-  // as carry that many: every CTA streams the same number of items, and the
-  // SMs left with one CTA have room for the next launch's CTAs to become
-  // resident while this one runs.  (1,020 items of the 261,120-token verify:
-  // 255 CTAs of 4 items rather than 304 of 3 or 4 -- the layer step 28.5
-  // against 29.0 us, though the scoring launch alone takes 8.7 against 8.6.)
+  // as carry that many, so every CTA streams the same number of items.
+  // (1,020 items of the 261,120-token verify: 255 CTAs of 4 items rather
+  // than 304 of 3 or 4 -- the layer step 28.5 against 29.0 us in a 12-layer
+  // graph, though the scoring launch alone takes 8.7 against 8.6; 300 CTAs
+  // of 3.4 items took 29.1.)
   const int64_t ctas = (int64_t)sms * kTmaCtasPerSm;
   const int64_t per_cta = (n_items + ctas - 1) / ctas;
   const unsigned grid = (unsigned)((n_items + per_cta - 1) / per_cta);
