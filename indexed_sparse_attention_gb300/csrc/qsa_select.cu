@@ -311,8 +311,11 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
   __shared__ uint32_t s_cnt;
   const SelLayout L(max_nb);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < L.cg; i += NT) sm[i] = 0u;          // the three histograms
-  for (int i = L.selw + tid; i < L.total; i += NT) sm[i] = 0u;   // the two bitmaps
+  // The three histograms and the two bitmaps, 16 bytes per store (every
+  // region starts and ends on a multiple of 4 words).
+  uint4* sm4 = reinterpret_cast<uint4*>(sm);
+  for (int i = tid; i < L.cg / 4; i += NT) sm4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = L.selw / 4 + tid; i < L.total / 4; i += NT) sm4[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
     s_res[0] = 0u;
     s_res[1] = 0u;
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(NT, MINB) select_kernel(const SelectParams<NSE
       q += __popc(bal);
     }
   }
-  for (int i = tid; i < kBins; i += NT) h1[i] = 0u;   // reused by radix level 2
+  for (int i = tid; i < kBins / 4; i += NT) sm4[L.h1 / 4 + i] = make_uint4(0u, 0u, 0u, 0u);   // reused by radix level 2
   __syncthreads();
 
   uint32_t n_list = 0u;
@@ -527,8 +530,10 @@ __global__ void __launch_bounds__(kThreads) merge_select_kernel(const MergeSelec
   __shared__ int32_t out_s[QSA_MAX_TOP_K];
   const SelLayout L(max_union);
   const int tid = threadIdx.x;
-  for (int i = tid; i < L.cg; i += kThreads) sm[i] = 0u;          // the three histograms
-  for (int i = L.selw + tid; i < L.total; i += kThreads) sm[i] = 0u;   // the two bitmaps
+  // The three histograms and the two bitmaps, 16 bytes per store.
+  uint4* sm4 = reinterpret_cast<uint4*>(sm);
+  for (int i = tid; i < L.cg / 4; i += kThreads) sm4[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = L.selw / 4 + tid; i < L.total / 4; i += kThreads) sm4[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
     s_res[0] = 0u;
     s_res[1] = 0u;
