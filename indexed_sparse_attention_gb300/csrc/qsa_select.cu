@@ -79,15 +79,8 @@ __device__ __forceinline__ uint32_t warp_prefix(uint32_t v, uint32_t* wt, uint32
   if (lane == 0) wt[warp] = v;
   __syncthreads();
   const uint32_t w = lane < NT / 32 ? wt[lane] : 0u;
-  uint32_t before = lane < warp ? w : 0u;
-  uint32_t all = w;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    all += __shfl_xor_sync(0xffffffffu, all, o);
-  }
-  *total = all;
-  return before;
+  *total = __reduce_add_sync(0xffffffffu, w);
+  return __reduce_add_sync(0xffffffffu, lane < warp ? w : 0u);
 }
 
 // Exclusive prefix sum of v over the CTA in thread order (same contract on wt).
