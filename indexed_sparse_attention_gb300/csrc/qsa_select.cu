@@ -43,6 +43,10 @@ constexpr int kGroupCap = 1024;                    // candidate groups read back
 constexpr int kListCap = 8192;                     // candidate (key, id) pairs kept
 constexpr int kLoadBatch = 4;                                  // group maxima a thread loads per pass
 constexpr int kChunkBatch = 4;                                  // float4 chunks a thread loads per pass
+// Every region of SelLayout starts on a multiple of 4 words (the clears and
+// the list's chunk loads use 16-byte accesses).
+static_assert(kBins % 4 == 0 && kBins3 % 4 == 0 && kGroupCap % 4 == 0 && kListCap % 4 == 0,
+              "shared-memory regions on 16-byte boundaries");
 
 
 // Shared-memory layout (32-bit words); R1 holds the group-maximum keys, then
