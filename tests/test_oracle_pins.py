@@ -346,6 +346,26 @@ def test_threads_do_not_change_results():
         np.testing.assert_array_equal(a[key], b[key])
 
 
+def test_layer_step_reads_nothing_past_a_row():
+    # A row at position p sees tokens 0..p only (causal, hipfire section 02):
+    # its scores, selection, output and lse must not change when the cache is
+    # cut right after p.  This is the reading under which rows inside a
+    # longer cache are a descriptor with L = p + 1; a visibility bound taken
+    # from the cache length rather than the row's position fails it.  Every
+    # row here chooses 512 of more than 512 blocks.
+    x = make_layer(L=6001, M=3, seed=13, head_dim=32)
+    row_pos = [2500, 4001, 5998]
+    full = oracle.layer_step(x.q_idx, x.idxk, x.q, x.k, x.v, row_pos)
+    for r, p in enumerate(row_pos):
+        cut = oracle.layer_step(x.q_idx[r:r + 1], x.idxk[:p + 1], x.q[r:r + 1], x.k[:, :p + 1], x.v[:, :p + 1], [p])
+        nb = oracle.visible_blocks(p)
+        assert nb > 512 and int(cut["cnt"][0]) == int(full["cnt"][r]) == 512
+        np.testing.assert_array_equal(cut["scores"][0, :nb], full["scores"][r, :nb])
+        np.testing.assert_array_equal(cut["sel"][0], full["sel"][r])
+        np.testing.assert_array_equal(cut["out"][0], full["out"][r])
+        np.testing.assert_array_equal(cut["lse"][0], full["lse"][r])
+
+
 # ------------------------------------------------------------------ fp8 K/V state (E4M3 + f16 scale)
 _FINITE = [c for c in range(256) if c not in (0x7F, 0xFF)]
 
